@@ -1,0 +1,453 @@
+"""SGEMM benchmark on GB300: TFLOPS and fraction of the FP32 roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+A step is one C = alpha*A*B + beta*C call through the C ABI on the
+8192 x 8192 x 8192 workload (row-major FP32, alpha = 1, beta = 0, A and B
+i.i.d. N(0,1) from seed 3), inputs resident in HBM.  Rank 0 prints one JSON
+line.  Under torchrun every rank runs its own independent replica of the
+step (the GEMM has no exchange step), so ``value`` is the FLOPs of all ranks
+over the slowest rank's time ("weak" scaling).
+
+``--impl reference`` times the FP64 CPU oracle on the same workload instead
+(a bounded slab of output rows per step, on the host cores), the only arm
+this library has to compare against.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SGEMM TFLOPS on 1 GB300 at 2048³/8192³; % of FP32 FFMA peak (roofline)"
+WORKLOAD = "8192^3"
+SECONDARY = "2048^3"
+L2_BYTES = 129 * 2 ** 20
+FP32_LANES_PER_SM = 128
+# nominal dense tensor rates (PFLOP/s) used only to scale a measured bf16 peak to tf32
+NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--path", choices=("auto", "ffma", "tf32x3"), default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+def flops(p):
+    return 2.0 * p.m * p.n * p.k
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = None
+        self.windows = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            sel = []
+        fd, self.path = tempfile.mkstemp(prefix="sgemm_clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "nvidia-smi unavailable"}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[3], parts[5:9]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[4][i].lower() == "active"})
+        power = [float(r[3]) for r in inside if r[3].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons,
+                "samples": len(inside),
+                "power_w_median": statistics.median(power) if power else None}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "dense_fp32_gemm_06_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as fh:
+                h.update(name.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel_family):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh).get(kernel_family)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_hash") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh)
+    except (OSError, ValueError):
+        return None
+
+
+def oracle_sample(p, seconds):
+    """Times the FP64 oracle on a slab of output rows sized to ~`seconds`;
+    returns (tflops, rows, seconds, threads)."""
+    import oracle
+    oracle.build()
+    threads = oracle.max_threads()
+    rows = max(1, min(p.m, threads))
+    t = time.perf_counter()
+    oracle.problem_f64(p, rows=(0, rows))
+    dt = time.perf_counter() - t
+    rows = int(max(1, min(p.m, rows * max(1.0, seconds / max(dt, 1e-6)))))
+    t = time.perf_counter()
+    oracle.problem_f64(p, rows=(0, rows))
+    dt = time.perf_counter() - t
+    return 2.0 * rows * p.n * p.k / dt / 1e12, rows, dt, threads
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    from dense_fp32_gemm_06_gb300 import inputs
+    p = inputs.workload(WORKLOAD)
+    oracle.build()
+    threads = oracle.max_threads()
+    # size one step to ~ (budget / steps) seconds of CPU work
+    budget = 150.0
+    per_step = max(0.5, min(10.0, budget / max(1, args.steps + args.warmup)))
+    t = time.perf_counter()
+    oracle.problem_f64(p, rows=(0, threads))
+    dt = time.perf_counter() - t
+    rows = int(max(1, min(p.m, threads * per_step / max(dt, 1e-6))))
+    for _ in range(args.warmup):
+        oracle.problem_f64(p, rows=(0, rows))
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        oracle.problem_f64(p, rows=(0, rows))
+        times.append(time.perf_counter() - t)
+    total = sum(times)
+    value = 2.0 * rows * p.n * p.k * len(times) / total / 1e12
+    sample = f"output rows 0..{rows - 1} of the 8192^3 workload ({rows} x 8192 outputs, k = 8192) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded splitmix64)",
+        "config": {"workload": "sgemm 8192x8192x8192 row-major, alpha=1 beta=0, A,B N(0,1) seed 3",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def time_launches(fn, stream, steps, flush=None):
+    """Per-launch CUDA-event durations (ms) on `stream`."""
+    import torch
+    evs = []
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def run_ours(args, rank, world):
+    import torch
+    import torch.distributed as dist
+    from dense_fp32_gemm_06_gb300 import binding, inputs
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    path = {"auto": binding.PATH_AUTO, "ffma": binding.PATH_FFMA, "tf32x3": binding.PATH_TF32X3}[args.path]
+    stream = torch.cuda.current_stream()
+    sptr = stream.cuda_stream
+
+    p = inputs.workload(WORKLOAD)
+    A_h = torch.from_numpy(p.A).pin_memory()
+    B_h = torch.from_numpy(p.B).pin_memory()
+    C_h = torch.from_numpy(p.C0).pin_memory()
+    A = A_h.cuda()
+    B = B_h.cuda()
+    C = C_h.cuda()
+    torch.cuda.synchronize()
+
+    st, plan = binding.plan(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                            C.data_ptr(), p.ldc, path=path,
+                            num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
+    if st:
+        raise SystemExit(f"plan failed: {binding.status_string(st)}")
+    launches_per_step = 1
+
+    def step():
+        s = binding.sgemm_raw(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                              C.data_ptr(), p.ldc, sptr, path)
+        if s:
+            raise SystemExit(f"sgemm failed: {binding.status_string(s)}")
+
+    # quick self-check on sampled outputs before timing
+    step()
+    torch.cuda.synchronize()
+    import oracle
+    rows, cols = inputs.sample_indices(p.m, p.n, 256, seed=p.seed + 2000)
+    R, E = oracle.problem_f64_sampled(p, rows, cols)
+    got = C.cpu().numpy()[rows, cols]
+    ok, worst, _ = oracle.within_tolerance(got, R, E, p.beta, None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev)
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    per = []
+    ev0.record(stream)
+    for _ in range(args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        per.append((a, b))
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+    total_ms = ev0.elapsed_time(ev1)
+    launch_ms = [a.elapsed_time(b) for a, b in per]
+    if world > 1:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    value = flops(p) * args.steps * world / (total_ms * 1e-3) / 1e12
+    med_ms = statistics.median(launch_ms)
+    mean_ms = sum(launch_ms) / len(launch_ms)
+
+    # ---- roofline of the dominant (only) kernel
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    achieved = flops(p) / (mean_ms * 1e-3) / 1e12
+    if plan["path"] == binding.PATH_FFMA:
+        mhz = clocks.get("sm_mhz") or 2070.0
+        peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak,
+                "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x {mhz:.0f} MHz "
+                              f"(median SM clock sampled during the timed region)",
+                "traffic": traffic_record("ffma")}
+        roof["frac_at_max_clock"] = achieved / (sms * FP32_LANES_PER_SM * 2 * 2070e6 / 1e12)
+    else:
+        mp = measured_peaks()
+        bf16 = (mp or {}).get("bf16_tflops", 1900.0)
+        tf32 = bf16 * NOMINAL_TF32_OVER_BF16
+        roof = {"bound": "tensor", "achieved": 3 * achieved, "peak": tf32, "unit": "TFLOP/s",
+                "frac": 3 * achieved / tf32,
+                "peak_basis": f"measured bf16 {bf16} TFLOP/s ({'of measured' if mp else 'of fallback'}) "
+                              f"x nominal tf32/bf16 ratio 1.1/2.25; achieved counts the three TF32 "
+                              f"products per FP32 product",
+                "traffic": traffic_record("tf32x3")}
+
+    # ---- end to end through the same C call, host buffers, copies timed
+    h2d = A_h.numel() * 4 + B_h.numel() * 4 + (C_h.numel() * 4 if p.beta != 0 else 0)
+    d2h = C_h.numel() * 4
+    out_h = torch.empty_like(C_h).pin_memory()
+
+    def e2e_step():
+        A.copy_(A_h, non_blocking=True)
+        B.copy_(B_h, non_blocking=True)
+        if p.beta != 0:
+            C.copy_(C_h, non_blocking=True)
+        step()
+        out_h.copy_(C, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    e2e = {"value": flops(p) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+           "steps": args.e2e_steps}
+
+    # ---- secondary size (2048^3, fits in L2: flushed between launches)
+    secondary = None
+    if not args.no_secondary:
+        q = inputs.workload(SECONDARY)
+        qA = torch.from_numpy(q.A).cuda()
+        qB = torch.from_numpy(q.B).cuda()
+        qC = torch.from_numpy(q.C0).cuda()
+        scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+
+        def qstep():
+            s = binding.sgemm_raw(q.m, q.n, q.k, q.alpha, qA.data_ptr(), q.lda, qB.data_ptr(), q.ldb, q.beta,
+                                  qC.data_ptr(), q.ldc, sptr, path)
+            if s:
+                raise SystemExit(f"sgemm failed: {binding.status_string(s)}")
+
+        for _ in range(5):
+            qstep()
+        ms = time_launches(qstep, stream, 30, flush=lambda: scratch.fill_(1.0))
+        qmed = statistics.median(ms)
+        secondary = {"workload": "sgemm 2048x2048x2048 row-major, alpha=1 beta=0, A,B U[-1,1] seed 1",
+                     "value": flops(q) / (qmed * 1e-3) / 1e12, "unit": "TFLOPS", "median_ms": qmed,
+                     "launches": len(ms), "l2": "flushed (256 MB write) before every launch"}
+        del scratch
+
+    # ---- CPU baseline: the oracle on a bounded slab of the same workload
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tf, nrows, secs, threads = oracle_sample(p, args.cpu_seconds)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
+               "sample": f"output rows 0..{nrows - 1} of the 8192^3 workload ({nrows} x 8192 outputs, "
+                         f"k = 8192, FP64), {secs:.1f} s"}
+
+    if rank == 0:
+        path_name = {binding.PATH_FFMA: "ffma", binding.PATH_TF32X3: "tf32x3"}.get(plan["path"], "?")
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "median_ms": med_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded splitmix64, N(0,1) via Box-Muller)",
+            "config": {"workload": "sgemm 8192x8192x8192 row-major fp32, alpha=1 beta=0, A,B N(0,1) seed 3",
+                       "path": path_name, "kernel_plan": plan,
+                       "l2": "inputs larger than L2 (768 MB of A, B, C vs 129 MB)",
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "check": {"sampled_outputs": int(len(rows)), "within_tolerance": ok,
+                                 "worst_ratio": worst}},
+            "roofline": roof,
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": args.steps * launches_per_step,
+            "cpu_baseline": cpu,
+            "secondary": secondary,
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
+    try:
+        return run_ours(args, rank, world)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

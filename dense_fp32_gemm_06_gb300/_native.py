@@ -1,0 +1,137 @@
+"""Builds and loads the C-ABI CUDA library (in-tree, sm_103a only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import platform
+import shutil
+import subprocess
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+CSRC = os.path.join(_PKG, "csrc")
+INCLUDE = os.path.join(_ROOT, "include")
+LIB_DIR = os.path.join(_PKG, "_lib")
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
+SOURCES = ["sgemm_api.cu"]
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SgemmError(RuntimeError):
+    """A non-zero status from the C ABI, or a missing library."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"sgemm status {status}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return os.path.join(LIB_DIR, f"libsgemm_gb300_{platform.machine()}.so")
+
+
+def _deps():
+    out = [os.path.join(INCLUDE, "sgemm_gb300.h")]
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            out.append(os.path.join(CSRC, name))
+    return out
+
+
+def _stale(target: str) -> bool:
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(d) > t for d in _deps())
+
+
+def nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise SgemmError(-1, "nvcc not found: cannot build the CUDA library")
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compiles csrc/*.cu into one shared library for sm_103a (objects in
+    parallel, then one link).  Skips the work when the library is newer than
+    every source."""
+    target = lib_path()
+    if not force and not _stale(target):
+        return target
+    os.makedirs(LIB_DIR, exist_ok=True)
+    obj_dir = os.path.join(LIB_DIR, f"obj_{platform.machine()}")
+    os.makedirs(obj_dir, exist_ok=True)
+    cc = nvcc()
+    procs = []
+    objs = []
+    for src in SOURCES:
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
+        objs.append(obj)
+        cmd = [cc, *ARCH_FLAGS, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+    for cmd, p in procs:
+        out, _ = p.communicate()
+        if verbose or p.returncode:
+            print(out.decode(errors="replace"))
+        if p.returncode:
+            raise SgemmError(-1, "nvcc failed: " + " ".join(cmd))
+    tmp = target + f".tmp{os.getpid()}"
+    link = [cc, *ARCH_FLAGS, "-shared", "-o", tmp, *objs]
+    r = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+    if r.returncode:
+        print(r.stdout.decode(errors="replace"))
+        raise SgemmError(-1, "nvcc link failed")
+    os.replace(tmp, target)
+    return target
+
+
+# Exported symbols, in the order the header declares them.
+EXPORTS = ["sgemm", "sgemm_ex", "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_plan_for",
+           "sgemm_device_status", "sgemm_version"]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_int) for name in (
+        "path", "kernel", "bm", "bn", "bk", "rm", "rn", "threads", "stages", "grid", "tiles",
+        "k_tiles", "smem_bytes", "b_vec", "c_vec", "group_m")]
+
+
+def _declare(lib):
+    i, f, vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+    gemm = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
+    lib.sgemm.argtypes = gemm
+    lib.sgemm.restype = i
+    lib.sgemm_ex.argtypes = gemm + [i]
+    lib.sgemm_ex.restype = i
+    lib.sgemm_status_string.argtypes = [i]
+    lib.sgemm_status_string.restype = ctypes.c_char_p
+    lib.sgemm_last_cuda_error.argtypes = []
+    lib.sgemm_last_cuda_error.restype = i
+    lib.sgemm_plan_for.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, i, i, ctypes.POINTER(Plan)]
+    lib.sgemm_plan_for.restype = i
+    lib.sgemm_device_status.argtypes = [ctypes.POINTER(i), i]
+    lib.sgemm_device_status.restype = i
+    lib.sgemm_version.argtypes = []
+    lib.sgemm_version.restype = ctypes.c_char_p
+    return lib
+
+
+def load(build_if_missing: bool = True):
+    """The loaded library (ctypes.CDLL).  Raises SgemmError when it is not
+    built and cannot be built -- there is no fallback implementation."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = lib_path()
+            if build_if_missing:
+                path = build()
+            if not os.path.exists(path):
+                raise SgemmError(-1, f"CUDA library not built ({path}); run __graft_entry__.build()")
+            _lib = _declare(ctypes.CDLL(path))
+        return _lib

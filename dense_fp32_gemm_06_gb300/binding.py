@@ -1,0 +1,88 @@
+"""Python binding of the C ABI (argument marshalling only).
+
+Every step of the GEMM runs in the CUDA library; this module turns torch
+CUDA tensors (or raw device pointers) into the C call's pointers, leading
+dimensions and stream, and turns a non-zero status into ``SgemmError``.
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _native
+from ._native import SgemmError
+
+PATH_AUTO = 0
+PATH_FFMA = 1
+PATH_TF32X3 = 2
+
+
+def status_string(status: int) -> str:
+    return _native.load().sgemm_status_string(int(status)).decode()
+
+
+def _check(status: int):
+    if status:
+        lib = _native.load()
+        msg = lib.sgemm_status_string(status).decode()
+        if status == 100:
+            msg += f" (cudaError {lib.sgemm_last_cuda_error()})"
+        raise SgemmError(status, msg)
+
+
+def sgemm_raw(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, stream=0,
+              path=PATH_AUTO) -> int:
+    """Direct C call on raw device pointers (ints); returns the status."""
+    lib = _native.load()
+    return lib.sgemm_ex(int(m), int(n), int(k), ctypes.c_float(alpha), ctypes.c_void_p(A_ptr or None),
+                        int(lda), ctypes.c_void_p(B_ptr or None), int(ldb), ctypes.c_float(beta),
+                        ctypes.c_void_p(C_ptr or None), int(ldc), ctypes.c_void_p(stream or None),
+                        int(path))
+
+
+def plan(m, n, k, alpha=1.0, A_ptr=16, lda=None, B_ptr=16, ldb=None, beta=0.0, C_ptr=16, ldc=None,
+         path=PATH_AUTO, num_sms=152):
+    """The launch plan the library would use (host only, no GPU needed);
+    returns (status, dict)."""
+    lib = _native.load()
+    lda = max(1, k) if lda is None else lda
+    ldb = max(1, n) if ldb is None else ldb
+    ldc = max(1, n) if ldc is None else ldc
+    p = _native.Plan()
+    st = lib.sgemm_plan_for(int(m), int(n), int(k), ctypes.c_float(alpha), ctypes.c_void_p(A_ptr or None),
+                            int(lda), ctypes.c_void_p(B_ptr or None), int(ldb), ctypes.c_float(beta),
+                            ctypes.c_void_p(C_ptr or None), int(ldc), int(path), int(num_sms),
+                            ctypes.byref(p))
+    return st, {name: getattr(p, name) for name, _ in _native.Plan._fields_}
+
+
+def _row_major(t, name):
+    import torch
+    if t.dtype != torch.float32 or not t.is_cuda or t.dim() != 2:
+        raise SgemmError(-1, f"{name} must be a 2-D float32 CUDA tensor")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise SgemmError(-1, f"{name} must have unit column stride (row-major)")
+    return max(t.stride(0), 1) if t.shape[0] > 1 else max(t.shape[1], 1)
+
+
+def sgemm_ex(A, B, C, alpha=1.0, beta=0.0, *, path=PATH_AUTO, stream=None):
+    """C = alpha * A @ B + beta * C in place on row-major float32 CUDA tensors
+    (A: m x k, B: k x n, C: m x n; any row strides).  Runs on ``stream``
+    (default: torch's current stream of C's device).  Returns C."""
+    import torch
+    m, k = A.shape
+    k2, n = B.shape
+    if k2 != k or tuple(C.shape) != (m, n):
+        raise SgemmError(-1, f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    lda, ldb, ldc = _row_major(A, "A"), _row_major(B, "B"), _row_major(C, "C")
+    lda, ldb, ldc = max(lda, k, 1), max(ldb, n, 1), max(ldc, n, 1)
+    if stream is None:
+        stream = torch.cuda.current_stream(C.device).cuda_stream
+    with torch.cuda.device(C.device):
+        _check(sgemm_raw(m, n, k, alpha, A.data_ptr(), lda, B.data_ptr(), ldb, beta, C.data_ptr(), ldc,
+                         stream, path))
+    return C
+
+
+def sgemm(A, B, C, alpha=1.0, beta=0.0, *, stream=None):
+    """C = alpha * A @ B + beta * C (the library's own kernel choice)."""
+    return sgemm_ex(A, B, C, alpha, beta, path=PATH_AUTO, stream=stream)

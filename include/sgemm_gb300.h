@@ -1,0 +1,136 @@
+/*
+ * sgemm_gb300.h -- C ABI of a single-precision GEMM for NVIDIA GB300 (sm_103a).
+ *
+ *     C = alpha * A * B + beta * C        A: m x k, B: k x n, C: m x n, FP32
+ *
+ * Operation.  C_ij = sum_{t=0}^{k-1} A_it * B_tj is the GEMM definition of
+ * hatrix.site "GEMM优化原理" (section 问题定义, first equation; also
+ * aerisun.top "GPU 访存与计算优化", section "Naive GEMM 的重复读取").  The pages
+ * call the kernel with two float scalars next to the three matrices and the
+ * three sizes (blog.lightlisten.com "gemm优化", the ncu launch line in section
+ * 实际测试：ncu); they say nothing further about the scalars, so alpha and beta
+ * take the BLAS meaning: beta == 0 makes C write-only (its old contents are
+ * never read, so NaN there does not propagate), and alpha == 0 or k == 0
+ * gives C = beta * C without reading A or B.
+ *
+ * Layout.  Row-major with leading dimensions, as the pages' loads assume
+ * (aerisun.top, section "Shared Tiling 与 block 内复用"):
+ *     A(i,t) = A[i*lda + t],  B(t,j) = B[t*ldb + j],  C(i,j) = C[i*ldc + j].
+ * Offsets are computed in 64 bits.  Any lda >= max(1,k), ldb >= max(1,n),
+ * ldc >= max(1,n) and any 4-byte-aligned pointers are accepted; 16-byte
+ * aligned bases with leading dimensions that are multiples of 4 take the
+ * vectorised / TMA loads, everything else the 4-byte zero-filling loads.
+ *
+ * Ownership.  A, B and C are device pointers owned by the caller (any memory
+ * the current device can address).  The library keeps no pointer after the
+ * call returns.  Per device it lazily caches kernel attributes and (for the
+ * tensor-core path) a device-resident status word; it never allocates per
+ * call.  C must not overlap A or B.
+ *
+ * Execution.  Every entry point that takes a stream enqueues its kernels on
+ * `stream` (0 = the legacy default stream) of the current device and returns
+ * without synchronising; errors raised later by the GPU surface at the
+ * caller's next synchronisation.  Calls are thread-safe.
+ *
+ * Errors.  The return value is a status:
+ *     0                      success;
+ *     1 .. 11                argument i (1-based, BLAS "info" convention) is
+ *                            invalid: 1 m < 0, 2 n < 0, 3 k < 0,
+ *                            5 A == NULL while m*n*k > 0 and alpha != 0,
+ *                            6 lda < max(1,k), 7 B == NULL (same rule as A),
+ *                            8 ldb < max(1,n), 10 C == NULL while m*n > 0,
+ *                            11 ldc < max(1,n); also 5/7/10 for a pointer not
+ *                            4-byte aligned;
+ *     SGEMM_STATUS_BAD_PATH  sgemm_ex() asked for an unknown path;
+ *     SGEMM_STATUS_UNSUPPORTED  the requested path cannot run this problem
+ *                            (e.g. the tensor-core path with A or B rows not
+ *                            16-byte aligned);
+ *     SGEMM_STATUS_CUDA_ERROR  a CUDA runtime call or launch failed; the CUDA
+ *                            error code is kept per thread and returned by
+ *                            sgemm_last_cuda_error().
+ * On any non-zero status nothing has been enqueued.
+ */
+#ifndef SGEMM_GB300_H
+#define SGEMM_GB300_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SGEMM_STATUS_OK 0
+#define SGEMM_STATUS_BAD_PATH 98
+#define SGEMM_STATUS_UNSUPPORTED 99
+#define SGEMM_STATUS_CUDA_ERROR 100
+
+/* Kernel families sgemm_ex() can be asked for. */
+#define SGEMM_PATH_AUTO 0   /* the library's choice (what sgemm() runs)        */
+#define SGEMM_PATH_FFMA 1   /* CUDA-core FP32 FFMA, exact FP32 products        */
+#define SGEMM_PATH_TF32X3 2 /* tcgen05 tensor cores, 3xTF32 split precision    */
+
+/*
+ * sgemm -- C = alpha * A * B + beta * C on `stream`.  See the file comment
+ * for layout, ownership and status codes.
+ */
+int sgemm(int m, int n, int k, float alpha,
+          const float *A, int lda, const float *B, int ldb,
+          float beta, float *C, int ldc, cudaStream_t stream);
+
+/*
+ * sgemm_ex -- as sgemm, with the kernel family chosen by `path`
+ * (SGEMM_PATH_*).  SGEMM_PATH_AUTO is identical to sgemm().
+ */
+int sgemm_ex(int m, int n, int k, float alpha,
+             const float *A, int lda, const float *B, int ldb,
+             float beta, float *C, int ldc, cudaStream_t stream, int path);
+
+/* Static, NUL-terminated description of a status code. */
+const char *sgemm_status_string(int status);
+
+/* cudaError_t value of the last SGEMM_STATUS_CUDA_ERROR on this thread. */
+int sgemm_last_cuda_error(void);
+
+/*
+ * Launch plan the library would use for a problem (host only: reads no
+ * memory, needs no GPU).  The pointers are inspected for alignment only.
+ * num_sms is the SM count of the target device (152 on GB300).
+ */
+typedef struct sgemm_plan {
+    int path;          /* SGEMM_PATH_FFMA or SGEMM_PATH_TF32X3; 0 = no kernel (m or n is 0) */
+    int kernel;        /* 0 main GEMM kernel, 1 C = beta*C scale kernel                        */
+    int bm, bn, bk;    /* CTA tile (rows of C, columns of C, k per pipeline stage)             */
+    int rm, rn;        /* per-thread register tile of C (FFMA path; 0 otherwise)               */
+    int threads;       /* threads per CTA                                                      */
+    int stages;        /* shared-memory pipeline depth                                         */
+    int grid;          /* CTAs launched                                                        */
+    int tiles;         /* output tiles = ceil(m/bm) * ceil(n/bn)                               */
+    int k_tiles;       /* pipeline stages consumed per tile = ceil(k/bk)                       */
+    int smem_bytes;    /* dynamic shared memory per CTA                                        */
+    int b_vec;         /* 1: B loaded 16 bytes at a time / by TMA                              */
+    int c_vec;         /* 1: C read and written 16 bytes at a time                             */
+    int group_m;       /* tile rows per raster group (L2 reuse)                                */
+} sgemm_plan;
+
+int sgemm_plan_for(int m, int n, int k, float alpha,
+                   const float *A, int lda, const float *B, int ldb,
+                   float beta, const float *C, int ldc, int path, int num_sms,
+                   sgemm_plan *plan);
+
+/*
+ * Device-side status word of the tensor-core path on the current device: its
+ * pipeline waits are bounded, and a wait that runs out sets a non-zero code
+ * (the kernel then abandons its tile instead of hanging).  Synchronises the
+ * device, copies the word to *flag and, when `clear` is non-zero, resets it.
+ */
+int sgemm_device_status(int *flag, int clear);
+
+/* Library version string, e.g. "sgemm_gb300 0.1 (sm_103a)". */
+const char *sgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_GB300_H */

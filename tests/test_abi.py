@@ -1,0 +1,109 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function the header declares, validates arguments with the documented
+status codes, and plans launches whose tile bookkeeping agrees with the
+two-level blocking model."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from dense_fp32_gemm_06_gb300 import _native, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sgemm_gb300.h")
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(sgemm\w*)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_expected_functions():
+    names = header_functions()
+    assert set(names) == set(_native.EXPORTS), names
+
+
+def test_library_loads_and_exports_every_symbol():
+    lib = _native.load()
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_version_and_status_strings():
+    lib = _native.load()
+    assert b"sm_103a" in lib.sgemm_version()
+    for st in (0, 1, 2, 3, 5, 6, 7, 8, 10, 11, 98, 99, 100):
+        s = binding.status_string(st)
+        assert s and s != "unknown status"
+    assert binding.status_string(12345) == "unknown status"
+
+
+VALID = dict(m=4, n=5, k=6, alpha=1.0, A=256, lda=6, B=512, ldb=5, beta=0.0, C=1024, ldc=5)
+
+
+def call(**over):
+    a = dict(VALID)
+    a.update(over)
+    # Every case below is rejected (or is a no-op) before any CUDA call, so
+    # the fake pointers are never dereferenced.
+    return binding.sgemm_raw(a["m"], a["n"], a["k"], a["alpha"], a["A"], a["lda"], a["B"], a["ldb"],
+                             a["beta"], a["C"], a["ldc"], 0, a.get("path", 0))
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(m=-1), 1), (dict(n=-1), 2), (dict(k=-1), 3),
+    (dict(A=0), 5), (dict(A=258), 5), (dict(lda=5), 6), (dict(B=0), 7), (dict(B=514), 7),
+    (dict(ldb=4), 8), (dict(C=0), 10), (dict(C=1026), 10), (dict(ldc=4), 11),
+    (dict(k=0, lda=0), 6), (dict(n=0, ldb=0), 8),
+    (dict(m=-1, n=-1), 1), (dict(lda=1, ldc=1), 6),
+    (dict(path=7), 98),
+])
+def test_invalid_arguments(over, status):
+    assert call(**over) == status
+
+
+@pytest.mark.parametrize("over", [dict(m=0), dict(n=0), dict(m=0, A=0, B=0, C=0), dict(n=0, C=0, B=0)])
+def test_empty_output_is_a_noop(over):
+    assert call(**over) == 0
+
+
+def test_null_operands_allowed_when_unused():
+    # alpha == 0 or k == 0: A and B are not read; plan only (no launch)
+    st, p = binding.plan(4, 5, 6, alpha=0.0, A_ptr=0, B_ptr=0)
+    assert st == 0 and p["kernel"] == 1
+    st, p = binding.plan(4, 5, 0, A_ptr=0, B_ptr=0, lda=1)
+    assert st == 0 and p["kernel"] == 1
+
+
+def test_plan_matches_blocking_model():
+    """The FFMA plan's grid, threads and slab count at 2048^3 are the
+    two-level blocking's M*N blocks, X*Y threads and K big iterations for
+    the plan's own tile (bm, bn, bk, rm, rn)."""
+    st, p = binding.plan(2048, 2048, 2048, path=binding.PATH_FFMA)
+    assert st == 0
+    c = oracle.tiling_counts(2048, 2048, 2048, p["bm"], p["bn"], p["bk"], p["rm"], p["rn"])
+    assert p["grid"] == p["tiles"] == c["blocks"]
+    assert p["threads"] == c["threads_per_block"]
+    assert p["k_tiles"] == c["big_iterations"]
+    assert p["smem_bytes"] <= 227 * 1024
+
+
+def test_plan_ragged_shapes_cover_the_output():
+    for m, n, k in ((1000, 1500, 777), (1, 1, 1), (129, 257, 17), (16384, 128, 8192)):
+        st, p = binding.plan(m, n, k, lda=k, path=binding.PATH_FFMA)
+        assert st == 0
+        assert p["tiles"] == -(-m // p["bm"]) * -(-n // p["bn"])
+        assert p["grid"] >= 1 and p["k_tiles"] == -(-k // p["bk"])
+
+
+def test_plan_alignment_flags():
+    st, p = binding.plan(64, 64, 64, B_ptr=16, C_ptr=16)
+    assert (p["b_vec"], p["c_vec"]) == (1, 1)
+    st, p = binding.plan(64, 64, 64, B_ptr=20, C_ptr=16)
+    assert (p["b_vec"], p["c_vec"]) == (0, 1)
+    st, p = binding.plan(64, 66, 64, ldb=66, ldc=66)
+    assert (p["b_vec"], p["c_vec"]) == (0, 0)
