@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--shape", default=None,
+                    help="m,n,k of a smaller square-workload stand-in (profiling captures)")
     return ap.parse_args()
 
 
@@ -132,28 +134,41 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- helpers
 
-def kernel_source_hash():
+# sources that define each kernel family (a traffic figure is void once any changes)
+KERNEL_SOURCES = {
+    "ffma": ["ffma_sgemm.cuh", "ptx.cuh"],
+    "tf32x3": ["tf32x3_sgemm.cuh", "ptx.cuh"],
+}
+
+
+def kernel_source_hash(family):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp32_gemm_06_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
+    for name in KERNEL_SOURCES[family]:
+        try:
             with open(os.path.join(csrc, name), "rb") as fh:
                 h.update(name.encode() + fh.read())
+        except OSError:
+            h.update(name.encode() + b"<missing>")
     return h.hexdigest()[:16]
 
 
-def traffic_record(kernel_family):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel sources changed since it was captured."""
+def traffic_record(kernel_family, units):
+    """DRAM bytes per launch (read + write) of the kernel from the committed
+    ncu summary, scaled to `units` (output elements of the launch) when the
+    capture was of a different size; None when the kernel sources changed
+    since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
             rec = json.load(fh).get(kernel_family)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash():
+    if not rec or rec.get("source_hash") != kernel_source_hash(kernel_family):
         return None
-    return rec.get("dram_bytes_per_launch")
+    if rec.get("units") == units:
+        return rec.get("dram_bytes_per_launch")
+    return None
 
 
 def measured_peaks():
@@ -243,6 +258,22 @@ def time_launches(fn, stream, steps, flush=None):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def time_e2e(e2e_step, stream, steps, p, world, h2d, d2h):
+    import torch
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": flops(p) * world / (ms * 1e-3) / 1e12, "unit": "TFLOPS",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+
+
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -254,7 +285,11 @@ def run_ours(args, rank, world):
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
 
-    p = inputs.workload(WORKLOAD)
+    if args.shape:
+        m, n, k = (int(x) for x in args.shape.split(","))
+        p = inputs.workload(WORKLOAD, m=m, n=n, k=k)
+    else:
+        p = inputs.workload(WORKLOAD)
     A_h = torch.from_numpy(p.A).pin_memory()
     B_h = torch.from_numpy(p.B).pin_memory()
     C_h = torch.from_numpy(p.C0).pin_memory()
@@ -334,7 +369,7 @@ def run_ours(args, rank, world):
                 "frac": achieved / peak,
                 "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x {mhz:.0f} MHz "
                               f"(median SM clock sampled during the timed region)",
-                "traffic": traffic_record("ffma")}
+                "traffic": traffic_record("ffma", p.m * p.n * p.k)}
         roof["frac_at_max_clock"] = achieved / (sms * FP32_LANES_PER_SM * 2 * 2070e6 / 1e12)
     else:
         mp = measured_peaks()
@@ -345,7 +380,7 @@ def run_ours(args, rank, world):
                 "peak_basis": f"measured bf16 {bf16} TFLOP/s ({'of measured' if mp else 'of fallback'}) "
                               f"x nominal tf32/bf16 ratio 1.1/2.25; achieved counts the three TF32 "
                               f"products per FP32 product",
-                "traffic": traffic_record("tf32x3")}
+                "traffic": traffic_record("tf32x3", p.m * p.n * p.k)}
 
     # ---- end to end through the same C call, host buffers, copies timed
     h2d = A_h.numel() * 4 + B_h.numel() * 4 + (C_h.numel() * 4 if p.beta != 0 else 0)
@@ -360,19 +395,9 @@ def run_ours(args, rank, world):
         step()
         out_h.copy_(C, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    e2e = {"value": flops(p) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-           "steps": args.e2e_steps}
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = time_e2e(e2e_step, stream, args.e2e_steps, p, world, h2d, d2h)
 
     # ---- secondary size (2048^3, fits in L2: flushed between launches)
     secondary = None

@@ -1,5 +1,7 @@
 // C ABI of the GB300 SGEMM library: argument checks, launch planning and
 // kernel launches.  Declared in include/sgemm_gb300.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -24,6 +26,12 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+
+// Kernel ids in sgemm_plan::kernel.
+constexpr int kKernelFfmaCpAsync = 0;
+constexpr int kKernelScale = 1;
+constexpr int kKernelFfmaTma = 2;
 
 int fail_cuda(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -32,8 +40,8 @@ int fail_cuda(cudaError_t e) {
 
 template <bool BV, bool CV>
 cudaError_t set_ffma_attr() {
-    return cudaFuncSetAttribute(ffma::ffma_sgemm_kernel<BV, CV>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, ffma::SMEM_BYTES);
+    return cudaFuncSetAttribute(ffma::ffma_sgemm_kernel<ffma::Default, BV, CV>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, ffma::Default::SMEM_BYTES);
 }
 
 // One-time per-device set-up: SM count and kernel attributes.
@@ -51,6 +59,14 @@ int device_state(DeviceState **out) {
         if ((e = set_ffma_attr<true, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_ffma_attr<false, true>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_ffma_attr<false, false>()) != cudaSuccess) return fail_cuda(e);
+        if (g_encode_tiled == nullptr) {
+            cudaDriverEntryPointQueryResult q;
+            void *fn = nullptr;
+            e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+            if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return fail_cuda(e != cudaSuccess ? e : cudaErrorSymbolNotFound);
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
         d.ready = true;
     }
     *out = &d;
@@ -78,20 +94,22 @@ int check_args(int m, int n, int k, float alpha, const float *A, int lda, const 
     return 0;
 }
 
+bool tma_ok(const void *p, int ld) { return aligned(p, 16) && (ld % 4) == 0; }
+
 int plan(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
          const float *C, int ldc, int path, int num_sms, sgemm_plan *pl) {
-    (void)A;
     (void)beta;
-    (void)num_sms;
     std::memset(pl, 0, sizeof(*pl));
     if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
         return SGEMM_STATUS_BAD_PATH;
     if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc)) return bad;
     if (m == 0 || n == 0) return SGEMM_STATUS_OK;
     if (path == SGEMM_PATH_TF32X3) return SGEMM_STATUS_UNSUPPORTED;
+    if (num_sms <= 0) num_sms = 1;
     pl->path = SGEMM_PATH_FFMA;
+    pl->c_vec = aligned(C, 16) && (ldc % 4) == 0;
     if (k == 0 || alpha == 0.f) {
-        pl->kernel = 1;
+        pl->kernel = kKernelScale;
         pl->threads = 256;
         const long long total = (long long)m * n;
         long long blocks = (total + 255) / 256;
@@ -99,29 +117,43 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         pl->c_vec = 0;
         return SGEMM_STATUS_OK;
     }
-    pl->kernel = 0;
-    pl->bm = ffma::BM;
-    pl->bn = ffma::BN;
-    pl->bk = ffma::BK;
-    pl->rm = ffma::RM;
-    pl->rn = ffma::RN;
-    pl->threads = ffma::THREADS;
-    pl->stages = ffma::STAGES;
-    const int tiles_m = (m + ffma::BM - 1) / ffma::BM;
-    const int tiles_n = (n + ffma::BN - 1) / ffma::BN;
+    pl->kernel = kKernelFfmaCpAsync;
+    pl->bm = ffma::Default::BM;
+    pl->bn = ffma::Default::BN;
+    pl->bk = ffma::Default::BK;
+    pl->rm = ffma::Default::TM;
+    pl->rn = ffma::Default::TN;
+    pl->threads = ffma::Default::THREADS;
+    pl->stages = ffma::Default::STAGES;
+    pl->smem_bytes = ffma::Default::SMEM_BYTES;
+    pl->b_vec = aligned(B, 16) && (ldb % 4) == 0;
+    const int tiles_m = (m + pl->bm - 1) / pl->bm;
+    const int tiles_n = (n + pl->bn - 1) / pl->bn;
     pl->tiles = tiles_m * tiles_n;
     pl->grid = pl->tiles;
-    pl->k_tiles = (k + ffma::BK - 1) / ffma::BK;
-    pl->smem_bytes = ffma::SMEM_BYTES;
-    pl->b_vec = aligned(B, 16) && (ldb % 4) == 0;
-    pl->c_vec = aligned(C, 16) && (ldc % 4) == 0;
+    pl->k_tiles = (k + pl->bk - 1) / pl->bk;
     pl->group_m = tiles_m < 8 ? tiles_m : 8;
+    return SGEMM_STATUS_OK;
+}
+
+// 2-D row-major FP32 tensor map: `rows` x `cols` with a row pitch of `ld`
+// floats, copied in boxes of box_rows x box_cols.
+int make_tensor_map(CUtensorMap *map, const float *base, int rows, int cols, int ld, int box_rows, int box_cols,
+                    CUtensorMapSwizzle swizzle) {
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
     return SGEMM_STATUS_OK;
 }
 
 template <bool BV, bool CV>
 void launch_ffma(const GemmArgs &a, const sgemm_plan &pl, cudaStream_t s) {
-    ffma::ffma_sgemm_kernel<BV, CV><<<pl.grid, pl.threads, pl.smem_bytes, s>>>(a);
+    ffma::ffma_sgemm_kernel<ffma::Default, BV, CV><<<pl.grid, pl.threads, pl.smem_bytes, s>>>(a);
 }
 
 }  // namespace
@@ -130,13 +162,17 @@ extern "C" {
 
 int sgemm_ex(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb,
              float beta, float *C, int ldc, cudaStream_t stream, int path) {
+    if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
+        return SGEMM_STATUS_BAD_PATH;
+    if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc)) return bad;
+    if (m == 0 || n == 0) return SGEMM_STATUS_OK;
     DeviceState *dev = nullptr;
-    sgemm_plan pl;
-    int st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, 0, &pl);
+    int st = device_state(&dev);
     if (st != SGEMM_STATUS_OK) return st;
-    if (pl.path == 0) return SGEMM_STATUS_OK;   // m == 0 or n == 0
-    if ((st = device_state(&dev)) != SGEMM_STATUS_OK) return st;
-    if (pl.kernel == 1) {
+    sgemm_plan pl;
+    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, dev->sms, &pl);
+    if (st != SGEMM_STATUS_OK) return st;
+    if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
     } else {
         GemmArgs a;
@@ -200,10 +236,15 @@ const char *sgemm_status_string(int status) {
 int sgemm_last_cuda_error(void) { return g_last_cuda_error; }
 
 int sgemm_device_status(int *flag, int clear) {
-    (void)clear;
-    if (flag) *flag = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail_cuda(e);
+    int v = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_sgemm_status, sizeof(int))) != cudaSuccess) return fail_cuda(e);
+    if (flag) *flag = v;
+    if (clear) {
+        const int zero = 0;
+        if ((e = cudaMemcpyToSymbol(g_sgemm_status, &zero, sizeof(int))) != cudaSuccess) return fail_cuda(e);
+    }
     return SGEMM_STATUS_OK;
 }
 

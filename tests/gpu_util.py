@@ -53,10 +53,12 @@ class Placed:
             win = np.full(rows * ld, SENTINEL, dtype=np.float32)
             win[:span] = host[start:start + span]
             win = win.reshape(rows, ld)
-            gaps = win[:, cols:]
+            # the gaps between rows (ld > cols) hold the generator's padding
+            # (NaN) for C0 and must be untouched; the last row has no gap
+            # inside the span (what follows it is the sentinel guard above)
+            gaps = win[:rows - 1, cols:]
             if ld > cols:
-                # row gaps hold the generator's padding (NaN) for C0; they must be untouched
-                orig = np.ascontiguousarray(self.p.C0).reshape(rows, ld)[:, cols:]
+                orig = np.ascontiguousarray(self.p.C0).reshape(rows, ld)[:rows - 1, cols:]
                 same = (gaps == orig) | (np.isnan(gaps) & np.isnan(orig))
                 ok = ok and bool(np.all(same))
             return np.ascontiguousarray(win[:, :cols]), ok
