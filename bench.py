@@ -43,8 +43,8 @@ NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--path", choices=("auto", "ffma", "tf32x3"), default="auto")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -136,8 +136,8 @@ class ClockSampler:
 
 # sources that define each kernel family (a traffic figure is void once any changes)
 KERNEL_SOURCES = {
-    "ffma": ["ffma_sgemm.cuh", "ptx.cuh"],
-    "tf32x3": ["tf32x3_sgemm.cuh", "ptx.cuh"],
+    "ffma": ["ffma_sgemm.cuh", "ptx.cuh", "raster.cuh"],
+    "tf32x3": ["tf32x3_sgemm.cuh", "tcgen05.cuh", "ptx.cuh", "raster.cuh"],
 }
 
 
@@ -303,8 +303,6 @@ def run_ours(args, rank, world):
                             num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
     if st:
         raise SystemExit(f"plan failed: {binding.status_string(st)}")
-    launches_per_step = 1
-
     def step():
         s = binding.sgemm_raw(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
                               C.data_ptr(), p.ldc, sptr, path)
@@ -359,28 +357,57 @@ def run_ours(args, rank, world):
     med_ms = statistics.median(launch_ms)
     mean_ms = sum(launch_ms) / len(launch_ms)
 
-    # ---- roofline of the dominant (only) kernel
+    # ---- roofline of the dominant kernel
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    achieved = flops(p) / (mean_ms * 1e-3) / 1e12
+    mhz = clocks.get("sm_mhz") or 2070.0
+    ffma_peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
+    ffma_basis = (f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x {mhz:.0f} MHz "
+                  f"(median SM clock sampled during the timed region)")
     if plan["path"] == binding.PATH_FFMA:
-        mhz = clocks.get("sm_mhz") or 2070.0
-        peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
-        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak,
-                "peak_basis": f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x {mhz:.0f} MHz "
-                              f"(median SM clock sampled during the timed region)",
+        # the step is the one FFMA kernel
+        launches_per_step = 1
+        achieved = flops(p) / (mean_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "kernel": "ffma_sgemm_kernel", "achieved": achieved, "peak": ffma_peak,
+                "unit": "TFLOP/s", "frac": achieved / ffma_peak, "peak_basis": ffma_basis,
                 "traffic": traffic_record("ffma", p.m * p.n * p.k)}
-        roof["frac_at_max_clock"] = achieved / (sms * FP32_LANES_PER_SM * 2 * 2070e6 / 1e12)
     else:
+        # the step is split_a + split_bt + the tcgen05 GEMM; the GEMM kernel
+        # alone is timed on operands split once, through the split-GEMM call
+        launches_per_step = 3
+        ka = binding.ka_of(p.k)
+        a_hi = torch.empty(p.m * ka, device="cuda")
+        a_lo = torch.empty_like(a_hi)
+        b_hi = torch.empty(p.n * ka, device="cuda")
+        b_lo = torch.empty_like(b_hi)
+        binding.tf32x3_split_a(A[:, :p.k], a_hi, a_lo)
+        binding.tf32x3_split_b(B[:, :p.n], b_hi, b_lo)
+
+        def gemm_only():
+            s = binding.tf32x3_split_gemm_raw(p.m, p.n, p.k, p.alpha, a_hi.data_ptr(), a_lo.data_ptr(),
+                                               b_hi.data_ptr(), b_lo.data_ptr(), p.beta, C.data_ptr(), p.ldc,
+                                               sptr)
+            if s:
+                raise SystemExit(f"split gemm failed: {binding.status_string(s)}")
+
+        for _ in range(3):
+            gemm_only()
+        gm = time_launches(gemm_only, stream, min(args.steps, 100))
+        gemm_ms = sum(gm) / len(gm)
+        del a_hi, a_lo, b_hi, b_lo
+        achieved = flops(p) / (gemm_ms * 1e-3) / 1e12
         mp = measured_peaks()
         bf16 = (mp or {}).get("bf16_tflops", 1900.0)
         tf32 = bf16 * NOMINAL_TF32_OVER_BF16
-        roof = {"bound": "tensor", "achieved": 3 * achieved, "peak": tf32, "unit": "TFLOP/s",
-                "frac": 3 * achieved / tf32,
-                "peak_basis": f"measured bf16 {bf16} TFLOP/s ({'of measured' if mp else 'of fallback'}) "
-                              f"x nominal tf32/bf16 ratio 1.1/2.25; achieved counts the three TF32 "
-                              f"products per FP32 product",
+        roof = {"bound": "tensor", "kernel": "tf32x3_gemm_kernel", "achieved": achieved, "peak": tf32 / 3,
+                "unit": "TFLOP/s", "frac": achieved / (tf32 / 3),
+                "peak_basis": f"TF32 dense peak / 3 (three TF32 products per FP32 product); TF32 peak = "
+                              f"measured bf16 {bf16} TFLOP/s ({'of measured' if mp else 'of fallback'}) x "
+                              f"nominal tf32/bf16 ratio 1.1/2.25 = {tf32:.1f} TFLOP/s",
+                "gemm_kernel_ms": gemm_ms, "split_kernels_ms": mean_ms - gemm_ms,
+                "tensor_pipe_tflops": 3 * achieved,
                 "traffic": traffic_record("tf32x3", p.m * p.n * p.k)}
+    roof["ffma_peak_tflops"] = ffma_peak
+    roof["value_over_ffma_peak"] = value / world / ffma_peak
 
     # ---- end to end through the same C call, host buffers, copies timed
     h2d = A_h.numel() * 4 + B_h.numel() * 4 + (C_h.numel() * 4 if p.beta != 0 else 0)
@@ -423,6 +450,21 @@ def run_ours(args, rank, world):
                      "launches": len(ms), "l2": "flushed (256 MB write) before every launch"}
         del scratch
 
+    # ---- the CUDA-core FFMA path on the same workload, for comparison
+    ffma = None
+    if plan["path"] != binding.PATH_FFMA and not args.no_secondary:
+        def ffma_step():
+            s = binding.sgemm_raw(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                                  C.data_ptr(), p.ldc, sptr, binding.PATH_FFMA)
+            if s:
+                raise SystemExit(f"sgemm failed: {binding.status_string(s)}")
+        for _ in range(2):
+            ffma_step()
+        fm = time_launches(ffma_step, stream, 10)
+        f_ms = sum(fm) / len(fm)
+        ffma = {"value": flops(p) / (f_ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms": f_ms, "launches": len(fm),
+                "frac_of_ffma_peak": flops(p) / (f_ms * 1e-3) / 1e12 / ffma_peak}
+
     # ---- CPU baseline: the oracle on a bounded slab of the same workload
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -436,7 +478,8 @@ def run_ours(args, rank, world):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "median_ms": med_ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "tf32x3" if plan["path"] == binding.PATH_TF32X3 else "f32",
             "data": "synthetic (seeded splitmix64, N(0,1) via Box-Muller)",
             "config": {"workload": "sgemm 8192x8192x8192 row-major fp32, alpha=1 beta=0, A,B N(0,1) seed 3",
                        "path": path_name, "kernel_plan": plan,
@@ -450,6 +493,7 @@ def run_ours(args, rank, world):
             "gpu_launches": args.steps * launches_per_step,
             "cpu_baseline": cpu,
             "secondary": secondary,
+            "ffma_path": ffma,
         }
         print(json.dumps(line), flush=True)
     return 0

@@ -92,8 +92,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 # Exported symbols, in the order the header declares them.
-EXPORTS = ["sgemm", "sgemm_ex", "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_plan_for",
-           "sgemm_device_status", "sgemm_version"]
+EXPORTS = ["sgemm", "sgemm_ex", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", "sgemm_tf32x3_split_gemm",
+           "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_plan_for", "sgemm_device_status",
+           "sgemm_version"]
 
 
 class Plan(ctypes.Structure):
@@ -109,6 +110,12 @@ def _declare(lib):
     lib.sgemm.restype = i
     lib.sgemm_ex.argtypes = gemm + [i]
     lib.sgemm_ex.restype = i
+    lib.sgemm_tf32x3_split_a.argtypes = [i, i, vp, i, vp, vp, vp]
+    lib.sgemm_tf32x3_split_a.restype = i
+    lib.sgemm_tf32x3_split_b.argtypes = [i, i, vp, i, vp, vp, vp]
+    lib.sgemm_tf32x3_split_b.restype = i
+    lib.sgemm_tf32x3_split_gemm.argtypes = [i, i, i, f, vp, vp, vp, vp, f, vp, i, vp]
+    lib.sgemm_tf32x3_split_gemm.restype = i
     lib.sgemm_status_string.argtypes = [i]
     lib.sgemm_status_string.restype = ctypes.c_char_p
     lib.sgemm_last_cuda_error.argtypes = []

@@ -86,3 +86,44 @@ def sgemm_ex(A, B, C, alpha=1.0, beta=0.0, *, path=PATH_AUTO, stream=None):
 def sgemm(A, B, C, alpha=1.0, beta=0.0, *, stream=None):
     """C = alpha * A @ B + beta * C (the library's own kernel choice)."""
     return sgemm_ex(A, B, C, alpha, beta, path=PATH_AUTO, stream=stream)
+
+
+def ka_of(k: int) -> int:
+    """Row pitch (floats) of the 3xTF32 split operands: k rounded up to 4."""
+    return (int(k) + 3) & ~3
+
+
+def tf32x3_split_a(A, a_hi, a_lo, *, stream=None):
+    """Splits row-major A (m x k) into TF32 hi/lo parts, each m x ka."""
+    import torch
+    m, k = A.shape
+    lda = _row_major(A, "A")
+    lda = max(lda, k, 1)
+    if stream is None:
+        stream = torch.cuda.current_stream(A.device).cuda_stream
+    with torch.cuda.device(A.device):
+        _check(_native.load().sgemm_tf32x3_split_a(m, k, ctypes.c_void_p(A.data_ptr()), lda,
+                                                   ctypes.c_void_p(a_hi.data_ptr()),
+                                                   ctypes.c_void_p(a_lo.data_ptr()), ctypes.c_void_p(stream or None)))
+
+
+def tf32x3_split_b(B, bt_hi, bt_lo, *, stream=None):
+    """Splits row-major B (k x n) into TF32 hi/lo parts of B^T, each n x ka."""
+    import torch
+    k, n = B.shape
+    ldb = max(_row_major(B, "B"), n, 1)
+    if stream is None:
+        stream = torch.cuda.current_stream(B.device).cuda_stream
+    with torch.cuda.device(B.device):
+        _check(_native.load().sgemm_tf32x3_split_b(k, n, ctypes.c_void_p(B.data_ptr()), ldb,
+                                                   ctypes.c_void_p(bt_hi.data_ptr()),
+                                                   ctypes.c_void_p(bt_lo.data_ptr()), ctypes.c_void_p(stream or None)))
+
+
+def tf32x3_split_gemm_raw(m, n, k, alpha, a_hi, a_lo, bt_hi, bt_lo, beta, C_ptr, ldc, stream=0) -> int:
+    """C = alpha * A @ B + beta * C from split operands (raw device pointers);
+    returns the status."""
+    return _native.load().sgemm_tf32x3_split_gemm(
+        int(m), int(n), int(k), ctypes.c_float(alpha), ctypes.c_void_p(a_hi or None),
+        ctypes.c_void_p(a_lo or None), ctypes.c_void_p(bt_hi or None), ctypes.c_void_p(bt_lo or None),
+        ctypes.c_float(beta), ctypes.c_void_p(C_ptr or None), int(ldc), ctypes.c_void_p(stream or None))

@@ -37,6 +37,7 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "raster.cuh"
 
 namespace sgemm_gb300 {
 
@@ -52,19 +53,6 @@ struct GemmArgs {
     int tiles_m, tiles_n;
     int group_m;
 };
-
-// Maps a linear CTA index onto (tile row, tile column): tiles are taken
-// column by column inside groups of `group_m` tile rows.
-__device__ __forceinline__ void raster_tile(int tile, int tiles_m, int tiles_n, int group_m, int &tm,
-                                            int &tn) {
-    const int per_group = group_m * tiles_n;
-    const int group = tile / per_group;
-    const int first_m = group * group_m;
-    const int rows = min(tiles_m - first_m, group_m);
-    const int in_group = tile - group * per_group;
-    tm = first_m + in_group % rows;
-    tn = in_group / rows;
-}
 
 namespace ffma {
 

@@ -10,6 +10,7 @@
 
 #include "../../include/sgemm_gb300.h"
 #include "ffma_sgemm.cuh"
+#include "tf32x3_sgemm.cuh"
 
 using namespace sgemm_gb300;
 
@@ -31,7 +32,7 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 // Kernel ids in sgemm_plan::kernel.
 constexpr int kKernelFfmaCpAsync = 0;
 constexpr int kKernelScale = 1;
-constexpr int kKernelFfmaTma = 2;
+constexpr int kKernelTf32x3 = 2;
 
 int fail_cuda(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -59,6 +60,12 @@ int device_state(DeviceState **out) {
         if ((e = set_ffma_attr<true, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_ffma_attr<false, true>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_ffma_attr<false, false>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      tf32x3::SMEM_BYTES)) != cudaSuccess)
+            return fail_cuda(e);
+        if ((e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      tf32x3::SMEM_BYTES)) != cudaSuccess)
+            return fail_cuda(e);
         if (g_encode_tiled == nullptr) {
             cudaDriverEntryPointQueryResult q;
             void *fn = nullptr;
@@ -94,8 +101,6 @@ int check_args(int m, int n, int k, float alpha, const float *A, int lda, const 
     return 0;
 }
 
-bool tma_ok(const void *p, int ld) { return aligned(p, 16) && (ld % 4) == 0; }
-
 int plan(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
          const float *C, int ldc, int path, int num_sms, sgemm_plan *pl) {
     (void)beta;
@@ -104,9 +109,14 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         return SGEMM_STATUS_BAD_PATH;
     if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc)) return bad;
     if (m == 0 || n == 0) return SGEMM_STATUS_OK;
-    if (path == SGEMM_PATH_TF32X3) return SGEMM_STATUS_UNSUPPORTED;
     if (num_sms <= 0) num_sms = 1;
-    pl->path = SGEMM_PATH_FFMA;
+    // AUTO: the tensor-core path for every problem with enough work to fill
+    // the GPU (it is ~5x the FFMA rate at 2048^3 and beyond) and for long k
+    // (its chunked accumulation holds the bound where a plain sequential
+    // FP32 sum over k drifts); the FFMA path for small problems.
+    const bool use_tc = path == SGEMM_PATH_TF32X3 ||
+                        (path == SGEMM_PATH_AUTO && ((long long)m * n * k >= (1LL << 27) || k > 8192));
+    pl->path = use_tc ? SGEMM_PATH_TF32X3 : SGEMM_PATH_FFMA;
     pl->c_vec = aligned(C, 16) && (ldc % 4) == 0;
     if (k == 0 || alpha == 0.f) {
         pl->kernel = kKernelScale;
@@ -115,6 +125,23 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         long long blocks = (total + 255) / 256;
         pl->grid = (int)(blocks < 4096 ? blocks : 4096);
         pl->c_vec = 0;
+        return SGEMM_STATUS_OK;
+    }
+    if (use_tc) {
+        pl->kernel = kKernelTf32x3;
+        pl->bm = tf32x3::BM;
+        pl->bn = tf32x3::BN;
+        pl->bk = tf32x3::BK;
+        pl->threads = tf32x3::THREADS;
+        pl->stages = tf32x3::STAGES;
+        pl->smem_bytes = tf32x3::SMEM_BYTES;
+        pl->b_vec = 1;
+        const int tiles_m = (m + pl->bm - 1) / pl->bm;
+        const int tiles_n = (n + pl->bn - 1) / pl->bn;
+        pl->tiles = tiles_m * tiles_n;
+        pl->grid = pl->tiles;
+        pl->k_tiles = (k + pl->bk - 1) / pl->bk;
+        pl->group_m = tiles_m < 8 ? tiles_m : 8;
         return SGEMM_STATUS_OK;
     }
     pl->kernel = kKernelFfmaCpAsync;
@@ -151,6 +178,73 @@ int make_tensor_map(CUtensorMap *map, const float *base, int rows, int cols, int
     return SGEMM_STATUS_OK;
 }
 
+int ka_of(int k) { return (k + 3) & ~3; }
+
+// A (m x k, lda) -> a_hi, a_lo (m x ka).
+int launch_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream) {
+    if (m == 0 || k == 0) return SGEMM_STATUS_OK;
+    const int gx = (k + 255) / 256;
+    const int gy = m < 65535 ? m : 65535;
+    tf32x3::split_a_kernel<<<dim3(gx, gy), 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k));
+    return SGEMM_STATUS_OK;
+}
+
+// B (k x n, ldb) -> bt_hi, bt_lo (B^T, n x ka).
+int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, cudaStream_t stream) {
+    if (n == 0 || k == 0) return SGEMM_STATUS_OK;
+    const long long gx = (n + 31) / 32, gy = (k + 31) / 32;
+    tf32x3::split_bt_kernel<<<dim3((unsigned)(gx < 2147483647 ? gx : 2147483647), (unsigned)(gy < 65535 ? gy : 65535)),
+                              256, 0, stream>>>(B, ldb, k, n, bt_hi, bt_lo, ka_of(k));
+    return SGEMM_STATUS_OK;
+}
+
+// The tcgen05 GEMM on split operands (row pitch ka).
+int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const float *a_lo, const float *bt_hi,
+                      const float *bt_lo, float beta, float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream) {
+    const int ka = ka_of(k);
+    CUtensorMap t_ahi, t_alo, t_bhi, t_blo;
+    int st = make_tensor_map(&t_ahi, a_hi, m, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st) st = make_tensor_map(&t_alo, a_lo, m, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st) st = make_tensor_map(&t_bhi, bt_hi, n, k, ka, tf32x3::BN, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st) st = make_tensor_map(&t_blo, bt_lo, n, k, ka, tf32x3::BN, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (st) return st;
+    tf32x3::Params a;
+    a.m = m;
+    a.n = n;
+    a.k = k;
+    a.alpha = alpha;
+    a.beta = beta;
+    a.C = C;
+    a.ldc = ldc;
+    a.tiles_m = (m + pl.bm - 1) / pl.bm;
+    a.tiles_n = (n + pl.bn - 1) / pl.bn;
+    a.group_m = pl.group_m;
+    if (pl.c_vec)
+        tf32x3::tf32x3_gemm_kernel<true><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(t_ahi, t_alo, t_bhi, t_blo, a);
+    else
+        tf32x3::tf32x3_gemm_kernel<false><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(t_ahi, t_alo, t_bhi, t_blo,
+                                                                                         a);
+    return SGEMM_STATUS_OK;
+}
+
+// 3xTF32 path of sgemm: split A and B^T into a stream-ordered scratch
+// buffer, run the tcgen05 GEMM, release the scratch.
+int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+                  float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream) {
+    const size_t a_elems = (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
+    float *ws = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), 2 * (a_elems + b_elems) * sizeof(float), stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    float *a_hi = ws, *a_lo = ws + a_elems, *b_hi = a_lo + a_elems, *b_lo = b_hi + b_elems;
+    launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
+    launch_split_b(k, n, B, ldb, b_hi, b_lo, stream);
+    const int st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream);
+    e = cudaFreeAsync(ws, stream);
+    if (st) return st;
+    if (e != cudaSuccess) return fail_cuda(e);
+    return SGEMM_STATUS_OK;
+}
+
 template <bool BV, bool CV>
 void launch_ffma(const GemmArgs &a, const sgemm_plan &pl, cudaStream_t s) {
     ffma::ffma_sgemm_kernel<ffma::Default, BV, CV><<<pl.grid, pl.threads, pl.smem_bytes, s>>>(a);
@@ -174,6 +268,8 @@ int sgemm_ex(int m, int n, int k, float alpha, const float *A, int lda, const fl
     if (st != SGEMM_STATUS_OK) return st;
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
+    } else if (pl.kernel == kKernelTf32x3) {
+        if ((st = launch_tf32x3(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, pl, stream))) return st;
     } else {
         GemmArgs a;
         a.m = m;
@@ -203,6 +299,67 @@ int sgemm_ex(int m, int n, int k, float alpha, const float *A, int lda, const fl
     return SGEMM_STATUS_OK;
 }
 
+int sgemm_tf32x3_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream) {
+    if (m < 0) return 1;
+    if (k < 0) return 2;
+    const bool work = (long long)m * k > 0;
+    if (work && (A == nullptr || !aligned(A, 4))) return 3;
+    if (lda < imax(1, k)) return 4;
+    if (work && (a_hi == nullptr || !aligned(a_hi, 16))) return 5;
+    if (work && (a_lo == nullptr || !aligned(a_lo, 16))) return 6;
+    if (!work) return SGEMM_STATUS_OK;
+    DeviceState *dev = nullptr;
+    if (int st = device_state(&dev)) return st;
+    launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SGEMM_STATUS_OK : fail_cuda(e);
+}
+
+int sgemm_tf32x3_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, cudaStream_t stream) {
+    if (k < 0) return 1;
+    if (n < 0) return 2;
+    const bool work = (long long)k * n > 0;
+    if (work && (B == nullptr || !aligned(B, 4))) return 3;
+    if (ldb < imax(1, n)) return 4;
+    if (work && (bt_hi == nullptr || !aligned(bt_hi, 16))) return 5;
+    if (work && (bt_lo == nullptr || !aligned(bt_lo, 16))) return 6;
+    if (!work) return SGEMM_STATUS_OK;
+    DeviceState *dev = nullptr;
+    if (int st = device_state(&dev)) return st;
+    launch_split_b(k, n, B, ldb, bt_hi, bt_lo, stream);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SGEMM_STATUS_OK : fail_cuda(e);
+}
+
+int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const float *a_lo,
+                            const float *bt_hi, const float *bt_lo, float beta, float *C, int ldc,
+                            cudaStream_t stream) {
+    if (m < 0) return 1;
+    if (n < 0) return 2;
+    if (k < 0) return 3;
+    const bool need_ab = (long long)m * n * k > 0 && alpha != 0.f;
+    const float *ops[4] = {a_hi, a_lo, bt_hi, bt_lo};
+    for (int i = 0; i < 4; ++i)
+        if (need_ab && (ops[i] == nullptr || !aligned(ops[i], 16))) return 5 + i;
+    if ((long long)m * n > 0 && (C == nullptr || !aligned(C, 4))) return 10;
+    if (ldc < imax(1, n)) return 11;
+    if (m == 0 || n == 0) return SGEMM_STATUS_OK;
+    DeviceState *dev = nullptr;
+    if (int st = device_state(&dev)) return st;
+    sgemm_plan pl;
+    // the plan of the tensor-core path for this shape (operand pointers only
+    // matter to the FFMA path's alignment choice)
+    int st = plan(m, n, k, alpha, a_hi, imax(1, k), a_hi, imax(1, n), beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl);
+    if (st) return st;
+    if (pl.kernel == kKernelScale) {
+        scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
+    } else if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, bt_hi, bt_lo, beta, C, ldc, pl, stream))) {
+        return st;
+    }
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SGEMM_STATUS_OK : fail_cuda(e);
+}
+
 int sgemm(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
           float *C, int ldc, cudaStream_t stream) {
     return sgemm_ex(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, stream, SGEMM_PATH_AUTO);
@@ -227,7 +384,7 @@ const char *sgemm_status_string(int status) {
         case 10: return "invalid argument 10: C is NULL or not 4-byte aligned";
         case 11: return "invalid argument 11: ldc < max(1, n)";
         case SGEMM_STATUS_BAD_PATH: return "unknown kernel path";
-        case SGEMM_STATUS_UNSUPPORTED: return "the requested path cannot run this problem";
+        case SGEMM_STATUS_UNSUPPORTED: return "no plan structure given";
         case SGEMM_STATUS_CUDA_ERROR: return "CUDA runtime error (see sgemm_last_cuda_error)";
         default: return "unknown status";
     }

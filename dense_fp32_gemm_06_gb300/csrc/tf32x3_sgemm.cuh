@@ -1,0 +1,322 @@
+// 3xTF32 split-precision SGEMM on the sm_103a tensor cores (tcgen05, TMEM).
+//
+// Not on the pages (they only describe CUDA-core FFMA kernels); this is the
+// tensor-core path for the same C = alpha*A*B + beta*C.  Each FP32 operand
+// x is split into two TF32 numbers, hi = tf32(x) and lo = tf32(x - hi), and
+//     a*b ~= a_hi*b_hi + a_hi*b_lo + a_lo*b_hi,
+// every product exact in the tensor core and accumulated in FP32 in tensor
+// memory.  With round-to-nearest splits |a_lo| <= 2^-11 |a|, the dropped
+// a_lo*b_lo term and the rounding of the lo parts stay below ~3 * 2^-22
+// |a||b| per product, well inside the FP32 acceptance bound
+// |C - r| <= 1e-5 * sum_t |A_it||B_tj| + 1e-6 |beta C0|.
+//
+// Two steps per call:
+//  1. split kernels (HBM-bound): A (any lda, any 4-byte alignment) becomes
+//     A_hi, A_lo, m x ka row-major (ka = k rounded up to 4, 16-byte rows);
+//     B becomes B^T_hi, B^T_lo, n x ka, transposed through a padded 32 x 33
+//     shared tile (coalesced reads and writes).  Both operands of the MMA
+//     are then K-major;
+//  2. the GEMM kernel: one CTA per 128 x 256 tile of C, 10 warps.
+//     warp 0 lane 0: TMA producer -- per 16-deep k slab, four boxes (A_hi,
+//       A_lo 128 x 16; B_hi, B_lo 256 x 16, 64-byte rows with the 64-byte
+//       swizzle) into a 4-stage ring, completing on the slot's "full"
+//       mbarrier; a slot is refilled after the MMA commit for it arrives on
+//       its "empty" mbarrier;
+//     warp 1: allocates 512 TMEM columns (two 128 x 256 FP32 accumulators);
+//       lane 0 issues, per 8-deep k step, the three tcgen05.mma kind::tf32
+//       (128 x 256 x 8) and commits each slab back to its "empty" barrier;
+//     warps 2-9: FP32 accumulation on the CUDA cores.  The tensor core's
+//       own FP32 accumulation is not round-to-nearest: its error is biased
+//       and grows with the number of accumulation steps (measured: 0.31 of
+//       the bound at k = 8192 on N(0,1) data, and it would exceed the bound on
+//       non-negative data).  So the MMA accumulates only KC = 128 k at a
+//       time, alternating between the two TMEM accumulators; for each such
+//       chunk these warps load their part (32 lanes = rows, 128 columns)
+//       with tcgen05.ld and add it into FP32 registers with round-to-nearest
+//       adds, then release the TMEM buffer.  After the last chunk they write
+//       alpha*acc + beta*C for rows < m, columns < n (C not read when
+//       beta == 0).
+//     TMA zero-fills rows past m, columns past n and k past the end, so the
+//     MMA never sees an index test.  Every mbarrier wait is bounded (2 s):
+//     a wait that runs out records a code in the library status word,
+//     stops issuing, lets issued copies and MMAs complete (bounded), skips
+//     the stores and frees TMEM before the CTA exits.
+#pragma once
+#include <cuda.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "raster.cuh"
+#include "tcgen05.cuh"
+
+namespace sgemm_gb300 {
+namespace tf32x3 {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 16;   // 64-byte rows
+constexpr int STAGES = 4;
+constexpr int UMMA_K = 8;
+constexpr int KC = 128;                                   // k per tensor-core accumulation chunk
+constexpr int CHUNK_STAGES = KC / BK;
+constexpr int A_TILE = BM * BK * 4;                       // 8 KB
+constexpr int B_TILE = BN * BK * 4;                       // 16 KB
+constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;      // 48 KB: A_hi, A_lo, B_hi, B_lo
+constexpr int ACC_WARPS = 8;
+constexpr int ACC_THREADS = 32 * ACC_WARPS;
+constexpr int THREADS = 64 + ACC_THREADS;                 // producer warp, MMA warp, 8 accumulator warps
+constexpr int TMEM_COLS = 2 * BN;                         // two accumulators
+constexpr int COLS_PER_THREAD = BN / 2;                   // two warps per 32-lane group
+constexpr int BAR_REGION = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_REGION;
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+static_assert(BK * 4 == 64, "one 64-byte swizzle row per operand row");
+static_assert(KC % BK == 0, "chunks are whole slabs");
+static_assert(TMEM_COLS <= 512, "tensor memory columns");
+
+constexpr int kStatusProducer = 0x201;
+constexpr int kStatusMma = 0x202;
+constexpr int kStatusAccumulate = 0x203;
+constexpr int kStatusDrain = 0x204;
+constexpr int kStatusMmaBuffer = 0x205;
+
+struct Params {
+    int m, n, k;
+    float alpha, beta;
+    float *C;
+    long long ldc;
+    int tiles_m, tiles_n, group_m;
+};
+
+// ---------------------------------------------------------------- split kernels
+
+// A (m x k, row pitch lda) -> hi, lo (m x ka, row pitch ka).
+__global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ A, long long lda, int m, int k,
+                                                      float *__restrict__ hi, float *__restrict__ lo, int ka) {
+    for (int row = blockIdx.y; row < m; row += gridDim.y) {
+        const float *src = A + (long long)row * lda;
+        float *h = hi + (long long)row * ka;
+        float *l = lo + (long long)row * ka;
+        for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < k; t += gridDim.x * blockDim.x) {
+            const float x = src[t];
+            const float xh = tc::round_tf32(x);
+            h[t] = xh;
+            l[t] = tc::round_tf32(x - xh);
+        }
+    }
+}
+
+// B (k x n, row pitch ldb) -> hi, lo of B^T (n x ka, row pitch ka).
+__global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__ B, long long ldb, int k, int n,
+                                                       float *__restrict__ hi, float *__restrict__ lo, int ka) {
+    __shared__ float tile[32][33];
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
+    for (int t0 = blockIdx.y * 32; t0 < k; t0 += gridDim.y * 32) {
+        for (int j0 = blockIdx.x * 32; j0 < n; j0 += gridDim.x * 32) {
+#pragma unroll
+            for (int r = ty; r < 32; r += 8) {
+                const int t = t0 + r, j = j0 + tx;
+                tile[r][tx] = (t < k && j < n) ? B[(long long)t * ldb + j] : 0.f;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int r = ty; r < 32; r += 8) {
+                const int j = j0 + r, t = t0 + tx;
+                if (j < n && t < k) {
+                    const float x = tile[tx][r];
+                    const float xh = tc::round_tf32(x);
+                    hi[(long long)j * ka + t] = xh;
+                    lo[(long long)j * ka + t] = tc::round_tf32(x - xh);
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// ---------------------------------------------------------------- GEMM kernel
+
+template <bool C_VEC>
+__global__ void __launch_bounds__(THREADS, 1)
+    tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
+                       const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
+                       const Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *const smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t stage0 = smem_u32(smem);
+    uint8_t *const bars = smem + STAGES * STAGE_BYTES;
+    const uint32_t bar_full = smem_u32(bars);            // [STAGES] TMA landed
+    const uint32_t bar_empty = bar_full + 8 * STAGES;    // [STAGES] MMAs done reading the slot
+    const uint32_t bar_tfull = bar_empty + 8 * STAGES;   // [2] chunk accumulated in TMEM buffer b
+    const uint32_t bar_tempty = bar_tfull + 16;          // [2] TMEM buffer b drained to registers
+    const uint32_t bar_done = bar_tempty + 16;           // every MMA issued has completed
+    uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * (2 * STAGES + 5));
+    volatile int *const abort_flag = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int tm, tn;
+    raster_tile(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    const int m0 = tm * BM, n0 = tn * BN;
+    const int KT = (p.k + BK - 1) / BK;
+    const int NC = (KT + CHUNK_STAGES - 1) / CHUNK_STAGES;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + 8 * b, 1);
+            mbar_init(bar_tempty + 8 * b, ACC_THREADS);
+        }
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmAhi);
+        tma_prefetch_desc(&tmAlo);
+        tma_prefetch_desc(&tmBhi);
+        tma_prefetch_desc(&tmBlo);
+    }
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int kt = 0; kt < KT; ++kt) {
+                const int s = kt % STAGES;
+                if (kt >= STAGES && !mbar_wait(bar_empty + 8 * s, ((kt / STAGES) - 1) & 1, kStatusProducer)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                const uint32_t st = stage0 + s * STAGE_BYTES;
+                const uint32_t fb = bar_full + 8 * s;
+                mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                tma_load_2d(st, &tmAhi, kt * BK, m0, fb);
+                tma_load_2d(st + A_TILE, &tmAlo, kt * BK, m0, fb);
+                tma_load_2d(st + 2 * A_TILE, &tmBhi, kt * BK, n0, fb);
+                tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kt * BK, n0, fb);
+                ++issued;
+            }
+            if (*abort_flag) {
+                // every copy issued must land before the CTA leaves
+                for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+                    mbar_wait(bar_full + 8 * (j % STAGES), (j / STAGES) & 1, kStatusDrain);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_tf32_f32<BM, BN>();
+            for (int kt = 0; kt < KT; ++kt) {
+                const int c = kt / CHUNK_STAGES, b = c & 1;
+                const bool chunk_first = kt % CHUNK_STAGES == 0;
+                const bool chunk_last = kt % CHUNK_STAGES == CHUNK_STAGES - 1 || kt == KT - 1;
+                // TMEM buffer b is reused once the accumulator warps drained chunk c - 2
+                if (chunk_first && c >= 2 && !mbar_wait(bar_tempty + 8 * b, ((c >> 1) - 1) & 1, kStatusMmaBuffer)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const int s = kt % STAGES;
+                if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusMma)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::fence_after_sync();
+                const uint32_t st = stage0 + s * STAGE_BYTES;
+                const uint32_t d = tmem + (uint32_t)(b * BN);
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                    const uint32_t off = kk * UMMA_K * 4;   // 32 bytes along the 64-byte row
+                    const uint64_t a_hi = tc::desc_kmajor_sw64(st + off);
+                    const uint64_t a_lo = tc::desc_kmajor_sw64(st + A_TILE + off);
+                    const uint64_t b_hi = tc::desc_kmajor_sw64(st + 2 * A_TILE + off);
+                    const uint64_t b_lo = tc::desc_kmajor_sw64(st + 2 * A_TILE + B_TILE + off);
+                    tc::mma_tf32(d, a_hi, b_hi, idesc, (chunk_first && kk == 0) ? 0u : 1u);
+                    tc::mma_tf32(d, a_hi, b_lo, idesc, 1u);
+                    tc::mma_tf32(d, a_lo, b_hi, idesc, 1u);
+                }
+                tc::commit(bar_empty + 8 * s);
+                if (chunk_last) tc::commit(bar_tfull + 8 * b);
+            }
+            // fires once every MMA issued has completed (TMEM may then be freed)
+            tc::commit(bar_done);
+            mbar_wait(bar_done, 0, kStatusDrain);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ accumulator warps (2..9)
+        const int lane_grp = warp & 3;                       // TMEM lanes 32*lane_grp .. +31
+        const int half = (warp - 2) >> 2;                    // columns half*128 .. +127
+        const uint32_t taddr = tmem + ((uint32_t)(lane_grp * 32) << 16) + (uint32_t)(half * COLS_PER_THREAD);
+        float acc[COLS_PER_THREAD];
+#pragma unroll
+        for (int j = 0; j < COLS_PER_THREAD; ++j) acc[j] = 0.f;
+        bool ok = true;
+        for (int c = 0; c < NC; ++c) {
+            const int b = c & 1;
+            if (!mbar_wait(bar_tfull + 8 * b, (c >> 1) & 1, kStatusAccumulate)) {
+                ok = false;
+                break;
+            }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int q = 0; q < COLS_PER_THREAD / 16; ++q) {
+                uint32_t v[16];
+                tc::ld_32x32b_x16(taddr + (uint32_t)(b * BN + q * 16), v);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[q * 16 + i] += __uint_as_float(v[i]);
+            }
+            tc::fence_before_sync();
+            mbar_arrive(bar_tempty + 8 * b);
+        }
+        const int row = m0 + lane_grp * 32 + lane;
+        if (ok && *abort_flag == 0 && row < p.m) {
+            const float alpha = p.alpha, beta = p.beta;
+            float *crow = p.C + (long long)row * p.ldc;
+            const int col0 = n0 + half * COLS_PER_THREAD;
+#pragma unroll
+            for (int q = 0; q < COLS_PER_THREAD / 4; ++q) {
+                const int col = col0 + 4 * q;
+                const float *a = &acc[4 * q];
+                if (C_VEC && col + 3 < p.n) {
+                    float4 o;
+                    if (beta != 0.f) {
+                        const float4 c4 = *reinterpret_cast<const float4 *>(crow + col);
+                        o = make_float4(fmaf(alpha, a[0], beta * c4.x), fmaf(alpha, a[1], beta * c4.y),
+                                        fmaf(alpha, a[2], beta * c4.z), fmaf(alpha, a[3], beta * c4.w));
+                    } else {
+                        o = make_float4(alpha * a[0], alpha * a[1], alpha * a[2], alpha * a[3]);
+                    }
+                    *reinterpret_cast<float4 *>(crow + col) = o;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (col + e < p.n)
+                            crow[col + e] = beta != 0.f ? fmaf(alpha, a[e], beta * crow[col + e]) : alpha * a[e];
+                    }
+                }
+            }
+        }
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace tf32x3
+}  // namespace sgemm_gb300

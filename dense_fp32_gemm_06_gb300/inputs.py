@@ -22,6 +22,8 @@ each starting at an even draw index:
   ``(2p, 2p+1)`` of the matrix, ``u1 = ((d0 >> 11) + 1) * 2^-53`` in (0, 1],
   ``u2 = (d1 >> 11) * 2^-53``; element ``2p`` gets ``r cos(2 pi u2)`` and
   ``2p+1`` gets ``r sin(2 pi u2)``, ``r = sqrt(-2 ln u1)``, rounded to FP32.
+* ``uniform01``: ``u`` itself, in [0, 1) (non-negative operands: every
+  partial sum grows, the hardest case for a biased accumulation);
 * ``int``: ``floor(9u) - 4`` with ``u`` as for ``uniform`` -- integers in
   {-4..4}, the "integer twin" whose every product and partial sum is exact
   in FP32 while ``16 * k < 2^24``.
@@ -65,6 +67,8 @@ def _fill(dist: str, seed: int, offset: int, count: int) -> np.ndarray:
         hi = min(count, lo + _CHUNK)
         if dist == "uniform":
             out[lo:hi] = (_u24(splitmix64(seed, offset + lo, hi - lo)) * 2.0 - 1.0).astype(np.float32)
+        elif dist == "uniform01":
+            out[lo:hi] = _u24(splitmix64(seed, offset + lo, hi - lo)).astype(np.float32)
         elif dist == "int":
             out[lo:hi] = (np.floor(_u24(splitmix64(seed, offset + lo, hi - lo)) * 9.0) - 4.0).astype(np.float32)
         elif dist == "normal":

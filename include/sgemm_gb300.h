@@ -17,15 +17,18 @@
  * (aerisun.top, section "Shared Tiling 与 block 内复用"):
  *     A(i,t) = A[i*lda + t],  B(t,j) = B[t*ldb + j],  C(i,j) = C[i*ldc + j].
  * Offsets are computed in 64 bits.  Any lda >= max(1,k), ldb >= max(1,n),
- * ldc >= max(1,n) and any 4-byte-aligned pointers are accepted; 16-byte
- * aligned bases with leading dimensions that are multiples of 4 take the
- * vectorised / TMA loads, everything else the 4-byte zero-filling loads.
+ * ldc >= max(1,n) and any 4-byte-aligned pointers are accepted by both
+ * paths (the FFMA path copies A 4 bytes at a time and B / C 16 bytes at a
+ * time where their rows are 16-byte aligned; the tensor-core path re-lays
+ * A and B out itself, see the split calls below).
  *
  * Ownership.  A, B and C are device pointers owned by the caller (any memory
  * the current device can address).  The library keeps no pointer after the
- * call returns.  Per device it lazily caches kernel attributes and (for the
- * tensor-core path) a device-resident status word; it never allocates per
- * call.  C must not overlap A or B.
+ * call returns.  Per device it lazily caches kernel attributes.  The FFMA
+ * path allocates nothing; the tensor-core path takes its split operands
+ * (8 * (m + n) * ka bytes, ka = k rounded up to 4) from the device's default
+ * stream-ordered memory pool for the duration of the call
+ * (cudaMallocAsync / cudaFreeAsync on `stream`).  C must not overlap A or B.
  *
  * Execution.  Every entry point that takes a stream enqueues its kernels on
  * `stream` (0 = the legacy default stream) of the current device and returns
@@ -42,9 +45,7 @@
  *                            11 ldc < max(1,n); also 5/7/10 for a pointer not
  *                            4-byte aligned;
  *     SGEMM_STATUS_BAD_PATH  sgemm_ex() asked for an unknown path;
- *     SGEMM_STATUS_UNSUPPORTED  the requested path cannot run this problem
- *                            (e.g. the tensor-core path with A or B rows not
- *                            16-byte aligned);
+ *     SGEMM_STATUS_UNSUPPORTED  sgemm_plan_for() was given a NULL plan;
  *     SGEMM_STATUS_CUDA_ERROR  a CUDA runtime call or launch failed; the CUDA
  *                            error code is kept per thread and returned by
  *                            sgemm_last_cuda_error().
@@ -66,7 +67,8 @@ extern "C" {
 #define SGEMM_STATUS_CUDA_ERROR 100
 
 /* Kernel families sgemm_ex() can be asked for. */
-#define SGEMM_PATH_AUTO 0   /* the library's choice (what sgemm() runs)        */
+#define SGEMM_PATH_AUTO 0   /* the library's choice (what sgemm() runs): TF32X3 when
+                               m*n*k >= 2^27 or k > 8192, else FFMA              */
 #define SGEMM_PATH_FFMA 1   /* CUDA-core FP32 FFMA, exact FP32 products        */
 #define SGEMM_PATH_TF32X3 2 /* tcgen05 tensor cores, 3xTF32 split precision    */
 
@@ -86,6 +88,41 @@ int sgemm_ex(int m, int n, int k, float alpha,
              const float *A, int lda, const float *B, int ldb,
              float beta, float *C, int ldc, cudaStream_t stream, int path);
 
+/*
+ * 3xTF32 split operands.  The pages describe only CUDA-core FFMA kernels;
+ * the tensor-core path computes the same C = alpha*A*B + beta*C by writing
+ * each FP32 operand x as two TF32 numbers, hi = tf32(x) and
+ * lo = tf32(x - hi) (both rounded to nearest), and summing
+ * a_hi*b_hi + a_hi*b_lo + a_lo*b_hi on the tensor cores in 128-deep chunks
+ * whose sums are added in FP32 on the CUDA cores.  sgemm_ex(...,
+ * SGEMM_PATH_TF32X3) does all of it with a stream-ordered scratch buffer
+ * (cudaMallocAsync / cudaFreeAsync on `stream`); a caller that multiplies
+ * the same operand many times can split it once with these calls and reuse
+ * it.
+ *
+ * Split layout: ka = k rounded up to a multiple of 4.  a_hi, a_lo are
+ * m x ka row-major (row pitch ka floats); bt_hi, bt_lo hold B TRANSPOSED,
+ * n x ka row-major.  Columns k .. ka-1 are never read or written.  Every
+ * split array must be 16-byte aligned and hold rows*ka floats; the caller
+ * owns them.
+ *
+ * Status: 0, or the 1-based position of the first invalid argument
+ * (sizes < 0; A/B NULL or not 4-byte aligned; lda < max(1,k),
+ * ldb < max(1,n); a split array NULL or not 16-byte aligned while there is
+ * work), or SGEMM_STATUS_CUDA_ERROR.  Asynchronous on `stream`.
+ */
+int sgemm_tf32x3_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream);
+int sgemm_tf32x3_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, cudaStream_t stream);
+
+/*
+ * C = alpha * A * B + beta * C from split operands (argument positions as
+ * in sgemm: 5..8 are a_hi, a_lo, bt_hi, bt_lo; 10 C; 11 ldc).  Runs only
+ * the tensor-core GEMM kernel (k == 0 or alpha == 0: C = beta * C).
+ */
+int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const float *a_lo,
+                            const float *bt_hi, const float *bt_lo, float beta, float *C, int ldc,
+                            cudaStream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *sgemm_status_string(int status);
 
@@ -99,7 +136,8 @@ int sgemm_last_cuda_error(void);
  */
 typedef struct sgemm_plan {
     int path;          /* SGEMM_PATH_FFMA or SGEMM_PATH_TF32X3; 0 = no kernel (m or n is 0) */
-    int kernel;        /* 0 main GEMM kernel, 1 C = beta*C scale kernel                        */
+    int kernel;        /* 0 FFMA GEMM kernel, 1 C = beta*C scale kernel, 2 3xTF32 tensor-core
+                          GEMM (launched after the two split kernels)                          */
     int bm, bn, bk;    /* CTA tile (rows of C, columns of C, k per pipeline stage)             */
     int rm, rn;        /* per-thread register tile of C (FFMA path; 0 otherwise)               */
     int threads;       /* threads per CTA                                                      */

@@ -107,3 +107,53 @@ def test_plan_alignment_flags():
     assert (p["b_vec"], p["c_vec"]) == (0, 1)
     st, p = binding.plan(64, 66, 64, ldb=66, ldc=66)
     assert (p["b_vec"], p["c_vec"]) == (0, 0)
+
+
+def _split_a(**over):
+    a = dict(m=4, k=6, A=256, lda=6, hi=512, lo=1024)
+    a.update(over)
+    lib = _native.load()
+    return lib.sgemm_tf32x3_split_a(a["m"], a["k"], a["A"] or None, a["lda"], a["hi"] or None, a["lo"] or None, None)
+
+
+def _split_b(**over):
+    a = dict(k=6, n=5, B=256, ldb=5, hi=512, lo=1024)
+    a.update(over)
+    lib = _native.load()
+    return lib.sgemm_tf32x3_split_b(a["k"], a["n"], a["B"] or None, a["ldb"], a["hi"] or None, a["lo"] or None, None)
+
+
+def _split_gemm(**over):
+    a = dict(m=4, n=5, k=6, alpha=1.0, ah=256, al=512, bh=768, bl=1024, beta=0.0, C=2048, ldc=5)
+    a.update(over)
+    return binding.tf32x3_split_gemm_raw(a["m"], a["n"], a["k"], a["alpha"], a["ah"], a["al"], a["bh"], a["bl"],
+                                         a["beta"], a["C"], a["ldc"], 0)
+
+
+@pytest.mark.parametrize("fn,over,status", [
+    (_split_a, dict(m=-1), 1), (_split_a, dict(k=-1), 2), (_split_a, dict(A=0), 3), (_split_a, dict(A=258), 3),
+    (_split_a, dict(lda=5), 4), (_split_a, dict(hi=0), 5), (_split_a, dict(hi=520), 5), (_split_a, dict(lo=1028), 6),
+    (_split_a, dict(m=0, A=0, hi=0, lo=0), 0), (_split_a, dict(k=0, lda=1, A=0, hi=0, lo=0), 0),
+    (_split_b, dict(k=-1), 1), (_split_b, dict(n=-1), 2), (_split_b, dict(B=0), 3), (_split_b, dict(ldb=4), 4),
+    (_split_b, dict(hi=8), 5), (_split_b, dict(lo=0), 6), (_split_b, dict(n=0, ldb=1, B=0, hi=0, lo=0), 0),
+    (_split_gemm, dict(m=-1), 1), (_split_gemm, dict(n=-1), 2), (_split_gemm, dict(k=-1), 3),
+    (_split_gemm, dict(ah=0), 5), (_split_gemm, dict(al=520), 6), (_split_gemm, dict(bh=8), 7),
+    (_split_gemm, dict(bl=0), 8), (_split_gemm, dict(C=0), 10), (_split_gemm, dict(C=2050), 10),
+    (_split_gemm, dict(ldc=4), 11), (_split_gemm, dict(m=0, ah=0, al=0, bh=0, bl=0, C=0), 0),
+])
+def test_split_api_arguments(fn, over, status):
+    # every case is rejected, or is a no-op, before any CUDA call
+    assert fn(**over) == status
+
+
+def test_auto_policy():
+    """AUTO takes the tensor-core path from 2^27 multiply-adds or k > 8192,
+    the FFMA path below."""
+    assert binding.plan(256, 256, 256)[1]["path"] == binding.PATH_FFMA
+    assert binding.plan(512, 512, 512)[1]["path"] == binding.PATH_TF32X3
+    assert binding.plan(8192, 8192, 8192)[1]["path"] == binding.PATH_TF32X3
+    assert binding.plan(16, 16, 8193)[1]["path"] == binding.PATH_TF32X3
+    assert binding.plan(1000, 1500, 777, lda=777)[1]["path"] == binding.PATH_TF32X3
+    st, p = binding.plan(2048, 2048, 2048, path=binding.PATH_TF32X3)
+    assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"]) == (128, 256, 16, 320)
+    assert p["grid"] == p["tiles"] == 16 * 8 and p["k_tiles"] == 128

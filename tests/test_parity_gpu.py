@@ -131,6 +131,22 @@ def test_unaligned_lda_workload_twin(path):
     run_and_check(p, path, exact=True)
 
 
+@pytest.mark.parametrize("path,m,n,k", [
+    (binding.PATH_FFMA, 384, 200, 8192), (binding.PATH_FFMA, 130, 520, 8192),
+    (binding.PATH_TF32X3, 384, 200, 8192), (binding.PATH_TF32X3, 256, 256, 32768),
+    (binding.PATH_TF32X3, 130, 520, 65536), (binding.PATH_AUTO, 256, 256, 32768),
+], ids=lambda v: PATH_IDS.get(v, str(v)) if isinstance(v, int) and v < 3 else str(v))
+def test_nonnegative_long_k(path, m, n, k):
+    """Non-negative operands: every partial sum grows with t, so an
+    accumulation whose rounding is biased (not round-to-nearest) drifts
+    linearly in k and shows here first.  The FFMA path sums each output
+    sequentially in FP32 and is held to the bound up to k = 8192 (the
+    largest workload); the tensor-core path, which accumulates 128-deep
+    chunks in TMEM and adds the chunks in FP32 registers, to k = 65536."""
+    p = inputs.make_problem(m, n, k, alpha=1.0, beta=0.0, seed=k + m, a="uniform01", b="uniform01")
+    run_and_check(p, path)
+
+
 # ---------------------------------------------------------------- alpha, beta, k = 0
 
 @pytest.mark.parametrize("path", PATHS, ids=lambda p: PATH_IDS[p])
@@ -190,3 +206,49 @@ def test_stream_ordering():
     torch.cuda.synchronize()
     want = (A.double() @ B.double()).float()
     assert torch.equal(out, want)
+
+
+# ---------------------------------------------------------------- 3xTF32 split operands
+
+def test_tf32x3_split_operands():
+    """The split calls produce hi = TF32(x) (low 13 mantissa bits zero),
+    lo = TF32(x - hi), with |x - hi - lo| <= 2^-22 |x| and |lo| <= 2^-11 |x|;
+    B comes out transposed; the split GEMM equals the one-call path bit for
+    bit (same kernels, same operands)."""
+    p = inputs.make_problem(300, 260, 150, alpha=1.25, beta=0.5, seed=31, a="normal", b="uniform", c="uniform")
+    ka = binding.ka_of(p.k)
+    A = torch.from_numpy(p.A).cuda()
+    B = torch.from_numpy(p.B).cuda()
+    a_hi = torch.zeros(p.m * ka, device="cuda")
+    a_lo = torch.zeros_like(a_hi)
+    b_hi = torch.zeros(p.n * ka, device="cuda")
+    b_lo = torch.zeros_like(b_hi)
+    binding.tf32x3_split_a(A, a_hi, a_lo)
+    binding.tf32x3_split_b(B, b_hi, b_lo)
+    torch.cuda.synchronize()
+    ah = a_hi.view(p.m, ka)[:, :p.k].cpu().numpy()
+    al = a_lo.view(p.m, ka)[:, :p.k].cpu().numpy()
+    bh = b_hi.view(p.n, ka)[:, :p.k].cpu().numpy()
+    bl = b_lo.view(p.n, ka)[:, :p.k].cpu().numpy()
+    for x, hi, lo in ((p.A.astype(np.float64), ah, al), (p.B.T.astype(np.float64), bh, bl)):
+        assert np.all(hi.view(np.uint32) & 0x1FFF == 0) and np.all(lo.view(np.uint32) & 0x1FFF == 0)
+        assert np.all(np.abs(x - hi) <= 2.0 ** -11 * np.abs(x))
+        assert np.all(np.abs(x - hi.astype(np.float64) - lo.astype(np.float64)) <= 2.0 ** -22 * np.abs(x))
+    C1 = torch.from_numpy(p.C0).cuda()
+    C2 = C1.clone()
+    st = binding.tf32x3_split_gemm_raw(p.m, p.n, p.k, p.alpha, a_hi.data_ptr(), a_lo.data_ptr(), b_hi.data_ptr(),
+                                       b_lo.data_ptr(), p.beta, C1.data_ptr(), p.ldc,
+                                       torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    binding.sgemm_ex(A, B, C2, p.alpha, p.beta, path=binding.PATH_TF32X3)
+    torch.cuda.synchronize()
+    assert torch.equal(C1, C2)
+
+
+def test_device_status_clear_after_runs():
+    """No bounded wait gave up during the tests above."""
+    import ctypes
+    from dense_fp32_gemm_06_gb300 import _native
+    flag = ctypes.c_int(-1)
+    assert _native.load().sgemm_device_status(ctypes.byref(flag), 0) == 0
+    assert flag.value == 0
