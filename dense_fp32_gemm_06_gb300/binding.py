@@ -127,3 +127,17 @@ def tf32x3_split_gemm_raw(m, n, k, alpha, a_hi, a_lo, bt_hi, bt_lo, beta, C_ptr,
         int(m), int(n), int(k), ctypes.c_float(alpha), ctypes.c_void_p(a_hi or None),
         ctypes.c_void_p(a_lo or None), ctypes.c_void_p(bt_hi or None), ctypes.c_void_p(bt_lo or None),
         ctypes.c_float(beta), ctypes.c_void_p(C_ptr or None), int(ldc), ctypes.c_void_p(stream or None))
+
+
+NOALLOC_SCRATCH_FLOATS = 16 * 1024 * 1024
+
+
+def tf32x3_noalloc_raw(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, stream=0) -> int:
+    """The tensor-core sgemm that allocates no memory (its scratch is a fixed
+    64 MiB device array shared by every call); returns the status.  For
+    callers that must not allocate device memory while they run; calls that
+    overlap on the GPU race on the shared scratch."""
+    return _native.load().sgemm_tf32x3_noalloc(
+        int(m), int(n), int(k), ctypes.c_float(alpha), ctypes.c_void_p(A_ptr or None), int(lda),
+        ctypes.c_void_p(B_ptr or None), int(ldb), ctypes.c_float(beta), ctypes.c_void_p(C_ptr or None), int(ldc),
+        ctypes.c_void_p(stream or None))

@@ -245,6 +245,35 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
     return SGEMM_STATUS_OK;
 }
 
+// ---------------------------------------------------------------- no-allocation variant
+//
+// Scratch of sgemm_tf32x3_noalloc(): a fixed array in device global memory,
+// created when the module loads on a device and kept until the process
+// exits.  Host code must not use the array's name as a device address (on
+// the host it only names the symbol); the device address is looked up once
+// per device with cudaGetSymbolAddress while that device is current.
+static __device__ __align__(256) float g_noalloc_scratch[SGEMM_NOALLOC_SCRATCH_FLOATS];
+
+std::mutex g_noalloc_mu;
+float *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of this device's g_noalloc_scratch (looked up on first use).
+int noalloc_scratch(float **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return fail_cuda(cudaErrorInvalidDevice);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) return fail_cuda(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
+        g_noalloc_ptr[dev] = static_cast<float *>(p);
+    }
+    *out = g_noalloc_ptr[dev];
+    return SGEMM_STATUS_OK;
+}
+
 template <bool BV, bool CV>
 void launch_ffma(const GemmArgs &a, const sgemm_plan &pl, cudaStream_t s) {
     ffma::ffma_sgemm_kernel<ffma::Default, BV, CV><<<pl.grid, pl.threads, pl.smem_bytes, s>>>(a);
@@ -360,6 +389,35 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
     return e == cudaSuccess ? SGEMM_STATUS_OK : fail_cuda(e);
 }
 
+int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb,
+                         float beta, float *C, int ldc, cudaStream_t stream) {
+    if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc)) return bad;
+    if (m == 0 || n == 0) return SGEMM_STATUS_OK;
+    const long long ka = (long long)ka_of(k);
+    if (2 * ((long long)m + n) * ka > (long long)SGEMM_NOALLOC_SCRATCH_FLOATS) return SGEMM_STATUS_TOO_LARGE;
+    DeviceState *dev = nullptr;
+    int st = device_state(&dev);
+    if (st != SGEMM_STATUS_OK) return st;
+    sgemm_plan pl;
+    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl);
+    if (st != SGEMM_STATUS_OK) return st;
+    if (pl.kernel == kKernelScale) {
+        scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
+    } else {
+        float *ws = nullptr;
+        if ((st = noalloc_scratch(&ws))) return st;
+        // the split kernels write every element the GEMM reads, so nothing
+        // left in the array by an earlier call is ever used
+        const size_t a_elems = (size_t)m * ka, b_elems = (size_t)n * ka;
+        float *a_hi = ws, *a_lo = ws + a_elems, *b_hi = a_lo + a_elems, *b_lo = b_hi + b_elems;
+        launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
+        launch_split_b(k, n, B, ldb, b_hi, b_lo, stream);
+        if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream))) return st;
+    }
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SGEMM_STATUS_OK : fail_cuda(e);
+}
+
 int sgemm(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
           float *C, int ldc, cudaStream_t stream) {
     return sgemm_ex(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, stream, SGEMM_PATH_AUTO);
@@ -383,6 +441,8 @@ const char *sgemm_status_string(int status) {
         case 8: return "invalid argument 8: ldb < max(1, n)";
         case 10: return "invalid argument 10: C is NULL or not 4-byte aligned";
         case 11: return "invalid argument 11: ldc < max(1, n)";
+        case SGEMM_STATUS_TOO_LARGE:
+            return "problem too large for the fixed no-allocation scratch (2*(m+n)*ka > SGEMM_NOALLOC_SCRATCH_FLOATS)";
         case SGEMM_STATUS_BAD_PATH: return "unknown kernel path";
         case SGEMM_STATUS_UNSUPPORTED: return "no plan structure given";
         case SGEMM_STATUS_CUDA_ERROR: return "CUDA runtime error (see sgemm_last_cuda_error)";

@@ -44,6 +44,8 @@
  *                            8 ldb < max(1,n), 10 C == NULL while m*n > 0,
  *                            11 ldc < max(1,n); also 5/7/10 for a pointer not
  *                            4-byte aligned;
+ *     SGEMM_STATUS_TOO_LARGE  sgemm_tf32x3_noalloc(): the problem does not fit
+ *                            its fixed scratch array;
  *     SGEMM_STATUS_BAD_PATH  sgemm_ex() asked for an unknown path;
  *     SGEMM_STATUS_UNSUPPORTED  sgemm_plan_for() was given a NULL plan;
  *     SGEMM_STATUS_CUDA_ERROR  a CUDA runtime call or launch failed; the CUDA
@@ -62,6 +64,7 @@ extern "C" {
 #endif
 
 #define SGEMM_STATUS_OK 0
+#define SGEMM_STATUS_TOO_LARGE 97
 #define SGEMM_STATUS_BAD_PATH 98
 #define SGEMM_STATUS_UNSUPPORTED 99
 #define SGEMM_STATUS_CUDA_ERROR 100
@@ -122,6 +125,40 @@ int sgemm_tf32x3_split_b(int k, int n, const float *B, int ldb, float *bt_hi, fl
 int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const float *a_lo,
                             const float *bt_hi, const float *bt_lo, float beta, float *C, int ldc,
                             cudaStream_t stream);
+
+/*
+ * sgemm_tf32x3_noalloc -- the tensor-core (3xTF32) sgemm with no memory
+ * allocation of any kind.  The pages have no counterpart to this entry
+ * point; it exists for callers that must not allocate device memory while
+ * they run: code executing inside an allocator callback or an out-of-memory
+ * handler, processes that reserve all of their device memory up front, and
+ * latency-critical loops that cannot afford cudaMalloc / cudaMallocAsync
+ * (which can synchronise, fail under memory pressure, or take a lock the
+ * caller already holds).
+ *
+ * Arguments, layout, results and status codes are those of sgemm() with the
+ * tensor-core path, plus SGEMM_STATUS_TOO_LARGE.  The split operands live in
+ * one fixed array of SGEMM_NOALLOC_SCRATCH_FLOATS floats (64 MiB) in device
+ * memory that every GPU which loads this library holds until the process
+ * exits; a problem needs 2 * (m + n) * ka of them (ka = k rounded up to 4),
+ * and a larger one is rejected with SGEMM_STATUS_TOO_LARGE before anything
+ * is enqueued (for m = n = k = 2048 it needs 8 * 2^20 * 2 = exactly the
+ * capacity).  No cudaMalloc, cudaMallocAsync, cudaFree or allocating library
+ * routine is called.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (cudaGetSymbolAddress, with the device current) and keeps it; make
+ * that first call before any stream capture is begun.  All calls share the
+ * one array and it keeps whatever the last call left there (nothing in it
+ * needs to start at zero: every element a call reads was written earlier in
+ * the same call).  Two calls whose work overlaps on the GPU -- on different
+ * streams, or on different host threads -- race on the array and corrupt
+ * each other's results; serialise them (one stream, or events).
+ */
+#define SGEMM_NOALLOC_SCRATCH_FLOATS (16 * 1024 * 1024)
+int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha,
+                         const float *A, int lda, const float *B, int ldb,
+                         float beta, float *C, int ldc, cudaStream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
 const char *sgemm_status_string(int status);
