@@ -1,13 +1,14 @@
-"""SGEMM benchmark on GB300: TFLOPS and fraction of the FP32 roofline.
+"""SGEMM benchmark on GB300: TFLOPS and fraction of the roofline.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--path auto|ffma|tf32x3]
 
 A step is one C = alpha*A*B + beta*C call through the C ABI on the
 8192 x 8192 x 8192 workload (row-major FP32, alpha = 1, beta = 0, A and B
-i.i.d. N(0,1) from seed 3), inputs resident in HBM.  Rank 0 prints one JSON
-line.  Under torchrun every rank runs its own independent replica of the
-step (the GEMM has no exchange step), so ``value`` is the FLOPs of all ranks
-over the slowest rank's time ("weak" scaling).
+i.i.d. N(0,1) from seed 3) by default, inputs resident in HBM.  Rank 0
+prints one JSON line.  Under torchrun every rank runs its own independent
+replica of the step (a GEMM has no exchange step), so ``value`` is the
+FLOPs of all ranks over the slowest rank's time ("weak" scaling).
 
 ``--impl reference`` times the FP64 CPU oracle on the same workload instead
 (a bounded slab of output rows per step, on the host cores), the only arm
@@ -25,40 +26,74 @@ import sys
 import tempfile
 import time
 
-import numpy as np
-
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "SGEMM TFLOPS on 1 GB300 at 2048³/8192³; % of FP32 FFMA peak (roofline)"
-WORKLOAD = "8192^3"
+DEFAULT_WORKLOAD = "8192^3"
 SECONDARY = "2048^3"
 L2_BYTES = 129 * 2 ** 20
 FP32_LANES_PER_SM = 128
 # nominal dense tensor rates (PFLOP/s) used only to scale a measured bf16 peak to tf32
 NOMINAL_TF32_OVER_BF16 = 1.1 / 2.25
 
+WORKLOAD_TEXT = {
+    "256^3": "sgemm 256x256x256 row-major fp32, alpha=1 beta=0, A,B U[-1,1] seed 0",
+    "2048^3": "sgemm 2048x2048x2048 row-major fp32, alpha=1 beta=0, A,B U[-1,1] seed 1",
+    "1000x1500x777": "sgemm 1000x1500x777 row-major fp32, lda=777 ldb=ldc=1500, alpha=1.5 beta=0.5, "
+                     "A,B U[-1,1], C0 N(0,1) seed 2",
+    "8192^3": "sgemm 8192x8192x8192 row-major fp32, alpha=1 beta=0, A,B N(0,1) seed 3",
+    "16384x128x8192": "sgemm 16384x128x8192 row-major fp32, alpha=1 beta=1, A,B,C0 U[-1,1] seed 4",
+}
 
-def parse():
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--path", choices=("auto", "ffma", "tf32x3"), default="auto")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_TEXT), default=DEFAULT_WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--shape", default=None,
-                    help="m,n,k of a smaller square-workload stand-in (profiling captures)")
-    return ap.parse_args()
+                    help="m,n,k of a smaller stand-in of the 8192^3 workload (profiling captures)")
+    return ap.parse_args(argv)
 
 
 def flops(p):
     return 2.0 * p.m * p.n * p.k
+
+
+def tflops(p, ms, count=1):
+    """TFLOPS of `count` problems `p` done in `ms` milliseconds (2mnk per
+    problem, the FLOP count the pages' figures use)."""
+    return flops(p) * count / (ms * 1e-3) / 1e12
+
+
+def max_over_ranks(value, world):
+    """The largest `value` over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_problem(args):
+    from dense_fp32_gemm_06_gb300 import inputs
+    if args.shape:
+        m, n, k = (int(x) for x in args.shape.split(","))
+        return inputs.workload(DEFAULT_WORKLOAD, m=m, n=n, k=k), f"sgemm {m}x{n}x{k} stand-in of 8192^3"
+    return inputs.workload(args.workload), WORKLOAD_TEXT[args.workload]
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -72,8 +107,6 @@ class ClockSampler:
 
     def __init__(self, device_index):
         self.proc = None
-        self.path = None
-        self.windows = []
         try:
             import torch
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
@@ -89,9 +122,6 @@ class ClockSampler:
                  "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, ValueError):
             self.proc = None
-
-    def mark(self):
-        return time.time()
 
     def stop(self):
         if self.proc is not None:
@@ -155,9 +185,8 @@ def kernel_source_hash(family):
 
 def traffic_record(kernel_family, units):
     """DRAM bytes per launch (read + write) of the kernel from the committed
-    ncu summary, scaled to `units` (output elements of the launch) when the
-    capture was of a different size; None when the kernel sources changed
-    since the capture."""
+    ncu summary when it was captured on this size (`units` = m*n*k), else
+    None; None too when the kernel sources changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
@@ -202,17 +231,17 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import oracle
-    from dense_fp32_gemm_06_gb300 import inputs
-    p = inputs.workload(WORKLOAD)
+    p, text = load_problem(args)
     oracle.build()
     threads = oracle.max_threads()
     # size one step to ~ (budget / steps) seconds of CPU work
     budget = 150.0
     per_step = max(0.5, min(10.0, budget / max(1, args.steps + args.warmup)))
+    probe = min(p.m, threads)
     t = time.perf_counter()
-    oracle.problem_f64(p, rows=(0, threads))
+    oracle.problem_f64(p, rows=(0, probe))
     dt = time.perf_counter() - t
-    rows = int(max(1, min(p.m, threads * per_step / max(dt, 1e-6))))
+    rows = int(max(1, min(p.m, probe * per_step / max(dt, 1e-6))))
     for _ in range(args.warmup):
         oracle.problem_f64(p, rows=(0, rows))
     times = []
@@ -222,14 +251,14 @@ def run_reference(args, rank, world):
         times.append(time.perf_counter() - t)
     total = sum(times)
     value = 2.0 * rows * p.n * p.k * len(times) / total / 1e12
-    sample = f"output rows 0..{rows - 1} of the 8192^3 workload ({rows} x 8192 outputs, k = 8192) per step"
+    sample = (f"output rows 0..{rows - 1} of the {args.workload} workload ({rows} x {p.n} outputs, "
+              f"k = {p.k}) per step, FP64")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded splitmix64)",
-        "config": {"workload": "sgemm 8192x8192x8192 row-major, alpha=1 beta=0, A,B N(0,1) seed 3",
-                   "sample": sample},
+        "config": {"workload": text, "sample": sample},
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -270,26 +299,24 @@ def time_e2e(e2e_step, stream, steps, p, world, h2d, d2h):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / steps
-    return {"value": flops(p) * world / (ms * 1e-3) / 1e12, "unit": "TFLOPS",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps}
+    return {"value": tflops(p, ms, world), "unit": "TFLOPS", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps}
 
 
 def run_ours(args, rank, world):
     import torch
     import torch.distributed as dist
     from dense_fp32_gemm_06_gb300 import binding, inputs
+    import oracle
 
     dev = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(dev)
     path = {"auto": binding.PATH_AUTO, "ffma": binding.PATH_FFMA, "tf32x3": binding.PATH_TF32X3}[args.path]
     stream = torch.cuda.current_stream()
     sptr = stream.cuda_stream
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
 
-    if args.shape:
-        m, n, k = (int(x) for x in args.shape.split(","))
-        p = inputs.workload(WORKLOAD, m=m, n=n, k=k)
-    else:
-        p = inputs.workload(WORKLOAD)
+    p, workload_text = load_problem(args)
     A_h = torch.from_numpy(p.A).pin_memory()
     B_h = torch.from_numpy(p.B).pin_memory()
     C_h = torch.from_numpy(p.C0).pin_memory()
@@ -297,12 +324,17 @@ def run_ours(args, rank, world):
     B = B_h.cuda()
     C = C_h.cuda()
     torch.cuda.synchronize()
+    operand_bytes = 4 * (A.numel() + B.numel() + C.numel())
+    # inputs smaller than twice L2 are flushed (a 2 x L2 write) before every timed launch
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda") \
+        if operand_bytes < 2 * L2_BYTES else None
+    flush = (lambda: flush_buf.fill_(1.0)) if flush_buf is not None else None
 
     st, plan = binding.plan(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
-                            C.data_ptr(), p.ldc, path=path,
-                            num_sms=torch.cuda.get_device_properties(dev).multi_processor_count)
+                            C.data_ptr(), p.ldc, path=path, num_sms=sms)
     if st:
         raise SystemExit(f"plan failed: {binding.status_string(st)}")
+
     def step():
         s = binding.sgemm_raw(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
                               C.data_ptr(), p.ldc, sptr, path)
@@ -312,11 +344,12 @@ def run_ours(args, rank, world):
     # quick self-check on sampled outputs before timing
     step()
     torch.cuda.synchronize()
-    import oracle
     rows, cols = inputs.sample_indices(p.m, p.n, 256, seed=p.seed + 2000)
     R, E = oracle.problem_f64_sampled(p, rows, cols)
     got = C.cpu().numpy()[rows, cols]
-    ok, worst, _ = oracle.within_tolerance(got, R, E, p.beta, None)
+    ok, worst, _ = oracle.within_tolerance(got, R, E, p.beta, p.C0[rows, cols] if p.beta != 0 else None)
+    # beta != 0 accumulates into C: restore C0 before timing
+    C.copy_(C_h)
 
     for _ in range(args.warmup):
         step()
@@ -333,6 +366,8 @@ def run_ours(args, rank, world):
     per = []
     ev0.record(stream)
     for _ in range(args.steps):
+        if flush is not None:
+            flush()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
@@ -347,26 +382,24 @@ def run_ours(args, rank, world):
     time.sleep(0.25)
     sampler.stop()
     clocks = sampler.summary(t0, t1)
-    total_ms = ev0.elapsed_time(ev1)
     launch_ms = [a.elapsed_time(b) for a, b in per]
-    if world > 1:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    value = flops(p) * args.steps * world / (total_ms * 1e-3) / 1e12
+    # with L2 flushes between launches the bracket includes the flushes, so
+    # the timed region is the sum of the launches' own event intervals
+    total_ms = sum(launch_ms) if flush is not None else ev0.elapsed_time(ev1)
+    total_ms = max_over_ranks(total_ms, world)
+    value = tflops(p, total_ms / args.steps, world)
     med_ms = statistics.median(launch_ms)
     mean_ms = sum(launch_ms) / len(launch_ms)
 
     # ---- roofline of the dominant kernel
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mhz = clocks.get("sm_mhz") or 2070.0
     ffma_peak = sms * FP32_LANES_PER_SM * 2 * mhz * 1e6 / 1e12
     ffma_basis = (f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 FLOP x {mhz:.0f} MHz "
                   f"(median SM clock sampled during the timed region)")
     if plan["path"] == binding.PATH_FFMA:
-        # the step is the one FFMA kernel
+        # the step is the one FFMA kernel (or the C = beta*C kernel)
         launches_per_step = 1
-        achieved = flops(p) / (mean_ms * 1e-3) / 1e12
+        achieved = tflops(p, mean_ms)
         roof = {"bound": "alu", "kernel": "ffma_sgemm_kernel", "achieved": achieved, "peak": ffma_peak,
                 "unit": "TFLOP/s", "frac": achieved / ffma_peak, "peak_basis": ffma_basis,
                 "traffic": traffic_record("ffma", p.m * p.n * p.k)}
@@ -391,10 +424,10 @@ def run_ours(args, rank, world):
 
         for _ in range(3):
             gemm_only()
-        gm = time_launches(gemm_only, stream, min(args.steps, 100))
+        gm = time_launches(gemm_only, stream, min(args.steps, 100), flush=flush)
         gemm_ms = sum(gm) / len(gm)
         del a_hi, a_lo, b_hi, b_lo
-        achieved = flops(p) / (gemm_ms * 1e-3) / 1e12
+        achieved = tflops(p, gemm_ms)
         mp = measured_peaks()
         bf16 = (mp or {}).get("bf16_tflops", 1900.0)
         tf32 = bf16 * NOMINAL_TF32_OVER_BF16
@@ -426,9 +459,9 @@ def run_ours(args, rank, world):
     if args.e2e_steps > 0:
         e2e = time_e2e(e2e_step, stream, args.e2e_steps, p, world, h2d, d2h)
 
-    # ---- secondary size (2048^3, fits in L2: flushed between launches)
+    # ---- secondary size (2048^3 fits in L2: flushed before every launch)
     secondary = None
-    if not args.no_secondary:
+    if not args.no_secondary and args.workload != SECONDARY and not args.shape:
         q = inputs.workload(SECONDARY)
         qA = torch.from_numpy(q.A).cuda()
         qB = torch.from_numpy(q.B).cuda()
@@ -445,9 +478,8 @@ def run_ours(args, rank, world):
             qstep()
         ms = time_launches(qstep, stream, 30, flush=lambda: scratch.fill_(1.0))
         qmed = statistics.median(ms)
-        secondary = {"workload": "sgemm 2048x2048x2048 row-major, alpha=1 beta=0, A,B U[-1,1] seed 1",
-                     "value": flops(q) / (qmed * 1e-3) / 1e12, "unit": "TFLOPS", "median_ms": qmed,
-                     "launches": len(ms), "l2": "flushed (256 MB write) before every launch"}
+        secondary = {"workload": WORKLOAD_TEXT[SECONDARY], "value": tflops(q, qmed), "unit": "TFLOPS",
+                     "median_ms": qmed, "launches": len(ms), "l2": "flushed (2 x L2 write) before every launch"}
         del scratch
 
     # ---- the CUDA-core FFMA path on the same workload, for comparison
@@ -460,18 +492,30 @@ def run_ours(args, rank, world):
                 raise SystemExit(f"sgemm failed: {binding.status_string(s)}")
         for _ in range(2):
             ffma_step()
-        fm = time_launches(ffma_step, stream, 10)
+        torch.cuda.synchronize()
+        fs = ClockSampler(dev)
+        time.sleep(0.3)
+        f0 = time.time()
+        # about 1.5 s of FFMA work, at least 10 launches
+        count = max(10, int(1.5 / max(1e-6, flops(p) / 60e12)))
+        fm = time_launches(ffma_step, stream, count, flush=flush)
+        f1 = time.time()
+        time.sleep(0.25)
+        fs.stop()
+        fclk = fs.summary(f0, f1)
         f_ms = sum(fm) / len(fm)
-        ffma = {"value": flops(p) / (f_ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms": f_ms, "launches": len(fm),
-                "frac_of_ffma_peak": flops(p) / (f_ms * 1e-3) / 1e12 / ffma_peak}
+        fmhz = fclk.get("sm_mhz") or 2070.0
+        fpeak = sms * FP32_LANES_PER_SM * 2 * fmhz * 1e6 / 1e12
+        ffma = {"value": tflops(p, f_ms), "unit": "TFLOPS", "ms": f_ms, "launches": len(fm),
+                "frac_of_ffma_peak": tflops(p, f_ms) / fpeak, "ffma_peak_tflops": fpeak, "clocks": fclk}
 
     # ---- CPU baseline: the oracle on a bounded slab of the same workload
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tf, nrows, secs, threads = oracle_sample(p, args.cpu_seconds)
         cpu = {"value": tf, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
-               "sample": f"output rows 0..{nrows - 1} of the 8192^3 workload ({nrows} x 8192 outputs, "
-                         f"k = 8192, FP64), {secs:.1f} s"}
+               "sample": f"output rows 0..{nrows - 1} of the workload ({nrows} x {p.n} outputs, "
+                         f"k = {p.k}, FP64), {secs:.1f} s"}
 
     if rank == 0:
         path_name = {binding.PATH_FFMA: "ffma", binding.PATH_TF32X3: "tf32x3"}.get(plan["path"], "?")
@@ -480,10 +524,11 @@ def run_ours(args, rank, world):
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "median_ms": med_ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "tf32x3" if plan["path"] == binding.PATH_TF32X3 else "f32",
-            "data": "synthetic (seeded splitmix64, N(0,1) via Box-Muller)",
-            "config": {"workload": "sgemm 8192x8192x8192 row-major fp32, alpha=1 beta=0, A,B N(0,1) seed 3",
-                       "path": path_name, "kernel_plan": plan,
-                       "l2": "inputs larger than L2 (768 MB of A, B, C vs 129 MB)",
+            "data": "synthetic (seeded splitmix64)",
+            "config": {"workload": workload_text, "path": path_name, "kernel_plan": plan,
+                       "l2": ("flushed (2 x L2 write) before every timed launch; value from the launches' "
+                              "own event intervals") if flush is not None else
+                             f"inputs larger than L2 ({operand_bytes / 2**20:.0f} MB of A, B, C vs 129 MB)",
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "check": {"sampled_outputs": int(len(rows)), "within_tolerance": ok,
                                  "worst_ratio": worst}},
@@ -499,8 +544,8 @@ def run_ours(args, rank, world):
     return 0
 
 
-def main():
-    args = parse()
+def main(argv=None):
+    args = parse(argv)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
