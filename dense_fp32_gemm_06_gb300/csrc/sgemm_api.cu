@@ -45,6 +45,12 @@ cudaError_t set_ffma_attr() {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, ffma::Default::SMEM_BYTES);
 }
 
+template <class Cfg, bool CV>
+cudaError_t set_tc_attr() {
+    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Cfg::SMEM_BYTES);
+}
+
 // One-time per-device set-up: SM count and kernel attributes.
 int device_state(DeviceState **out) {
     int dev = 0;
@@ -60,12 +66,10 @@ int device_state(DeviceState **out) {
         if ((e = set_ffma_attr<true, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_ffma_attr<false, true>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_ffma_attr<false, false>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      tf32x3::SMEM_BYTES)) != cudaSuccess)
-            return fail_cuda(e);
-        if ((e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      tf32x3::SMEM_BYTES)) != cudaSuccess)
-            return fail_cuda(e);
+        if ((e = set_tc_attr<tf32x3::Wide, true>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_tc_attr<tf32x3::Wide, false>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_tc_attr<tf32x3::Narrow, true>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_tc_attr<tf32x3::Narrow, false>()) != cudaSuccess) return fail_cuda(e);
         if (g_encode_tiled == nullptr) {
             cudaDriverEntryPointQueryResult q;
             void *fn = nullptr;
@@ -130,13 +134,18 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
     if (use_tc) {
         pl->kernel = kKernelTf32x3;
         pl->bm = tf32x3::BM;
-        pl->bn = tf32x3::BN;
         pl->bk = tf32x3::BK;
         pl->threads = tf32x3::THREADS;
-        pl->stages = tf32x3::STAGES;
-        pl->smem_bytes = tf32x3::SMEM_BYTES;
         pl->b_vec = 1;
+        // tile width: the one with the smaller (waves x width) estimate; a
+        // 128-wide MMA is taken to do 10% less useful work per cycle
         const int tiles_m = (m + pl->bm - 1) / pl->bm;
+        const long long t256 = (long long)tiles_m * ((n + 255) / 256), t128 = (long long)tiles_m * ((n + 127) / 128);
+        const long long w256 = (t256 + num_sms - 1) / num_sms, w128 = (t128 + num_sms - 1) / num_sms;
+        const bool narrow = 10 * 128 * w128 * 11 < 10 * 256 * w256 * 10 || n <= 128;
+        pl->bn = narrow ? tf32x3::Narrow::BN : tf32x3::Wide::BN;
+        pl->stages = narrow ? tf32x3::Narrow::STAGES : tf32x3::Wide::STAGES;
+        pl->smem_bytes = narrow ? tf32x3::Narrow::SMEM_BYTES : tf32x3::Wide::SMEM_BYTES;
         const int tiles_n = (n + pl->bn - 1) / pl->bn;
         pl->tiles = tiles_m * tiles_n;
         pl->grid = pl->tiles;
@@ -181,20 +190,35 @@ int make_tensor_map(CUtensorMap *map, const float *base, int rows, int cols, int
 int ka_of(int k) { return (k + 3) & ~3; }
 
 // A (m x k, lda) -> a_hi, a_lo (m x ka).
+// Grids of the split kernels: about 8 blocks of 256 threads per SM, each
+// looping over its share (they are HBM-bound).
+constexpr int kSplitBlocks = 8 * 160;
+
 int launch_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream) {
     if (m == 0 || k == 0) return SGEMM_STATUS_OK;
-    const int gx = (k + 255) / 256;
-    const int gy = m < 65535 ? m : 65535;
-    tf32x3::split_a_kernel<<<dim3(gx, gy), 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k));
+    const bool vec = aligned(A, 16) && (lda % 4) == 0;
+    const int per_row = vec ? (k / 4 > 0 ? k / 4 : 1) : k;
+    int gx = (per_row + 255) / 256;
+    if (gx > 16) gx = 16;
+    int gy = kSplitBlocks / gx;
+    if (gy < 1) gy = 1;
+    if (gy > m) gy = m;
+    if (gy > 65535) gy = 65535;
+    if (vec)
+        tf32x3::split_a_kernel<true><<<dim3(gx, gy), 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k));
+    else
+        tf32x3::split_a_kernel<false><<<dim3(gx, gy), 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k));
     return SGEMM_STATUS_OK;
 }
 
 // B (k x n, ldb) -> bt_hi, bt_lo (B^T, n x ka).
 int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, cudaStream_t stream) {
     if (n == 0 || k == 0) return SGEMM_STATUS_OK;
-    const long long gx = (n + 31) / 32, gy = (k + 31) / 32;
-    tf32x3::split_bt_kernel<<<dim3((unsigned)(gx < 2147483647 ? gx : 2147483647), (unsigned)(gy < 65535 ? gy : 65535)),
-                              256, 0, stream>>>(B, ldb, k, n, bt_hi, bt_lo, ka_of(k));
+    long long gx = (n + 63) / 64, gy = (k + 31) / 32;
+    if (gx > kSplitBlocks) gx = kSplitBlocks;
+    if (gy > kSplitBlocks / gx) gy = kSplitBlocks / gx > 0 ? kSplitBlocks / gx : 1;
+    tf32x3::split_bt_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(B, ldb, k, n, bt_hi, bt_lo,
+                                                                                 ka_of(k));
     return SGEMM_STATUS_OK;
 }
 
@@ -205,8 +229,8 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     CUtensorMap t_ahi, t_alo, t_bhi, t_blo;
     int st = make_tensor_map(&t_ahi, a_hi, m, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st) st = make_tensor_map(&t_alo, a_lo, m, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st) st = make_tensor_map(&t_bhi, bt_hi, n, k, ka, tf32x3::BN, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st) st = make_tensor_map(&t_blo, bt_lo, n, k, ka, tf32x3::BN, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st) st = make_tensor_map(&t_bhi, bt_hi, n, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st) st = make_tensor_map(&t_blo, bt_lo, n, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st) return st;
     tf32x3::Params a;
     a.m = m;
@@ -219,11 +243,21 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     a.tiles_m = (m + pl.bm - 1) / pl.bm;
     a.tiles_n = (n + pl.bn - 1) / pl.bn;
     a.group_m = pl.group_m;
-    if (pl.c_vec)
-        tf32x3::tf32x3_gemm_kernel<true><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(t_ahi, t_alo, t_bhi, t_blo, a);
-    else
-        tf32x3::tf32x3_gemm_kernel<false><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(t_ahi, t_alo, t_bhi, t_blo,
-                                                                                         a);
+    if (pl.bn == tf32x3::Narrow::BN) {
+        if (pl.c_vec)
+            tf32x3::tf32x3_gemm_kernel<tf32x3::Narrow, true><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(
+                t_ahi, t_alo, t_bhi, t_blo, a);
+        else
+            tf32x3::tf32x3_gemm_kernel<tf32x3::Narrow, false><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(
+                t_ahi, t_alo, t_bhi, t_blo, a);
+    } else {
+        if (pl.c_vec)
+            tf32x3::tf32x3_gemm_kernel<tf32x3::Wide, true><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(
+                t_ahi, t_alo, t_bhi, t_blo, a);
+        else
+            tf32x3::tf32x3_gemm_kernel<tf32x3::Wide, false><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(
+                t_ahi, t_alo, t_bhi, t_blo, a);
+    }
     return SGEMM_STATUS_OK;
 }
 

@@ -16,7 +16,8 @@
 //     B becomes B^T_hi, B^T_lo, n x ka, transposed through a padded 32 x 33
 //     shared tile (coalesced reads and writes).  Both operands of the MMA
 //     are then K-major;
-//  2. the GEMM kernel: one CTA per 128 x 256 tile of C, 10 warps.
+//  2. the GEMM kernel: one CTA per 128 x BN tile of C (BN = 256, or 128 for
+//     narrow or few-tile problems; the rest of this comment says 256), 10 warps.
 //     warp 0 lane 0: TMA producer -- per 16-deep k slab, four boxes (A_hi,
 //       A_lo 128 x 16; B_hi, B_lo 256 x 16, 64-byte rows with the 64-byte
 //       swizzle) into a 4-stage ring, completing on the slot's "full"
@@ -54,26 +55,33 @@ namespace sgemm_gb300 {
 namespace tf32x3 {
 
 constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 16;   // 64-byte rows
-constexpr int STAGES = 4;
 constexpr int UMMA_K = 8;
 constexpr int KC = 128;                                   // k per tensor-core accumulation chunk
 constexpr int CHUNK_STAGES = KC / BK;
 constexpr int A_TILE = BM * BK * 4;                       // 8 KB
-constexpr int B_TILE = BN * BK * 4;                       // 16 KB
-constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;      // 48 KB: A_hi, A_lo, B_hi, B_lo
 constexpr int ACC_WARPS = 8;
 constexpr int ACC_THREADS = 32 * ACC_WARPS;
 constexpr int THREADS = 64 + ACC_THREADS;                 // producer warp, MMA warp, 8 accumulator warps
-constexpr int TMEM_COLS = 2 * BN;                         // two accumulators
-constexpr int COLS_PER_THREAD = BN / 2;                   // two warps per 32-lane group
 constexpr int BAR_REGION = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_REGION;
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 static_assert(BK * 4 == 64, "one 64-byte swizzle row per operand row");
 static_assert(KC % BK == 0, "chunks are whole slabs");
-static_assert(TMEM_COLS <= 512, "tensor memory columns");
+
+// Tile width BN (256, or 128 for narrow / few-tile problems) and ring depth.
+template <int BN_, int STAGES_>
+struct Config {
+    static constexpr int BN = BN_, STAGES = STAGES_;
+    static constexpr int B_TILE = BN * BK * 4;
+    static constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;   // A_hi, A_lo, B_hi, B_lo
+    static constexpr int TMEM_COLS = 2 * BN;                      // two accumulators
+    static constexpr int COLS_PER_THREAD = BN / 2;                // two warps per 32-lane group
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_REGION;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "power-of-two TMEM allocation");
+    static_assert(COLS_PER_THREAD % 16 == 0, "accumulator warps load 16 columns at a time");
+};
+using Wide = Config<256, 4>;     // 48 KB stages
+using Narrow = Config<128, 6>;   // 32 KB stages
 
 constexpr int kStatusProducer = 0x201;
 constexpr int kStatusMma = 0x202;
@@ -91,43 +99,70 @@ struct Params {
 
 // ---------------------------------------------------------------- split kernels
 
-// A (m x k, row pitch lda) -> hi, lo (m x ka, row pitch ka).
+__device__ __forceinline__ void split_one(float x, float &h, float &l) {
+    h = tc::round_tf32(x);
+    l = tc::round_tf32(x - h);
+}
+
+// A (m x k, row pitch lda) -> hi, lo (m x ka, row pitch ka).  VEC: A and
+// lda 16-byte aligned, so every row is read as float4 except a k % 4 tail
+// (read element by element: the bytes past k may lie outside A).
+template <bool VEC>
 __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ A, long long lda, int m, int k,
                                                       float *__restrict__ hi, float *__restrict__ lo, int ka) {
+    const int full4 = VEC ? k / 4 : 0;               // float4 chunks entirely inside the row
+    const int scal0 = 4 * full4;                      // first element done one at a time
     for (int row = blockIdx.y; row < m; row += gridDim.y) {
         const float *src = A + (long long)row * lda;
         float *h = hi + (long long)row * ka;
         float *l = lo + (long long)row * ka;
-        for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < k; t += gridDim.x * blockDim.x) {
-            const float x = src[t];
-            const float xh = tc::round_tf32(x);
+        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < full4; c += gridDim.x * blockDim.x) {
+            const float4 x = __ldg(reinterpret_cast<const float4 *>(src) + c);
+            float4 xh, xl;
+            split_one(x.x, xh.x, xl.x);
+            split_one(x.y, xh.y, xl.y);
+            split_one(x.z, xh.z, xl.z);
+            split_one(x.w, xh.w, xl.w);
+            reinterpret_cast<float4 *>(h)[c] = xh;
+            reinterpret_cast<float4 *>(l)[c] = xl;
+        }
+        for (int t = scal0 + blockIdx.x * blockDim.x + threadIdx.x; t < k; t += gridDim.x * blockDim.x) {
+            float xh, xl;
+            split_one(__ldg(src + t), xh, xl);
             h[t] = xh;
-            l[t] = tc::round_tf32(x - xh);
+            l[t] = xl;
         }
     }
 }
 
-// B (k x n, row pitch ldb) -> hi, lo of B^T (n x ka, row pitch ka).
+// B (k x n, row pitch ldb) -> hi, lo of B^T (n x ka, row pitch ka), through
+// a 32 (k) x 64 (n) shared tile padded to 65 columns: reads of B and writes
+// of B^T are both 128-byte coalesced per warp, and the column reads of the
+// tile hit 32 different banks.
 __global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__ B, long long ldb, int k, int n,
                                                        float *__restrict__ hi, float *__restrict__ lo, int ka) {
-    __shared__ float tile[32][33];
+    __shared__ float tile[32][65];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
     for (int t0 = blockIdx.y * 32; t0 < k; t0 += gridDim.y * 32) {
-        for (int j0 = blockIdx.x * 32; j0 < n; j0 += gridDim.x * 32) {
+        for (int j0 = blockIdx.x * 64; j0 < n; j0 += gridDim.x * 64) {
 #pragma unroll
             for (int r = ty; r < 32; r += 8) {
-                const int t = t0 + r, j = j0 + tx;
-                tile[r][tx] = (t < k && j < n) ? B[(long long)t * ldb + j] : 0.f;
+                const int t = t0 + r;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int j = j0 + 32 * q + tx;
+                    tile[r][32 * q + tx] = (t < k && j < n) ? __ldg(B + (long long)t * ldb + j) : 0.f;
+                }
             }
             __syncthreads();
 #pragma unroll
-            for (int r = ty; r < 32; r += 8) {
+            for (int r = ty; r < 64; r += 8) {
                 const int j = j0 + r, t = t0 + tx;
                 if (j < n && t < k) {
-                    const float x = tile[tx][r];
-                    const float xh = tc::round_tf32(x);
+                    float xh, xl;
+                    split_one(tile[tx][r], xh, xl);
                     hi[(long long)j * ka + t] = xh;
-                    lo[(long long)j * ka + t] = tc::round_tf32(x - xh);
+                    lo[(long long)j * ka + t] = xl;
                 }
             }
             __syncthreads();
@@ -137,11 +172,13 @@ __global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__
 
 // ---------------------------------------------------------------- GEMM kernel
 
-template <bool C_VEC>
+template <class Cfg, bool C_VEC>
 __global__ void __launch_bounds__(THREADS, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
                        const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
                        const Params p) {
+    constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, B_TILE = Cfg::B_TILE, STAGE_BYTES = Cfg::STAGE_BYTES;
+    constexpr int TMEM_COLS = Cfg::TMEM_COLS, COLS_PER_THREAD = Cfg::COLS_PER_THREAD;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *const smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t stage0 = smem_u32(smem);
