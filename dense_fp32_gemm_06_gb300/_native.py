@@ -100,7 +100,7 @@ EXPORTS = ["sgemm", "sgemm_ex", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", 
 class Plan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "path", "kernel", "bm", "bn", "bk", "rm", "rn", "threads", "stages", "grid", "tiles",
-        "k_tiles", "smem_bytes", "b_vec", "c_vec", "group_m")]
+        "k_tiles", "smem_bytes", "b_vec", "c_vec", "group_m", "split_k")]
 
 
 def _declare(lib):

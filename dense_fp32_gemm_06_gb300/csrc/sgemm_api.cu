@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -23,6 +24,9 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     bool ready = false;
     int sms = 0;
+    // clusters of S CTAs (S = 2..8) of the tensor-core kernel that fit on the
+    // device at once, for the 256- and 128-wide tiles ([0] and [1])
+    int max_clusters[2][9] = {};
 };
 
 std::mutex g_mu;
@@ -51,6 +55,25 @@ cudaError_t set_tc_attr() {
                                 Cfg::SMEM_BYTES);
 }
 
+// Clusters of S CTAs of the tensor-core kernel that can be resident at once
+// (thread-block clusters cannot span GPCs, so this is below sms / S).
+template <class Cfg>
+cudaError_t max_clusters_of(int S, int *out) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(S * 64), 1, 1);
+    cfg.blockDim = dim3((unsigned)tf32x3::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)Cfg::SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)S;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    *out = 0;
+    return cudaOccupancyMaxActiveClusters(out, tf32x3::tf32x3_gemm_kernel<Cfg, true>, &cfg);
+}
+
 // One-time per-device set-up: SM count and kernel attributes.
 int device_state(DeviceState **out) {
     int dev = 0;
@@ -70,6 +93,10 @@ int device_state(DeviceState **out) {
         if ((e = set_tc_attr<tf32x3::Wide, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Narrow, true>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Narrow, false>()) != cudaSuccess) return fail_cuda(e);
+        for (int S = 2; S <= 8; ++S) {
+            if ((e = max_clusters_of<tf32x3::Wide>(S, &d.max_clusters[0][S])) != cudaSuccess) return fail_cuda(e);
+            if ((e = max_clusters_of<tf32x3::Narrow>(S, &d.max_clusters[1][S])) != cudaSuccess) return fail_cuda(e);
+        }
         if (g_encode_tiled == nullptr) {
             cudaDriverEntryPointQueryResult q;
             void *fn = nullptr;
@@ -105,8 +132,10 @@ int check_args(int m, int n, int k, float alpha, const float *A, int lda, const 
     return 0;
 }
 
+// max_clusters: the device's cluster capacity table (DeviceState), or NULL
+// for a host-only plan, which assumes 8 GPCs of num_sms / 8 SMs.
 int plan(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
-         const float *C, int ldc, int path, int num_sms, sgemm_plan *pl) {
+         const float *C, int ldc, int path, int num_sms, sgemm_plan *pl, const int (*max_clusters)[9] = nullptr) {
     (void)beta;
     std::memset(pl, 0, sizeof(*pl));
     if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
@@ -121,6 +150,7 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
     const bool use_tc = path == SGEMM_PATH_TF32X3 ||
                         (path == SGEMM_PATH_AUTO && ((long long)m * n * k >= (1LL << 27) || k > 8192));
     pl->path = use_tc ? SGEMM_PATH_TF32X3 : SGEMM_PATH_FFMA;
+    pl->split_k = 1;
     pl->c_vec = aligned(C, 16) && (ldc % 4) == 0;
     if (k == 0 || alpha == 0.f) {
         pl->kernel = kKernelScale;
@@ -137,19 +167,63 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         pl->bk = tf32x3::BK;
         pl->threads = tf32x3::THREADS;
         pl->b_vec = 1;
-        // tile width: the one with the smaller (waves x width) estimate; a
-        // 128-wide MMA is taken to do 10% less useful work per cycle
+        // Tile width BN and split-K factor S: the pair with the smallest
+        // estimated time waves x ceil(KT / S) x (slab time) (+ a fixed cost
+        // for a split's cluster reduction).  Slab times, measured on GB300:
+        // a 256-wide slab ~0.5 us, a 128-wide one ~0.375 us (1.5x the time
+        // per FLOP); a split adds ~6 us.  Units below: 1/8 us.  Waves count
+        // CTAs against the SMs (S = 1) or clusters against the clusters that
+        // fit at once (S > 1); a split must fit in one wave and leave each
+        // CTA >= 8 slabs (128 k).
         const int tiles_m = (m + pl->bm - 1) / pl->bm;
-        const long long t256 = (long long)tiles_m * ((n + 255) / 256), t128 = (long long)tiles_m * ((n + 127) / 128);
-        const long long w256 = (t256 + num_sms - 1) / num_sms, w128 = (t128 + num_sms - 1) / num_sms;
-        const bool narrow = 10 * 128 * w128 * 11 < 10 * 256 * w256 * 10 || n <= 128;
-        pl->bn = narrow ? tf32x3::Narrow::BN : tf32x3::Wide::BN;
+        const long long KT = (k + tf32x3::BK - 1) / tf32x3::BK;
+        // tuning overrides for benchmarks and tests: SGEMM_GB300_TILE_N (128
+        // or 256) and SGEMM_GB300_SPLIT_K (1..8) pin the choice below
+        const char *env_bn = std::getenv("SGEMM_GB300_TILE_N");
+        const char *env_s = std::getenv("SGEMM_GB300_SPLIT_K");
+        const int force_bn = env_bn ? std::atoi(env_bn) : 0;
+        const int force_s = env_s ? std::atoi(env_s) : 0;
+        long long best = -1;
+        int best_bn = tf32x3::Wide::BN, best_s = 1;
+        for (int bn : {tf32x3::Wide::BN, tf32x3::Narrow::BN}) {
+            if (force_bn == tf32x3::Wide::BN || force_bn == tf32x3::Narrow::BN) {
+                if (bn != force_bn) continue;
+            } else if (bn == tf32x3::Wide::BN && n <= tf32x3::Narrow::BN) {
+                continue;
+            }
+            const int wi = bn == tf32x3::Wide::BN ? 0 : 1;
+            const long long slab = bn == tf32x3::Wide::BN ? 4 : 3;
+            const long long tiles = (long long)tiles_m * ((n + bn - 1) / bn);
+            for (int S = 1; S <= 8; ++S) {
+                if (force_s >= 1 && force_s <= 8) {
+                    if (S != force_s) continue;
+                } else if (S > 1 && KT / S < 8) {
+                    break;
+                }
+                long long slots = num_sms;   // CTAs (S = 1) or clusters (S > 1) resident at once
+                if (S > 1) {
+                    slots = max_clusters ? max_clusters[wi][S] : 8LL * ((num_sms / 8) / S);
+                    // a split only pays when all of its clusters run in one wave
+                    if (slots <= 0 || (tiles > slots && !(force_s >= 1 && force_s <= 8))) continue;
+                }
+                const long long waves = (tiles + slots - 1) / slots;
+                const long long cost = waves * ((KT + S - 1) / S) * slab + (S > 1 ? 48 : 0);
+                if (best < 0 || cost < best) {
+                    best = cost;
+                    best_bn = bn;
+                    best_s = S;
+                }
+            }
+        }
+        const bool narrow = best_bn == tf32x3::Narrow::BN;
+        pl->bn = best_bn;
+        pl->split_k = best_s;
         pl->stages = narrow ? tf32x3::Narrow::STAGES : tf32x3::Wide::STAGES;
         pl->smem_bytes = narrow ? tf32x3::Narrow::SMEM_BYTES : tf32x3::Wide::SMEM_BYTES;
         const int tiles_n = (n + pl->bn - 1) / pl->bn;
         pl->tiles = tiles_m * tiles_n;
-        pl->grid = pl->tiles;
-        pl->k_tiles = (k + pl->bk - 1) / pl->bk;
+        pl->grid = pl->tiles * pl->split_k;
+        pl->k_tiles = (int)KT;
         pl->group_m = tiles_m < 8 ? tiles_m : 8;
         return SGEMM_STATUS_OK;
     }
@@ -243,21 +317,31 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     a.tiles_m = (m + pl.bm - 1) / pl.bm;
     a.tiles_n = (n + pl.bn - 1) / pl.bn;
     a.group_m = pl.group_m;
-    if (pl.bn == tf32x3::Narrow::BN) {
-        if (pl.c_vec)
-            tf32x3::tf32x3_gemm_kernel<tf32x3::Narrow, true><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(
-                t_ahi, t_alo, t_bhi, t_blo, a);
-        else
-            tf32x3::tf32x3_gemm_kernel<tf32x3::Narrow, false><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(
-                t_ahi, t_alo, t_bhi, t_blo, a);
-    } else {
-        if (pl.c_vec)
-            tf32x3::tf32x3_gemm_kernel<tf32x3::Wide, true><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(
-                t_ahi, t_alo, t_bhi, t_blo, a);
-        else
-            tf32x3::tf32x3_gemm_kernel<tf32x3::Wide, false><<<pl.grid, pl.threads, pl.smem_bytes, stream>>>(
-                t_ahi, t_alo, t_bhi, t_blo, a);
-    }
+    // clusters of split_k CTAs (consecutive in x) share a tile
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)pl.split_k;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pl.split_k > 1 ? 1 : 0;
+    cudaError_t e;
+    if (pl.bn == tf32x3::Narrow::BN)
+        e = pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<tf32x3::Narrow, true>, t_ahi, t_alo, t_bhi,
+                                          t_blo, a)
+                     : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<tf32x3::Narrow, false>, t_ahi, t_alo,
+                                          t_bhi, t_blo, a);
+    else
+        e = pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<tf32x3::Wide, true>, t_ahi, t_alo, t_bhi,
+                                          t_blo, a)
+                     : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<tf32x3::Wide, false>, t_ahi, t_alo, t_bhi,
+                                          t_blo, a);
+    if (e != cudaSuccess) return fail_cuda(e);
     return SGEMM_STATUS_OK;
 }
 
@@ -327,7 +411,7 @@ int sgemm_ex(int m, int n, int k, float alpha, const float *A, int lda, const fl
     int st = device_state(&dev);
     if (st != SGEMM_STATUS_OK) return st;
     sgemm_plan pl;
-    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, dev->sms, &pl);
+    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, dev->sms, &pl, dev->max_clusters);
     if (st != SGEMM_STATUS_OK) return st;
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
@@ -412,7 +496,8 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
     sgemm_plan pl;
     // the plan of the tensor-core path for this shape (operand pointers only
     // matter to the FFMA path's alignment choice)
-    int st = plan(m, n, k, alpha, a_hi, imax(1, k), a_hi, imax(1, n), beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl);
+    int st = plan(m, n, k, alpha, a_hi, imax(1, k), a_hi, imax(1, n), beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl,
+                  dev->max_clusters);
     if (st) return st;
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
@@ -433,7 +518,7 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
     int st = device_state(&dev);
     if (st != SGEMM_STATUS_OK) return st;
     sgemm_plan pl;
-    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl);
+    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl, dev->max_clusters);
     if (st != SGEMM_STATUS_OK) return st;
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);

@@ -37,6 +37,14 @@
 //       adds, then release the TMEM buffer.  After the last chunk they write
 //       alpha*acc + beta*C for rows < m, columns < n (C not read when
 //       beta == 0).
+//     Split-K for problems with too few tiles to fill the GPU: the grid is
+//     launched in clusters of S CTAs (S <= 8) that share one tile, CTA r
+//     taking k slabs [r*KT/S, (r+1)*KT/S).  Each parks its FP32 partial
+//     tile in its own shared memory; after a cluster barrier CTA r sums
+//     rows [r*128/S, (r+1)*128/S) over all S partials in rank order through
+//     distributed shared memory (ld.shared::cluster) and writes them to C,
+//     then a second cluster barrier keeps every partial alive until read.
+//     The reduction order is fixed, so results do not depend on timing.
 //     TMA zero-fills rows past m, columns past n and k past the end, so the
 //     MMA never sees an index test.  Every mbarrier wait is bounded (2 s):
 //     a wait that runs out records a code in the library status word,
@@ -179,6 +187,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                        const Params p) {
     constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, B_TILE = Cfg::B_TILE, STAGE_BYTES = Cfg::STAGE_BYTES;
     constexpr int TMEM_COLS = Cfg::TMEM_COLS, COLS_PER_THREAD = Cfg::COLS_PER_THREAD;
+    constexpr int PART_PITCH = BN + 4;   // floats per row of a parked split-K partial tile
+    static_assert(BM * PART_PITCH * 4 <= STAGES * STAGE_BYTES, "partial tile fits the stage memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *const smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     const uint32_t stage0 = smem_u32(smem);
@@ -192,10 +202,15 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // split-K: the CTAs of a cluster share one output tile and take
+    // consecutive ranges of its k slabs (a cluster of one without split-K)
+    const uint32_t nsplit = tc::cluster_nctarank(), rank = tc::cluster_ctarank();
     int tm, tn;
-    raster_tile(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+    raster_tile(blockIdx.x / nsplit, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN;
-    const int KT = (p.k + BK - 1) / BK;
+    const int KT_ALL = (p.k + BK - 1) / BK;
+    const int kt0 = (int)((long long)KT_ALL * rank / nsplit);
+    const int KT = (int)((long long)KT_ALL * (rank + 1) / nsplit) - kt0;   // slabs of this CTA
     const int NC = (KT + CHUNK_STAGES - 1) / CHUNK_STAGES;
 
     if (threadIdx.x == 0) {
@@ -238,10 +253,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t st = stage0 + s * STAGE_BYTES;
                 const uint32_t fb = bar_full + 8 * s;
                 mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                tma_load_2d(st, &tmAhi, kt * BK, m0, fb);
-                tma_load_2d(st + A_TILE, &tmAlo, kt * BK, m0, fb);
-                tma_load_2d(st + 2 * A_TILE, &tmBhi, kt * BK, n0, fb);
-                tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kt * BK, n0, fb);
+                const int kx = (kt0 + kt) * BK;
+                tma_load_2d(st, &tmAhi, kx, m0, fb);
+                tma_load_2d(st + A_TILE, &tmAlo, kx, m0, fb);
+                tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, n0, fb);
+                tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, n0, fb);
                 ++issued;
             }
             if (*abort_flag) {
@@ -303,6 +319,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int b = c & 1;
             if (!mbar_wait(bar_tfull + 8 * b, (c >> 1) & 1, kStatusAccumulate)) {
                 ok = false;
+                *abort_flag = 1;
                 break;
             }
             tc::fence_after_sync();
@@ -318,7 +335,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_arrive(bar_tempty + 8 * b);
         }
         const int row = m0 + lane_grp * 32 + lane;
-        if (ok && *abort_flag == 0 && row < p.m) {
+        if (nsplit > 1) {
+            // park the partial tile in this CTA's (now idle) stage memory,
+            // rows PART_PITCH floats apart (4 banks apart: conflict-free)
+            float *part = reinterpret_cast<float *>(smem) + (lane_grp * 32 + lane) * PART_PITCH +
+                          half * COLS_PER_THREAD;
+#pragma unroll
+            for (int q = 0; q < COLS_PER_THREAD / 4; ++q)
+                reinterpret_cast<float4 *>(part)[q] =
+                    make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        } else if (ok && *abort_flag == 0 && row < p.m) {
             const float alpha = p.alpha, beta = p.beta;
             float *crow = p.C + (long long)row * p.ldc;
             const int col0 = n0 + half * COLS_PER_THREAD;
@@ -349,6 +375,57 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     tc::fence_before_sync();
     __syncthreads();
+    if (nsplit > 1) {
+        // ------------------------------------------------------------ cluster reduction
+        // every partial is parked; CTA `rank` sums rows [r0, r1) of the tile
+        // over the cluster's CTAs in rank order (a fixed order: the result
+        // does not depend on timing) and writes them to C
+        tc::cluster_sync();
+        const uint32_t part0 = smem_u32(smem);
+        const uint32_t abort_addr = smem_u32(const_cast<int *>(abort_flag));
+        int any_abort = 0;
+        for (uint32_t q = 0; q < nsplit; ++q) any_abort |= tc::ld_cluster_s32(tc::map_shared_rank(abort_addr, q));
+        const int r0 = (int)(BM * rank / nsplit), r1 = (int)(BM * (rank + 1) / nsplit);
+        const float alpha = p.alpha, beta = p.beta;
+        if (!any_abort) {
+            for (int idx = threadIdx.x; idx < (r1 - r0) * (BN / 4); idx += THREADS) {
+                const int r = r0 + idx / (BN / 4), c4 = idx % (BN / 4);
+                const int row = m0 + r, col = n0 + 4 * c4;
+                const uint32_t off = part0 + (uint32_t)(r * PART_PITCH + 4 * c4) * 4u;
+                float4 sum = tc::ld_cluster_v4(tc::map_shared_rank(off, 0));
+                for (uint32_t q = 1; q < nsplit; ++q) {
+                    const float4 v = tc::ld_cluster_v4(tc::map_shared_rank(off, q));
+                    sum.x += v.x;
+                    sum.y += v.y;
+                    sum.z += v.z;
+                    sum.w += v.w;
+                }
+                if (row >= p.m) continue;
+                float *crow = p.C + (long long)row * p.ldc;
+                const float a[4] = {sum.x, sum.y, sum.z, sum.w};
+                if (C_VEC && col + 3 < p.n) {
+                    float4 o;
+                    if (beta != 0.f) {
+                        const float4 c = *reinterpret_cast<const float4 *>(crow + col);
+                        o = make_float4(fmaf(alpha, a[0], beta * c.x), fmaf(alpha, a[1], beta * c.y),
+                                        fmaf(alpha, a[2], beta * c.z), fmaf(alpha, a[3], beta * c.w));
+                    } else {
+                        o = make_float4(alpha * a[0], alpha * a[1], alpha * a[2], alpha * a[3]);
+                    }
+                    *reinterpret_cast<float4 *>(crow + col) = o;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (col + e < p.n)
+                            crow[col + e] = beta != 0.f ? fmaf(alpha, a[e], beta * crow[col + e]) : alpha * a[e];
+                    }
+                }
+            }
+        }
+        // no CTA leaves while another may still read its partial
+        __syncwarp();
+        tc::cluster_sync();
+    }
     if (warp == 1) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, TMEM_COLS);

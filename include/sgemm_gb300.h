@@ -179,13 +179,14 @@ typedef struct sgemm_plan {
     int rm, rn;        /* per-thread register tile of C (FFMA path; 0 otherwise)               */
     int threads;       /* threads per CTA                                                      */
     int stages;        /* shared-memory pipeline depth                                         */
-    int grid;          /* CTAs launched                                                        */
+    int grid;          /* CTAs launched (tiles * split_k)                                      */
     int tiles;         /* output tiles = ceil(m/bm) * ceil(n/bn)                               */
     int k_tiles;       /* pipeline stages consumed per tile = ceil(k/bk)                       */
     int smem_bytes;    /* dynamic shared memory per CTA                                        */
     int b_vec;         /* 1: B loaded 16 bytes at a time / by TMA                              */
     int c_vec;         /* 1: C read and written 16 bytes at a time                             */
     int group_m;       /* tile rows per raster group (L2 reuse)                                */
+    int split_k;       /* CTAs sharing one tile along k (a thread-block cluster; 1 = no split) */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

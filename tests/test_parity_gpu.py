@@ -252,3 +252,43 @@ def test_device_status_clear_after_runs():
     flag = ctypes.c_int(-1)
     assert _native.load().sgemm_device_status(ctypes.byref(flag), 0) == 0
     assert flag.value == 0
+
+
+# ---------------------------------------------------------------- split-K clusters
+
+@pytest.mark.parametrize("m,n,k,beta", [
+    (256, 256, 8192, 0.0), (300, 700, 5000, 0.75), (129, 257, 4096, -1.0), (1000, 1500, 777, 0.5),
+    (64, 64, 65536, 0.0), (400, 300, 3000, 2.0),
+])
+def test_split_k_clusters(m, n, k, beta):
+    """Problems with few tiles split k over a cluster of CTAs that reduce
+    their partial tiles through distributed shared memory."""
+    st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3)
+    assert st == 0 and plan["split_k"] > 1, plan
+    p = inputs.make_problem(m, n, k, alpha=1.25, beta=beta, seed=m + n + k, a="normal", b="uniform",
+                            c="uniform" if beta else None)
+    run_and_check(p, binding.PATH_TF32X3)
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 256, 8192), (300, 700, 5000), (1000, 1500, 777)])
+def test_split_k_integer_twin_bit_exact(m, n, k):
+    """Partial sums of integers are exact, so the split result is too."""
+    st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3)
+    assert st == 0 and plan["split_k"] > 1
+    p = inputs.make_problem(m, n, k, alpha=2.0, beta=0.5, seed=7 * k, a="int", b="int", c="int")
+    run_and_check(p, binding.PATH_TF32X3, exact=True)
+
+
+def test_split_k_is_deterministic():
+    """The cluster reduction adds partials in a fixed order: repeated calls
+    give identical bits."""
+    p = inputs.make_problem(300, 700, 5000, alpha=1.0, beta=0.0, seed=99, a="normal", b="normal")
+    A = torch.from_numpy(p.A).cuda()
+    B = torch.from_numpy(p.B).cuda()
+    outs = []
+    for _ in range(3):
+        C = torch.zeros(p.m, p.n, device="cuda")
+        binding.sgemm_ex(A, B, C, 1.0, 0.0, path=binding.PATH_TF32X3)
+        outs.append(C)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
