@@ -92,7 +92,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 # Exported symbols, in the order the header declares them.
-EXPORTS = ["sgemm", "sgemm_ex", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", "sgemm_tf32x3_split_gemm",
+EXPORTS = ["sgemm", "sgemm_ex", "sgemm_op", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", "sgemm_tf32x3_split_gemm",
            "sgemm_tf32x3_noalloc", "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_plan_for", "sgemm_device_status",
            "sgemm_version"]
 
@@ -100,7 +100,7 @@ EXPORTS = ["sgemm", "sgemm_ex", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", 
 class Plan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "path", "kernel", "bm", "bn", "bk", "rm", "rn", "threads", "stages", "grid", "tiles",
-        "k_tiles", "smem_bytes", "b_vec", "c_vec", "group_m", "split_k")]
+        "k_tiles", "smem_bytes", "b_vec", "c_vec", "group_m", "split_k", "op_a", "op_b", "a_vec")]
 
 
 def _declare(lib):
@@ -110,6 +110,8 @@ def _declare(lib):
     lib.sgemm.restype = i
     lib.sgemm_ex.argtypes = gemm + [i]
     lib.sgemm_ex.restype = i
+    lib.sgemm_op.argtypes = [i, i] + gemm + [i]
+    lib.sgemm_op.restype = i
     lib.sgemm_tf32x3_split_a.argtypes = [i, i, vp, i, vp, vp, vp]
     lib.sgemm_tf32x3_split_a.restype = i
     lib.sgemm_tf32x3_split_b.argtypes = [i, i, vp, i, vp, vp, vp]

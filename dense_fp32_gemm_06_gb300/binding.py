@@ -141,3 +141,51 @@ def tf32x3_noalloc_raw(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc,
         int(m), int(n), int(k), ctypes.c_float(alpha), ctypes.c_void_p(A_ptr or None), int(lda),
         ctypes.c_void_p(B_ptr or None), int(ldb), ctypes.c_float(beta), ctypes.c_void_p(C_ptr or None), int(ldc),
         ctypes.c_void_p(stream or None))
+
+
+OP_N = 0
+OP_T = 1
+
+
+def sgemm_op_raw(op_a, op_b, m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, stream=0,
+                 path=PATH_AUTO) -> int:
+    """C = alpha * op(A) @ op(B) + beta * C on raw device pointers (op_a /
+    op_b = OP_N or OP_T, every matrix row-major); returns the status."""
+    return _native.load().sgemm_op(
+        int(op_a), int(op_b), int(m), int(n), int(k), ctypes.c_float(alpha), ctypes.c_void_p(A_ptr or None),
+        int(lda), ctypes.c_void_p(B_ptr or None), int(ldb), ctypes.c_float(beta), ctypes.c_void_p(C_ptr or None),
+        int(ldc), ctypes.c_void_p(stream or None), int(path))
+
+
+def _as_op(t, name):
+    """(op, ld) for a 2-D float32 CUDA tensor: a row-major tensor is used as
+    is (OP_N), a transposed view of a row-major tensor (unit stride on the
+    first axis) reads the underlying matrix transposed (OP_T)."""
+    import torch
+    if t.dtype != torch.float32 or not t.is_cuda or t.dim() != 2:
+        raise SgemmError(-1, f"{name} must be a 2-D float32 CUDA tensor")
+    rows, cols = t.shape
+    if cols <= 1 or t.stride(1) == 1:
+        return OP_N, max(t.stride(0) if rows > 1 else cols, cols, 1)
+    if rows <= 1 or t.stride(0) == 1:
+        return OP_T, max(t.stride(1) if cols > 1 else rows, rows, 1)
+    raise SgemmError(-1, f"{name} must be row-major or a transposed view of a row-major tensor")
+
+
+def matmul(A, B, C, alpha=1.0, beta=0.0, *, path=PATH_AUTO, stream=None):
+    """C = alpha * A @ B + beta * C, where A and B may each be row-major or a
+    transposed view (``X.t()``) of a row-major tensor; C must be row-major."""
+    import torch
+    m, k = A.shape
+    k2, n = B.shape
+    if k2 != k or tuple(C.shape) != (m, n):
+        raise SgemmError(-1, f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    op_a, lda = _as_op(A, "A")
+    op_b, ldb = _as_op(B, "B")
+    ldc = max(_row_major(C, "C"), n, 1)
+    if stream is None:
+        stream = torch.cuda.current_stream(C.device).cuda_stream
+    with torch.cuda.device(C.device):
+        _check(sgemm_op_raw(op_a, op_b, m, n, k, alpha, A.data_ptr(), lda, B.data_ptr(), ldb, beta, C.data_ptr(),
+                            ldc, stream, path))
+    return C

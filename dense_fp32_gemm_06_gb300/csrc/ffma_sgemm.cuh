@@ -12,16 +12,18 @@
 //    "GPU 访存与计算优化", section 数据搬运与计算流水线): a slab is waited for
 //    before use, and a buffer is refilled only after the barrier that proves
 //    every warp has finished reading it;
-//  * A is scattered into shared memory transposed, as [BK][BM+4], by 4-byte
-//    copies: each warp copies a 4-row x 8-column patch (four full 32-byte
-//    sectors of global memory) and, because the row pitch BM+4 is 4 banks
-//    past a multiple of 32, its 32 stores land in 32 different banks.  The
-//    same 4-byte copies serve any lda and any alignment and zero-fill the m
-//    and k tails (out-of-range inputs are zero and every thread reaches every
-//    barrier: aerisun.top, section "Shared Tiling 与 block 内复用");
-//  * B is copied row by row as [BK][BN], 16 bytes per copy when its rows
-//    are 16-byte aligned, else 4 bytes; partial 16-byte copies zero-fill the
-//    n tail;
+//  * both operands land in shared memory k-major, as [BK][rows]: the rows
+//    of C for A, the columns of C for B.  An operand stored with k
+//    contiguous (A untransposed, B transposed) is scattered there by 4-byte
+//    copies (ScatterLoader): each warp copies a 4-row x 8-column patch (four
+//    full 32-byte sectors of global memory) and, because the row pitch is 4
+//    banks past a multiple of 32, its 32 stores land in 32 different banks.
+//    An operand stored with its rows contiguous (A transposed, B
+//    untransposed) is copied row by row (DirectLoader), 16 bytes per copy
+//    when its rows are 16-byte aligned, else 4 bytes.  Both serve any leading
+//    dimension and alignment and zero-fill the tails (out-of-range inputs
+//    are zero and every thread reaches every barrier: aerisun.top, section
+//    "Shared Tiling 与 block 内复用");
 //  * each thread accumulates a TM x TN register tile made of 4 x 4 blocks:
 //    rows a_off + 32g + {0..3}, columns b_off + 16h + {0..3}.  Every fragment
 //    read is one 16-byte shared load (LDS.128), and a warp (8 x 4 lanes) reads
@@ -52,6 +54,7 @@ struct GemmArgs {
     long long ldc;
     int tiles_m, tiles_n;
     int group_m;
+    int c_vec;   // C rows 16-byte aligned: float4 epilogue
 };
 
 namespace ffma {
@@ -66,124 +69,149 @@ struct Config {
     static constexpr int WARPS_N = BN / WARP_N;
     static constexpr int WARPS = WARPS_M * WARPS_N;
     static constexpr int THREADS = 32 * WARPS;
-    static constexpr int A_LD = BM + 4;              // floats per k-row of the transposed A slab
-    static constexpr int A_STAGE = BK * A_LD;        // floats
-    static constexpr int B_STAGE = BK * BN;          // floats
-    static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
-    static constexpr int A_CHUNKS = (BM / 4) * (BK / 8);   // 32-element patches per slab
-    static constexpr int A_PER_WARP = A_CHUNKS / WARPS;
-    static constexpr int B_VEC_PER_THREAD = BK * BN / 4 / THREADS;
-    static constexpr int B_SCALAR_PER_THREAD = BK * BN / THREADS;
 
     static_assert(TM % 4 == 0 && TN % 4 == 0, "register tile is made of 4 x 4 blocks");
     static_assert(BM % WARP_M == 0 && BN % WARP_N == 0, "warps tile the CTA tile");
-    static_assert(BK % 8 == 0 && BM % 4 == 0, "A patches are 4 rows x 8 columns");
-    static_assert(A_CHUNKS % WARPS == 0, "A patches split evenly over warps");
-    static_assert((BK * BN / 4) % THREADS == 0, "B float4s split evenly over threads");
-    static_assert((A_LD % 32) == 4, "A pitch must sit 4 banks past a multiple of 32");
-    static_assert((A_LD * 4) % 16 == 0, "A rows must keep 16-byte fragment alignment");
     static_assert(STAGES >= 2, "at least double buffering");
 };
 
-// Per-thread state of the slab loader.  Every address a thread copies from
-// is fixed up to the slab offset k0, so it is computed once: the A rows of a
-// thread are A_ROW_STEP apart, its B rows B_ROW_STEP apart.  Interior slabs
-// (the whole BM x BK / BK x BN box inside the matrices) take copies with no
-// predicate; edge slabs test every element and zero-fill.
-template <class Cfg, bool B_VEC>
-struct SlabLoader {
-    static constexpr int A_ROW_STEP = (Cfg::WARPS / (Cfg::BK / 8)) * 4;
-    static constexpr int B_ROWS_PER_PASS = B_VEC ? Cfg::THREADS / (Cfg::BN / 4) : Cfg::THREADS / Cfg::BN;
-    static_assert(Cfg::WARPS % (Cfg::BK / 8) == 0, "A patches of one thread share a column");
+// An operand seen as a `rows` x k matrix (rows of C for A, columns of C for B).
+struct Operand {
+    const float *ptr;
+    long long ld;
+    int rows, k;
+};
 
-    const float *a_src;      // A + (m0 + row0) * lda + kc   (row clamped into the matrix)
-    const float *b_src;      // B + brow0 * ldb + n0 + bcol  (clamped)
-    uint32_t a_dst, b_dst;   // shared byte offsets inside a stage
-    int a_row0, a_kc, b_row0, b_col;
-    long long a_step, b_step;   // A_ROW_STEP * lda, B_ROWS_PER_PASS * ldb (elements)
-    bool interior_mn;
+// Operand stored with k contiguous -- element (r, t) at ptr[r*ld + t] --
+// scattered into the k-major slab [BK][R+4] by 4-byte copies: warp w copies
+// 4-row x 8-column patches, one element per lane, so that global reads are
+// four full 32-byte sectors and the 32 shared stores hit 32 banks (the pitch
+// R+4 is 4 banks past a multiple of 32).  A thread's copies share one column
+// and step ROW_STEP rows.  Interior slabs (R x BK box inside the operand)
+// copy without predicates; edge slabs test each element and zero-fill.
+template <int R, int BK, int THREADS>
+struct ScatterLoader {
+    static constexpr int WARPS = THREADS / 32;
+    static constexpr int LD = R + 4;
+    static constexpr int CHUNKS = (R / 4) * (BK / 8);       // 32-element patches per slab
+    static constexpr int PER_THREAD = CHUNKS / WARPS;
+    static constexpr int ROW_STEP = (WARPS / (BK / 8)) * 4;
+    static_assert(BK % 8 == 0 && R % 4 == 0, "patches are 4 rows x 8 columns");
+    static_assert(CHUNKS % WARPS == 0 && WARPS % (BK / 8) == 0, "patches split evenly, one column per thread");
+    static_assert((LD % 32) == 4 && (LD * 4) % 16 == 0, "conflict-free scatter, 16-byte fragment rows");
 
-    __device__ __forceinline__ SlabLoader(const GemmArgs &p, int m0, int n0, int tid) {
+    const float *src;   // element (r_base + row0, kc), row clamped into the operand
+    long long step;     // ROW_STEP rows
+    uint32_t dst;       // byte offset in the slab
+    int row0, kc;
+    bool interior_r;
+
+    __device__ __forceinline__ ScatterLoader(const Operand &o, int r_base, int tid) {
         const int warp = tid >> 5, lane = tid & 31;
-        a_row0 = (warp / (Cfg::BK / 8)) * 4 + (lane >> 3);
-        a_kc = (warp % (Cfg::BK / 8)) * 8 + (lane & 7);
-        const int ar = min(m0 + a_row0, p.m - 1);
-        a_src = p.A + (long long)ar * p.lda + a_kc;
-        a_step = (long long)A_ROW_STEP * p.lda;
-        a_dst = (uint32_t)(a_kc * Cfg::A_LD + a_row0) * 4u;
-        if constexpr (B_VEC) {
-            b_row0 = tid / (Cfg::BN / 4);
-            b_col = (tid % (Cfg::BN / 4)) * 4;
-        } else {
-            b_row0 = tid / Cfg::BN;
-            b_col = tid % Cfg::BN;
-        }
-        b_src = p.B + (long long)b_row0 * p.ldb + min(n0 + b_col, p.n - 1);
-        b_step = (long long)B_ROWS_PER_PASS * p.ldb;
-        b_dst = (uint32_t)(b_row0 * Cfg::BN + b_col) * 4u;
-        interior_mn = m0 + Cfg::BM <= p.m && n0 + Cfg::BN <= p.n;
+        row0 = (warp / (BK / 8)) * 4 + (lane >> 3);
+        kc = (warp % (BK / 8)) * 8 + (lane & 7);
+        src = o.ptr + (long long)min(r_base + row0, o.rows - 1) * o.ld + kc;
+        step = (long long)ROW_STEP * o.ld;
+        dst = (uint32_t)(kc * LD + row0) * 4u;
+        interior_r = r_base + R <= o.rows;
     }
 
-    __device__ __forceinline__ void load(const GemmArgs &p, uint32_t As, uint32_t Bs, int m0, int n0, int k0) const {
-        if (interior_mn && k0 + Cfg::BK <= p.k) {
-            const float *a = a_src + k0;
+    __device__ __forceinline__ void load(const Operand &o, uint32_t slab, int r_base, int k0) const {
+        if (interior_r && k0 + BK <= o.k) {
+            const float *a = src + k0;
 #pragma unroll
-            for (int j = 0; j < Cfg::A_PER_WARP; ++j, a += a_step)
-                cp_async_4(As + a_dst + j * A_ROW_STEP * 4, a, 4u);
-            const float *b = b_src + (long long)k0 * p.ldb;
-            if constexpr (B_VEC) {
-#pragma unroll
-                for (int j = 0; j < Cfg::B_VEC_PER_THREAD; ++j, b += b_step)
-                    cp_async_16(Bs + b_dst + j * B_ROWS_PER_PASS * Cfg::BN * 4, b, 16u);
-            } else {
-#pragma unroll
-                for (int j = 0; j < Cfg::B_SCALAR_PER_THREAD; ++j, b += b_step)
-                    cp_async_4(Bs + b_dst + j * B_ROWS_PER_PASS * Cfg::BN * 4, b, 4u);
-            }
+            for (int j = 0; j < PER_THREAD; ++j, a += step) cp_async_4(slab + dst + j * ROW_STEP * 4, a, 4u);
             return;
         }
-        // edge slab: predicate every copy, zero-fill what lies outside
-        {
-            const bool k_ok = k0 + a_kc < p.k;
-            const float *a = a_src + (k_ok ? k0 : 0);
+        const bool k_ok = k0 + kc < o.k;
+        const float *a = src + (k_ok ? k0 : 0);
 #pragma unroll
-            for (int j = 0; j < Cfg::A_PER_WARP; ++j) {
-                const bool ok = k_ok && m0 + a_row0 + j * A_ROW_STEP < p.m;
-                cp_async_4(As + a_dst + j * A_ROW_STEP * 4, ok ? a + j * a_step : p.A, ok ? 4u : 0u);
-            }
-        }
-        if constexpr (B_VEC) {
-            const int left = p.n - (n0 + b_col);
-            const uint32_t bytes = left >= 4 ? 16u : (left > 0 ? 4u * left : 0u);
-#pragma unroll
-            for (int j = 0; j < Cfg::B_VEC_PER_THREAD; ++j) {
-                const int kr = k0 + b_row0 + j * B_ROWS_PER_PASS;
-                const uint32_t nb = kr < p.k ? bytes : 0u;
-                cp_async_16(Bs + b_dst + j * B_ROWS_PER_PASS * Cfg::BN * 4,
-                            nb ? b_src + (long long)(k0 + j * B_ROWS_PER_PASS) * p.ldb : p.B, nb);
-            }
-        } else {
-            const bool n_ok = n0 + b_col < p.n;
-#pragma unroll
-            for (int j = 0; j < Cfg::B_SCALAR_PER_THREAD; ++j) {
-                const int kr = k0 + b_row0 + j * B_ROWS_PER_PASS;
-                const bool ok = n_ok && kr < p.k;
-                cp_async_4(Bs + b_dst + j * B_ROWS_PER_PASS * Cfg::BN * 4,
-                           ok ? b_src + (long long)(k0 + j * B_ROWS_PER_PASS) * p.ldb : p.B, ok ? 4u : 0u);
-            }
+        for (int j = 0; j < PER_THREAD; ++j) {
+            const bool ok = k_ok && r_base + row0 + j * ROW_STEP < o.rows;
+            cp_async_4(slab + dst + j * ROW_STEP * 4, ok ? a + j * step : o.ptr, ok ? 4u : 0u);
         }
     }
 };
 
-template <class Cfg, bool B_VEC, bool C_VEC>
+// Operand stored with its rows contiguous -- element (r, t) at
+// ptr[t*ld + r] -- copied row by row into the slab [BK][R], 16 bytes per
+// copy when VEC (base and ld 16-byte aligned), else 4 bytes; a partial
+// 16-byte copy zero-fills the row tail.
+template <int R, int BK, int THREADS, bool VEC>
+struct DirectLoader {
+    static constexpr int LD = R;
+    static constexpr int W = VEC ? 4 : 1;                    // floats per copy
+    static constexpr int PER_ROW = R / W;
+    static constexpr int PER_THREAD = BK * PER_ROW / THREADS;
+    static constexpr int ROWS_PER_PASS = THREADS / PER_ROW;
+    static_assert(THREADS % PER_ROW == 0 && (BK * PER_ROW) % THREADS == 0, "copies split evenly");
+    static_assert((LD * 4) % 16 == 0, "16-byte fragment rows");
+
+    const float *src;   // element (r_base + c, kk0), column clamped into the operand
+    long long step;     // ROWS_PER_PASS k-rows
+    uint32_t dst;
+    int kk0, c;
+    bool interior_r;
+
+    __device__ __forceinline__ DirectLoader(const Operand &o, int r_base, int tid) {
+        kk0 = tid / PER_ROW;
+        c = (tid % PER_ROW) * W;
+        src = o.ptr + (long long)kk0 * o.ld + min(r_base + c, o.rows - 1);
+        step = (long long)ROWS_PER_PASS * o.ld;
+        dst = (uint32_t)(kk0 * LD + c) * 4u;
+        interior_r = r_base + R <= o.rows;
+    }
+
+    __device__ __forceinline__ void load(const Operand &o, uint32_t slab, int r_base, int k0) const {
+        if (interior_r && k0 + BK <= o.k) {
+            const float *b = src + (long long)k0 * o.ld;
+#pragma unroll
+            for (int j = 0; j < PER_THREAD; ++j, b += step) {
+                if constexpr (VEC)
+                    cp_async_16(slab + dst + j * ROWS_PER_PASS * LD * 4, b, 16u);
+                else
+                    cp_async_4(slab + dst + j * ROWS_PER_PASS * LD * 4, b, 4u);
+            }
+            return;
+        }
+        uint32_t bytes;
+        if constexpr (VEC) {
+            const int left = o.rows - (r_base + c);
+            bytes = left >= 4 ? 16u : (left > 0 ? 4u * left : 0u);
+        } else {
+            bytes = r_base + c < o.rows ? 4u : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < PER_THREAD; ++j) {
+            const int kr = k0 + kk0 + j * ROWS_PER_PASS;
+            const uint32_t nb = kr < o.k ? bytes : 0u;
+            const float *b = nb ? src + (long long)(k0 + j * ROWS_PER_PASS) * o.ld : o.ptr;
+            if constexpr (VEC)
+                cp_async_16(slab + dst + j * ROWS_PER_PASS * LD * 4, b, nb);
+            else
+                cp_async_4(slab + dst + j * ROWS_PER_PASS * LD * 4, b, nb);
+        }
+    }
+};
+
+// Shared-memory sizes of a kernel instance.
+template <class Cfg, class AL, class BL>
+struct Layout {
+    static constexpr int A_STAGE = Cfg::BK * AL::LD;   // floats
+    static constexpr int B_STAGE = Cfg::BK * BL::LD;
+    static constexpr int SMEM_BYTES = Cfg::STAGES * (A_STAGE + B_STAGE) * 4;
+};
+
+template <class Cfg, class AL, class BL>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kernel(const GemmArgs p) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
-    constexpr int TM = Cfg::TM, TN = Cfg::TN, A_LD = Cfg::A_LD;
+    constexpr int TM = Cfg::TM, TN = Cfg::TN, A_LD = AL::LD, B_LD = BL::LD;
+    constexpr int A_STAGE = Layout<Cfg, AL, BL>::A_STAGE, B_STAGE = Layout<Cfg, AL, BL>::B_STAGE;
     constexpr int GM = TM / 4, GN = TN / 4;   // 4 x 4 blocks per thread
 
     extern __shared__ __align__(16) float smem[];
-    float *const As = smem;                            // [STAGES][BK][A_LD]
-    float *const Bs = smem + STAGES * Cfg::A_STAGE;    // [STAGES][BK][BN]
+    float *const As = smem;                      // [STAGES][BK][A_LD]
+    float *const Bs = smem + STAGES * A_STAGE;   // [STAGES][BK][B_LD]
 
     const int tid = threadIdx.x;
     int tm, tn;
@@ -195,13 +223,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
     const int a_off = (warp / Cfg::WARPS_N) * Cfg::WARP_M + (lane >> 2) * 4;
     const int b_off = (warp % Cfg::WARPS_N) * Cfg::WARP_N + (lane & 3) * 4;
 
-    const SlabLoader<Cfg, B_VEC> loader(p, m0, n0, tid);
+    const Operand oa{p.A, p.lda, p.m, p.k}, ob{p.B, p.ldb, p.n, p.k};
+    const AL la(oa, m0, tid);
+    const BL lb(ob, n0, tid);
     const uint32_t As_u32 = smem_u32(As), Bs_u32 = smem_u32(Bs);
 
     // prologue: slabs 0 .. STAGES-2 in flight
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
-        if (s < KT) loader.load(p, As_u32 + s * Cfg::A_STAGE * 4, Bs_u32 + s * Cfg::B_STAGE * 4, m0, n0, s * BK);
+        if (s < KT) {
+            la.load(oa, As_u32 + s * A_STAGE * 4, m0, s * BK);
+            lb.load(ob, Bs_u32 + s * B_STAGE * 4, n0, s * BK);
+        }
         cp_async_commit();
     }
 
@@ -218,13 +251,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
             const int nk = kt + STAGES - 1;
             if (nk < KT) {
                 const int s = nk % STAGES;
-                loader.load(p, As_u32 + s * Cfg::A_STAGE * 4, Bs_u32 + s * Cfg::B_STAGE * 4, m0, n0, nk * BK);
+                la.load(oa, As_u32 + s * A_STAGE * 4, m0, nk * BK);
+                lb.load(ob, Bs_u32 + s * B_STAGE * 4, n0, nk * BK);
             }
             cp_async_commit();
         }
         const int s = kt % STAGES;
-        const float *as = As + s * Cfg::A_STAGE + a_off;
-        const float *bs = Bs + s * Cfg::B_STAGE + b_off;
+        const float *as = As + s * A_STAGE + a_off;
+        const float *bs = Bs + s * B_STAGE + b_off;
 
         float4 fa[2][GM], fb[2][GN];
 #pragma unroll
@@ -241,7 +275,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
                     fa[nxt][g] = *reinterpret_cast<const float4 *>(as + (kk + 1) * A_LD + 32 * g);
 #pragma unroll
                 for (int h = 0; h < GN; ++h)
-                    fb[nxt][h] = *reinterpret_cast<const float4 *>(bs + (kk + 1) * BN + 16 * h);
+                    fb[nxt][h] = *reinterpret_cast<const float4 *>(bs + (kk + 1) * B_LD + 16 * h);
             }
             float a[TM], b[TN];
 #pragma unroll
@@ -277,7 +311,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
         for (int h = 0; h < GN; ++h) {
             const int col = n0 + b_off + 16 * h;
             const float *v = &acc[i][4 * h];
-            if (C_VEC && col + 3 < p.n) {
+            if (p.c_vec && col + 3 < p.n) {
                 float4 o;
                 if (beta != 0.f) {
                     const float4 c = *reinterpret_cast<const float4 *>(crow + col);

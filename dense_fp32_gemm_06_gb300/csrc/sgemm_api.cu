@@ -43,10 +43,41 @@ int fail_cuda(cudaError_t e) {
     return SGEMM_STATUS_CUDA_ERROR;
 }
 
-template <bool BV, bool CV>
+// FFMA operand loaders by storage: k contiguous -> ScatterLoader; rows
+// contiguous -> DirectLoader with 16-byte (rows 16-byte aligned) or 4-byte
+// copies.  Loader kinds: 0 scatter, 1 direct 16-byte, 2 direct 4-byte.
+using FCfg = ffma::Default;
+using ALoadScatter = ffma::ScatterLoader<FCfg::BM, FCfg::BK, FCfg::THREADS>;
+using ALoadVec = ffma::DirectLoader<FCfg::BM, FCfg::BK, FCfg::THREADS, true>;
+using ALoadScalar = ffma::DirectLoader<FCfg::BM, FCfg::BK, FCfg::THREADS, false>;
+using BLoadScatter = ffma::ScatterLoader<FCfg::BN, FCfg::BK, FCfg::THREADS>;
+using BLoadVec = ffma::DirectLoader<FCfg::BN, FCfg::BK, FCfg::THREADS, true>;
+using BLoadScalar = ffma::DirectLoader<FCfg::BN, FCfg::BK, FCfg::THREADS, false>;
+
+template <class AL, class BL>
 cudaError_t set_ffma_attr() {
-    return cudaFuncSetAttribute(ffma::ffma_sgemm_kernel<ffma::Default, BV, CV>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, ffma::Default::SMEM_BYTES);
+    return cudaFuncSetAttribute(ffma::ffma_sgemm_kernel<FCfg, AL, BL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                ffma::Layout<FCfg, AL, BL>::SMEM_BYTES);
+}
+
+template <class AL>
+cudaError_t set_ffma_attr_all_b() {
+    cudaError_t e = set_ffma_attr<AL, BLoadScatter>();
+    if (e == cudaSuccess) e = set_ffma_attr<AL, BLoadVec>();
+    if (e == cudaSuccess) e = set_ffma_attr<AL, BLoadScalar>();
+    return e;
+}
+
+template <class AL>
+int ffma_smem_b(int bkind) {
+    return bkind == 0 ? ffma::Layout<FCfg, AL, BLoadScatter>::SMEM_BYTES
+                      : bkind == 1 ? ffma::Layout<FCfg, AL, BLoadVec>::SMEM_BYTES
+                                   : ffma::Layout<FCfg, AL, BLoadScalar>::SMEM_BYTES;
+}
+
+int ffma_smem_bytes(int akind, int bkind) {
+    return akind == 0 ? ffma_smem_b<ALoadScatter>(bkind)
+                      : akind == 1 ? ffma_smem_b<ALoadVec>(bkind) : ffma_smem_b<ALoadScalar>(bkind);
 }
 
 template <class Cfg, bool CV>
@@ -85,10 +116,9 @@ int device_state(DeviceState **out) {
     if (!d.ready) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr<true, true>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr<true, false>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr<false, true>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr<false, false>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_ffma_attr_all_b<ALoadScatter>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_ffma_attr_all_b<ALoadVec>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_ffma_attr_all_b<ALoadScalar>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Wide, true>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Wide, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Narrow, true>()) != cudaSuccess) return fail_cuda(e);
@@ -117,16 +147,18 @@ int imax(int a, int b) { return a > b ? a : b; }
 
 // BLAS-style argument check; returns the 1-based position of the first bad
 // argument, or 0.
+// op_a / op_b: SGEMM_OP_N (A stored m x k, B stored k x n) or SGEMM_OP_T
+// (A stored k x m, B stored n x k); positions are those of sgemm().
 int check_args(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb,
-               const float *C, int ldc) {
+               const float *C, int ldc, int op_a = SGEMM_OP_N, int op_b = SGEMM_OP_N) {
     if (m < 0) return 1;
     if (n < 0) return 2;
     if (k < 0) return 3;
     const bool need_ab = (long long)m * n * k > 0 && alpha != 0.f;
     if (need_ab && (A == nullptr || !aligned(A, 4))) return 5;
-    if (lda < imax(1, k)) return 6;
+    if (lda < imax(1, op_a == SGEMM_OP_N ? k : m)) return 6;
     if (need_ab && (B == nullptr || !aligned(B, 4))) return 7;
-    if (ldb < imax(1, n)) return 8;
+    if (ldb < imax(1, op_b == SGEMM_OP_N ? n : k)) return 8;
     if ((long long)m * n > 0 && (C == nullptr || !aligned(C, 4))) return 10;
     if (ldc < imax(1, n)) return 11;
     return 0;
@@ -135,14 +167,17 @@ int check_args(int m, int n, int k, float alpha, const float *A, int lda, const 
 // max_clusters: the device's cluster capacity table (DeviceState), or NULL
 // for a host-only plan, which assumes 8 GPCs of num_sms / 8 SMs.
 int plan(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
-         const float *C, int ldc, int path, int num_sms, sgemm_plan *pl, const int (*max_clusters)[9] = nullptr) {
+         const float *C, int ldc, int path, int num_sms, sgemm_plan *pl, const int (*max_clusters)[9] = nullptr,
+         int op_a = SGEMM_OP_N, int op_b = SGEMM_OP_N) {
     (void)beta;
     std::memset(pl, 0, sizeof(*pl));
     if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
         return SGEMM_STATUS_BAD_PATH;
-    if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc)) return bad;
+    if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc, op_a, op_b)) return bad;
     if (m == 0 || n == 0) return SGEMM_STATUS_OK;
     if (num_sms <= 0) num_sms = 1;
+    pl->op_a = op_a;
+    pl->op_b = op_b;
     // AUTO: the tensor-core path for every problem with enough work to fill
     // the GPU (it is ~5x the FFMA rate at 2048^3 and beyond) and for long k
     // (its chunked accumulation holds the bound where a plain sequential
@@ -235,8 +270,11 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
     pl->rn = ffma::Default::TN;
     pl->threads = ffma::Default::THREADS;
     pl->stages = ffma::Default::STAGES;
-    pl->smem_bytes = ffma::Default::SMEM_BYTES;
-    pl->b_vec = aligned(B, 16) && (ldb % 4) == 0;
+    // rows-contiguous operands take 16-byte copies when their rows are 16-byte aligned
+    pl->a_vec = op_a == SGEMM_OP_T && aligned(A, 16) && (lda % 4) == 0;
+    pl->b_vec = op_b == SGEMM_OP_N && aligned(B, 16) && (ldb % 4) == 0;
+    pl->smem_bytes = ffma_smem_bytes(op_a == SGEMM_OP_N ? 0 : (pl->a_vec ? 1 : 2),
+                                     op_b == SGEMM_OP_T ? 0 : (pl->b_vec ? 1 : 2));
     const int tiles_m = (m + pl->bm - 1) / pl->bm;
     const int tiles_n = (n + pl->bn - 1) / pl->bn;
     pl->tiles = tiles_m * tiles_n;
@@ -354,8 +392,12 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
     cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), 2 * (a_elems + b_elems) * sizeof(float), stream);
     if (e != cudaSuccess) return fail_cuda(e);
     float *a_hi = ws, *a_lo = ws + a_elems, *b_hi = a_lo + a_elems, *b_lo = b_hi + b_elems;
-    launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
-    launch_split_b(k, n, B, ldb, b_hi, b_lo, stream);
+    // both split operands are k-contiguous (K-major): an operand stored with
+    // k contiguous is split in place order, one stored k-major is transposed
+    if (pl.op_a == SGEMM_OP_N) launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
+    else launch_split_b(k, m, A, lda, a_hi, a_lo, stream);
+    if (pl.op_b == SGEMM_OP_N) launch_split_b(k, n, B, ldb, b_hi, b_lo, stream);
+    else launch_split_a(n, k, B, ldb, b_hi, b_lo, stream);
     const int st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream);
     e = cudaFreeAsync(ws, stream);
     if (st) return st;
@@ -392,26 +434,43 @@ int noalloc_scratch(float **out) {
     return SGEMM_STATUS_OK;
 }
 
-template <bool BV, bool CV>
-void launch_ffma(const GemmArgs &a, const sgemm_plan &pl, cudaStream_t s) {
-    ffma::ffma_sgemm_kernel<ffma::Default, BV, CV><<<pl.grid, pl.threads, pl.smem_bytes, s>>>(a);
+template <class AL, class BL>
+void launch_ffma_t(const GemmArgs &a, int grid, cudaStream_t s) {
+    ffma::ffma_sgemm_kernel<FCfg, AL, BL><<<grid, FCfg::THREADS, ffma::Layout<FCfg, AL, BL>::SMEM_BYTES, s>>>(a);
+}
+
+template <class AL>
+void launch_ffma_b(int bkind, const GemmArgs &a, int grid, cudaStream_t s) {
+    if (bkind == 0) launch_ffma_t<AL, BLoadScatter>(a, grid, s);
+    else if (bkind == 1) launch_ffma_t<AL, BLoadVec>(a, grid, s);
+    else launch_ffma_t<AL, BLoadScalar>(a, grid, s);
+}
+
+void launch_ffma(const sgemm_plan &pl, const GemmArgs &a, cudaStream_t s) {
+    const int akind = pl.op_a == SGEMM_OP_N ? 0 : (pl.a_vec ? 1 : 2);
+    const int bkind = pl.op_b == SGEMM_OP_T ? 0 : (pl.b_vec ? 1 : 2);
+    if (akind == 0) launch_ffma_b<ALoadScatter>(bkind, a, pl.grid, s);
+    else if (akind == 1) launch_ffma_b<ALoadVec>(bkind, a, pl.grid, s);
+    else launch_ffma_b<ALoadScalar>(bkind, a, pl.grid, s);
 }
 
 }  // namespace
 
 extern "C" {
 
-int sgemm_ex(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb,
-             float beta, float *C, int ldc, cudaStream_t stream, int path) {
+int sgemm_op(int op_a, int op_b, int m, int n, int k, float alpha, const float *A, int lda, const float *B,
+             int ldb, float beta, float *C, int ldc, cudaStream_t stream, int path) {
+    if (op_a != SGEMM_OP_N && op_a != SGEMM_OP_T) return 1;
+    if (op_b != SGEMM_OP_N && op_b != SGEMM_OP_T) return 2;
     if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
         return SGEMM_STATUS_BAD_PATH;
-    if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc)) return bad;
+    if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc, op_a, op_b)) return bad + 2;
     if (m == 0 || n == 0) return SGEMM_STATUS_OK;
     DeviceState *dev = nullptr;
     int st = device_state(&dev);
     if (st != SGEMM_STATUS_OK) return st;
     sgemm_plan pl;
-    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, dev->sms, &pl, dev->max_clusters);
+    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, dev->sms, &pl, dev->max_clusters, op_a, op_b);
     if (st != SGEMM_STATUS_OK) return st;
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
@@ -433,17 +492,18 @@ int sgemm_ex(int m, int n, int k, float alpha, const float *A, int lda, const fl
         a.tiles_m = (m + pl.bm - 1) / pl.bm;
         a.tiles_n = (n + pl.bn - 1) / pl.bn;
         a.group_m = pl.group_m;
-        if (pl.b_vec) {
-            if (pl.c_vec) launch_ffma<true, true>(a, pl, stream);
-            else launch_ffma<true, false>(a, pl, stream);
-        } else {
-            if (pl.c_vec) launch_ffma<false, true>(a, pl, stream);
-            else launch_ffma<false, false>(a, pl, stream);
-        }
+        a.c_vec = pl.c_vec;
+        launch_ffma(pl, a, stream);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail_cuda(e);
     return SGEMM_STATUS_OK;
+}
+
+int sgemm_ex(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb,
+             float beta, float *C, int ldc, cudaStream_t stream, int path) {
+    const int st = sgemm_op(SGEMM_OP_N, SGEMM_OP_N, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, stream, path);
+    return st >= 3 && st <= 13 ? st - 2 : st;   // sgemm()'s argument positions
 }
 
 int sgemm_tf32x3_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream) {

@@ -92,6 +92,25 @@ int sgemm_ex(int m, int n, int k, float alpha,
              float beta, float *C, int ldc, cudaStream_t stream, int path);
 
 /*
+ * sgemm_op -- C = alpha * op(A) * op(B) + beta * C, op(A) m x k, op(B) k x n,
+ * every matrix row-major.  The pages define only the untransposed product
+ * (hatrix.site "GEMM优化原理", section 问题定义); the transposed forms are the
+ * same sum over t with the operands read in the other order:
+ *   op_a == SGEMM_OP_N: A stored m x k, op(A)(i,t) = A[i*lda + t], lda >= max(1,k);
+ *   op_a == SGEMM_OP_T: A stored k x m, op(A)(i,t) = A[t*lda + i], lda >= max(1,m);
+ *   op_b == SGEMM_OP_N: B stored k x n, op(B)(t,j) = B[t*ldb + j], ldb >= max(1,n);
+ *   op_b == SGEMM_OP_T: B stored n x k, op(B)(t,j) = B[j*ldb + t], ldb >= max(1,k).
+ * (Column-major BLAS data maps onto this by C^T = op(B)^T op(A)^T.)
+ * Status positions count op_a as 1 and op_b as 2 (m is 3, ..., ldc 13).
+ */
+#define SGEMM_OP_N 0
+#define SGEMM_OP_T 1
+int sgemm_op(int op_a, int op_b, int m, int n, int k, float alpha,
+             const float *A, int lda, const float *B, int ldb,
+             float beta, float *C, int ldc, cudaStream_t stream, int path);
+
+
+/*
  * 3xTF32 split operands.  The pages describe only CUDA-core FFMA kernels;
  * the tensor-core path computes the same C = alpha*A*B + beta*C by writing
  * each FP32 operand x as two TF32 numbers, hi = tf32(x) and
@@ -187,6 +206,8 @@ typedef struct sgemm_plan {
     int c_vec;         /* 1: C read and written 16 bytes at a time                             */
     int group_m;       /* tile rows per raster group (L2 reuse)                                */
     int split_k;       /* CTAs sharing one tile along k (a thread-block cluster; 1 = no split) */
+    int op_a, op_b;    /* SGEMM_OP_N / SGEMM_OP_T of the problem planned                      */
+    int a_vec;         /* 1: A (stored k x m) loaded 16 bytes at a time (FFMA path)            */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

@@ -157,3 +157,13 @@ def test_auto_policy():
     st, p = binding.plan(2048, 2048, 2048, path=binding.PATH_TF32X3)
     assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"]) == (128, 256, 16, 320)
     assert p["grid"] == p["tiles"] == 16 * 8 and p["k_tiles"] == 128
+
+
+def test_op_argument_checks():
+    """sgemm_op rejects bad ops and leading dimensions before any CUDA call."""
+    assert binding.sgemm_op_raw(2, 0, 4, 4, 4, 1.0, 256, 4, 512, 4, 0.0, 1024, 4) == 1
+    assert binding.sgemm_op_raw(0, 5, 4, 4, 4, 1.0, 256, 4, 512, 4, 0.0, 1024, 4) == 2
+    # op(A) = A^T with A stored k x m: lda must cover m
+    assert binding.sgemm_op_raw(1, 0, 8, 4, 4, 1.0, 256, 4, 512, 4, 0.0, 1024, 4) == 8
+    # op(B) = B^T with B stored n x k: ldb must cover k
+    assert binding.sgemm_op_raw(0, 1, 4, 4, 8, 1.0, 256, 8, 512, 4, 0.0, 1024, 4) == 10
