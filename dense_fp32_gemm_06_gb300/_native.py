@@ -92,7 +92,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 
 # Exported symbols, in the order the header declares them.
-EXPORTS = ["sgemm", "sgemm_ex", "sgemm_op", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", "sgemm_tf32x3_split_gemm",
+EXPORTS = ["sgemm", "sgemm_ex", "sgemm_op", "sgemm_strided_batched", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", "sgemm_tf32x3_split_gemm",
            "sgemm_tf32x3_noalloc", "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_plan_for", "sgemm_device_status",
            "sgemm_version"]
 
@@ -112,6 +112,9 @@ def _declare(lib):
     lib.sgemm_ex.restype = i
     lib.sgemm_op.argtypes = [i, i] + gemm + [i]
     lib.sgemm_op.restype = i
+    ll = ctypes.c_longlong
+    lib.sgemm_strided_batched.argtypes = [i, i, i, i, i, f, vp, i, ll, vp, i, ll, f, vp, i, ll, i, vp, i]
+    lib.sgemm_strided_batched.restype = i
     lib.sgemm_tf32x3_split_a.argtypes = [i, i, vp, i, vp, vp, vp]
     lib.sgemm_tf32x3_split_a.restype = i
     lib.sgemm_tf32x3_split_b.argtypes = [i, i, vp, i, vp, vp, vp]

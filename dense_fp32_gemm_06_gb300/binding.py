@@ -189,3 +189,37 @@ def matmul(A, B, C, alpha=1.0, beta=0.0, *, path=PATH_AUTO, stream=None):
         _check(sgemm_op_raw(op_a, op_b, m, n, k, alpha, A.data_ptr(), lda, B.data_ptr(), ldb, beta, C.data_ptr(),
                             ldc, stream, path))
     return C
+
+
+def sgemm_strided_batched_raw(op_a, op_b, m, n, k, alpha, A_ptr, lda, stride_a, B_ptr, ldb, stride_b, beta, C_ptr,
+                              ldc, stride_c, batch, stream=0, path=PATH_AUTO) -> int:
+    """`batch` problems C_b = alpha * op(A_b) @ op(B_b) + beta * C_b with
+    A_b = A + b*stride_a (floats), and so on; returns the status."""
+    return _native.load().sgemm_strided_batched(
+        int(op_a), int(op_b), int(m), int(n), int(k), ctypes.c_float(alpha), ctypes.c_void_p(A_ptr or None),
+        int(lda), int(stride_a), ctypes.c_void_p(B_ptr or None), int(ldb), int(stride_b), ctypes.c_float(beta),
+        ctypes.c_void_p(C_ptr or None), int(ldc), int(stride_c), int(batch), ctypes.c_void_p(stream or None),
+        int(path))
+
+
+def bmm(A, B, C, alpha=1.0, beta=0.0, *, path=PATH_AUTO, stream=None):
+    """C[b] = alpha * A[b] @ B[b] + beta * C[b] for 3-D float32 CUDA tensors
+    whose last two axes are row-major (or, for A and B, transposed views of
+    row-major matrices) and whose first axis has a constant stride (0
+    broadcasts one matrix over the batch)."""
+    import torch
+    if A.dim() != 3 or B.dim() != 3 or C.dim() != 3:
+        raise SgemmError(-1, "bmm takes 3-D tensors")
+    batch, m, k = A.shape
+    _, k2, n = B.shape
+    if k2 != k or tuple(C.shape) != (batch, m, n) or B.shape[0] != batch:
+        raise SgemmError(-1, f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, C {tuple(C.shape)}")
+    op_a, lda = _as_op(A[0], "A")
+    op_b, ldb = _as_op(B[0], "B")
+    ldc = max(_row_major(C[0], "C"), n, 1)
+    if stream is None:
+        stream = torch.cuda.current_stream(C.device).cuda_stream
+    with torch.cuda.device(C.device):
+        _check(sgemm_strided_batched_raw(op_a, op_b, m, n, k, alpha, A.data_ptr(), lda, A.stride(0), B.data_ptr(),
+                                         ldb, B.stride(0), beta, C.data_ptr(), ldc, C.stride(0), batch, stream, path))
+    return C

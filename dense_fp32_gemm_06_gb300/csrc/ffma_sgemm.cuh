@@ -55,6 +55,8 @@ struct GemmArgs {
     int tiles_m, tiles_n;
     int group_m;
     int c_vec;   // C rows 16-byte aligned: float4 epilogue
+    // strided batch: problem blockIdx.y uses A + y*stride_a, B + y*stride_b, C + y*stride_c
+    long long stride_a, stride_b, stride_c;
 };
 
 namespace ffma {
@@ -223,7 +225,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
     const int a_off = (warp / Cfg::WARPS_N) * Cfg::WARP_M + (lane >> 2) * 4;
     const int b_off = (warp % Cfg::WARPS_N) * Cfg::WARP_N + (lane & 3) * 4;
 
-    const Operand oa{p.A, p.lda, p.m, p.k}, ob{p.B, p.ldb, p.n, p.k};
+    const long long bz = blockIdx.y;   // problem of a strided batch
+    const Operand oa{p.A + bz * p.stride_a, p.lda, p.m, p.k}, ob{p.B + bz * p.stride_b, p.ldb, p.n, p.k};
+    float *const Cb = p.C + bz * p.stride_c;
     const AL la(oa, m0, tid);
     const BL lb(ob, n0, tid);
     const uint32_t As_u32 = smem_u32(As), Bs_u32 = smem_u32(Bs);
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
     for (int i = 0; i < TM; ++i) {
         const int row = m0 + a_off + 32 * (i / 4) + (i % 4);
         if (row >= p.m) continue;
-        float *crow = p.C + (long long)row * p.ldc;
+        float *crow = Cb + (long long)row * p.ldc;
 #pragma unroll
         for (int h = 0; h < GN; ++h) {
             const int col = n0 + b_off + 16 * h;
@@ -338,8 +342,10 @@ using Default = Config<128, 128, 32, 3, 8, 8, 2>;
 
 }  // namespace ffma
 
-// C = beta * C over an m x n window (beta == 0 writes zeros without reading).
-__global__ void scale_c_kernel(float *C, long long ldc, int m, int n, float beta) {
+// C = beta * C over an m x n window (beta == 0 writes zeros without reading);
+// blockIdx.y selects the problem of a strided batch (C + y*stride_c).
+__global__ void scale_c_kernel(float *C, long long ldc, int m, int n, float beta, long long stride_c) {
+    C += blockIdx.y * stride_c;
     const long long total = (long long)m * n;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {

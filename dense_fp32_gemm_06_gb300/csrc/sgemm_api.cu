@@ -145,6 +145,12 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int imax(int a, int b) { return a > b ? a : b; }
 
+// A strided batch of problems: problem b uses A + b*sa, B + b*sb, C + b*sc.
+struct Batch {
+    int count = 1;
+    long long sa = 0, sb = 0, sc = 0;
+};
+
 // BLAS-style argument check; returns the 1-based position of the first bad
 // argument, or 0.
 // op_a / op_b: SGEMM_OP_N (A stored m x k, B stored k x n) or SGEMM_OP_T
@@ -168,7 +174,7 @@ int check_args(int m, int n, int k, float alpha, const float *A, int lda, const 
 // for a host-only plan, which assumes 8 GPCs of num_sms / 8 SMs.
 int plan(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
          const float *C, int ldc, int path, int num_sms, sgemm_plan *pl, const int (*max_clusters)[9] = nullptr,
-         int op_a = SGEMM_OP_N, int op_b = SGEMM_OP_N) {
+         int op_a = SGEMM_OP_N, int op_b = SGEMM_OP_N, int batch = 1) {
     (void)beta;
     std::memset(pl, 0, sizeof(*pl));
     if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
@@ -228,7 +234,7 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
             }
             const int wi = bn == tf32x3::Wide::BN ? 0 : 1;
             const long long slab = bn == tf32x3::Wide::BN ? 4 : 3;
-            const long long tiles = (long long)tiles_m * ((n + bn - 1) / bn);
+            const long long tiles = (long long)tiles_m * ((n + bn - 1) / bn) * (batch > 0 ? batch : 1);
             for (int S = 1; S <= 8; ++S) {
                 if (force_s >= 1 && force_s <= 8) {
                     if (S != force_s) continue;
@@ -306,8 +312,9 @@ int ka_of(int k) { return (k + 3) & ~3; }
 // looping over its share (they are HBM-bound).
 constexpr int kSplitBlocks = 8 * 160;
 
-int launch_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream) {
-    if (m == 0 || k == 0) return SGEMM_STATUS_OK;
+int launch_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream,
+                   int batch = 1, long long src_batch = 0, long long dst_batch = 0) {
+    if (m == 0 || k == 0 || batch == 0) return SGEMM_STATUS_OK;
     const bool vec = aligned(A, 16) && (lda % 4) == 0;
     const int per_row = vec ? (k / 4 > 0 ? k / 4 : 1) : k;
     int gx = (per_row + 255) / 256;
@@ -316,33 +323,45 @@ int launch_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_
     if (gy < 1) gy = 1;
     if (gy > m) gy = m;
     if (gy > 65535) gy = 65535;
-    if (vec)
-        tf32x3::split_a_kernel<true><<<dim3(gx, gy), 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k));
+    // with a batch, fewer rows per problem in flight
+    if (batch > 1) gy = gy / batch > 0 ? gy / batch : 1;
+    const dim3 grid(gx, gy, batch);
+    if (vec && (src_batch % 4) == 0)
+        tf32x3::split_a_kernel<true><<<grid, 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k), src_batch,
+                                                               dst_batch);
     else
-        tf32x3::split_a_kernel<false><<<dim3(gx, gy), 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k));
+        tf32x3::split_a_kernel<false><<<grid, 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k), src_batch,
+                                                                dst_batch);
     return SGEMM_STATUS_OK;
 }
 
 // B (k x n, ldb) -> bt_hi, bt_lo (B^T, n x ka).
-int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, cudaStream_t stream) {
-    if (n == 0 || k == 0) return SGEMM_STATUS_OK;
+int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, cudaStream_t stream,
+                   int batch = 1, long long src_batch = 0, long long dst_batch = 0) {
+    if (n == 0 || k == 0 || batch == 0) return SGEMM_STATUS_OK;
     long long gx = (n + 63) / 64, gy = (k + 31) / 32;
-    if (gx > kSplitBlocks) gx = kSplitBlocks;
-    if (gy > kSplitBlocks / gx) gy = kSplitBlocks / gx > 0 ? kSplitBlocks / gx : 1;
-    tf32x3::split_bt_kernel<<<dim3((unsigned)gx, (unsigned)gy), 256, 0, stream>>>(B, ldb, k, n, bt_hi, bt_lo,
-                                                                                 ka_of(k));
+    const long long budget = batch > 1 ? (kSplitBlocks / batch > 0 ? kSplitBlocks / batch : 1) : kSplitBlocks;
+    if (gx > budget) gx = budget;
+    if (gy > budget / gx) gy = budget / gx > 0 ? budget / gx : 1;
+    tf32x3::split_bt_kernel<<<dim3((unsigned)gx, (unsigned)gy, (unsigned)batch), 256, 0, stream>>>(
+        B, ldb, k, n, bt_hi, bt_lo, ka_of(k), src_batch, dst_batch);
     return SGEMM_STATUS_OK;
 }
 
 // The tcgen05 GEMM on split operands (row pitch ka).
+// batch > 1: the split operands of the batch's problems are stacked, problem
+// b's A rows at b*m and B^T rows at b*n (tiles overhanging m or n read the
+// next problem's rows, which only reach outputs that are never stored).
 int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const float *a_lo, const float *bt_hi,
-                      const float *bt_lo, float beta, float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream) {
+                      const float *bt_lo, float beta, float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream,
+                      int batch = 1, long long stride_c = 0) {
     const int ka = ka_of(k);
     CUtensorMap t_ahi, t_alo, t_bhi, t_blo;
-    int st = make_tensor_map(&t_ahi, a_hi, m, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st) st = make_tensor_map(&t_alo, a_lo, m, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st) st = make_tensor_map(&t_bhi, bt_hi, n, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st) st = make_tensor_map(&t_blo, bt_lo, n, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    const int am = m * batch, bn = n * batch;
+    int st = make_tensor_map(&t_ahi, a_hi, am, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st) st = make_tensor_map(&t_alo, a_lo, am, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st) st = make_tensor_map(&t_bhi, bt_hi, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st) st = make_tensor_map(&t_blo, bt_lo, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st) return st;
     tf32x3::Params a;
     a.m = m;
@@ -355,9 +374,10 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     a.tiles_m = (m + pl.bm - 1) / pl.bm;
     a.tiles_n = (n + pl.bn - 1) / pl.bn;
     a.group_m = pl.group_m;
-    // clusters of split_k CTAs (consecutive in x) share a tile
+    a.stride_c = stride_c;
+    // clusters of split_k CTAs (consecutive in x) share a tile; y = batch
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
+    cfg.gridDim = dim3((unsigned)pl.grid, (unsigned)batch, 1);
     cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
     cfg.stream = stream;
@@ -386,19 +406,22 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
 // 3xTF32 path of sgemm: split A and B^T into a stream-ordered scratch
 // buffer, run the tcgen05 GEMM, release the scratch.
 int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
-                  float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream) {
+                  float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream, const Batch &bt = Batch()) {
     const size_t a_elems = (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
+    const size_t cnt = (size_t)bt.count;
     float *ws = nullptr;
-    cudaError_t e = cudaMallocAsync(reinterpret_cast<void **>(&ws), 2 * (a_elems + b_elems) * sizeof(float), stream);
+    cudaError_t e =
+        cudaMallocAsync(reinterpret_cast<void **>(&ws), 2 * cnt * (a_elems + b_elems) * sizeof(float), stream);
     if (e != cudaSuccess) return fail_cuda(e);
-    float *a_hi = ws, *a_lo = ws + a_elems, *b_hi = a_lo + a_elems, *b_lo = b_hi + b_elems;
+    float *a_hi = ws, *a_lo = ws + cnt * a_elems, *b_hi = a_lo + cnt * a_elems, *b_lo = b_hi + cnt * b_elems;
     // both split operands are k-contiguous (K-major): an operand stored with
     // k contiguous is split in place order, one stored k-major is transposed
-    if (pl.op_a == SGEMM_OP_N) launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
-    else launch_split_b(k, m, A, lda, a_hi, a_lo, stream);
-    if (pl.op_b == SGEMM_OP_N) launch_split_b(k, n, B, ldb, b_hi, b_lo, stream);
-    else launch_split_a(n, k, B, ldb, b_hi, b_lo, stream);
-    const int st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream);
+    if (pl.op_a == SGEMM_OP_N) launch_split_a(m, k, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
+    else launch_split_b(k, m, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
+    if (pl.op_b == SGEMM_OP_N) launch_split_b(k, n, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
+    else launch_split_a(n, k, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
+    const int st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream, bt.count,
+                                     bt.sc);
     e = cudaFreeAsync(ws, stream);
     if (st) return st;
     if (e != cudaSuccess) return fail_cuda(e);
@@ -435,69 +458,119 @@ int noalloc_scratch(float **out) {
 }
 
 template <class AL, class BL>
-void launch_ffma_t(const GemmArgs &a, int grid, cudaStream_t s) {
+void launch_ffma_t(const GemmArgs &a, dim3 grid, cudaStream_t s) {
     ffma::ffma_sgemm_kernel<FCfg, AL, BL><<<grid, FCfg::THREADS, ffma::Layout<FCfg, AL, BL>::SMEM_BYTES, s>>>(a);
 }
 
 template <class AL>
-void launch_ffma_b(int bkind, const GemmArgs &a, int grid, cudaStream_t s) {
+void launch_ffma_b(int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s) {
     if (bkind == 0) launch_ffma_t<AL, BLoadScatter>(a, grid, s);
     else if (bkind == 1) launch_ffma_t<AL, BLoadVec>(a, grid, s);
     else launch_ffma_t<AL, BLoadScalar>(a, grid, s);
 }
 
-void launch_ffma(const sgemm_plan &pl, const GemmArgs &a, cudaStream_t s) {
+void launch_ffma(const sgemm_plan &pl, const GemmArgs &a, int batch, cudaStream_t s) {
     const int akind = pl.op_a == SGEMM_OP_N ? 0 : (pl.a_vec ? 1 : 2);
     const int bkind = pl.op_b == SGEMM_OP_T ? 0 : (pl.b_vec ? 1 : 2);
-    if (akind == 0) launch_ffma_b<ALoadScatter>(bkind, a, pl.grid, s);
-    else if (akind == 1) launch_ffma_b<ALoadVec>(bkind, a, pl.grid, s);
-    else launch_ffma_b<ALoadScalar>(bkind, a, pl.grid, s);
+    const dim3 grid((unsigned)pl.grid, (unsigned)batch, 1);
+    if (akind == 0) launch_ffma_b<ALoadScatter>(bkind, a, grid, s);
+    else if (akind == 1) launch_ffma_b<ALoadVec>(bkind, a, grid, s);
+    else launch_ffma_b<ALoadScalar>(bkind, a, grid, s);
 }
 
 }  // namespace
 
 extern "C" {
 
-int sgemm_op(int op_a, int op_b, int m, int n, int k, float alpha, const float *A, int lda, const float *B,
-             int ldb, float beta, float *C, int ldc, cudaStream_t stream, int path) {
+int sgemm_strided_batched(int op_a, int op_b, int m, int n, int k, float alpha, const float *A, int lda,
+                          long long stride_a, const float *B, int ldb, long long stride_b, float beta, float *C,
+                          int ldc, long long stride_c, int batch, cudaStream_t stream, int path) {
     if (op_a != SGEMM_OP_N && op_a != SGEMM_OP_T) return 1;
     if (op_b != SGEMM_OP_N && op_b != SGEMM_OP_T) return 2;
     if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
         return SGEMM_STATUS_BAD_PATH;
-    if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc, op_a, op_b)) return bad + 2;
-    if (m == 0 || n == 0) return SGEMM_STATUS_OK;
+    // argument positions: op_a 1, op_b 2, m 3, n 4, k 5, alpha 6, A 7, lda 8,
+    // stride_a 9, B 10, ldb 11, stride_b 12, beta 13, C 14, ldc 15,
+    // stride_c 16, batch 17
+    if (m < 0) return 3;
+    if (n < 0) return 4;
+    if (k < 0) return 5;
+    if (batch == 0) return SGEMM_STATUS_OK;   // an empty batch reads and writes nothing
+    if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc, op_a, op_b)) {
+        static const int pos[12] = {0, 3, 4, 5, 6, 7, 8, 10, 11, 13, 14, 15};
+        return pos[bad];
+    }
+    if (stride_a < 0) return 9;
+    if (stride_b < 0) return 12;
+    if (batch < 0) return 17;
+    // the batch's C matrices must not overlap
+    if (batch > 1 && (long long)m * n > 0 && stride_c < (long long)(m - 1) * ldc + n) return 16;
+    if (m == 0 || n == 0 || batch == 0) return SGEMM_STATUS_OK;
     DeviceState *dev = nullptr;
     int st = device_state(&dev);
     if (st != SGEMM_STATUS_OK) return st;
-    sgemm_plan pl;
-    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, dev->sms, &pl, dev->max_clusters, op_a, op_b);
-    if (st != SGEMM_STATUS_OK) return st;
-    if (pl.kernel == kKernelScale) {
-        scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
-    } else if (pl.kernel == kKernelTf32x3) {
-        if ((st = launch_tf32x3(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, pl, stream))) return st;
-    } else {
-        GemmArgs a;
-        a.m = m;
-        a.n = n;
-        a.k = k;
-        a.alpha = alpha;
-        a.beta = beta;
-        a.A = A;
-        a.lda = lda;
-        a.B = B;
-        a.ldb = ldb;
-        a.C = C;
-        a.ldc = ldc;
-        a.tiles_m = (m + pl.bm - 1) / pl.bm;
-        a.tiles_n = (n + pl.bn - 1) / pl.bn;
-        a.group_m = pl.group_m;
-        a.c_vec = pl.c_vec;
-        launch_ffma(pl, a, stream);
+    // grid.y carries the batch (<= 65535 per launch) and the stacked split
+    // operands need 32-bit TMA row coordinates: larger batches go in chunks
+    long long chunk = 65535;
+    const long long mn = m > n ? m : n;
+    if (chunk * mn > 2147483647LL) chunk = 2147483647LL / mn;
+    for (long long b0 = 0; b0 < batch; b0 += chunk) {
+        const int cnt = (int)(batch - b0 < chunk ? batch - b0 : chunk);
+        const float *Ab = A ? A + b0 * stride_a : A;
+        const float *Bb = B ? B + b0 * stride_b : B;
+        float *Cb = C + b0 * stride_c;
+        sgemm_plan pl;
+        st = plan(m, n, k, alpha, Ab, lda, Bb, ldb, beta, Cb, ldc, path, dev->sms, &pl, dev->max_clusters, op_a, op_b,
+                  cnt);
+        if (st != SGEMM_STATUS_OK) return st;
+        // 16-byte accesses need every problem's base aligned, not only the first
+        if (stride_c % 4) pl.c_vec = 0;
+        if (stride_a % 4) pl.a_vec = 0;
+        if (stride_b % 4) pl.b_vec = 0;
+        Batch bt;
+        bt.count = cnt;
+        bt.sa = stride_a;
+        bt.sb = stride_b;
+        bt.sc = stride_c;
+        if (pl.kernel == kKernelScale) {
+            scale_c_kernel<<<dim3(pl.grid, cnt), pl.threads, 0, stream>>>(Cb, ldc, m, n, beta, stride_c);
+        } else if (pl.kernel == kKernelTf32x3) {
+            if ((st = launch_tf32x3(m, n, k, alpha, Ab, lda, Bb, ldb, beta, Cb, ldc, pl, stream, bt))) return st;
+        } else {
+            GemmArgs a;
+            a.m = m;
+            a.n = n;
+            a.k = k;
+            a.alpha = alpha;
+            a.beta = beta;
+            a.A = Ab;
+            a.lda = lda;
+            a.B = Bb;
+            a.ldb = ldb;
+            a.C = Cb;
+            a.ldc = ldc;
+            a.tiles_m = (m + pl.bm - 1) / pl.bm;
+            a.tiles_n = (n + pl.bn - 1) / pl.bn;
+            a.group_m = pl.group_m;
+            a.c_vec = pl.c_vec;
+            a.stride_a = stride_a;
+            a.stride_b = stride_b;
+            a.stride_c = stride_c;
+            launch_ffma(pl, a, cnt, stream);
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_cuda(e);
     }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail_cuda(e);
     return SGEMM_STATUS_OK;
+}
+
+int sgemm_op(int op_a, int op_b, int m, int n, int k, float alpha, const float *A, int lda, const float *B,
+             int ldb, float beta, float *C, int ldc, cudaStream_t stream, int path) {
+    const int st = sgemm_strided_batched(op_a, op_b, m, n, k, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc, 0, 1,
+                                         stream, path);
+    // back to sgemm_op's positions (no strides)
+    static const int pos[18] = {0, 1, 2, 3, 4, 5, 6, 7, 8, 0, 9, 10, 0, 11, 12, 13, 0, 0};
+    return st >= 1 && st <= 17 ? pos[st] : st;
 }
 
 int sgemm_ex(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb,
@@ -560,7 +633,7 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
                   dev->max_clusters);
     if (st) return st;
     if (pl.kernel == kKernelScale) {
-        scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
+        scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
     } else if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, bt_hi, bt_lo, beta, C, ldc, pl, stream))) {
         return st;
     }
@@ -581,7 +654,7 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
     st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl, dev->max_clusters);
     if (st != SGEMM_STATUS_OK) return st;
     if (pl.kernel == kKernelScale) {
-        scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta);
+        scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
     } else {
         float *ws = nullptr;
         if ((st = noalloc_scratch(&ws))) return st;

@@ -103,6 +103,10 @@ struct Params {
     float *C;
     long long ldc;
     int tiles_m, tiles_n, group_m;
+    // strided batch: problem blockIdx.y reads rows y*m .. of the split A and
+    // y*n .. of the split B^T (the batch's operands stacked as one tall
+    // matrix) and writes C + y*stride_c
+    long long stride_c;
 };
 
 // ---------------------------------------------------------------- split kernels
@@ -117,7 +121,12 @@ __device__ __forceinline__ void split_one(float x, float &h, float &l) {
 // (read element by element: the bytes past k may lie outside A).
 template <bool VEC>
 __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ A, long long lda, int m, int k,
-                                                      float *__restrict__ hi, float *__restrict__ lo, int ka) {
+                                                      float *__restrict__ hi, float *__restrict__ lo, int ka,
+                                                      long long src_batch, long long dst_batch) {
+    // problem blockIdx.z of a strided batch
+    A += blockIdx.z * src_batch;
+    hi += blockIdx.z * dst_batch;
+    lo += blockIdx.z * dst_batch;
     const int full4 = VEC ? k / 4 : 0;               // float4 chunks entirely inside the row
     const int scal0 = 4 * full4;                      // first element done one at a time
     for (int row = blockIdx.y; row < m; row += gridDim.y) {
@@ -148,7 +157,11 @@ __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ 
 // of B^T are both 128-byte coalesced per warp, and the column reads of the
 // tile hit 32 different banks.
 __global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__ B, long long ldb, int k, int n,
-                                                       float *__restrict__ hi, float *__restrict__ lo, int ka) {
+                                                       float *__restrict__ hi, float *__restrict__ lo, int ka,
+                                                       long long src_batch, long long dst_batch) {
+    B += blockIdx.z * src_batch;
+    hi += blockIdx.z * dst_batch;
+    lo += blockIdx.z * dst_batch;
     __shared__ float tile[32][65];
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
     for (int t0 = blockIdx.y * 32; t0 < k; t0 += gridDim.y * 32) {
@@ -208,6 +221,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     int tm, tn;
     raster_tile(blockIdx.x / nsplit, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     const int m0 = tm * BM, n0 = tn * BN;
+    // rows of this batch problem's operands inside the stacked split arrays
+    const int arow0 = (int)blockIdx.y * p.m + m0, brow0 = (int)blockIdx.y * p.n + n0;
+    float *const Cb = p.C + (long long)blockIdx.y * p.stride_c;
     const int KT_ALL = (p.k + BK - 1) / BK;
     const int kt0 = (int)((long long)KT_ALL * rank / nsplit);
     const int KT = (int)((long long)KT_ALL * (rank + 1) / nsplit) - kt0;   // slabs of this CTA
@@ -254,10 +270,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t fb = bar_full + 8 * s;
                 mbar_arrive_expect_tx(fb, STAGE_BYTES);
                 const int kx = (kt0 + kt) * BK;
-                tma_load_2d(st, &tmAhi, kx, m0, fb);
-                tma_load_2d(st + A_TILE, &tmAlo, kx, m0, fb);
-                tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, n0, fb);
-                tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, n0, fb);
+                tma_load_2d(st, &tmAhi, kx, arow0, fb);
+                tma_load_2d(st + A_TILE, &tmAlo, kx, arow0, fb);
+                tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, brow0, fb);
+                tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, brow0, fb);
                 ++issued;
             }
             if (*abort_flag) {
@@ -346,7 +362,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
         } else if (ok && *abort_flag == 0 && row < p.m) {
             const float alpha = p.alpha, beta = p.beta;
-            float *crow = p.C + (long long)row * p.ldc;
+            float *crow = Cb + (long long)row * p.ldc;
             const int col0 = n0 + half * COLS_PER_THREAD;
 #pragma unroll
             for (int q = 0; q < COLS_PER_THREAD / 4; ++q) {
@@ -401,7 +417,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     sum.w += v.w;
                 }
                 if (row >= p.m) continue;
-                float *crow = p.C + (long long)row * p.ldc;
+                float *crow = Cb + (long long)row * p.ldc;
                 const float a[4] = {sum.x, sum.y, sum.z, sum.w};
                 if (C_VEC && col + 3 < p.n) {
                     float4 o;

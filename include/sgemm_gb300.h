@@ -109,6 +109,25 @@ int sgemm_op(int op_a, int op_b, int m, int n, int k, float alpha,
              const float *A, int lda, const float *B, int ldb,
              float beta, float *C, int ldc, cudaStream_t stream, int path);
 
+/*
+ * sgemm_strided_batched -- `batch` independent products of one shape,
+ *     C_b = alpha * op(A_b) * op(B_b) + beta * C_b,   b = 0 .. batch-1,
+ * with A_b = A + b*stride_a, B_b = B + b*stride_b, C_b = C + b*stride_c
+ * (strides in floats).  Not on the pages; the same operation per problem.
+ * A stride of 0 shares that operand across the batch; the C matrices must
+ * not overlap (stride_c >= (m-1)*ldc + n when batch > 1).  Each path runs
+ * the whole batch in one launch per kernel (grid y = problem; batches
+ * beyond 65535 problems go in chunks).  Status positions: op_a 1, op_b 2,
+ * m 3, n 4, k 5, A 7, lda 8, stride_a 9, B 10, ldb 11, stride_b 12, C 14,
+ * ldc 15, stride_c 16, batch 17.  batch == 0 is a no-op (the pointers
+ * are not looked at).
+ */
+int sgemm_strided_batched(int op_a, int op_b, int m, int n, int k, float alpha,
+                          const float *A, int lda, long long stride_a,
+                          const float *B, int ldb, long long stride_b,
+                          float beta, float *C, int ldc, long long stride_c,
+                          int batch, cudaStream_t stream, int path);
+
 
 /*
  * 3xTF32 split operands.  The pages describe only CUDA-core FFMA kernels;

@@ -167,3 +167,23 @@ def test_op_argument_checks():
     assert binding.sgemm_op_raw(1, 0, 8, 4, 4, 1.0, 256, 4, 512, 4, 0.0, 1024, 4) == 8
     # op(B) = B^T with B stored n x k: ldb must cover k
     assert binding.sgemm_op_raw(0, 1, 4, 4, 8, 1.0, 256, 8, 512, 4, 0.0, 1024, 4) == 10
+
+
+def test_strided_batched_argument_checks():
+    """Positions: op_a 1, op_b 2, m 3, n 4, k 5, A 7, lda 8, stride_a 9, B 10,
+    ldb 11, stride_b 12, C 14, ldc 15, stride_c 16, batch 17."""
+    def call(**o):
+        a = dict(op_a=0, op_b=0, m=4, n=5, k=6, A=256, lda=6, sa=24, B=512, ldb=5, sb=30, C=1024, ldc=5, sc=20,
+                 batch=3)
+        a.update(o)
+        return binding.sgemm_strided_batched_raw(a["op_a"], a["op_b"], a["m"], a["n"], a["k"], 1.0, a["A"],
+                                                 a["lda"], a["sa"], a["B"], a["ldb"], a["sb"], 0.0, a["C"], a["ldc"],
+                                                 a["sc"], a["batch"], 0)
+    assert call(op_a=3) == 1 and call(op_b=-1) == 2
+    assert call(m=-1) == 3 and call(n=-1) == 4 and call(k=-1) == 5
+    assert call(A=0) == 7 and call(lda=5) == 8 and call(sa=-1) == 9
+    assert call(B=0) == 10 and call(ldb=4) == 11 and call(sb=-4) == 12
+    assert call(C=0) == 14 and call(ldc=4) == 15
+    assert call(sc=19) == 16          # C matrices would overlap: (m-1)*ldc + n = 20
+    assert call(batch=-1) == 17
+    assert call(batch=0) == 0 and call(m=0) == 0
