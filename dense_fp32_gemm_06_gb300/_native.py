@@ -93,7 +93,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 # Exported symbols, in the order the header declares them.
 EXPORTS = ["sgemm", "sgemm_ex", "sgemm_op", "sgemm_strided_batched", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", "sgemm_tf32x3_split_gemm",
-           "sgemm_tf32x3_noalloc", "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_plan_for", "sgemm_device_status",
+           "sgemm_tf32x3_noalloc", "reduce_sum_f32", "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_plan_for", "sgemm_device_status",
            "sgemm_version"]
 
 
@@ -123,6 +123,8 @@ def _declare(lib):
     lib.sgemm_tf32x3_split_gemm.restype = i
     lib.sgemm_tf32x3_noalloc.argtypes = gemm
     lib.sgemm_tf32x3_noalloc.restype = i
+    lib.reduce_sum_f32.argtypes = [vp, ctypes.c_longlong, vp, vp]
+    lib.reduce_sum_f32.restype = i
     lib.sgemm_status_string.argtypes = [i]
     lib.sgemm_status_string.restype = ctypes.c_char_p
     lib.sgemm_last_cuda_error.argtypes = []

@@ -223,3 +223,40 @@ def bmm(A, B, C, alpha=1.0, beta=0.0, *, path=PATH_AUTO, stream=None):
         _check(sgemm_strided_batched_raw(op_a, op_b, m, n, k, alpha, A.data_ptr(), lda, A.stride(0), B.data_ptr(),
                                          ldb, B.stride(0), beta, C.data_ptr(), ldc, C.stride(0), batch, stream, path))
     return C
+
+
+REDUCE_THREADS = 512          # threads per block of the reduction kernel
+REDUCE_BLOCKS_PER_SM = 4
+
+
+def reduce_sum_raw(x_ptr, n, out_ptr, stream=0) -> int:
+    """*out = sum of the n floats at x (device pointers); returns the status."""
+    return _native.load().reduce_sum_f32(ctypes.c_void_p(x_ptr or None), int(n), ctypes.c_void_p(out_ptr or None),
+                                         ctypes.c_void_p(stream or None))
+
+
+def reduce_sum(x, out=None, *, stream=None):
+    """Sum of a contiguous float32 CUDA tensor, as a 1-element tensor."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise SgemmError(-1, "x must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    with torch.cuda.device(x.device):
+        _check(reduce_sum_raw(x.data_ptr(), x.numel(), out.data_ptr(), stream))
+    return out
+
+
+def reduce_tree_depth(n: int, num_sms: int = 152, vec: bool = True) -> int:
+    """Depth of the summation tree the reduction kernel uses for n values:
+    the longest chain of additions any partial sum goes through (per-thread
+    sequential sums, the 4-accumulator and shuffle combines, the per-block
+    combine, and the block commits to *out), for the bound gamma_h sum|x|."""
+    threads = REDUCE_THREADS
+    blocks = max(1, min(-(-n // (16 * threads)), num_sms * REDUCE_BLOCKS_PER_SM)) if n else 1
+    # one accumulator's sequential adds: 16-byte loads feed 4 accumulators,
+    # 4-byte loads (misaligned x) all go to one; +1 for the tail
+    per_acc = -(-n // (blocks * threads * (4 if vec else 1))) + 1
+    return per_acc + 2 + 5 + 5 + blocks

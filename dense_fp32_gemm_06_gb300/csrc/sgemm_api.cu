@@ -12,6 +12,7 @@
 #include "../../include/sgemm_gb300.h"
 #include "ffma_sgemm.cuh"
 #include "tf32x3_sgemm.cuh"
+#include "reduce_sum.cuh"
 
 using namespace sgemm_gb300;
 
@@ -679,6 +680,29 @@ int sgemm_plan_for(int m, int n, int k, float alpha, const float *A, int lda, co
                    float beta, const float *C, int ldc, int path, int num_sms, sgemm_plan *out) {
     if (out == nullptr) return SGEMM_STATUS_UNSUPPORTED;
     return plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, num_sms, out);
+}
+
+int reduce_sum_f32(const float *x, long long n, float *out, cudaStream_t stream) {
+    if (n < 0) return 2;
+    if (n > 0 && (x == nullptr || !aligned(x, 4))) return 1;
+    if (out == nullptr || !aligned(out, 4)) return 3;
+    DeviceState *dev = nullptr;
+    if (int st = device_state(&dev)) return st;
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float), stream);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (n > 0) {
+        long long blocks = (n + 4LL * reduce::THREADS * 4 - 1) / (4LL * reduce::THREADS * 4);
+        const long long cap = (long long)dev->sms * reduce::BLOCKS_PER_SM;
+        if (blocks > cap) blocks = cap;
+        if (blocks < 1) blocks = 1;
+        if (aligned(x, 16))
+            reduce::reduce_sum_kernel<true><<<(unsigned)blocks, reduce::THREADS, 0, stream>>>(x, n, out);
+        else
+            reduce::reduce_sum_kernel<false><<<(unsigned)blocks, reduce::THREADS, 0, stream>>>(x, n, out);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return SGEMM_STATUS_OK;
 }
 
 const char *sgemm_status_string(int status) {

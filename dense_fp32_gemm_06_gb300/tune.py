@@ -82,6 +82,20 @@ def sweep(m, n, k, reps=20, widths=(256, 128), splits=(1, 2, 3, 4, 6, 8), max_ct
     return auto, results
 
 
+def reduce_bandwidth(n=1 << 28, reps=50):
+    """GB/s of reduce_sum_f32 on n floats (4n bytes read per call), CUDA
+    events, median of `reps` calls (n = 2^28: 1 GiB, far larger than L2)."""
+    import torch
+    from . import binding
+    x = torch.empty(n, device="cuda").uniform_(-1, 1)
+    out = torch.empty(1, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        binding.reduce_sum(x, out)
+    us = _median_us(lambda: binding.reduce_sum(x, out), lambda: None, stream, reps)
+    return 4.0 * n / (us * 1e-6) / 1e9, us
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--shapes", nargs="+", default=["1000,1500,777", "256,256,8192", "300,700,5000",
@@ -89,7 +103,12 @@ def main(argv=None):
                                                     "500,500,300", "4096,4096,1024", "1024,1024,16384",
                                                     "2048,1024,8192"])
     ap.add_argument("--reps", type=int, default=20)
+    ap.add_argument("--reduce", type=int, default=0, help="measure reduce_sum_f32 on this many floats instead")
     args = ap.parse_args(argv)
+    if args.reduce:
+        gbs, us = reduce_bandwidth(args.reduce)
+        print(f"reduce_sum_f32 n={args.reduce} {us:.1f} us {gbs:.1f} GB/s", flush=True)
+        return
     for spec in args.shapes:
         m, n, k = (int(x) for x in spec.split(","))
         auto, res = sweep(m, n, k, reps=args.reps)

@@ -198,6 +198,20 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha,
                          const float *A, int lda, const float *B, int ldb,
                          float beta, float *C, int ldc, cudaStream_t stream);
 
+/*
+ * reduce_sum_f32 -- *out = sum_{i<n} x[i] (FP32), the block reduction of
+ * aerisun.top "GPU 访存与计算优化", section "Reduce 的分层归约": per-thread
+ * register sums over a grid-stride loop, warp shuffles, a shared-memory
+ * combine per block and one atomic add per block into *out (which the call
+ * zeroes first on `stream`).  x and out are device pointers (x 4-byte
+ * aligned; 16-byte aligned x takes 16-byte loads).  The order in which
+ * blocks commit is not fixed, so the last bits of the sum may differ
+ * between runs; the error is within gamma_h * sum|x_i| for the summation
+ * tree depth h.  Status: 1 x NULL / misaligned while n > 0, 2 n < 0,
+ * 3 out NULL / misaligned, SGEMM_STATUS_CUDA_ERROR.  n == 0 gives 0.
+ */
+int reduce_sum_f32(const float *x, long long n, float *out, cudaStream_t stream);
+
 /* Static, NUL-terminated description of a status code. */
 const char *sgemm_status_string(int status);
 

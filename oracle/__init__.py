@@ -20,6 +20,10 @@ Contents
   (sections 问题定义, 基于 shared memory 计算, 基于 register 计算 and
   一个具体的例子): grid sizes, threads, iterations and the read counts of the
   three storage levels.
+* ``sum_f64`` / ``sum_within_tolerance`` -- the array sum s = sum_i x_i of
+  aerisun.top "GPU 访存与计算优化" (section "Reduce 的分层归约"), in FP64, and
+  the bound gamma_h * sum_i |x_i| every FP32 summation tree of depth h meets
+  (h additions on the longest chain, each rounding by at most u = 2^-24).
 * ``ideal_intensity`` / ``cta_intensity`` -- the arithmetic-intensity formulas
   of aerisun.top "GPU 访存与计算优化" (sections "GEMM 的理想复用与实际访存" and
   "Shared Tiling 与 block 内复用").
@@ -76,6 +80,8 @@ def _lib():
             lib.oracle_sgemm_f64_sampled.argtypes = [i64, f64, vp, i64, vp, i64, f64, vp, i64,
                                                      i64, vp, vp, vp, vp, ci]
             lib.oracle_sgemm_f64_sampled.restype = None
+            lib.oracle_sum_f64.argtypes = [vp, i64, vp, vp]
+            lib.oracle_sum_f64.restype = None
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ci
             _LIB = lib
@@ -219,3 +225,24 @@ def cta_intensity(BM, BN, bytes_per_elem=4):
     """FLOP per byte a BM x BN output tile does on one BK-deep slab it loads
     once: 2*BM*BN*BK / (4*(BM*BK + BK*BN)) = BM*BN / (2*(BM + BN)) for FP32."""
     return 2.0 * BM * BN / (bytes_per_elem * (BM + BN))
+
+
+def sum_f64(x):
+    """(s, a): the FP64 sum of the float32 values x and the sum of |x|."""
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+    s = ctypes.c_double(0.0)
+    a = ctypes.c_double(0.0)
+    _lib().oracle_sum_f64(_ptr(x) if x.size else None, x.size, ctypes.byref(s), ctypes.byref(a))
+    return s.value, a.value
+
+
+def sum_tolerance(abs_sum, depth):
+    """gamma_h * sum|x| with gamma_h = h u / (1 - h u), u = 2^-24: the error
+    bound of any FP32 summation whose longest chain has h additions."""
+    u = 2.0 ** -24
+    hu = depth * u
+    return hu / (1.0 - hu) * abs_sum
+
+
+def sum_within_tolerance(got, s, abs_sum, depth):
+    return bool(np.isfinite(got)) and abs(float(got) - s) <= sum_tolerance(abs_sum, depth)

@@ -21,6 +21,10 @@
  * output).  Alongside r the oracle returns the error scale
  * E_ij = sum_t |A_it| * |B_tj|, which the FP32 tolerance is stated in.
  *
+ * Also the array sum s = sum_i x_i of aerisun.top "GPU 访存与计算优化"
+ * (section "Reduce 的分层归约", first formula), in FP64 in increasing i, with
+ * the scale sum_i |x_i| its FP32 error bound is stated in.
+ *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (contraction is
  * off so x86 and Arm builds give the same FP64 bits).
  */
@@ -118,4 +122,16 @@ void oracle_sgemm_f64_sampled(int64_t k, double alpha,
         R[s] = v;
         E[s] = err;
     }
+}
+
+/* s = sum_{i<n} x_i and a = sum_{i<n} |x_i|, FP64, increasing i. */
+void oracle_sum_f64(const float *x, int64_t n, double *s, double *a) {
+    double acc = 0.0, abs_acc = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = (double)x[i];
+        acc += v;
+        abs_acc += fabs(v);
+    }
+    *s = acc;
+    *a = abs_acc;
 }
