@@ -100,7 +100,8 @@ EXPORTS = ["sgemm", "sgemm_ex", "sgemm_op", "sgemm_strided_batched", "sgemm_tf32
 class Plan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "path", "kernel", "bm", "bn", "bk", "rm", "rn", "threads", "stages", "grid", "tiles",
-        "k_tiles", "smem_bytes", "b_vec", "c_vec", "group_m", "split_k", "op_a", "op_b", "a_vec")]
+        "k_tiles", "smem_bytes", "b_vec", "c_vec", "group_m", "split_k", "op_a", "op_b", "a_vec",
+        "a_in_kernel")]
 
 
 def _declare(lib):

@@ -83,8 +83,12 @@ int ffma_smem_bytes(int akind, int bkind) {
 
 template <class Cfg, bool CV>
 cudaError_t set_tc_attr() {
-    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                Cfg::SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    return e;
 }
 
 // Clusters of S CTAs of the tensor-core kernel that can be resident at once
@@ -103,7 +107,7 @@ cudaError_t max_clusters_of(int S, int *out) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     *out = 0;
-    return cudaOccupancyMaxActiveClusters(out, tf32x3::tf32x3_gemm_kernel<Cfg, true>, &cfg);
+    return cudaOccupancyMaxActiveClusters(out, tf32x3::tf32x3_gemm_kernel<Cfg, true, false>, &cfg);
 }
 
 // One-time per-device set-up: SM count and kernel attributes.
@@ -257,6 +261,23 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
                 }
             }
         }
+        // A is split inside the GEMM (two extra warps split each raw slab in
+        // shared memory, no pass over A through HBM) when the kernel can read
+        // A itself by TMA (untransposed, 16-byte rows, one problem).  The
+        // pre-pass moves 12 bytes per element of A (read 4, write 8) and the
+        // GEMM then reads 8 more; the in-kernel split reads 4 bytes per
+        // element per tile column but re-splits A once per tile column, which
+        // costs shared-memory bandwidth next to the MMA.  Measured on GB300
+        // (whole call, m = k = 8192): 2.4x faster at n = 512, 1.65x at 1024,
+        // 1.27x at 2048, 1.10x at 4096, even at 8192; so n <= 4096.
+        // SGEMM_GB300_SPLIT_A_IN (0 / 1) pins it.
+        const char *env_ain = std::getenv("SGEMM_GB300_SPLIT_A_IN");
+        const bool a_tma = op_a == SGEMM_OP_N && aligned(A, 16) && (lda % 4) == 0 && batch == 1;
+        if (env_ain && (env_ain[0] == '0' || env_ain[0] == '1'))
+            pl->a_in_kernel = a_tma && env_ain[0] == '1';
+        else
+            pl->a_in_kernel = a_tma && n <= 4096;
+        pl->threads = tf32x3::threads_for(pl->a_in_kernel != 0);
         const bool narrow = best_bn == tf32x3::Narrow::BN;
         pl->bn = best_bn;
         pl->split_k = best_s;
@@ -350,17 +371,34 @@ int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *b
 }
 
 // The tcgen05 GEMM on split operands (row pitch ka).
+template <class Cfg>
+cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, const sgemm_plan &pl, const CUtensorMap &ahi,
+                      const CUtensorMap &alo, const CUtensorMap &bhi, const CUtensorMap &blo,
+                      const tf32x3::Params &a) {
+    if (pl.a_in_kernel)
+        return pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, true, true>, ahi, alo, bhi, blo, a)
+                        : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, true>, ahi, alo, bhi, blo,
+                                             a);
+    return pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, true, false>, ahi, alo, bhi, blo, a)
+                    : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, false>, ahi, alo, bhi, blo, a);
+}
+
 // batch > 1: the split operands of the batch's problems are stacked, problem
 // b's A rows at b*m and B^T rows at b*n (tiles overhanging m or n read the
 // next problem's rows, which only reach outputs that are never stored).
 int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const float *a_lo, const float *bt_hi,
                       const float *bt_lo, float beta, float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream,
-                      int batch = 1, long long stride_c = 0) {
+                      int batch = 1, long long stride_c = 0, int a_ld = 0) {
     const int ka = ka_of(k);
     CUtensorMap t_ahi, t_alo, t_bhi, t_blo;
     const int am = m * batch, bn = n * batch;
-    int st = make_tensor_map(&t_ahi, a_hi, am, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st) st = make_tensor_map(&t_alo, a_lo, am, k, ka, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    // with the A split in the kernel, a_hi is the caller's A (row pitch
+    // a_ld) and a_lo is not read
+    const int a_pitch = pl.a_in_kernel ? a_ld : ka;
+    int st = make_tensor_map(&t_ahi, a_hi, am, k, a_pitch, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st)
+        st = make_tensor_map(&t_alo, pl.a_in_kernel ? a_hi : a_lo, am, k, a_pitch, tf32x3::BM, tf32x3::BK,
+                             CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st) st = make_tensor_map(&t_bhi, bt_hi, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st) st = make_tensor_map(&t_blo, bt_lo, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st) return st;
@@ -391,15 +429,9 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     cfg.numAttrs = pl.split_k > 1 ? 1 : 0;
     cudaError_t e;
     if (pl.bn == tf32x3::Narrow::BN)
-        e = pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<tf32x3::Narrow, true>, t_ahi, t_alo, t_bhi,
-                                          t_blo, a)
-                     : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<tf32x3::Narrow, false>, t_ahi, t_alo,
-                                          t_bhi, t_blo, a);
+        e = launch_tc<tf32x3::Narrow>(cfg, pl, t_ahi, t_alo, t_bhi, t_blo, a);
     else
-        e = pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<tf32x3::Wide, true>, t_ahi, t_alo, t_bhi,
-                                          t_blo, a)
-                     : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<tf32x3::Wide, false>, t_ahi, t_alo, t_bhi,
-                                          t_blo, a);
+        e = launch_tc<tf32x3::Wide>(cfg, pl, t_ahi, t_alo, t_bhi, t_blo, a);
     if (e != cudaSuccess) return fail_cuda(e);
     return SGEMM_STATUS_OK;
 }
@@ -408,7 +440,7 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
 // buffer, run the tcgen05 GEMM, release the scratch.
 int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
                   float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream, const Batch &bt = Batch()) {
-    const size_t a_elems = (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
+    const size_t a_elems = pl.a_in_kernel ? 0 : (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
     const size_t cnt = (size_t)bt.count;
     float *ws = nullptr;
     cudaError_t e =
@@ -417,12 +449,18 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
     float *a_hi = ws, *a_lo = ws + cnt * a_elems, *b_hi = a_lo + cnt * a_elems, *b_lo = b_hi + cnt * b_elems;
     // both split operands are k-contiguous (K-major): an operand stored with
     // k contiguous is split in place order, one stored k-major is transposed
-    if (pl.op_a == SGEMM_OP_N) launch_split_a(m, k, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
-    else launch_split_b(k, m, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
+    if (pl.a_in_kernel) {
+        a_hi = const_cast<float *>(A);   // the GEMM reads A itself and splits it in shared memory
+        a_lo = nullptr;
+    } else if (pl.op_a == SGEMM_OP_N) {
+        launch_split_a(m, k, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
+    } else {
+        launch_split_b(k, m, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
+    }
     if (pl.op_b == SGEMM_OP_N) launch_split_b(k, n, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
     else launch_split_a(n, k, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
     const int st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream, bt.count,
-                                     bt.sc);
+                                     bt.sc, lda);
     e = cudaFreeAsync(ws, stream);
     if (st) return st;
     if (e != cudaSuccess) return fail_cuda(e);
@@ -633,6 +671,8 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
     int st = plan(m, n, k, alpha, a_hi, imax(1, k), a_hi, imax(1, n), beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl,
                   dev->max_clusters);
     if (st) return st;
+    pl.a_in_kernel = 0;   // the operands are split already
+    pl.threads = tf32x3::threads_for(false);
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
     } else if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, bt_hi, bt_lo, beta, C, ldc, pl, stream))) {
@@ -654,6 +694,8 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
     sgemm_plan pl;
     st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl, dev->max_clusters);
     if (st != SGEMM_STATUS_OK) return st;
+    pl.a_in_kernel = 0;   // this entry point splits A into its fixed scratch
+    pl.threads = tf32x3::threads_for(false);
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
     } else {

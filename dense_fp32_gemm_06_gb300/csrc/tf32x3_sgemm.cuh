@@ -15,9 +15,11 @@
 //     A_hi, A_lo, m x ka row-major (ka = k rounded up to 4, 16-byte rows);
 //     B becomes B^T_hi, B^T_lo, n x ka, transposed through a padded 32 x 33
 //     shared tile (coalesced reads and writes).  Both operands of the MMA
-//     are then K-major;
+//     are then K-major.  A skips this pass when the GEMM kernel splits it
+//     itself from a raw TMA load (A_IN, at the kernel);
 //  2. the GEMM kernel: one CTA per 128 x BN tile of C (BN = 256, or 128 for
-//     narrow or few-tile problems; the rest of this comment says 256), 10 warps.
+//     narrow or few-tile problems; the rest of this comment says 256), 10 warps
+//     (12 when the kernel splits A itself, below).
 //     warp 0 lane 0: TMA producer -- per 16-deep k slab, four boxes (A_hi,
 //       A_lo 128 x 16; B_hi, B_lo 256 x 16, 64-byte rows with the 64-byte
 //       swizzle) into a 4-stage ring, completing on the slot's "full"
@@ -71,6 +73,12 @@ constexpr int A_TILE = BM * BK * 4;                       // 8 KB
 constexpr int ACC_WARPS = 8;
 constexpr int ACC_THREADS = 32 * ACC_WARPS;
 constexpr int THREADS = 64 + ACC_THREADS;                 // producer warp, MMA warp, 8 accumulator warps
+constexpr int CONV_WARPS = 2;                             // A splitters when A is split in the kernel
+constexpr int CONV_THREADS = 32 * CONV_WARPS;
+// Threads per CTA: 10 warps, or 12 with the A splitters.  Either way three
+// warps share a sub-partition's register file, so the per-thread register
+// cap (168) is the same.
+__host__ __device__ constexpr int threads_for(bool a_in) { return a_in ? THREADS + CONV_THREADS : THREADS; }
 constexpr int BAR_REGION = 256;
 static_assert(BK * 4 == 64, "one 64-byte swizzle row per operand row");
 static_assert(KC % BK == 0, "chunks are whole slabs");
@@ -96,6 +104,7 @@ constexpr int kStatusMma = 0x202;
 constexpr int kStatusAccumulate = 0x203;
 constexpr int kStatusDrain = 0x204;
 constexpr int kStatusMmaBuffer = 0x205;
+constexpr int kStatusSplit = 0x206;
 
 struct Params {
     int m, n, k;
@@ -193,14 +202,22 @@ __global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__
 
 // ---------------------------------------------------------------- GEMM kernel
 
-template <class Cfg, bool C_VEC>
-__global__ void __launch_bounds__(THREADS, 1)
+// A_IN: A is split here instead of by split_a_kernel -- TMA loads the raw
+// FP32 A slab into the A_hi slot, two extra warps (10, 11) turn it into hi
+// (in place) and lo (the A_lo slot) as soon as it lands, make the writes
+// visible to the tensor core's proxy and arrive on the slot's "converted"
+// barrier, which the MMA issuer waits for besides "full".  The splitters
+// run ahead of the MMA by up to the ring depth, so the split hides behind
+// the tensor core instead of costing an HBM round trip of A.
+template <class Cfg, bool C_VEC, bool A_IN = false>
+__global__ void __launch_bounds__(threads_for(A_IN), 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
                        const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
                        const Params p) {
     constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, B_TILE = Cfg::B_TILE, STAGE_BYTES = Cfg::STAGE_BYTES;
     constexpr int TMEM_COLS = Cfg::TMEM_COLS, COLS_PER_THREAD = Cfg::COLS_PER_THREAD;
     constexpr int PART_PITCH = BN + 4;   // floats per row of a parked split-K partial tile
+    constexpr int NTHREADS = threads_for(A_IN);
     static_assert(BM * PART_PITCH * 4 <= STAGES * STAGE_BYTES, "partial tile fits the stage memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *const smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -213,6 +230,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bar_done = bar_tempty + 16;           // every MMA issued has completed
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * (2 * STAGES + 5));
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 8);
+    const uint32_t bar_conv = bar_done + 24;             // [STAGES] A slab split in place (A_IN)
+    static_assert(8 * (3 * STAGES + 7) <= BAR_REGION, "barrier region");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // split-K: the CTAs of a cluster share one output tile and take
@@ -239,6 +258,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar_tempty + 8 * b, ACC_THREADS);
         }
         mbar_init(bar_done, 1);
+        if (A_IN)
+            for (int s = 0; s < STAGES; ++s) mbar_init(bar_conv + 8 * s, CONV_THREADS);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmAhi);
@@ -268,10 +289,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (*abort_flag) break;
                 const uint32_t st = stage0 + s * STAGE_BYTES;
                 const uint32_t fb = bar_full + 8 * s;
-                mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                mbar_arrive_expect_tx(fb, A_IN ? STAGE_BYTES - A_TILE : STAGE_BYTES);
                 const int kx = (kt0 + kt) * BK;
-                tma_load_2d(st, &tmAhi, kx, arow0, fb);
-                tma_load_2d(st + A_TILE, &tmAlo, kx, arow0, fb);
+                tma_load_2d(st, &tmAhi, kx, arow0, fb);   // raw A when A_IN
+                if (!A_IN) tma_load_2d(st + A_TILE, &tmAlo, kx, arow0, fb);
                 tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, brow0, fb);
                 tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, brow0, fb);
                 ++issued;
@@ -296,7 +317,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 const int s = kt % STAGES;
-                if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusMma)) {
+                if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusMma) ||
+                    (A_IN && !mbar_wait(bar_conv + 8 * s, (kt / STAGES) & 1, kStatusMma))) {
                     *abort_flag = 1;
                     break;
                 }
@@ -322,6 +344,36 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_wait(bar_done, 0, kStatusDrain);
         }
         __syncwarp();
+    } else if (A_IN && warp >= 2 + ACC_WARPS) {
+        // ------------------------------------------------------------ A splitters (warps 10, 11)
+        const int ct = threadIdx.x - (64 + ACC_THREADS);   // 0 .. CONV_THREADS - 1
+        for (int kt = 0; kt < KT; ++kt) {
+            const int s = kt % STAGES;
+            if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusSplit)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            // raw slab -> hi in place, lo into the A_lo slot (same swizzled
+            // positions: the split is elementwise)
+            float4 *hi = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES);
+            float4 *lo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + A_TILE);
+            float4 x[A_TILE / 16 / CONV_THREADS];
+#pragma unroll
+            for (int j = 0; j < A_TILE / 16 / CONV_THREADS; ++j) x[j] = hi[ct + j * CONV_THREADS];
+#pragma unroll
+            for (int j = 0; j < A_TILE / 16 / CONV_THREADS; ++j) {
+                float4 h, l;
+                split_one(x[j].x, h.x, l.x);
+                split_one(x[j].y, h.y, l.y);
+                split_one(x[j].z, h.z, l.z);
+                split_one(x[j].w, h.w, l.w);
+                hi[ct + j * CONV_THREADS] = h;
+                lo[ct + j * CONV_THREADS] = l;
+            }
+            tc::fence_proxy_async_smem();
+            mbar_arrive(bar_conv + 8 * s);
+        }
     } else {
         // ------------------------------------------------------------ accumulator warps (2..9)
         const int lane_grp = warp & 3;                       // TMEM lanes 32*lane_grp .. +31
@@ -404,7 +456,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int r0 = (int)(BM * rank / nsplit), r1 = (int)(BM * (rank + 1) / nsplit);
         const float alpha = p.alpha, beta = p.beta;
         if (!any_abort) {
-            for (int idx = threadIdx.x; idx < (r1 - r0) * (BN / 4); idx += THREADS) {
+            for (int idx = threadIdx.x; idx < (r1 - r0) * (BN / 4); idx += NTHREADS) {
                 const int r = r0 + idx / (BN / 4), c4 = idx % (BN / 4);
                 const int row = m0 + r, col = n0 + 4 * c4;
                 const uint32_t off = part0 + (uint32_t)(r * PART_PITCH + 4 * c4) * 4u;

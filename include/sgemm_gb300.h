@@ -241,6 +241,7 @@ typedef struct sgemm_plan {
     int split_k;       /* CTAs sharing one tile along k (a thread-block cluster; 1 = no split) */
     int op_a, op_b;    /* SGEMM_OP_N / SGEMM_OP_T of the problem planned                      */
     int a_vec;         /* 1: A (stored k x m) loaded 16 bytes at a time (FFMA path)            */
+    int a_in_kernel;   /* 1: the tensor-core GEMM splits A itself (no split pass over A)       */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

@@ -155,8 +155,36 @@ def test_auto_policy():
     assert binding.plan(16, 16, 8193)[1]["path"] == binding.PATH_TF32X3
     assert binding.plan(1000, 1500, 777, lda=777)[1]["path"] == binding.PATH_TF32X3
     st, p = binding.plan(2048, 2048, 2048, path=binding.PATH_TF32X3)
-    assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"]) == (128, 256, 16, 320)
+    assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"]) == (128, 256, 16, 384)
     assert p["grid"] == p["tiles"] == 16 * 8 and p["k_tiles"] == 128
+
+
+def test_in_kernel_split_policy(monkeypatch):
+    """The tensor-core GEMM splits A itself (12 warps) when it can load A by
+    TMA -- untransposed, 16-byte aligned rows, one problem -- and n <= 4096;
+    otherwise a pre-pass splits A and the kernel runs 10 warps.  The tuning
+    variable pins the choice but cannot make an unaligned A eligible."""
+    monkeypatch.delenv("SGEMM_GB300_SPLIT_A_IN", raising=False)
+    TC = binding.PATH_TF32X3
+
+    def ain(m, n, k, **kw):
+        st, p = binding.plan(m, n, k, path=TC, **kw)
+        assert st == 0
+        assert p["threads"] == (384 if p["a_in_kernel"] else 320)
+        return p["a_in_kernel"]
+
+    assert ain(16384, 128, 8192) == 1
+    assert ain(8192, 4096, 8192) == 1
+    assert ain(8192, 4097, 8192) == 0
+    assert ain(8192, 8192, 8192) == 0
+    assert ain(1000, 1500, 777) == 0                 # lda = 777: rows not 16-byte aligned
+    assert ain(1000, 1500, 777, lda=780) == 1
+    assert ain(1000, 1500, 780, A_ptr=20) == 0       # A not 16-byte aligned
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "0")
+    assert ain(16384, 128, 8192) == 0
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "1")
+    assert ain(8192, 8192, 8192) == 1
+    assert ain(1000, 1500, 777) == 0
 
 
 def test_op_argument_checks():
