@@ -168,6 +168,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "ffma": ["ffma_sgemm.cuh", "ptx.cuh", "raster.cuh"],
     "tf32x3": ["tf32x3_sgemm.cuh", "tcgen05.cuh", "ptx.cuh", "raster.cuh"],
+    "tf32x3_a_in": ["tf32x3_sgemm.cuh", "tcgen05.cuh", "ptx.cuh", "raster.cuh"],
 }
 
 
@@ -185,18 +186,20 @@ def kernel_source_hash(family):
 
 def traffic_record(kernel_family, units):
     """DRAM bytes per launch (read + write) of the kernel from the committed
-    ncu summary when it was captured on this size (`units` = m*n*k), else
-    None; None too when the kernel sources changed since the capture."""
+    ncu summaries (`profiles/traffic.json`: per kernel family, one record per
+    captured size) when one was captured on this size (`units` = m*n*k),
+    else None; None too when the kernel sources changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
-            rec = json.load(fh).get(kernel_family)
+            recs = json.load(fh).get(kernel_family)
     except (OSError, ValueError):
         return None
-    if not rec or rec.get("source_hash") != kernel_source_hash(kernel_family):
-        return None
-    if rec.get("units") == units:
-        return rec.get("dram_bytes_per_launch")
+    if isinstance(recs, dict):
+        recs = [recs]
+    for rec in recs or ():
+        if rec.get("source_hash") == kernel_source_hash(kernel_family) and rec.get("units") == units:
+            return rec.get("dram_bytes_per_launch")
     return None
 
 
@@ -444,41 +447,61 @@ def run_ours(args, rank, world):
                 "unit": "TFLOP/s", "frac": achieved / ffma_peak, "peak_basis": ffma_basis,
                 "traffic": traffic_record("ffma", p.m * p.n * p.k)}
     else:
-        # the step is split_a + split_bt + the tcgen05 GEMM; the GEMM kernel
-        # alone is timed on operands split once, through the split-GEMM call
-        launches_per_step = 3
         ka = binding.ka_of(p.k)
-        a_hi = torch.empty(p.m * ka, device="cuda")
-        a_lo = torch.empty_like(a_hi)
         b_hi = torch.empty(p.n * ka, device="cuda")
         b_lo = torch.empty_like(b_hi)
-        binding.tf32x3_split_a(A[:, :p.k], a_hi, a_lo)
-        binding.tf32x3_split_b(B[:, :p.n], b_hi, b_lo)
+        a_in = bool(plan["a_in_kernel"])
+        if a_in:
+            # the step is split_bt + the tcgen05 GEMM splitting A itself; the
+            # GEMM kernel's time is the step's minus split_bt timed alone
+            launches_per_step = 2
 
-        def gemm_only():
-            s = binding.tf32x3_split_gemm_raw(p.m, p.n, p.k, p.alpha, a_hi.data_ptr(), a_lo.data_ptr(),
-                                               b_hi.data_ptr(), b_lo.data_ptr(), p.beta, C.data_ptr(), p.ldc,
-                                               sptr)
-            if s:
-                raise SystemExit(f"split gemm failed: {binding.status_string(s)}")
+            def split_b_only():
+                binding.tf32x3_split_b(B[:, :p.n], b_hi, b_lo)
 
-        for _ in range(3):
-            gemm_only()
-        gm = time_launches(gemm_only, stream, min(args.steps, 100), flush=flush)
-        gemm_ms = sum(gm) / len(gm)
-        del a_hi, a_lo, b_hi, b_lo
+            for _ in range(3):
+                split_b_only()
+            sb = time_launches(split_b_only, stream, min(args.steps, 100), flush=flush)
+            gemm_ms = mean_ms - sum(sb) / len(sb)
+            gemm_timing = "whole call minus split_bt_kernel timed alone (CUDA events)"
+        else:
+            # the step is split_a + split_bt + the tcgen05 GEMM; the GEMM
+            # kernel alone is timed on operands split once, through the
+            # split-GEMM call
+            launches_per_step = 3
+            a_hi = torch.empty(p.m * ka, device="cuda")
+            a_lo = torch.empty_like(a_hi)
+            binding.tf32x3_split_a(A[:, :p.k], a_hi, a_lo)
+            binding.tf32x3_split_b(B[:, :p.n], b_hi, b_lo)
+
+            def gemm_only():
+                s = binding.tf32x3_split_gemm_raw(p.m, p.n, p.k, p.alpha, a_hi.data_ptr(), a_lo.data_ptr(),
+                                                   b_hi.data_ptr(), b_lo.data_ptr(), p.beta, C.data_ptr(),
+                                                   p.ldc, sptr)
+                if s:
+                    raise SystemExit(f"split gemm failed: {binding.status_string(s)}")
+
+            for _ in range(3):
+                gemm_only()
+            gm = time_launches(gemm_only, stream, min(args.steps, 100), flush=flush)
+            gemm_ms = sum(gm) / len(gm)
+            gemm_timing = "split-GEMM call on operands split once (CUDA events)"
+            del a_hi, a_lo
+        del b_hi, b_lo
         achieved = tflops(p, gemm_ms)
         mp = measured_peaks()
         bf16 = (mp or {}).get("bf16_tflops", 1900.0)
         tf32 = bf16 * NOMINAL_TF32_OVER_BF16
-        roof = {"bound": "tensor", "kernel": "tf32x3_gemm_kernel", "achieved": achieved, "peak": tf32 / 3,
+        family = "tf32x3_a_in" if a_in else "tf32x3"
+        roof = {"bound": "tensor", "kernel": "tf32x3_gemm_kernel" + ("<A split in kernel>" if a_in else ""),
+                "achieved": achieved, "peak": tf32 / 3,
                 "unit": "TFLOP/s", "frac": achieved / (tf32 / 3),
                 "peak_basis": f"TF32 dense peak / 3 (three TF32 products per FP32 product); TF32 peak = "
                               f"measured bf16 {bf16} TFLOP/s ({'of measured' if mp else 'of fallback'}) x "
                               f"nominal tf32/bf16 ratio 1.1/2.25 = {tf32:.1f} TFLOP/s",
-                "gemm_kernel_ms": gemm_ms, "split_kernels_ms": mean_ms - gemm_ms,
-                "tensor_pipe_tflops": 3 * achieved,
-                "traffic": traffic_record("tf32x3", p.m * p.n * p.k)}
+                "gemm_kernel_ms": gemm_ms, "gemm_kernel_timing": gemm_timing,
+                "split_kernels_ms": mean_ms - gemm_ms, "tensor_pipe_tflops": 3 * achieved,
+                "traffic": traffic_record(family, p.m * p.n * p.k)}
     roof["ffma_peak_tflops"] = ffma_peak
     roof["value_over_ffma_peak"] = value / world / ffma_peak
 

@@ -98,3 +98,20 @@ def test_workload_names_match_the_generator():
     args = bench.parse(["--workload", "1000x1500x777"])
     p, text = bench.load_problem(args)
     assert (p.m, p.n, p.k, p.lda) == (1000, 1500, 777, 777) and "1000x1500x777" in text
+
+
+def test_traffic_record_matches_size_and_sources(tmp_path, monkeypatch):
+    """The ncu DRAM figure is reported only for the size it was captured on
+    and only while the kernel's sources are unchanged."""
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    h = bench.kernel_source_hash("tf32x3_a_in")
+    recs = {"tf32x3_a_in": [{"units": 10, "source_hash": h, "dram_bytes_per_launch": 111},
+                            {"units": 20, "source_hash": "stale", "dram_bytes_per_launch": 222}],
+            "ffma": {"units": 30, "source_hash": bench.kernel_source_hash("ffma"), "dram_bytes_per_launch": 333}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(recs))
+    assert bench.traffic_record("tf32x3_a_in", 10) == 111
+    assert bench.traffic_record("tf32x3_a_in", 20) is None      # sources changed since the capture
+    assert bench.traffic_record("tf32x3_a_in", 30) is None      # never captured at this size
+    assert bench.traffic_record("ffma", 30) == 333              # single-record form
+    assert bench.traffic_record("tf32x3", 10) is None
