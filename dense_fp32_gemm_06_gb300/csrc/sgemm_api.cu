@@ -28,6 +28,11 @@ struct DeviceState {
     // clusters of S CTAs (S = 2..8) of the tensor-core kernel that fit on the
     // device at once, for the 256- and 128-wide tiles ([0] and [1])
     int max_clusters[2][9] = {};
+    // stream-ordered pool of the tensor-core path's scratch; keeps up to
+    // its release threshold mapped between calls (the default pool's
+    // threshold is 0: every synchronize would unmap the scratch and the next
+    // call map it again, ~0.1 ms each time)
+    cudaMemPool_t pool = nullptr;
 };
 
 std::mutex g_mu;
@@ -81,12 +86,12 @@ int ffma_smem_bytes(int akind, int bkind) {
                       : akind == 1 ? ffma_smem_b<ALoadVec>(bkind) : ffma_smem_b<ALoadScalar>(bkind);
 }
 
-template <class Cfg, bool CV>
+template <class Cfg, bool CV, bool TRANS = false>
 cudaError_t set_tc_attr() {
-    cudaError_t e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV, false>,
+    cudaError_t e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV, false, TRANS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV, true>,
+        e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV, true, TRANS>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
     return e;
 }
@@ -128,9 +133,26 @@ int device_state(DeviceState **out) {
         if ((e = set_tc_attr<tf32x3::Wide, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Narrow, true>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Narrow, false>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_tc_attr<tf32x3::Wide, false, true>()) != cudaSuccess) return fail_cuda(e);
         for (int S = 2; S <= 8; ++S) {
             if ((e = max_clusters_of<tf32x3::Wide>(S, &d.max_clusters[0][S])) != cudaSuccess) return fail_cuda(e);
             if ((e = max_clusters_of<tf32x3::Narrow>(S, &d.max_clusters[1][S])) != cudaSuccess) return fail_cuda(e);
+        }
+        if (d.pool == nullptr) {
+            cudaMemPoolProps props = {};
+            props.allocType = cudaMemAllocationTypePinned;
+            props.location.type = cudaMemLocationTypeDevice;
+            props.location.id = dev;
+            if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) {
+                d.pool = nullptr;
+                return fail_cuda(e);
+            }
+            unsigned long long keep_mb = 2048;
+            if (const char *env = std::getenv("SGEMM_GB300_POOL_KEEP_MB"))
+                if (env[0] >= '0' && env[0] <= '9') keep_mb = std::strtoull(env, nullptr, 10);
+            cuuint64_t thr = (cuuint64_t)keep_mb << 20;
+            if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &thr)) != cudaSuccess)
+                return fail_cuda(e);
         }
         if (g_encode_tiled == nullptr) {
             cudaDriverEntryPointQueryResult q;
@@ -213,14 +235,16 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         pl->bk = tf32x3::BK;
         pl->threads = tf32x3::THREADS;
         pl->b_vec = 1;
-        // Tile width BN and split-K factor S: the pair with the smallest
-        // estimated time waves x ceil(KT / S) x (slab time) (+ a fixed cost
-        // for a split's cluster reduction).  Slab times, measured on GB300:
-        // a 256-wide slab ~0.5 us, a 128-wide one ~0.375 us (1.5x the time
-        // per FLOP); a split adds ~6 us.  Units below: 1/8 us.  Waves count
-        // CTAs against the SMs (S = 1) or clusters against the clusters that
-        // fit at once (S > 1); a split must fit in one wave and leave each
-        // CTA >= 8 slabs (128 k).
+        // Tile shape and split-K factor S: the pair with the smallest
+        // estimated time waves x ceil(KT / S) x (slab time) (+ the cost of a
+        // split's cluster reduction).  Slab times, measured on GB300: a
+        // 256-wide slab ~0.5 us, a 128-wide one ~0.375 us (1.5x the time per
+        // FLOP), a transposed 256 x 128 one ~0.66 us (split-K cases: its
+        // 16 KB of A to split and its column-wise stores); a split adds
+        // ~5 us + 0.9 us per CTA of the cluster.  Units below: 1/32 us.
+        // Waves count CTAs against the SMs (S = 1) or
+        // clusters against the clusters that fit at once (S > 1); a split
+        // must fit in one wave and leave each CTA >= 8 slabs (128 k).
         const int tiles_m = (m + pl->bm - 1) / pl->bm;
         const long long KT = (k + tf32x3::BK - 1) / tf32x3::BK;
         // tuning overrides for benchmarks and tests: SGEMM_GB300_TILE_N (128
@@ -229,17 +253,32 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         const char *env_s = std::getenv("SGEMM_GB300_SPLIT_K");
         const int force_bn = env_bn ? std::atoi(env_bn) : 0;
         const int force_s = env_s ? std::atoi(env_s) : 0;
+        // Candidates: 256-wide tiles, 128-wide tiles, and for n <= 128 the
+        // transposed tile (C^T = B^T A^T: 256 rows of C by 128 columns), which
+        // keeps the MMA 256 wide -- a 128 x 128 x 8 MMA takes about as long
+        // as a 128 x 256 x 8 one.  SGEMM_GB300_TRANS (0 / 1) pins the last.
+        const char *env_tr = std::getenv("SGEMM_GB300_TRANS");
+        const int force_tr = env_tr && (env_tr[0] == '0' || env_tr[0] == '1') ? env_tr[0] - '0' : -1;
         long long best = -1;
         int best_bn = tf32x3::Wide::BN, best_s = 1;
-        for (int bn : {tf32x3::Wide::BN, tf32x3::Narrow::BN}) {
-            if (force_bn == tf32x3::Wide::BN || force_bn == tf32x3::Narrow::BN) {
+        bool best_tr = false;
+        for (int cand = 0; cand < 3; ++cand) {
+            const bool tr = cand == 2;
+            const int bn = cand == 1 ? tf32x3::Narrow::BN : tf32x3::Wide::BN;
+            if (tr) {
+                if (force_tr == 0 || n > tf32x3::BM || (force_bn != 0 && force_tr != 1)) continue;
+            } else if (force_tr == 1 && n <= tf32x3::BM) {
+                continue;
+            } else if (force_bn == tf32x3::Wide::BN || force_bn == tf32x3::Narrow::BN) {
                 if (bn != force_bn) continue;
             } else if (bn == tf32x3::Wide::BN && n <= tf32x3::Narrow::BN) {
                 continue;
             }
             const int wi = bn == tf32x3::Wide::BN ? 0 : 1;
-            const long long slab = bn == tf32x3::Wide::BN ? 4 : 3;
-            const long long tiles = (long long)tiles_m * ((n + bn - 1) / bn) * (batch > 0 ? batch : 1);
+            const long long slab = tr ? 21 : bn == tf32x3::Wide::BN ? 16 : 12;
+            const long long tiles = tr ? (long long)((m + tf32x3::Wide::BN - 1) / tf32x3::Wide::BN) *
+                                             ((n + tf32x3::BM - 1) / tf32x3::BM) * (batch > 0 ? batch : 1)
+                                       : (long long)tiles_m * ((n + bn - 1) / bn) * (batch > 0 ? batch : 1);
             for (int S = 1; S <= 8; ++S) {
                 if (force_s >= 1 && force_s <= 8) {
                     if (S != force_s) continue;
@@ -253,11 +292,12 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
                     if (slots <= 0 || (tiles > slots && !(force_s >= 1 && force_s <= 8))) continue;
                 }
                 const long long waves = (tiles + slots - 1) / slots;
-                const long long cost = waves * ((KT + S - 1) / S) * slab + (S > 1 ? 48 : 0);
+                const long long cost = waves * ((KT + S - 1) / S) * slab + (S > 1 ? 160 + 28 * S : 0);
                 if (best < 0 || cost < best) {
                     best = cost;
                     best_bn = bn;
                     best_s = S;
+                    best_tr = tr;
                 }
             }
         }
@@ -279,15 +319,19 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
             pl->a_in_kernel = a_tma && n <= 4096;
         pl->threads = tf32x3::threads_for(pl->a_in_kernel != 0);
         const bool narrow = best_bn == tf32x3::Narrow::BN;
-        pl->bn = best_bn;
+        pl->trans = best_tr;
+        // bm x bn: the tile of C (256 x 128 when transposed)
+        pl->bm = best_tr ? tf32x3::Wide::BN : tf32x3::BM;
+        pl->bn = best_tr ? tf32x3::BM : best_bn;
         pl->split_k = best_s;
         pl->stages = narrow ? tf32x3::Narrow::STAGES : tf32x3::Wide::STAGES;
         pl->smem_bytes = narrow ? tf32x3::Narrow::SMEM_BYTES : tf32x3::Wide::SMEM_BYTES;
+        const int tiles_mt = (m + pl->bm - 1) / pl->bm;
         const int tiles_n = (n + pl->bn - 1) / pl->bn;
-        pl->tiles = tiles_m * tiles_n;
+        pl->tiles = tiles_mt * tiles_n;
         pl->grid = pl->tiles * pl->split_k;
         pl->k_tiles = (int)KT;
-        pl->group_m = tiles_m < 8 ? tiles_m : 8;
+        pl->group_m = tiles_mt < 8 ? tiles_mt : 8;
         return SGEMM_STATUS_OK;
     }
     pl->kernel = kKernelFfmaCpAsync;
@@ -375,6 +419,13 @@ template <class Cfg>
 cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, const sgemm_plan &pl, const CUtensorMap &ahi,
                       const CUtensorMap &alo, const CUtensorMap &bhi, const CUtensorMap &blo,
                       const tf32x3::Params &a) {
+    if constexpr (Cfg::BN == tf32x3::Wide::BN) {
+        if (pl.trans)   // C^T tiles (256-wide only): scalar stores along n, C_VEC unused
+            return pl.a_in_kernel ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, true, true>, ahi,
+                                                       alo, bhi, blo, a)
+                                  : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, false, true>, ahi,
+                                                       alo, bhi, blo, a);
+    }
     if (pl.a_in_kernel)
         return pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, true, true>, ahi, alo, bhi, blo, a)
                         : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, true>, ahi, alo, bhi, blo,
@@ -395,9 +446,10 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     // with the A split in the kernel, a_hi is the caller's A (row pitch
     // a_ld) and a_lo is not read
     const int a_pitch = pl.a_in_kernel ? a_ld : ka;
-    int st = make_tensor_map(&t_ahi, a_hi, am, k, a_pitch, tf32x3::BM, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    // boxes: a tile's rows of A (pl.bm) and of B^T (pl.bn)
+    int st = make_tensor_map(&t_ahi, a_hi, am, k, a_pitch, pl.bm, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st)
-        st = make_tensor_map(&t_alo, pl.a_in_kernel ? a_hi : a_lo, am, k, a_pitch, tf32x3::BM, tf32x3::BK,
+        st = make_tensor_map(&t_alo, pl.a_in_kernel ? a_hi : a_lo, am, k, a_pitch, pl.bm, tf32x3::BK,
                              CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st) st = make_tensor_map(&t_bhi, bt_hi, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st) st = make_tensor_map(&t_blo, bt_lo, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
@@ -428,7 +480,7 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     cfg.attrs = attr;
     cfg.numAttrs = pl.split_k > 1 ? 1 : 0;
     cudaError_t e;
-    if (pl.bn == tf32x3::Narrow::BN)
+    if (pl.bn == tf32x3::Narrow::BN && !pl.trans)
         e = launch_tc<tf32x3::Narrow>(cfg, pl, t_ahi, t_alo, t_bhi, t_blo, a);
     else
         e = launch_tc<tf32x3::Wide>(cfg, pl, t_ahi, t_alo, t_bhi, t_blo, a);
@@ -439,12 +491,14 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
 // 3xTF32 path of sgemm: split A and B^T into a stream-ordered scratch
 // buffer, run the tcgen05 GEMM, release the scratch.
 int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
-                  float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream, const Batch &bt = Batch()) {
+                  float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream, cudaMemPool_t pool,
+                  const Batch &bt = Batch()) {
     const size_t a_elems = pl.a_in_kernel ? 0 : (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
     const size_t cnt = (size_t)bt.count;
     float *ws = nullptr;
     cudaError_t e =
-        cudaMallocAsync(reinterpret_cast<void **>(&ws), 2 * cnt * (a_elems + b_elems) * sizeof(float), stream);
+        cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), 2 * cnt * (a_elems + b_elems) * sizeof(float), pool,
+                                stream);
     if (e != cudaSuccess) return fail_cuda(e);
     float *a_hi = ws, *a_lo = ws + cnt * a_elems, *b_hi = a_lo + cnt * a_elems, *b_lo = b_hi + cnt * b_elems;
     // both split operands are k-contiguous (K-major): an operand stored with
@@ -574,7 +628,8 @@ int sgemm_strided_batched(int op_a, int op_b, int m, int n, int k, float alpha, 
         if (pl.kernel == kKernelScale) {
             scale_c_kernel<<<dim3(pl.grid, cnt), pl.threads, 0, stream>>>(Cb, ldc, m, n, beta, stride_c);
         } else if (pl.kernel == kKernelTf32x3) {
-            if ((st = launch_tf32x3(m, n, k, alpha, Ab, lda, Bb, ldb, beta, Cb, ldc, pl, stream, bt))) return st;
+            if ((st = launch_tf32x3(m, n, k, alpha, Ab, lda, Bb, ldb, beta, Cb, ldc, pl, stream, dev->pool, bt)))
+                return st;
         } else {
             GemmArgs a;
             a.m = m;

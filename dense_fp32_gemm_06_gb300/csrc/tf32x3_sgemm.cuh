@@ -47,6 +47,12 @@
 //     distributed shared memory (ld.shared::cluster) and writes them to C,
 //     then a second cluster barrier keeps every partial alive until read.
 //     The reduction order is fixed, so results do not depend on timing.
+//     Narrow problems (n <= 128, TRANS): a 128 x 128 x 8 MMA takes about
+//     as long as a 128 x 256 x 8 one, so these compute tiles of
+//     C^T = B^T A^T instead -- the MMA's 128-row operand is B^T (the n side),
+//     its 256-row operand is A (256 rows of C per tile) -- and the
+//     accumulator warps store C^T's rows as columns of C (each warp's 32
+//     lanes are 32 consecutive columns: 128-byte stores).
 //     TMA zero-fills rows past m, columns past n and k past the end, so the
 //     MMA never sees an index test.  Every mbarrier wait is bounded (2 s):
 //     a wait that runs out records a code in the library status word,
@@ -123,6 +129,16 @@ struct Params {
 __device__ __forceinline__ void split_one(float x, float &h, float &l) {
     h = tc::round_tf32(x);
     l = tc::round_tf32(x - h);
+}
+
+// The lo part of x when x itself is the MMA's hi operand: a kind::tf32 MMA
+// reads an FP32 operand with its low 13 mantissa bits dropped (measured on
+// GB300: every output of x * I equals x truncated to TF32, ties and all), so
+// hi = trunc(x); x - hi is exact in FP32 and lo = tf32(x - hi), rounded to
+// nearest, with |x - hi - lo| <= 2^-11 |x - hi| < 2^-21 |x|.
+__device__ __forceinline__ float lo_of_raw(float x) {
+    const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    return tc::round_tf32(x - h);
 }
 
 // A (m x k, row pitch lda) -> hi, lo (m x ka, row pitch ka).  VEC: A and
@@ -203,13 +219,18 @@ __global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__
 // ---------------------------------------------------------------- GEMM kernel
 
 // A_IN: A is split here instead of by split_a_kernel -- TMA loads the raw
-// FP32 A slab into the A_hi slot, two extra warps (10, 11) turn it into hi
-// (in place) and lo (the A_lo slot) as soon as it lands, make the writes
-// visible to the tensor core's proxy and arrive on the slot's "converted"
-// barrier, which the MMA issuer waits for besides "full".  The splitters
-// run ahead of the MMA by up to the ring depth, so the split hides behind
-// the tensor core instead of costing an HBM round trip of A.
-template <class Cfg, bool C_VEC, bool A_IN = false>
+// FP32 A slab into A's hi slot and the MMA reads it as it is (hi = x with
+// the low 13 mantissa bits dropped, which is how a kind::tf32 MMA reads an
+// FP32 operand).  Two extra warps (10, 11) compute lo = tf32(x - hi) into
+// A's lo slot as soon as the slab lands, make the writes visible to the
+// tensor core's proxy and arrive on the slot's "converted" barrier.  The MMA
+// issuer sends the two products that do not need A's lo as soon as the slab
+// lands and waits for "converted" only before the third, so the split
+// overlaps the tensor core instead of costing an HBM round trip of A.
+// Error: |x - hi - lo| < 2^-21 |x| and |lo| < 2^-10 |x| (against 2^-22 and
+// 2^-11 for the pre-pass's round-to-nearest hi), so each product stays
+// within ~2^-20 |a b| of exact, far inside the FP32 acceptance bound.
+template <class Cfg, bool C_VEC, bool A_IN = false, bool TRANS = false>
 __global__ void __launch_bounds__(threads_for(A_IN), 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
                        const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
@@ -218,6 +239,9 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     constexpr int TMEM_COLS = Cfg::TMEM_COLS, COLS_PER_THREAD = Cfg::COLS_PER_THREAD;
     constexpr int PART_PITCH = BN + 4;   // floats per row of a parked split-K partial tile
     constexpr int NTHREADS = threads_for(A_IN);
+    constexpr bool CONV_PER_WARP = BN == 128;   // A splitters: one warp per slab (see there)
+    // where A sits in a stage (the MMA's A operand, or its B operand when TRANS)
+    constexpr int SPLIT_OFF = TRANS ? 2 * A_TILE : 0, SPLIT_BYTES = TRANS ? B_TILE : A_TILE;
     static_assert(BM * PART_PITCH * 4 <= STAGES * STAGE_BYTES, "partial tile fits the stage memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *const smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -239,7 +263,10 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     const uint32_t nsplit = tc::cluster_nctarank(), rank = tc::cluster_ctarank();
     int tm, tn;
     raster_tile(blockIdx.x / nsplit, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-    const int m0 = tm * BM, n0 = tn * BN;
+    // TRANS: the tile is BN rows of C by BM columns (C^T = B^T A^T: the
+    // MMA's 128-row operand is B^T, its BN-row operand is A)
+    constexpr int TILE_M = TRANS ? BN : BM, TILE_N = TRANS ? BM : BN;
+    const int m0 = tm * TILE_M, n0 = tn * TILE_N;
     // rows of this batch problem's operands inside the stacked split arrays
     const int arow0 = (int)blockIdx.y * p.m + m0, brow0 = (int)blockIdx.y * p.n + n0;
     float *const Cb = p.C + (long long)blockIdx.y * p.stride_c;
@@ -259,7 +286,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
         }
         mbar_init(bar_done, 1);
         if (A_IN)
-            for (int s = 0; s < STAGES; ++s) mbar_init(bar_conv + 8 * s, CONV_THREADS);
+            for (int s = 0; s < STAGES; ++s) mbar_init(bar_conv + 8 * s, CONV_PER_WARP ? 32 : CONV_THREADS);
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmAhi);
@@ -289,12 +316,21 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                 if (*abort_flag) break;
                 const uint32_t st = stage0 + s * STAGE_BYTES;
                 const uint32_t fb = bar_full + 8 * s;
-                mbar_arrive_expect_tx(fb, A_IN ? STAGE_BYTES - A_TILE : STAGE_BYTES);
+                mbar_arrive_expect_tx(fb, A_IN ? STAGE_BYTES - SPLIT_BYTES : STAGE_BYTES);
                 const int kx = (kt0 + kt) * BK;
-                tma_load_2d(st, &tmAhi, kx, arow0, fb);   // raw A when A_IN
-                if (!A_IN) tma_load_2d(st + A_TILE, &tmAlo, kx, arow0, fb);
-                tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, brow0, fb);
-                tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, brow0, fb);
+                // slots [MMA A hi | MMA A lo | MMA B hi | MMA B lo]; raw A
+                // into A's hi slot and nothing into its lo slot when A_IN
+                if constexpr (!TRANS) {
+                    tma_load_2d(st, &tmAhi, kx, arow0, fb);
+                    if (!A_IN) tma_load_2d(st + A_TILE, &tmAlo, kx, arow0, fb);
+                    tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, brow0, fb);
+                    tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, brow0, fb);
+                } else {
+                    tma_load_2d(st, &tmBhi, kx, brow0, fb);
+                    tma_load_2d(st + A_TILE, &tmBlo, kx, brow0, fb);
+                    tma_load_2d(st + 2 * A_TILE, &tmAhi, kx, arow0, fb);
+                    if (!A_IN) tma_load_2d(st + 2 * A_TILE + B_TILE, &tmAlo, kx, arow0, fb);
+                }
                 ++issued;
             }
             if (*abort_flag) {
@@ -317,24 +353,57 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                     break;
                 }
                 const int s = kt % STAGES;
-                if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusMma) ||
-                    (A_IN && !mbar_wait(bar_conv + 8 * s, (kt / STAGES) & 1, kStatusMma))) {
+                if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusMma)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc::fence_after_sync();
                 const uint32_t st = stage0 + s * STAGE_BYTES;
                 const uint32_t d = tmem + (uint32_t)(b * BN);
+                if constexpr (!A_IN) {
 #pragma unroll
-                for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                    const uint32_t off = kk * UMMA_K * 4;   // 32 bytes along the 64-byte row
-                    const uint64_t a_hi = tc::desc_kmajor_sw64(st + off);
-                    const uint64_t a_lo = tc::desc_kmajor_sw64(st + A_TILE + off);
-                    const uint64_t b_hi = tc::desc_kmajor_sw64(st + 2 * A_TILE + off);
-                    const uint64_t b_lo = tc::desc_kmajor_sw64(st + 2 * A_TILE + B_TILE + off);
-                    tc::mma_tf32(d, a_hi, b_hi, idesc, (chunk_first && kk == 0) ? 0u : 1u);
-                    tc::mma_tf32(d, a_hi, b_lo, idesc, 1u);
-                    tc::mma_tf32(d, a_lo, b_hi, idesc, 1u);
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint32_t off = kk * UMMA_K * 4;   // 32 bytes along the 64-byte row
+                        const uint64_t a_hi = tc::desc_kmajor_sw64(st + off);
+                        const uint64_t a_lo = tc::desc_kmajor_sw64(st + A_TILE + off);
+                        const uint64_t b_hi = tc::desc_kmajor_sw64(st + 2 * A_TILE + off);
+                        const uint64_t b_lo = tc::desc_kmajor_sw64(st + 2 * A_TILE + B_TILE + off);
+                        tc::mma_tf32(d, a_hi, b_hi, idesc, (chunk_first && kk == 0) ? 0u : 1u);
+                        tc::mma_tf32(d, a_hi, b_lo, idesc, 1u);
+                        tc::mma_tf32(d, a_lo, b_hi, idesc, 1u);
+                    }
+                } else {
+                    // A's hi slot holds raw A (read as hi = A with its low 13
+                    // bits dropped): the two products without A's lo go first,
+                    // the third once the splitters have written A's lo
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint32_t off = kk * UMMA_K * 4;
+                        const uint64_t a_hi = tc::desc_kmajor_sw64(st + off);
+                        const uint64_t a_lo = tc::desc_kmajor_sw64(st + A_TILE + off);
+                        const uint64_t b_hi = tc::desc_kmajor_sw64(st + 2 * A_TILE + off);
+                        const uint64_t b_lo = tc::desc_kmajor_sw64(st + 2 * A_TILE + B_TILE + off);
+                        tc::mma_tf32(d, a_hi, b_hi, idesc, (chunk_first && kk == 0) ? 0u : 1u);
+                        if (TRANS)
+                            tc::mma_tf32(d, a_lo, b_hi, idesc, 1u);   // B^T lo x raw A
+                        else
+                            tc::mma_tf32(d, a_hi, b_lo, idesc, 1u);   // raw A x B^T lo
+                    }
+                    if (!mbar_wait(bar_conv + 8 * s, (kt / STAGES) & 1, kStatusMma)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    tc::fence_after_sync();
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint32_t off = kk * UMMA_K * 4;
+                        if (TRANS)   // B^T hi x A lo
+                            tc::mma_tf32(d, tc::desc_kmajor_sw64(st + off),
+                                         tc::desc_kmajor_sw64(st + 2 * A_TILE + B_TILE + off), idesc, 1u);
+                        else         // A lo x B^T hi
+                            tc::mma_tf32(d, tc::desc_kmajor_sw64(st + A_TILE + off),
+                                         tc::desc_kmajor_sw64(st + 2 * A_TILE + off), idesc, 1u);
+                    }
                 }
                 tc::commit(bar_empty + 8 * s);
                 if (chunk_last) tc::commit(bar_tfull + 8 * b);
@@ -346,31 +415,32 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
         __syncwarp();
     } else if (A_IN && warp >= 2 + ACC_WARPS) {
         // ------------------------------------------------------------ A splitters (warps 10, 11)
-        const int ct = threadIdx.x - (64 + ACC_THREADS);   // 0 .. CONV_THREADS - 1
-        for (int kt = 0; kt < KT; ++kt) {
+        // 128-wide tiles give the tensor core ~400 cycles per slab, less
+        // than one slab's split takes end to end, so there each warp splits
+        // whole slabs, alternating (two in flight); 256-wide tiles leave
+        // enough time for both warps to split each slab together.
+        constexpr int CW = CONV_PER_WARP ? 32 : CONV_THREADS;   // threads per slab
+        const int ct = CONV_PER_WARP ? lane : (int)threadIdx.x - (64 + ACC_THREADS);
+        const int kt_first = CONV_PER_WARP ? warp - (2 + ACC_WARPS) : 0;
+        for (int kt = kt_first; kt < KT; kt += CONV_PER_WARP ? CONV_WARPS : 1) {
             const int s = kt % STAGES;
             if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusSplit)) {
                 *abort_flag = 1;
                 break;
             }
             if (*abort_flag) break;
-            // raw slab -> hi in place, lo into the A_lo slot (same swizzled
-            // positions: the split is elementwise)
-            float4 *hi = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES);
-            float4 *lo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + A_TILE);
-            float4 x[A_TILE / 16 / CONV_THREADS];
+            // the raw slab stays as A's hi (the MMA reads it as hi = x with
+            // its low 13 bits dropped); lo = tf32(x - hi) goes into A's lo
+            // slot at the same swizzled position (the split is elementwise)
+            const float4 *raw = reinterpret_cast<const float4 *>(smem + s * STAGE_BYTES + SPLIT_OFF);
+            float4 *lo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + SPLIT_OFF + SPLIT_BYTES);
+            float4 x[SPLIT_BYTES / 16 / CW];
 #pragma unroll
-            for (int j = 0; j < A_TILE / 16 / CONV_THREADS; ++j) x[j] = hi[ct + j * CONV_THREADS];
+            for (int j = 0; j < SPLIT_BYTES / 16 / CW; ++j) x[j] = raw[ct + j * CW];
 #pragma unroll
-            for (int j = 0; j < A_TILE / 16 / CONV_THREADS; ++j) {
-                float4 h, l;
-                split_one(x[j].x, h.x, l.x);
-                split_one(x[j].y, h.y, l.y);
-                split_one(x[j].z, h.z, l.z);
-                split_one(x[j].w, h.w, l.w);
-                hi[ct + j * CONV_THREADS] = h;
-                lo[ct + j * CONV_THREADS] = l;
-            }
+            for (int j = 0; j < SPLIT_BYTES / 16 / CW; ++j)
+                lo[ct + j * CW] = make_float4(lo_of_raw(x[j].x), lo_of_raw(x[j].y), lo_of_raw(x[j].z),
+                                              lo_of_raw(x[j].w));
             tc::fence_proxy_async_smem();
             mbar_arrive(bar_conv + 8 * s);
         }
@@ -402,7 +472,8 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
             tc::fence_before_sync();
             mbar_arrive(bar_tempty + 8 * b);
         }
-        const int row = m0 + lane_grp * 32 + lane;
+        // this thread's TMEM lane: a row of C, or a column of C when TRANS
+        const int row = (TRANS ? n0 : m0) + lane_grp * 32 + lane;
         if (nsplit > 1) {
             // park the partial tile in this CTA's (now idle) stage memory,
             // rows PART_PITCH floats apart (4 banks apart: conflict-free)
@@ -412,6 +483,21 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
             for (int q = 0; q < COLS_PER_THREAD / 4; ++q)
                 reinterpret_cast<float4 *>(part)[q] =
                     make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        } else if (TRANS) {
+            // C^T tile: lane = column `row` of C, registers = rows of C;
+            // the 32 lanes of a warp store 128 contiguous bytes of a C row
+            const int col = row;
+            if (ok && *abort_flag == 0 && col < p.n) {
+                const float alpha = p.alpha, beta = p.beta;
+                const int r0c = m0 + half * COLS_PER_THREAD;
+#pragma unroll
+                for (int j = 0; j < COLS_PER_THREAD; ++j) {
+                    if (r0c + j < p.m) {
+                        float *cp = Cb + (long long)(r0c + j) * p.ldc + col;
+                        *cp = beta != 0.f ? fmaf(alpha, acc[j], beta * *cp) : alpha * acc[j];
+                    }
+                }
+            }
         } else if (ok && *abort_flag == 0 && row < p.m) {
             const float alpha = p.alpha, beta = p.beta;
             float *crow = Cb + (long long)row * p.ldc;
@@ -457,7 +543,10 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
         const float alpha = p.alpha, beta = p.beta;
         if (!any_abort) {
             for (int idx = threadIdx.x; idx < (r1 - r0) * (BN / 4); idx += NTHREADS) {
-                const int r = r0 + idx / (BN / 4), c4 = idx % (BN / 4);
+                // TRANS: consecutive threads take consecutive tile rows (=
+                // columns of C), so the stores below stay coalesced
+                const int r = TRANS ? r0 + idx % (r1 - r0) : r0 + idx / (BN / 4);
+                const int c4 = TRANS ? idx / (r1 - r0) : idx % (BN / 4);
                 const int row = m0 + r, col = n0 + 4 * c4;
                 const uint32_t off = part0 + (uint32_t)(r * PART_PITCH + 4 * c4) * 4u;
                 float4 sum = tc::ld_cluster_v4(tc::map_shared_rank(off, 0));
@@ -468,9 +557,21 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                     sum.z += v.z;
                     sum.w += v.w;
                 }
+                const float a[4] = {sum.x, sum.y, sum.z, sum.w};
+                if constexpr (TRANS) {
+                    const int cc = n0 + r, rr = m0 + 4 * c4;   // column of C, first of 4 rows
+                    if (cc >= p.n) continue;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (rr + e < p.m) {
+                            float *cp = Cb + (long long)(rr + e) * p.ldc + cc;
+                            *cp = beta != 0.f ? fmaf(alpha, a[e], beta * *cp) : alpha * a[e];
+                        }
+                    }
+                    continue;
+                }
                 if (row >= p.m) continue;
                 float *crow = Cb + (long long)row * p.ldc;
-                const float a[4] = {sum.x, sum.y, sum.z, sum.w};
                 if (C_VEC && col + 3 < p.n) {
                     float4 o;
                     if (beta != 0.f) {

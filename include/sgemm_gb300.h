@@ -26,9 +26,14 @@
  * the current device can address).  The library keeps no pointer after the
  * call returns.  Per device it lazily caches kernel attributes.  The FFMA
  * path allocates nothing; the tensor-core path takes its split operands
- * (8 * (m + n) * ka bytes, ka = k rounded up to 4) from the device's default
- * stream-ordered memory pool for the duration of the call
- * (cudaMallocAsync / cudaFreeAsync on `stream`).  C must not overlap A or B.
+ * (8 * (m + n) * ka bytes, ka = k rounded up to 4; 8 * n * ka when the GEMM
+ * splits A itself) for the duration of the call from a stream-ordered
+ * memory pool that the library creates per device on first use
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`).  The pool keeps up
+ * to 2 GiB mapped between calls (environment variable
+ * SGEMM_GB300_POOL_KEEP_MB overrides it, read once per device), so repeated
+ * calls do not map and unmap device memory; it is released when the process
+ * exits.  C must not overlap A or B.
  *
  * Execution.  Every entry point that takes a stream enqueues its kernels on
  * `stream` (0 = the legacy default stream) of the current device and returns
@@ -137,7 +142,7 @@ int sgemm_strided_batched(int op_a, int op_b, int m, int n, int k, float alpha,
  * a_hi*b_hi + a_hi*b_lo + a_lo*b_hi on the tensor cores in 128-deep chunks
  * whose sums are added in FP32 on the CUDA cores.  sgemm_ex(...,
  * SGEMM_PATH_TF32X3) does all of it with a stream-ordered scratch buffer
- * (cudaMallocAsync / cudaFreeAsync on `stream`); a caller that multiplies
+ * (from the library's pool, on `stream`); a caller that multiplies
  * the same operand many times can split it once with these calls and reuse
  * it.
  *
@@ -242,6 +247,7 @@ typedef struct sgemm_plan {
     int op_a, op_b;    /* SGEMM_OP_N / SGEMM_OP_T of the problem planned                      */
     int a_vec;         /* 1: A (stored k x m) loaded 16 bytes at a time (FFMA path)            */
     int a_in_kernel;   /* 1: the tensor-core GEMM splits A itself (no split pass over A)       */
+    int trans;         /* 1: tensor-core tiles of C^T = B^T A^T (n <= 128; bm = 256, bn = 128) */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

@@ -215,3 +215,24 @@ def test_strided_batched_argument_checks():
     assert call(sc=19) == 16          # C matrices would overlap: (m-1)*ldc + n = 20
     assert call(batch=-1) == 17
     assert call(batch=0) == 0 and call(m=0) == 0
+
+
+def test_trans_tile_policy(monkeypatch):
+    """n <= 128 may take transposed 256 x 128 tiles (C^T = B^T A^T) when the
+    plan's estimate favours them; n > 128 never does; the tuning variable
+    pins the choice."""
+    for v in ("SGEMM_GB300_TRANS", "SGEMM_GB300_TILE_N", "SGEMM_GB300_SPLIT_K"):
+        monkeypatch.delenv(v, raising=False)
+    TC = binding.PATH_TF32X3
+    st, p = binding.plan(16384, 128, 8192, path=TC)
+    assert st == 0 and p["trans"] == 1 and (p["bm"], p["bn"], p["stages"]) == (256, 128, 4)
+    assert p["tiles"] == 64 and p["grid"] == 64 * p["split_k"]
+    assert binding.plan(65536, 64, 4096, path=TC)[1]["trans"] == 1
+    assert binding.plan(8192, 129, 8192, path=TC)[1]["trans"] == 0
+    assert binding.plan(8192, 8192, 8192, path=TC)[1]["trans"] == 0
+    monkeypatch.setenv("SGEMM_GB300_TRANS", "0")
+    assert binding.plan(16384, 128, 8192, path=TC)[1]["trans"] == 0
+    monkeypatch.setenv("SGEMM_GB300_TRANS", "1")
+    st, p = binding.plan(300, 100, 5000, path=TC)
+    assert p["trans"] == 1 and (p["bm"], p["bn"]) == (256, 128)
+    assert binding.plan(300, 200, 5000, path=TC)[1]["trans"] == 0
