@@ -451,24 +451,32 @@ def run_ours(args, rank, world):
         b_hi = torch.empty(p.n * ka, device="cuda")
         b_lo = torch.empty_like(b_hi)
         a_in = bool(plan["a_in_kernel"])
-        if a_in:
-            # the step is split_bt + the tcgen05 GEMM splitting A itself; the
-            # GEMM kernel's time is the step's minus split_bt timed alone
-            launches_per_step = 2
+        launches_per_step = 2 if a_in else 3
+        if a_in or plan["stream_k"] > 0:
+            # the GEMM kernel splits A itself, or runs stream-K with a
+            # workspace only the whole call provides: its time is the
+            # call's minus the split kernels timed alone
+            a_hi = a_lo = None
+            if not a_in:
+                a_hi = torch.empty(p.m * ka, device="cuda")
+                a_lo = torch.empty_like(a_hi)
 
-            def split_b_only():
+            def splits_only():
+                if not a_in:
+                    binding.tf32x3_split_a(A[:, :p.k], a_hi, a_lo)
                 binding.tf32x3_split_b(B[:, :p.n], b_hi, b_lo)
 
             for _ in range(3):
-                split_b_only()
-            sb = time_launches(split_b_only, stream, min(args.steps, 100), flush=flush)
+                splits_only()
+            sb = time_launches(splits_only, stream, min(args.steps, 100), flush=flush)
             gemm_ms = mean_ms - sum(sb) / len(sb)
-            gemm_timing = "whole call minus split_bt_kernel timed alone (CUDA events)"
+            gemm_timing = ("whole call minus " + ("split_bt_kernel" if a_in else "split_a_kernel + split_bt_kernel")
+                           + " timed alone (CUDA events)")
+            del a_hi, a_lo
         else:
             # the step is split_a + split_bt + the tcgen05 GEMM; the GEMM
             # kernel alone is timed on operands split once, through the
             # split-GEMM call
-            launches_per_step = 3
             a_hi = torch.empty(p.m * ka, device="cuda")
             a_lo = torch.empty_like(a_hi)
             binding.tf32x3_split_a(A[:, :p.k], a_hi, a_lo)
@@ -493,7 +501,9 @@ def run_ours(args, rank, world):
         bf16 = (mp or {}).get("bf16_tflops", 1900.0)
         tf32 = bf16 * NOMINAL_TF32_OVER_BF16
         family = "tf32x3_a_in" if a_in else "tf32x3"
-        roof = {"bound": "tensor", "kernel": "tf32x3_gemm_kernel" + ("<A split in kernel>" if a_in else ""),
+        traits = [t for t, on in (("A split in kernel", a_in), ("transposed tiles", plan["trans"]),
+                                  ("stream-K", plan["stream_k"] > 0)) if on]
+        roof = {"bound": "tensor", "kernel": "tf32x3_gemm_kernel" + (f"<{', '.join(traits)}>" if traits else ""),
                 "achieved": achieved, "peak": tf32 / 3,
                 "unit": "TFLOP/s", "frac": achieved / (tf32 / 3),
                 "peak_basis": f"TF32 dense peak / 3 (three TF32 products per FP32 product); TF32 peak = "

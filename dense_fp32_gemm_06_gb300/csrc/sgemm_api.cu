@@ -201,7 +201,7 @@ int check_args(int m, int n, int k, float alpha, const float *A, int lda, const 
 // for a host-only plan, which assumes 8 GPCs of num_sms / 8 SMs.
 int plan(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
          const float *C, int ldc, int path, int num_sms, sgemm_plan *pl, const int (*max_clusters)[9] = nullptr,
-         int op_a = SGEMM_OP_N, int op_b = SGEMM_OP_N, int batch = 1) {
+         int op_a = SGEMM_OP_N, int op_b = SGEMM_OP_N, int batch = 1, bool allow_sk = true) {
     (void)beta;
     std::memset(pl, 0, sizeof(*pl));
     if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
@@ -259,9 +259,28 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         // as a 128 x 256 x 8 one.  SGEMM_GB300_TRANS (0 / 1) pins the last.
         const char *env_tr = std::getenv("SGEMM_GB300_TRANS");
         const int force_tr = env_tr && (env_tr[0] == '0' || env_tr[0] == '1') ? env_tr[0] - '0' : -1;
+        // Stream-K: one persistent CTA per SM; the full waves of tiles run
+        // as whole tiles, the tiles of the last, partial wave are shared out
+        // evenly by slabs (so no SM idles in it); a tile split between CTAs
+        // is finished by the last of them through a workspace (~10 us).  Only
+        // for one problem and when the last wave has enough tiles that a
+        // tile meets few CTAs.  SGEMM_GB300_STREAM_K (0 / 1) pins it.
+        const char *env_sk = std::getenv("SGEMM_GB300_STREAM_K");
+        const int force_sk = env_sk && (env_sk[0] == '0' || env_sk[0] == '1') ? env_sk[0] - '0' : -1;
         long long best = -1;
         int best_bn = tf32x3::Wide::BN, best_s = 1;
-        bool best_tr = false;
+        bool best_tr = false, best_sk = false;
+        auto consider = [&](long long cost, int bn, int S, bool tr, bool skc) {
+            // a pinned stream-K choice beats every other candidate
+            const bool better = force_sk == 1 && skc != best_sk ? skc : (best < 0 || cost < best);
+            if (better) {
+                best = cost;
+                best_bn = bn;
+                best_s = S;
+                best_tr = tr;
+                best_sk = skc;
+            }
+        };
         for (int cand = 0; cand < 3; ++cand) {
             const bool tr = cand == 2;
             const int bn = cand == 1 ? tf32x3::Narrow::BN : tf32x3::Wide::BN;
@@ -293,13 +312,19 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
                 }
                 const long long waves = (tiles + slots - 1) / slots;
                 const long long cost = waves * ((KT + S - 1) / S) * slab + (S > 1 ? 160 + 28 * S : 0);
-                if (best < 0 || cost < best) {
-                    best = cost;
-                    best_bn = bn;
-                    best_s = S;
-                    best_tr = tr;
-                }
+                consider(cost, bn, S, tr, false);
             }
+            // stream-K: W = tiles / G full waves of whole tiles, then the R
+            // remaining tiles' slabs shared out evenly (every CTA must get at
+            // least one slab of them: R x KT >= G).  Measured: the fix-up of
+            // shared tiles costs ~10 us, and stream-K only pays when whole
+            // tiles would leave >= 10 % of the last wave's SMs idle (4096^3:
+            // 17 % faster; 8192^3, 3.8 % idle: 4 % slower).
+            const long long W = tiles / num_sms, R = tiles - W * num_sms;
+            const bool idle_tail = 10 * (num_sms - R) >= (W + 1) * num_sms;
+            if (allow_sk && force_sk != 0 && batch == 1 && !(force_s >= 1 && force_s <= 8) && R > 0 &&
+                R * KT >= num_sms && ((4 * R >= num_sms && idle_tail) || force_sk == 1))
+                consider(W * KT * slab + ((R * KT + num_sms - 1) / num_sms) * slab + 320, bn, 1, tr, true);
         }
         // A is split inside the GEMM (two extra warps split each raw slab in
         // shared memory, no pass over A through HBM) when the kernel can read
@@ -324,12 +349,13 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         pl->bm = best_tr ? tf32x3::Wide::BN : tf32x3::BM;
         pl->bn = best_tr ? tf32x3::BM : best_bn;
         pl->split_k = best_s;
+        pl->stream_k = best_sk ? num_sms : 0;
         pl->stages = narrow ? tf32x3::Narrow::STAGES : tf32x3::Wide::STAGES;
         pl->smem_bytes = narrow ? tf32x3::Narrow::SMEM_BYTES : tf32x3::Wide::SMEM_BYTES;
         const int tiles_mt = (m + pl->bm - 1) / pl->bm;
         const int tiles_n = (n + pl->bn - 1) / pl->bn;
         pl->tiles = tiles_mt * tiles_n;
-        pl->grid = pl->tiles * pl->split_k;
+        pl->grid = best_sk ? num_sms : pl->tiles * pl->split_k;
         pl->k_tiles = (int)KT;
         pl->group_m = tiles_mt < 8 ? tiles_mt : 8;
         return SGEMM_STATUS_OK;
@@ -439,8 +465,11 @@ cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, const sgemm_plan &pl, const
 // next problem's rows, which only reach outputs that are never stored).
 int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const float *a_lo, const float *bt_hi,
                       const float *bt_lo, float beta, float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream,
-                      int batch = 1, long long stride_c = 0, int a_ld = 0) {
+                      int batch = 1, long long stride_c = 0, int a_ld = 0, float *sk_ws = nullptr,
+                      int *sk_cnt = nullptr) {
     const int ka = ka_of(k);
+    // stream-K needs its workspace (callers that allocate nothing plan without it)
+    if (pl.stream_k > 0 && (sk_ws == nullptr || sk_cnt == nullptr || batch != 1)) return SGEMM_STATUS_UNSUPPORTED;
     CUtensorMap t_ahi, t_alo, t_bhi, t_blo;
     const int am = m * batch, bn = n * batch;
     // with the A split in the kernel, a_hi is the caller's A (row pitch
@@ -466,6 +495,9 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     a.tiles_n = (n + pl.bn - 1) / pl.bn;
     a.group_m = pl.group_m;
     a.stride_c = stride_c;
+    a.sk_ctas = pl.stream_k;
+    a.sk_ws = sk_ws;
+    a.sk_cnt = sk_cnt;
     // clusters of split_k CTAs (consecutive in x) share a tile; y = batch
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid, (unsigned)batch, 1);
@@ -495,12 +527,22 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
                   const Batch &bt = Batch()) {
     const size_t a_elems = pl.a_in_kernel ? 0 : (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
     const size_t cnt = (size_t)bt.count;
+    // stream-K: per-tile arrival counters, then two partial-tile slots per CTA
+    const size_t sk_cnt_floats = pl.stream_k > 0 ? ((size_t)pl.tiles + 3) / 4 * 4 : 0;
+    const size_t sk_ws_floats =
+        pl.stream_k > 0 ? (size_t)pl.stream_k * 2 * tf32x3::BM * (pl.trans ? tf32x3::Wide::BN : pl.bn) : 0;
     float *ws = nullptr;
-    cudaError_t e =
-        cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), 2 * cnt * (a_elems + b_elems) * sizeof(float), pool,
-                                stream);
+    cudaError_t e = cudaMallocFromPoolAsync(
+        reinterpret_cast<void **>(&ws), (2 * cnt * (a_elems + b_elems) + sk_cnt_floats + sk_ws_floats) * sizeof(float),
+        pool, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     float *a_hi = ws, *a_lo = ws + cnt * a_elems, *b_hi = a_lo + cnt * a_elems, *b_lo = b_hi + cnt * b_elems;
+    int *sk_cnt = pl.stream_k > 0 ? reinterpret_cast<int *>(b_lo + cnt * b_elems) : nullptr;
+    float *sk_ws = pl.stream_k > 0 ? b_lo + cnt * b_elems + sk_cnt_floats : nullptr;
+    if (sk_cnt != nullptr && (e = cudaMemsetAsync(sk_cnt, 0, (size_t)pl.tiles * sizeof(int), stream)) != cudaSuccess) {
+        cudaFreeAsync(ws, stream);
+        return fail_cuda(e);
+    }
     // both split operands are k-contiguous (K-major): an operand stored with
     // k contiguous is split in place order, one stored k-major is transposed
     if (pl.a_in_kernel) {
@@ -514,7 +556,7 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
     if (pl.op_b == SGEMM_OP_N) launch_split_b(k, n, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
     else launch_split_a(n, k, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
     const int st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream, bt.count,
-                                     bt.sc, lda);
+                                     bt.sc, lda, sk_ws, sk_cnt);
     e = cudaFreeAsync(ws, stream);
     if (st) return st;
     if (e != cudaSuccess) return fail_cuda(e);
@@ -724,7 +766,7 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
     // the plan of the tensor-core path for this shape (operand pointers only
     // matter to the FFMA path's alignment choice)
     int st = plan(m, n, k, alpha, a_hi, imax(1, k), a_hi, imax(1, n), beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl,
-                  dev->max_clusters);
+                  dev->max_clusters, SGEMM_OP_N, SGEMM_OP_N, 1, false);   // allocates nothing: no stream-K
     if (st) return st;
     pl.a_in_kernel = 0;   // the operands are split already
     pl.threads = tf32x3::threads_for(false);
@@ -747,7 +789,8 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
     int st = device_state(&dev);
     if (st != SGEMM_STATUS_OK) return st;
     sgemm_plan pl;
-    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl, dev->max_clusters);
+    st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl, dev->max_clusters,
+              SGEMM_OP_N, SGEMM_OP_N, 1, false);   // no stream-K workspace in the fixed scratch
     if (st != SGEMM_STATUS_OK) return st;
     pl.a_in_kernel = 0;   // this entry point splits A into its fixed scratch
     pl.threads = tf32x3::threads_for(false);

@@ -122,7 +122,82 @@ struct Params {
     // y*n .. of the split B^T (the batch's operands stacked as one tall
     // matrix) and writes C + y*stride_c
     long long stride_c;
+    // stream-K (sk_ctas > 0, grid = G = sk_ctas persistent CTAs, one
+    // problem): with tiles = W G + R, CTA g first takes whole tiles g,
+    // g + G, ..., g + (W - 1) G (the full waves, in raster order, so CTAs
+    // running at the same time share operand panels in L2), then slabs
+    // [T g / G, T (g + 1) / G) of the sequence "tile W G slabs 0..KT-1,
+    // tile W G + 1 slabs 0..KT-1, ..." of the R remaining tiles (T = R KT).
+    // A CTA that holds only part of a tile writes its partial sums to its
+    // slot of sk_ws (2 x BM x BN floats per CTA: slot 0 for the tile its run
+    // starts in, slot 1 for the one it ends in) and counts itself in
+    // sk_cnt[tile] (zeroed before the launch); the last of a tile's CTAs
+    // adds all partials in k order and writes the tile.
+    int sk_ctas;
+    float *sk_ws;
+    int *sk_cnt;
 };
+
+// Segment `si` of the work of CTA blockIdx.x -- one tile and a range
+// [k0, k0 + nk) of its kt_all slabs; false past the last.  Stream-K (see
+// Params): the whole tiles blockIdx.x + w G first, then the CTA's run of
+// the remaining tiles' slab sequence cut at tile boundaries.  Otherwise one
+// segment: split-K cluster rank `rank`'s share of tile blockIdx.x / nsplit
+// (possibly empty), or the whole tile.  Recomputed on demand so that no
+// role keeps iteration state next to its accumulators.
+__device__ __forceinline__ bool cta_segment(const Params &p, int kt_all, int tiles, uint32_t nsplit, uint32_t rank,
+                                            int si, int &tile, int &k0, int &nk) {
+    long long it0, it1;
+    if (p.sk_ctas > 0) {
+        const int whole = tiles / p.sk_ctas;
+        if (si < whole) {
+            tile = (int)blockIdx.x + si * p.sk_ctas;
+            k0 = 0;
+            nk = kt_all;
+            return true;
+        }
+        si -= whole;
+        const long long base = (long long)whole * p.sk_ctas * kt_all;
+        const long long T = (long long)(tiles - whole * p.sk_ctas) * kt_all;
+        it0 = base + T * blockIdx.x / p.sk_ctas;
+        it1 = base + T * (blockIdx.x + 1) / p.sk_ctas;
+    } else {
+        if (si > 0) return false;
+        tile = (int)(blockIdx.x / nsplit);
+        k0 = (int)((long long)kt_all * rank / nsplit);
+        nk = (int)((long long)kt_all * (rank + 1) / nsplit) - k0;
+        return true;
+    }
+    const long long t = it0 / kt_all + si, tb = t * kt_all;
+    if (tb >= it1) return false;
+    const long long lo = si == 0 ? it0 : tb;
+    const long long hi = it1 < tb + kt_all ? it1 : tb + kt_all;
+    tile = (int)t;
+    k0 = (int)(lo - tb);
+    nk = (int)(hi - lo);
+    return true;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Barrier `id` over `threads` threads that also returns whether any of them
+// passed true (every participant gets the same answer).
+__device__ __forceinline__ bool named_barrier_or(int id, int threads, bool v) {
+    uint32_t out;
+    asm volatile(
+        "{\n"
+        ".reg .pred p, q;\n"
+        "setp.ne.u32 q, %1, 0;\n"
+        "bar.red.or.pred p, %2, %3, q;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(out)
+        : "r"((uint32_t)v), "r"(id), "r"(threads)
+        : "memory");
+    return out != 0;
+}
 
 // ---------------------------------------------------------------- split kernels
 
@@ -254,6 +329,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     const uint32_t bar_done = bar_tempty + 16;           // every MMA issued has completed
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * (2 * STAGES + 5));
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 8);
+    volatile int *const sk_last = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 12);
     const uint32_t bar_conv = bar_done + 24;             // [STAGES] A slab split in place (A_IN)
     static_assert(8 * (3 * STAGES + 7) <= BAR_REGION, "barrier region");
 
@@ -261,19 +337,28 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     // split-K: the CTAs of a cluster share one output tile and take
     // consecutive ranges of its k slabs (a cluster of one without split-K)
     const uint32_t nsplit = tc::cluster_nctarank(), rank = tc::cluster_ctarank();
-    int tm, tn;
-    raster_tile(blockIdx.x / nsplit, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
     // TRANS: the tile is BN rows of C by BM columns (C^T = B^T A^T: the
     // MMA's 128-row operand is B^T, its BN-row operand is A)
     constexpr int TILE_M = TRANS ? BN : BM, TILE_N = TRANS ? BM : BN;
-    const int m0 = tm * TILE_M, n0 = tn * TILE_N;
-    // rows of this batch problem's operands inside the stacked split arrays
-    const int arow0 = (int)blockIdx.y * p.m + m0, brow0 = (int)blockIdx.y * p.n + n0;
     float *const Cb = p.C + (long long)blockIdx.y * p.stride_c;
     const int KT_ALL = (p.k + BK - 1) / BK;
-    const int kt0 = (int)((long long)KT_ALL * rank / nsplit);
-    const int KT = (int)((long long)KT_ALL * (rank + 1) / nsplit) - kt0;   // slabs of this CTA
-    const int NC = (KT + CHUNK_STAGES - 1) / CHUNK_STAGES;
+    const int tiles = p.tiles_m * p.tiles_n;
+    const bool sk = p.sk_ctas > 0;
+    // this CTA's work: whole tiles of the full waves and a share of the
+    // remaining tiles' slabs (stream-K), a consecutive range of one tile's
+    // slabs (split-K cluster rank `rank`), or one whole tile
+    // (cta_segment above walks it)
+    // origin in C of tile t, and rows of its operands inside the (stacked,
+    // when batched) operand arrays
+    auto tile_origin = [&](int t, int &m0, int &n0) {
+        int tm, tn;
+        raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+        m0 = tm * TILE_M;
+        n0 = tn * TILE_N;
+    };
+    // the split-K cluster's tile (its reduction below writes it)
+    int cl_m0 = 0, cl_n0 = 0;
+    if (nsplit > 1) tile_origin((int)(blockIdx.x / nsplit), cl_m0, cl_n0);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -306,36 +391,45 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int kt = 0; kt < KT; ++kt) {
-                const int s = kt % STAGES;
-                if (kt >= STAGES && !mbar_wait(bar_empty + 8 * s, ((kt / STAGES) - 1) & 1, kStatusProducer)) {
-                    *abort_flag = 1;
-                    break;
+            int tile, k0, nk, g = 0;   // g: slabs issued so far (ring position)
+            bool stop = false;
+            for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
+                int m0, n0;
+                tile_origin(tile, m0, n0);
+                const int arow0 = (int)blockIdx.y * p.m + m0, brow0 = (int)blockIdx.y * p.n + n0;
+                for (int kt = 0; kt < nk; ++kt, ++g) {
+                    const int s = g % STAGES;
+                    if (g >= STAGES && !mbar_wait(bar_empty + 8 * s, ((g / STAGES) - 1) & 1, kStatusProducer)) {
+                        *abort_flag = 1;
+                        stop = true;
+                        break;
+                    }
+                    if (*abort_flag) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t st = stage0 + s * STAGE_BYTES;
+                    const uint32_t fb = bar_full + 8 * s;
+                    mbar_arrive_expect_tx(fb, A_IN ? STAGE_BYTES - SPLIT_BYTES : STAGE_BYTES);
+                    const int kx = (k0 + kt) * BK;
+                    // slots [MMA A hi | MMA A lo | MMA B hi | MMA B lo]; raw A
+                    // into A's hi slot and nothing into its lo slot when A_IN
+                    if constexpr (!TRANS) {
+                        tma_load_2d(st, &tmAhi, kx, arow0, fb);
+                        if (!A_IN) tma_load_2d(st + A_TILE, &tmAlo, kx, arow0, fb);
+                        tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, brow0, fb);
+                        tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, brow0, fb);
+                    } else {
+                        tma_load_2d(st, &tmBhi, kx, brow0, fb);
+                        tma_load_2d(st + A_TILE, &tmBlo, kx, brow0, fb);
+                        tma_load_2d(st + 2 * A_TILE, &tmAhi, kx, arow0, fb);
+                        if (!A_IN) tma_load_2d(st + 2 * A_TILE + B_TILE, &tmAlo, kx, arow0, fb);
+                    }
                 }
-                if (*abort_flag) break;
-                const uint32_t st = stage0 + s * STAGE_BYTES;
-                const uint32_t fb = bar_full + 8 * s;
-                mbar_arrive_expect_tx(fb, A_IN ? STAGE_BYTES - SPLIT_BYTES : STAGE_BYTES);
-                const int kx = (kt0 + kt) * BK;
-                // slots [MMA A hi | MMA A lo | MMA B hi | MMA B lo]; raw A
-                // into A's hi slot and nothing into its lo slot when A_IN
-                if constexpr (!TRANS) {
-                    tma_load_2d(st, &tmAhi, kx, arow0, fb);
-                    if (!A_IN) tma_load_2d(st + A_TILE, &tmAlo, kx, arow0, fb);
-                    tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, brow0, fb);
-                    tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, brow0, fb);
-                } else {
-                    tma_load_2d(st, &tmBhi, kx, brow0, fb);
-                    tma_load_2d(st + A_TILE, &tmBlo, kx, brow0, fb);
-                    tma_load_2d(st + 2 * A_TILE, &tmAhi, kx, arow0, fb);
-                    if (!A_IN) tma_load_2d(st + 2 * A_TILE + B_TILE, &tmAlo, kx, arow0, fb);
-                }
-                ++issued;
             }
             if (*abort_flag) {
                 // every copy issued must land before the CTA leaves
-                for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+                for (int j = g > STAGES ? g - STAGES : 0; j < g; ++j)
                     mbar_wait(bar_full + 8 * (j % STAGES), (j / STAGES) & 1, kStatusDrain);
             }
         }
@@ -343,18 +437,26 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_tf32_f32<BM, BN>();
-            for (int kt = 0; kt < KT; ++kt) {
-                const int c = kt / CHUNK_STAGES, b = c & 1;
+            int tile, k0, nk, g = 0, cg = 0;   // g: slabs consumed, cg: chunks started
+            bool stop = false;
+            for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
+              for (int kt = 0; kt < nk; ++kt, ++g) {
+                // each segment's slabs accumulate in chunks of CHUNK_STAGES
+                // slabs, alternating between the two TMEM buffers
+                const int b = cg & 1;
                 const bool chunk_first = kt % CHUNK_STAGES == 0;
-                const bool chunk_last = kt % CHUNK_STAGES == CHUNK_STAGES - 1 || kt == KT - 1;
-                // TMEM buffer b is reused once the accumulator warps drained chunk c - 2
-                if (chunk_first && c >= 2 && !mbar_wait(bar_tempty + 8 * b, ((c >> 1) - 1) & 1, kStatusMmaBuffer)) {
+                const bool chunk_last = kt % CHUNK_STAGES == CHUNK_STAGES - 1 || kt == nk - 1;
+                // TMEM buffer b is reused once the accumulator warps drained chunk cg - 2
+                if (chunk_first && cg >= 2 &&
+                    !mbar_wait(bar_tempty + 8 * b, ((cg >> 1) - 1) & 1, kStatusMmaBuffer)) {
                     *abort_flag = 1;
+                    stop = true;
                     break;
                 }
-                const int s = kt % STAGES;
-                if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusMma)) {
+                const int s = g % STAGES;
+                if (!mbar_wait(bar_full + 8 * s, (g / STAGES) & 1, kStatusMma)) {
                     *abort_flag = 1;
+                    stop = true;
                     break;
                 }
                 tc::fence_after_sync();
@@ -389,8 +491,9 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                         else
                             tc::mma_tf32(d, a_hi, b_lo, idesc, 1u);   // raw A x B^T lo
                     }
-                    if (!mbar_wait(bar_conv + 8 * s, (kt / STAGES) & 1, kStatusMma)) {
+                    if (!mbar_wait(bar_conv + 8 * s, (g / STAGES) & 1, kStatusMma)) {
                         *abort_flag = 1;
+                        stop = true;
                         break;
                     }
                     tc::fence_after_sync();
@@ -406,7 +509,11 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                     }
                 }
                 tc::commit(bar_empty + 8 * s);
-                if (chunk_last) tc::commit(bar_tfull + 8 * b);
+                if (chunk_last) {
+                    tc::commit(bar_tfull + 8 * b);
+                    ++cg;
+                }
+              }
             }
             // fires once every MMA issued has completed (TMEM may then be freed)
             tc::commit(bar_done);
@@ -421,14 +528,22 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
         // enough time for both warps to split each slab together.
         constexpr int CW = CONV_PER_WARP ? 32 : CONV_THREADS;   // threads per slab
         const int ct = CONV_PER_WARP ? lane : (int)threadIdx.x - (64 + ACC_THREADS);
-        const int kt_first = CONV_PER_WARP ? warp - (2 + ACC_WARPS) : 0;
-        for (int kt = kt_first; kt < KT; kt += CONV_PER_WARP ? CONV_WARPS : 1) {
-            const int s = kt % STAGES;
-            if (!mbar_wait(bar_full + 8 * s, (kt / STAGES) & 1, kStatusSplit)) {
+        const int mine = CONV_PER_WARP ? warp - (2 + ACC_WARPS) : 0;
+        int tile, k0, nk, g = 0;   // g: slab sequence position (ring position)
+        bool stop = false;
+        for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
+          for (int kt = 0; kt < nk; ++kt, ++g) {
+            if (CONV_PER_WARP && (g % CONV_WARPS) != mine) continue;
+            const int s = g % STAGES;
+            if (!mbar_wait(bar_full + 8 * s, (g / STAGES) & 1, kStatusSplit)) {
                 *abort_flag = 1;
+                stop = true;
                 break;
             }
-            if (*abort_flag) break;
+            if (*abort_flag) {
+                stop = true;
+                break;
+            }
             // the raw slab stays as A's hi (the MMA reads it as hi = x with
             // its low 13 bits dropped); lo = tf32(x - hi) goes into A's lo
             // slot at the same swizzled position (the split is elementwise)
@@ -443,86 +558,194 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                                               lo_of_raw(x[j].w));
             tc::fence_proxy_async_smem();
             mbar_arrive(bar_conv + 8 * s);
+          }
         }
     } else {
         // ------------------------------------------------------------ accumulator warps (2..9)
         const int lane_grp = warp & 3;                       // TMEM lanes 32*lane_grp .. +31
         const int half = (warp - 2) >> 2;                    // columns half*128 .. +127
+        const int trow = lane_grp * 32 + lane;               // this thread's row of the tile (TMEM lane)
         const uint32_t taddr = tmem + ((uint32_t)(lane_grp * 32) << 16) + (uint32_t)(half * COLS_PER_THREAD);
         float acc[COLS_PER_THREAD];
-#pragma unroll
-        for (int j = 0; j < COLS_PER_THREAD; ++j) acc[j] = 0.f;
         bool ok = true;
-        for (int c = 0; c < NC; ++c) {
-            const int b = c & 1;
-            if (!mbar_wait(bar_tfull + 8 * b, (c >> 1) & 1, kStatusAccumulate)) {
-                ok = false;
-                *abort_flag = 1;
-                break;
-            }
-            tc::fence_after_sync();
+
+        // Quad q of this thread's part of the tile at (m0, n0): columns
+        // n0 + half*COLS_PER_THREAD + 4q .. +3 of its row of C, or (TRANS)
+        // rows m0 + half*COLS_PER_THREAD + 4q .. +3 of its column of C (the
+        // 32 lanes of a warp then cover 128 contiguous bytes of a C row).
+        // Stores go in blocks: the block's C values (beta != 0) are loaded
+        // first, so the loads are in flight together instead of each waiting
+        // behind the previous store to the same array.
+        auto load_c = [&](int m0, int n0, int q) -> float4 {
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (TRANS) {
+                const int col = n0 + trow, r = m0 + half * COLS_PER_THREAD + 4 * q;
+                if (col < p.n) {
 #pragma unroll
-            for (int q = 0; q < COLS_PER_THREAD / 16; ++q) {
-                uint32_t v[16];
-                tc::ld_32x32b_x16(taddr + (uint32_t)(b * BN + q * 16), v);
-                tc::wait_ld();
+                    for (int e = 0; e < 4; ++e)
+                        if (r + e < p.m) c[e] = Cb[(long long)(r + e) * p.ldc + col];
+                }
+            } else {
+                const int row = m0 + trow, col = n0 + half * COLS_PER_THREAD + 4 * q;
+                if (row < p.m) {
+                    const float *crow = Cb + (long long)row * p.ldc;
+                    if (C_VEC && col + 3 < p.n) return *reinterpret_cast<const float4 *>(crow + col);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[q * 16 + i] += __uint_as_float(v[i]);
-            }
-            tc::fence_before_sync();
-            mbar_arrive(bar_tempty + 8 * b);
-        }
-        // this thread's TMEM lane: a row of C, or a column of C when TRANS
-        const int row = (TRANS ? n0 : m0) + lane_grp * 32 + lane;
-        if (nsplit > 1) {
-            // park the partial tile in this CTA's (now idle) stage memory,
-            // rows PART_PITCH floats apart (4 banks apart: conflict-free)
-            float *part = reinterpret_cast<float *>(smem) + (lane_grp * 32 + lane) * PART_PITCH +
-                          half * COLS_PER_THREAD;
-#pragma unroll
-            for (int q = 0; q < COLS_PER_THREAD / 4; ++q)
-                reinterpret_cast<float4 *>(part)[q] =
-                    make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-        } else if (TRANS) {
-            // C^T tile: lane = column `row` of C, registers = rows of C;
-            // the 32 lanes of a warp store 128 contiguous bytes of a C row
-            const int col = row;
-            if (ok && *abort_flag == 0 && col < p.n) {
-                const float alpha = p.alpha, beta = p.beta;
-                const int r0c = m0 + half * COLS_PER_THREAD;
-#pragma unroll
-                for (int j = 0; j < COLS_PER_THREAD; ++j) {
-                    if (r0c + j < p.m) {
-                        float *cp = Cb + (long long)(r0c + j) * p.ldc + col;
-                        *cp = beta != 0.f ? fmaf(alpha, acc[j], beta * *cp) : alpha * acc[j];
-                    }
+                    for (int e = 0; e < 4; ++e)
+                        if (col + e < p.n) c[e] = crow[col + e];
                 }
             }
-        } else if (ok && *abort_flag == 0 && row < p.m) {
+            return make_float4(c[0], c[1], c[2], c[3]);
+        };
+        // C = alpha * v + beta * c for quad q (c: its C values, read when beta != 0)
+        auto put_quad = [&](int m0, int n0, int q, float4 v, float4 c4) {
             const float alpha = p.alpha, beta = p.beta;
-            float *crow = Cb + (long long)row * p.ldc;
-            const int col0 = n0 + half * COLS_PER_THREAD;
+            const float a[4] = {v.x, v.y, v.z, v.w}, c[4] = {c4.x, c4.y, c4.z, c4.w};
+            float o[4];
 #pragma unroll
-            for (int q = 0; q < COLS_PER_THREAD / 4; ++q) {
-                const int col = col0 + 4 * q;
-                const float *a = &acc[4 * q];
+            for (int e = 0; e < 4; ++e) o[e] = beta != 0.f ? fmaf(alpha, a[e], beta * c[e]) : alpha * a[e];
+            if constexpr (TRANS) {
+                const int col = n0 + trow, r = m0 + half * COLS_PER_THREAD + 4 * q;
+                if (col >= p.n) return;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (r + e < p.m) Cb[(long long)(r + e) * p.ldc + col] = o[e];
+            } else {
+                const int row = m0 + trow, col = n0 + half * COLS_PER_THREAD + 4 * q;
+                if (row >= p.m) return;
+                float *crow = Cb + (long long)row * p.ldc;
                 if (C_VEC && col + 3 < p.n) {
-                    float4 o;
-                    if (beta != 0.f) {
-                        const float4 c4 = *reinterpret_cast<const float4 *>(crow + col);
-                        o = make_float4(fmaf(alpha, a[0], beta * c4.x), fmaf(alpha, a[1], beta * c4.y),
-                                        fmaf(alpha, a[2], beta * c4.z), fmaf(alpha, a[3], beta * c4.w));
-                    } else {
-                        o = make_float4(alpha * a[0], alpha * a[1], alpha * a[2], alpha * a[3]);
-                    }
-                    *reinterpret_cast<float4 *>(crow + col) = o;
+                    *reinterpret_cast<float4 *>(crow + col) = make_float4(o[0], o[1], o[2], o[3]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (col + e < p.n)
-                            crow[col + e] = beta != 0.f ? fmaf(alpha, a[e], beta * crow[col + e]) : alpha * a[e];
+                    for (int e = 0; e < 4; ++e)
+                        if (col + e < p.n) crow[col + e] = o[e];
+                }
+            }
+        };
+        auto store_tile = [&](int m0, int n0) {
+            constexpr int EB = 4;   // quads per block
+            const bool read_c = p.beta != 0.f;
+#pragma unroll
+            for (int qb = 0; qb < COLS_PER_THREAD / 4; qb += EB) {
+                float4 c[EB];
+#pragma unroll
+                for (int u = 0; u < EB; ++u)
+                    c[u] = read_c ? load_c(m0, n0, qb + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < EB; ++u) {
+                    const int q = qb + u;
+                    put_quad(m0, n0, q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]), c[u]);
+                }
+            }
+        };
+
+        // stream-K: this CTA holds only part of tile t.  Publish the partial;
+        // the tile's last CTA to get here adds all of the tile's partials in
+        // k order (the same sum whichever CTA is last) and writes the tile.
+        auto sk_partial = [&](int t, int m0, int n0) {
+            // positions relative to the stream-K part of the sequence
+            const int sk_tail0 = tiles / p.sk_ctas * p.sk_ctas;   // first tile shared out by slabs
+            const long long T = (long long)(tiles - sk_tail0) * KT_ALL, G = p.sk_ctas;
+            const long long x0 = (long long)(t - sk_tail0) * KT_ALL, x1 = x0 + KT_ALL;
+            // the CTAs whose runs meet [x0, x1): g with T g / G < x1 and T (g + 1) / G > x0
+            const int g_first = (int)(((x0 + 1) * G - 1) / T), g_last = (int)((x1 * G - 1) / T);
+            // a CTA's slot: 0 for the tile its run starts in, 1 for the one it
+            // ends in.  Every contributor after the first starts inside the
+            // tile (slot 0); only the first may have started before it.
+            const int first_slot = T * g_first / G >= x0 ? 0 : 1;
+            const int my_slot = (int)blockIdx.x == g_first ? first_slot : 0;
+            constexpr int SLOT = BM * BN / 4;   // float4s per slot
+            float4 *const ws = reinterpret_cast<float4 *>(p.sk_ws);
+            float4 *mine = ws + ((size_t)blockIdx.x * 2 + my_slot) * SLOT;
+#pragma unroll
+            for (int q = 0; q < COLS_PER_THREAD / 4; ++q)
+                mine[(half * (COLS_PER_THREAD / 4) + q) * BM + trow] =
+                    make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+            __threadfence();
+            named_barrier_sync(1, ACC_THREADS);
+            if (threadIdx.x == 64) *sk_last = atomicAdd(p.sk_cnt + t, 1) == g_last - g_first;
+            named_barrier_sync(1, ACC_THREADS);
+            const bool last = *sk_last != 0;
+            named_barrier_sync(1, ACC_THREADS);   // the flag is read before it is next written
+            if (!last) return;
+            __threadfence();
+            // blocks of QB quads: each contributor's QB loads are in flight
+            // together (one L2 round trip per block and contributor)
+            constexpr int QB = 8;
+            const float4 *first = ws + ((size_t)g_first * 2 + first_slot) * SLOT;
+#pragma unroll 1
+            for (int qb = 0; qb < COLS_PER_THREAD / 4; qb += QB) {
+                const int idx0 = (half * (COLS_PER_THREAD / 4) + qb) * BM + trow;
+                float4 sum[QB];
+#pragma unroll
+                for (int u = 0; u < QB; ++u) sum[u] = __ldcg(first + idx0 + u * BM);
+#pragma unroll 1
+                for (int g = g_first + 1; g <= g_last; ++g) {
+                    const float4 *src = ws + (size_t)g * 2 * SLOT + idx0;
+                    float4 v[QB];
+#pragma unroll
+                    for (int u = 0; u < QB; ++u) v[u] = __ldcg(src + u * BM);
+#pragma unroll
+                    for (int u = 0; u < QB; ++u) {
+                        sum[u].x += v[u].x;
+                        sum[u].y += v[u].y;
+                        sum[u].z += v[u].z;
+                        sum[u].w += v[u].w;
                     }
                 }
+                const bool read_c = p.beta != 0.f;
+                float4 c[QB];
+#pragma unroll
+                for (int u = 0; u < QB; ++u)
+                    c[u] = read_c ? load_c(m0, n0, qb + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int u = 0; u < QB; ++u) put_quad(m0, n0, qb + u, sum[u], c[u]);
+            }
+        };
+
+        int tile, k0, nk, cg = 0;   // cg: chunks drained so far
+        for (int si = 0; cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
+#pragma unroll
+            for (int j = 0; j < COLS_PER_THREAD; ++j) acc[j] = 0.f;
+            const int nc = (nk + CHUNK_STAGES - 1) / CHUNK_STAGES;
+            for (int c = 0; c < nc && ok; ++c, ++cg) {
+                const int b = cg & 1;
+                if (!mbar_wait(bar_tfull + 8 * b, (cg >> 1) & 1, kStatusAccumulate)) {
+                    ok = false;
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::fence_after_sync();
+#pragma unroll
+                for (int q = 0; q < COLS_PER_THREAD / 16; ++q) {
+                    uint32_t v[16];
+                    tc::ld_32x32b_x16(taddr + (uint32_t)(b * BN + q * 16), v);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[q * 16 + i] += __uint_as_float(v[i]);
+                }
+                tc::fence_before_sync();
+                mbar_arrive(bar_tempty + 8 * b);
+            }
+            // leave together (the stream-K hand-off below synchronises
+            // these 256 threads, and a wait that ran out may have stopped
+            // only some of them)
+            if (named_barrier_or(1, ACC_THREADS, !ok || *abort_flag != 0)) break;
+            int m0, n0;
+            tile_origin(tile, m0, n0);
+            if (nsplit > 1) {
+                // park the partial tile in this CTA's (now idle) stage memory,
+                // rows PART_PITCH floats apart (4 banks apart: conflict-free)
+                float *part = reinterpret_cast<float *>(smem) + trow * PART_PITCH + half * COLS_PER_THREAD;
+#pragma unroll
+                for (int q = 0; q < COLS_PER_THREAD / 4; ++q)
+                    reinterpret_cast<float4 *>(part)[q] =
+                        make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+            } else if (sk && nk < KT_ALL) {
+                sk_partial(tile, m0, n0);
+            } else {
+                store_tile(m0, n0);
             }
         }
     }
@@ -547,7 +770,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                 // columns of C), so the stores below stay coalesced
                 const int r = TRANS ? r0 + idx % (r1 - r0) : r0 + idx / (BN / 4);
                 const int c4 = TRANS ? idx / (r1 - r0) : idx % (BN / 4);
-                const int row = m0 + r, col = n0 + 4 * c4;
+                const int row = cl_m0 + r, col = cl_n0 + 4 * c4;
                 const uint32_t off = part0 + (uint32_t)(r * PART_PITCH + 4 * c4) * 4u;
                 float4 sum = tc::ld_cluster_v4(tc::map_shared_rank(off, 0));
                 for (uint32_t q = 1; q < nsplit; ++q) {
@@ -559,7 +782,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                 }
                 const float a[4] = {sum.x, sum.y, sum.z, sum.w};
                 if constexpr (TRANS) {
-                    const int cc = n0 + r, rr = m0 + 4 * c4;   // column of C, first of 4 rows
+                    const int cc = cl_n0 + r, rr = cl_m0 + 4 * c4;   // column of C, first of 4 rows
                     if (cc >= p.n) continue;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {

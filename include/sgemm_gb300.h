@@ -248,6 +248,8 @@ typedef struct sgemm_plan {
     int a_vec;         /* 1: A (stored k x m) loaded 16 bytes at a time (FFMA path)            */
     int a_in_kernel;   /* 1: the tensor-core GEMM splits A itself (no split pass over A)       */
     int trans;         /* 1: tensor-core tiles of C^T = B^T A^T (n <= 128; bm = 256, bn = 128) */
+    int stream_k;      /* > 0: stream-K over this many CTAs (grid); each takes an equal share  */
+                       /*      of all tiles' k slabs, partial tiles meet in a workspace        */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

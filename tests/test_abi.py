@@ -156,7 +156,38 @@ def test_auto_policy():
     assert binding.plan(1000, 1500, 777, lda=777)[1]["path"] == binding.PATH_TF32X3
     st, p = binding.plan(2048, 2048, 2048, path=binding.PATH_TF32X3)
     assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"]) == (128, 256, 16, 384)
-    assert p["grid"] == p["tiles"] == 16 * 8 and p["k_tiles"] == 128
+    assert p["grid"] == p["tiles"] == 16 * 8 and p["k_tiles"] == 128 and p["stream_k"] == 0
+
+
+def test_stream_k_policy(monkeypatch):
+    """Stream-K (one CTA per SM: the full waves as whole tiles, the last
+    wave's tiles shared out by slabs) when whole tiles would leave >= 10 % of
+    the last wave idle and its estimate wins; never for batches, never when
+    a tile would meet too many CTAs (few tiles: split-K clusters instead),
+    never with fewer slabs than CTAs; the tuning variable pins it."""
+    for v in ("SGEMM_GB300_STREAM_K", "SGEMM_GB300_TRANS", "SGEMM_GB300_TILE_N", "SGEMM_GB300_SPLIT_K"):
+        monkeypatch.delenv(v, raising=False)
+    TC = binding.PATH_TF32X3
+    for shape in [(4096, 4096, 4096), (8192, 2048, 8192), (16384, 128, 8192), (65536, 64, 4096)]:
+        st, p = binding.plan(*shape, path=TC)
+        assert st == 0 and p["stream_k"] == 152 and p["grid"] == 152 and p["split_k"] == 1, (shape, p)
+    # 8192^3: 13.47 waves, 3.8 % of the last one idle; 2048^3: the estimate ties
+    for shape in [(8192, 8192, 8192), (2048, 2048, 2048), (3072, 3072, 3072)]:
+        st, p = binding.plan(*shape, path=TC)
+        assert p["stream_k"] == 0 and p["grid"] == p["tiles"] * p["split_k"], (shape, p)
+    st, p = binding.plan(256, 256, 8192, path=TC)          # 2 tiles: a split-K cluster instead
+    assert p["stream_k"] == 0 and p["split_k"] > 1
+    st, p = binding.plan(4096, 4096, 4096, path=TC, num_sms=64)
+    assert p["stream_k"] == 0 and p["grid"] == 512         # 8 full waves of 64
+    monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
+    st, p = binding.plan(4096, 4096, 4096, path=TC)
+    assert p["stream_k"] == 0 and p["grid"] == p["tiles"] * p["split_k"]
+    monkeypatch.setenv("SGEMM_GB300_STREAM_K", "1")
+    for shape in [(256, 256, 8192), (2048, 2048, 2048)]:    # pinned: taken whenever allowed
+        st, p = binding.plan(*shape, path=TC)
+        assert p["stream_k"] == 152 and p["grid"] == 152, (shape, p)
+    st, p = binding.plan(64, 64, 32, path=TC)               # 1 tile x 2 slabs < 152 CTAs
+    assert p["stream_k"] == 0
 
 
 def test_in_kernel_split_policy(monkeypatch):
@@ -226,7 +257,7 @@ def test_trans_tile_policy(monkeypatch):
     TC = binding.PATH_TF32X3
     st, p = binding.plan(16384, 128, 8192, path=TC)
     assert st == 0 and p["trans"] == 1 and (p["bm"], p["bn"], p["stages"]) == (256, 128, 4)
-    assert p["tiles"] == 64 and p["grid"] == 64 * p["split_k"]
+    assert p["tiles"] == 64 and p["grid"] == (p["stream_k"] or 64 * p["split_k"])
     assert binding.plan(65536, 64, 4096, path=TC)[1]["trans"] == 1
     assert binding.plan(8192, 129, 8192, path=TC)[1]["trans"] == 0
     assert binding.plan(8192, 8192, 8192, path=TC)[1]["trans"] == 0

@@ -260,9 +260,11 @@ def test_device_status_clear_after_runs():
     (256, 256, 8192, 0.0), (300, 700, 5000, 0.75), (129, 257, 4096, -1.0), (1000, 1500, 777, 0.5),
     (64, 64, 65536, 0.0), (400, 300, 3000, 2.0),
 ])
-def test_split_k_clusters(m, n, k, beta):
+def test_split_k_clusters(monkeypatch, m, n, k, beta):
     """Problems with few tiles split k over a cluster of CTAs that reduce
-    their partial tiles through distributed shared memory."""
+    their partial tiles through distributed shared memory (stream-K, which
+    the plan may prefer for some of these shapes, is pinned off)."""
+    monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
     st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3)
     assert st == 0 and plan["split_k"] > 1, plan
     p = inputs.make_problem(m, n, k, alpha=1.25, beta=beta, seed=m + n + k, a="normal", b="uniform",
@@ -271,8 +273,9 @@ def test_split_k_clusters(m, n, k, beta):
 
 
 @pytest.mark.parametrize("m,n,k", [(256, 256, 8192), (300, 700, 5000), (1000, 1500, 777)])
-def test_split_k_integer_twin_bit_exact(m, n, k):
+def test_split_k_integer_twin_bit_exact(monkeypatch, m, n, k):
     """Partial sums of integers are exact, so the split result is too."""
+    monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
     st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3)
     assert st == 0 and plan["split_k"] > 1
     p = inputs.make_problem(m, n, k, alpha=2.0, beta=0.5, seed=7 * k, a="int", b="int", c="int")

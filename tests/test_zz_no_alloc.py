@@ -33,10 +33,13 @@ def _device(arr):
     [(2048, 2048, 2048, 5), (129, 257, 1000, 6)],
 ])
 def test_noalloc_matches_regular_entry_point_twice(shapes, monkeypatch):
-    # the no-allocation entry point splits A with the pre-pass; the regular
-    # call is pinned to the same (it may otherwise split A inside the GEMM,
-    # which rounds hi differently) so both run the same kernels
+    # the no-allocation entry point splits A with the pre-pass and runs
+    # without stream-K (no workspace); the regular call is pinned to the
+    # same (it may otherwise split A inside the GEMM, which rounds hi
+    # differently, or add stream-K partial tiles in another order) so both
+    # run the same kernels
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "0")
+    monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
     stream = torch.cuda.current_stream().cuda_stream
     for m, n, k, seed in shapes:
         p = inputs.make_problem(m, n, k, alpha=1.5, beta=0.5, seed=seed, a="normal", b="uniform", c="uniform",
