@@ -103,4 +103,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *desc, int 
         : "memory");
 }
 
+// Programmatic dependent launch: a kernel launched as the dependent of the
+// previous kernel in its stream may start before that kernel completes;
+// griddep_wait() blocks the calling thread until the previous kernel has
+// completed and its memory operations are visible (a no-op for a kernel
+// launched normally).  griddep_launch_dependents() lets the next kernel in
+// the stream, if launched as a dependent, start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 }  // namespace sgemm_gb300

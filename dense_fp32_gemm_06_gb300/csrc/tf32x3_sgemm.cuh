@@ -223,6 +223,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ A, long long lda, int m, int k,
                                                       float *__restrict__ hi, float *__restrict__ lo, int ka,
                                                       long long src_batch, long long dst_batch) {
+    griddep_launch_dependents();   // the GEMM may start its set-up meanwhile
     // problem blockIdx.z of a strided batch
     A += blockIdx.z * src_batch;
     hi += blockIdx.z * dst_batch;
@@ -259,6 +260,7 @@ __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ 
 __global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__ B, long long ldb, int k, int n,
                                                        float *__restrict__ hi, float *__restrict__ lo, int ka,
                                                        long long src_batch, long long dst_batch) {
+    griddep_launch_dependents();   // the GEMM may start its set-up meanwhile
     B += blockIdx.z * src_batch;
     hi += blockIdx.z * dst_batch;
     lo += blockIdx.z * dst_batch;
@@ -391,6 +393,10 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // launched as the dependent of the split kernels, the CTA set
+            // itself up while they ran; the operands they write are read
+            // only after they have completed
+            griddep_wait();
             int tile, k0, nk, g = 0;   // g: slabs issued so far (ring position)
             bool stop = false;
             for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
