@@ -342,6 +342,10 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
             pl->a_in_kernel = a_tma && env_ain[0] == '1';
         else
             pl->a_in_kernel = a_tma && n <= 4096;
+        // otherwise, when the GEMM can still read A by TMA, it reads A's hi
+        // part from A itself too and the split pass writes only A's lo part
+        // (8 bytes per element of A through HBM instead of 12)
+        pl->a_lo_only = a_tma && !pl->a_in_kernel;
         pl->threads = tf32x3::threads_for(pl->a_in_kernel != 0);
         const bool narrow = best_bn == tf32x3::Narrow::BN;
         pl->trans = best_tr;
@@ -472,14 +476,14 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     if (pl.stream_k > 0 && (sk_ws == nullptr || sk_cnt == nullptr || batch != 1)) return SGEMM_STATUS_UNSUPPORTED;
     CUtensorMap t_ahi, t_alo, t_bhi, t_blo;
     const int am = m * batch, bn = n * batch;
-    // with the A split in the kernel, a_hi is the caller's A (row pitch
-    // a_ld) and a_lo is not read
-    const int a_pitch = pl.a_in_kernel ? a_ld : ka;
+    // a_hi is the caller's A (row pitch a_ld) when the GEMM splits A itself
+    // (a_lo is then not read) or when the split pass wrote only A's lo part
+    const int hi_pitch = pl.a_in_kernel || pl.a_lo_only ? a_ld : ka;
     // boxes: a tile's rows of A (pl.bm) and of B^T (pl.bn)
-    int st = make_tensor_map(&t_ahi, a_hi, am, k, a_pitch, pl.bm, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    int st = make_tensor_map(&t_ahi, a_hi, am, k, hi_pitch, pl.bm, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st)
-        st = make_tensor_map(&t_alo, pl.a_in_kernel ? a_hi : a_lo, am, k, a_pitch, pl.bm, tf32x3::BK,
-                             CU_TENSOR_MAP_SWIZZLE_64B);
+        st = pl.a_in_kernel ? make_tensor_map(&t_alo, a_hi, am, k, hi_pitch, pl.bm, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B)
+                            : make_tensor_map(&t_alo, a_lo, am, k, ka, pl.bm, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st) st = make_tensor_map(&t_bhi, bt_hi, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (!st) st = make_tensor_map(&t_blo, bt_lo, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
     if (st) return st;
@@ -541,7 +545,10 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
 int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
                   float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream, cudaMemPool_t pool, int num_sms,
                   const Batch &bt = Batch()) {
-    const size_t a_elems = pl.a_in_kernel ? 0 : (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
+    // scratch per problem: A's hi and lo parts (A's lo part only when
+    // a_lo_only, nothing when the GEMM splits A itself), B^T's hi and lo
+    const size_t a_elems = (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
+    const size_t a_hi_elems = pl.a_in_kernel || pl.a_lo_only ? 0 : a_elems, a_lo_elems = pl.a_in_kernel ? 0 : a_elems;
     const size_t cnt = (size_t)bt.count;
     // stream-K: per-tile arrival counters, then two partial-tile slots per CTA
     const size_t sk_cnt_floats = pl.stream_k > 0 ? ((size_t)pl.tiles + 3) / 4 * 4 : 0;
@@ -549,10 +556,10 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
         pl.stream_k > 0 ? (size_t)pl.stream_k * 2 * tf32x3::BM * (pl.trans ? tf32x3::Wide::BN : pl.bn) : 0;
     float *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(
-        reinterpret_cast<void **>(&ws), (2 * cnt * (a_elems + b_elems) + sk_cnt_floats + sk_ws_floats) * sizeof(float),
-        pool, stream);
+        reinterpret_cast<void **>(&ws),
+        (cnt * (a_hi_elems + a_lo_elems + 2 * b_elems) + sk_cnt_floats + sk_ws_floats) * sizeof(float), pool, stream);
     if (e != cudaSuccess) return fail_cuda(e);
-    float *a_hi = ws, *a_lo = ws + cnt * a_elems, *b_hi = a_lo + cnt * a_elems, *b_lo = b_hi + cnt * b_elems;
+    float *a_hi = ws, *a_lo = ws + cnt * a_hi_elems, *b_hi = a_lo + cnt * a_lo_elems, *b_lo = b_hi + cnt * b_elems;
     int *sk_cnt = pl.stream_k > 0 ? reinterpret_cast<int *>(b_lo + cnt * b_elems) : nullptr;
     float *sk_ws = pl.stream_k > 0 ? b_lo + cnt * b_elems + sk_cnt_floats : nullptr;
     if (sk_cnt != nullptr && (e = cudaMemsetAsync(sk_cnt, 0, (size_t)pl.tiles * sizeof(int), stream)) != cudaSuccess) {
@@ -564,6 +571,9 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
     if (pl.a_in_kernel) {
         a_hi = const_cast<float *>(A);   // the GEMM reads A itself and splits it in shared memory
         a_lo = nullptr;
+    } else if (pl.a_lo_only) {
+        a_hi = const_cast<float *>(A);   // the GEMM reads A itself as its hi operand
+        launch_split_a(m, k, A, lda, nullptr, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
     } else if (pl.op_a == SGEMM_OP_N) {
         launch_split_a(m, k, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
     } else {
@@ -790,6 +800,7 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
                   dev->max_clusters, SGEMM_OP_N, SGEMM_OP_N, 1, false);   // allocates nothing: no stream-K
     if (st) return st;
     pl.a_in_kernel = 0;   // the operands are split already
+    pl.a_lo_only = 0;
     pl.threads = tf32x3::threads_for(false);
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
@@ -814,6 +825,7 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
               SGEMM_OP_N, SGEMM_OP_N, 1, false);   // no stream-K workspace in the fixed scratch
     if (st != SGEMM_STATUS_OK) return st;
     pl.a_in_kernel = 0;   // this entry point splits A into its fixed scratch
+    pl.a_lo_only = aligned(A, 16) && (lda % 4) == 0;   // then only A's lo part (the GEMM reads hi from A)
     pl.threads = tf32x3::threads_for(false);
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
@@ -824,9 +836,15 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
         // left in the array by an earlier call is ever used
         const size_t a_elems = (size_t)m * ka, b_elems = (size_t)n * ka;
         float *a_hi = ws, *a_lo = ws + a_elems, *b_hi = a_lo + a_elems, *b_lo = b_hi + b_elems;
-        launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
+        if (pl.a_lo_only) {
+            launch_split_a(m, k, A, lda, nullptr, a_lo, stream);
+            a_hi = const_cast<float *>(A);
+        } else {
+            launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
+        }
         launch_split_b(k, n, B, ldb, b_hi, b_lo, stream);
-        if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream))) return st;
+        if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream, 1, 0, lda)))
+            return st;
     }
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SGEMM_STATUS_OK : fail_cuda(e);

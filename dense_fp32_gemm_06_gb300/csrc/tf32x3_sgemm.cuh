@@ -219,6 +219,8 @@ __device__ __forceinline__ float lo_of_raw(float x) {
 // A (m x k, row pitch lda) -> hi, lo (m x ka, row pitch ka).  VEC: A and
 // lda 16-byte aligned, so every row is read as float4 except a k % 4 tail
 // (read element by element: the bytes past k may lie outside A).
+// hi == nullptr: only lo, for a GEMM that reads A itself as its hi operand
+// (hi = A with its low 13 bits dropped, lo = tf32(A - hi); see lo_of_raw).
 template <bool VEC>
 __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ A, long long lda, int m, int k,
                                                       float *__restrict__ hi, float *__restrict__ lo, int ka,
@@ -226,16 +228,21 @@ __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ 
     griddep_launch_dependents();   // the GEMM may start its set-up meanwhile
     // problem blockIdx.z of a strided batch
     A += blockIdx.z * src_batch;
-    hi += blockIdx.z * dst_batch;
+    if (hi != nullptr) hi += blockIdx.z * dst_batch;
     lo += blockIdx.z * dst_batch;
     const int full4 = VEC ? k / 4 : 0;               // float4 chunks entirely inside the row
     const int scal0 = 4 * full4;                      // first element done one at a time
     for (int row = blockIdx.y; row < m; row += gridDim.y) {
         const float *src = A + (long long)row * lda;
-        float *h = hi + (long long)row * ka;
+        float *h = hi != nullptr ? hi + (long long)row * ka : nullptr;
         float *l = lo + (long long)row * ka;
         for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < full4; c += gridDim.x * blockDim.x) {
             const float4 x = __ldg(reinterpret_cast<const float4 *>(src) + c);
+            if (hi == nullptr) {
+                reinterpret_cast<float4 *>(l)[c] =
+                    make_float4(lo_of_raw(x.x), lo_of_raw(x.y), lo_of_raw(x.z), lo_of_raw(x.w));
+                continue;
+            }
             float4 xh, xl;
             split_one(x.x, xh.x, xl.x);
             split_one(x.y, xh.y, xl.y);
@@ -245,6 +252,10 @@ __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ 
             reinterpret_cast<float4 *>(l)[c] = xl;
         }
         for (int t = scal0 + blockIdx.x * blockDim.x + threadIdx.x; t < k; t += gridDim.x * blockDim.x) {
+            if (hi == nullptr) {
+                l[t] = lo_of_raw(__ldg(src + t));
+                continue;
+            }
             float xh, xl;
             split_one(__ldg(src + t), xh, xl);
             h[t] = xh;

@@ -250,6 +250,7 @@ typedef struct sgemm_plan {
     int trans;         /* 1: tensor-core tiles of C^T = B^T A^T (n <= 128; bm = 256, bn = 128) */
     int stream_k;      /* > 0: stream-K over this many CTAs (grid); each takes an equal share  */
                        /*      of all tiles' k slabs, partial tiles meet in a workspace        */
+    int a_lo_only;     /* 1: the split pass writes only A's lo part; the GEMM reads hi from A  */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

@@ -211,6 +211,13 @@ def test_in_kernel_split_policy(monkeypatch):
     assert ain(1000, 1500, 777) == 0                 # lda = 777: rows not 16-byte aligned
     assert ain(1000, 1500, 777, lda=780) == 1
     assert ain(1000, 1500, 780, A_ptr=20) == 0       # A not 16-byte aligned
+    # n > 4096: a split pass, which writes only A's lo part when TMA can read A
+    st, p = binding.plan(8192, 8192, 8192, path=TC)
+    assert (p["a_in_kernel"], p["a_lo_only"]) == (0, 1)
+    st, p = binding.plan(8192, 8192, 8190, path=TC)  # lda = 8190: rows not 16-byte aligned
+    assert (p["a_in_kernel"], p["a_lo_only"]) == (0, 0)
+    st, p = binding.plan(2048, 2048, 2048, path=TC)
+    assert (p["a_in_kernel"], p["a_lo_only"]) == (1, 0)
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "0")
     assert ain(16384, 128, 8192) == 0
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "1")
