@@ -38,7 +38,13 @@
  * Execution.  Every entry point that takes a stream enqueues its kernels on
  * `stream` (0 = the legacy default stream) of the current device and returns
  * without synchronising; errors raised later by the GPU surface at the
- * caller's next synchronisation.  Calls are thread-safe.
+ * caller's next synchronisation.  Calls are thread-safe, and calls on
+ * different streams may run at the same time (each takes its scratch from
+ * the pool in its own stream's order).  A call of sgemm, sgemm_ex, sgemm_op
+ * or sgemm_strided_batched may be captured into a CUDA graph once an earlier
+ * call has done the device's one-time set-up (kernel attributes, the
+ * scratch pool): its pool allocation, the counter reset of stream-K and its
+ * launches become graph nodes.
  *
  * Errors.  The return value is a status:
  *     0                      success;
