@@ -290,6 +290,32 @@ def time_launches(fn, stream, steps, flush=None):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def device_time_ms(fn, stream, reps, flush=None):
+    """Device time of one fn() launch sequence (ms): reps x (flush, fn)
+    enqueued back to back minus reps x flush alone, each bracketed by CUDA
+    events on `stream`.  For kernels shorter than the host's cost of a call,
+    where per-launch events would also count the GPU waiting for the host."""
+    import torch
+
+    def run(with_fn):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            if flush is not None:
+                flush()
+            if with_fn:
+                fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    run(True)   # warm
+    with_fn = min(run(True) for _ in range(3))
+    without = min(run(False) for _ in range(3))
+    return max(0.0, (with_fn - without) / reps)
+
+
 def time_e2e(p, world, host, step_on, steps):
     """End-to-end steps through the C ABI from pinned host memory: each step
     copies its A and B (and C0 when beta != 0) host -> device, runs the
@@ -468,10 +494,10 @@ def run_ours(args, rank, world):
 
             for _ in range(3):
                 splits_only()
-            sb = time_launches(splits_only, stream, min(args.steps, 100), flush=flush)
-            gemm_ms = mean_ms - sum(sb) / len(sb)
+            split_ms = device_time_ms(splits_only, stream, 20, flush=flush)
+            gemm_ms = mean_ms - split_ms
             gemm_timing = ("whole call minus " + ("split_bt_kernel" if a_in else "split_a_kernel + split_bt_kernel")
-                           + " timed alone (CUDA events)")
+                           + " timed alone (device time of 20 back-to-back launches, CUDA events)")
             del a_hi, a_lo
         else:
             # the step is split_a + split_bt + the tcgen05 GEMM; the GEMM
