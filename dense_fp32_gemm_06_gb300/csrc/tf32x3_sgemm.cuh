@@ -789,13 +789,21 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                 const int c4 = TRANS ? idx / (r1 - r0) : idx % (BN / 4);
                 const int row = cl_m0 + r, col = cl_n0 + 4 * c4;
                 const uint32_t off = part0 + (uint32_t)(r * PART_PITCH + 4 * c4) * 4u;
-                float4 sum = tc::ld_cluster_v4(tc::map_shared_rank(off, 0));
-                for (uint32_t q = 1; q < nsplit; ++q) {
-                    const float4 v = tc::ld_cluster_v4(tc::map_shared_rank(off, q));
-                    sum.x += v.x;
-                    sum.y += v.y;
-                    sum.z += v.z;
-                    sum.w += v.w;
+                // all S remote loads first (in flight together), then the
+                // adds in rank order
+                float4 v[8];
+#pragma unroll
+                for (uint32_t q = 0; q < 8; ++q)
+                    if (q < nsplit) v[q] = tc::ld_cluster_v4(tc::map_shared_rank(off, q));
+                float4 sum = v[0];
+#pragma unroll
+                for (uint32_t q = 1; q < 8; ++q) {
+                    if (q < nsplit) {
+                        sum.x += v[q].x;
+                        sum.y += v[q].y;
+                        sum.z += v[q].z;
+                        sum.w += v[q].w;
+                    }
                 }
                 const float a[4] = {sum.x, sum.y, sum.z, sum.w};
                 if constexpr (TRANS) {
