@@ -8,15 +8,19 @@
 // memory.  With round-to-nearest splits |a_lo| <= 2^-11 |a|, the dropped
 // a_lo*b_lo term and the rounding of the lo parts stay below ~3 * 2^-22
 // |a||b| per product, well inside the FP32 acceptance bound
-// |C - r| <= 1e-5 * sum_t |A_it||B_tj| + 1e-6 |beta C0|.
+// |C - r| <= 1e-5 * sum_t |A_it||B_tj| + 1e-6 |beta C0|.  When the GEMM
+// reads A's hi part straight from A (the MMA drops the low 13 bits: hi =
+// trunc(x), |lo| < 2^-10 |x|), the bound per product is ~2^-20 |a||b|.
 //
 // Two steps per call:
 //  1. split kernels (HBM-bound): A (any lda, any 4-byte alignment) becomes
 //     A_hi, A_lo, m x ka row-major (ka = k rounded up to 4, 16-byte rows);
-//     B becomes B^T_hi, B^T_lo, n x ka, transposed through a padded 32 x 33
-//     shared tile (coalesced reads and writes).  Both operands of the MMA
-//     are then K-major.  A skips this pass when the GEMM kernel splits it
-//     itself from a raw TMA load (A_IN, at the kernel);
+//     B becomes B^T_hi, B^T_lo, n x ka, transposed through a 32 x 64 shared
+//     tile padded to 65 columns (coalesced reads and writes).  Both operands
+//     of the MMA are then K-major.  When TMA can read A as it is, A skips
+//     this pass -- the GEMM kernel splits it from a raw TMA load (A_IN, at
+//     the kernel) -- or, for wide problems, the pass writes only A's lo part
+//     and the GEMM reads A's hi part from A;
 //  2. the GEMM kernel: one CTA per 128 x BN tile of C (BN = 256, or 128 for
 //     narrow or few-tile problems; the rest of this comment says 256), 10 warps
 //     (12 when the kernel splits A itself, below).
@@ -53,6 +57,12 @@
 //     its 256-row operand is A (256 rows of C per tile) -- and the
 //     accumulator warps store C^T's rows as columns of C (each warp's 32
 //     lanes are 32 consecutive columns: 128-byte stores).
+//     Stream-K (Params): persistent CTAs that take whole tiles for the full
+//     waves and share the last wave's tiles out by slabs, a shared tile
+//     being finished by the last of its CTAs from partials in a workspace.
+//     A GEMM that runs in one wave is launched as a programmatic dependent
+//     of the split kernels: it sets up while they finish, and its producer
+//     waits for them before the first load.
 //     TMA zero-fills rows past m, columns past n and k past the end, so the
 //     MMA never sees an index test.  Every mbarrier wait is bounded (2 s):
 //     a wait that runs out records a code in the library status word,
@@ -316,7 +326,7 @@ __global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__
 // lands and waits for "converted" only before the third, so the split
 // overlaps the tensor core instead of costing an HBM round trip of A.
 // Error: |x - hi - lo| < 2^-21 |x| and |lo| < 2^-10 |x| (against 2^-22 and
-// 2^-11 for the pre-pass's round-to-nearest hi), so each product stays
+// 2^-11 for a round-to-nearest hi), so each product stays
 // within ~2^-20 |a b| of exact, far inside the FP32 acceptance bound.
 template <class Cfg, bool C_VEC, bool A_IN = false, bool TRANS = false>
 __global__ void __launch_bounds__(threads_for(A_IN), 1)
