@@ -273,8 +273,8 @@ int sgemm_plan_for(int m, int n, int k, float alpha,
  * ring slot, 0x202 the MMA issuer for a loaded (or split) slab, 0x203 the
  * accumulator warps for a finished chunk, 0x204 a wait while draining after
  * an earlier timeout, 0x205 the MMA issuer for a free TMEM buffer, 0x206 the
- * splitter warps for a loaded slab, 0x207 reserved.  Each means the result of
- * that call is not valid.
+ * splitter warps for a loaded slab.  Each means the result of that call is
+ * not valid.
  */
 int sgemm_device_status(int *flag, int clear);
 
