@@ -41,8 +41,9 @@ def sgemm_raw(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, stream=0
 
 def plan(m, n, k, alpha=1.0, A_ptr=16, lda=None, B_ptr=16, ldb=None, beta=0.0, C_ptr=16, ldc=None,
          path=PATH_AUTO, num_sms=152):
-    """The launch plan the library would use (host only, no GPU needed);
-    returns (status, dict)."""
+    """The launch plan the library would use; returns (status, dict).
+    num_sms > 0: host only (no GPU needed) for a device with that many SMs;
+    num_sms=0: the plan a call on the current device would use."""
     lib = _native.load()
     lda = max(1, k) if lda is None else lda
     ldb = max(1, n) if ldb is None else ldb

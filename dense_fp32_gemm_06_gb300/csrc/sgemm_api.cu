@@ -316,15 +316,18 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
             }
             // stream-K: W = tiles / G full waves of whole tiles, then the R
             // remaining tiles' slabs shared out evenly (every CTA must get at
-            // least one slab of them: R x KT >= G).  Measured: the fix-up of
-            // shared tiles costs ~10 us, and stream-K only pays when whole
-            // tiles would leave >= 10 % of the last wave's SMs idle (4096^3:
-            // 17 % faster; 8192^3, 3.8 % idle: 4 % slower).
+            // least one slab of them: R x KT >= G).  Measured: the fix-up of a
+            // shared tile costs ~10 us, twice when a CTA's share is shorter
+            // than a tile (it then holds parts of two), and stream-K only
+            // pays when whole tiles would leave >= 10 % of the last wave's SMs
+            // idle (4096^3: 17 % faster; 8192^3, 3.8 % idle: 4 % slower).
             const long long W = tiles / num_sms, R = tiles - W * num_sms;
             const bool idle_tail = 10 * (num_sms - R) >= (W + 1) * num_sms;
             if (allow_sk && force_sk != 0 && batch == 1 && !(force_s >= 1 && force_s <= 8) && R > 0 &&
-                R * KT >= num_sms && ((4 * R >= num_sms && idle_tail) || force_sk == 1))
-                consider(W * KT * slab + ((R * KT + num_sms - 1) / num_sms) * slab + 320, bn, 1, tr, true);
+                R * KT >= num_sms && ((4 * R >= num_sms && idle_tail) || force_sk == 1)) {
+                const long long share = (R * KT + num_sms - 1) / num_sms;
+                consider(W * KT * slab + share * slab + (share < KT ? 640 : 320), bn, 1, tr, true);
+            }
         }
         // A is split inside the GEMM (two extra warps split each raw slab in
         // shared memory, no pass over A through HBM) when the kernel can read
@@ -858,6 +861,11 @@ int sgemm(int m, int n, int k, float alpha, const float *A, int lda, const float
 int sgemm_plan_for(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb,
                    float beta, const float *C, int ldc, int path, int num_sms, sgemm_plan *out) {
     if (out == nullptr) return SGEMM_STATUS_UNSUPPORTED;
+    if (num_sms == 0) {   // the current device, as a call would plan it
+        DeviceState *dev = nullptr;
+        if (int st = device_state(&dev)) return st;
+        return plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, dev->sms, out, dev->max_clusters);
+    }
     return plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, path, num_sms, out);
 }
 

@@ -230,9 +230,12 @@ const char *sgemm_status_string(int status);
 int sgemm_last_cuda_error(void);
 
 /*
- * Launch plan the library would use for a problem (host only: reads no
- * memory, needs no GPU).  The pointers are inspected for alignment only.
- * num_sms is the SM count of the target device (152 on GB300).
+ * Launch plan the library would use for a problem.  The pointers are
+ * inspected for alignment only.  num_sms > 0: host only (reads no memory,
+ * needs no GPU) for a device with that many SMs (152 on GB300), assuming
+ * clusters of S CTAs fill GPCs of num_sms / 8 SMs.  num_sms == 0: the plan
+ * for the current device, with its measured cluster capacity -- the plan a
+ * call made now would use (the device's one-time set-up runs if needed).
  */
 typedef struct sgemm_plan {
     int path;          /* SGEMM_PATH_FFMA or SGEMM_PATH_TF32X3; 0 = no kernel (m or n is 0) */

@@ -274,3 +274,13 @@ def test_trans_tile_policy(monkeypatch):
     st, p = binding.plan(300, 100, 5000, path=TC)
     assert p["trans"] == 1 and (p["bm"], p["bn"]) == (256, 128)
     assert binding.plan(300, 200, 5000, path=TC)[1]["trans"] == 0
+
+
+def test_device_plan_needs_a_device():
+    """num_sms=0 asks for the current device's plan; without a usable device
+    that is a CUDA error (status 100), reported, not guessed."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    st, _ = binding.plan(2048, 2048, 2048, num_sms=0)
+    assert st == 100

@@ -93,7 +93,7 @@ def test_batch_integer_twin_bit_exact(path):
 def test_split_k_inside_a_batch():
     """A batch whose tiles are few enough that each problem's tile is split
     over a cluster."""
-    st, plan = binding.plan(256, 256, 8192, lda=8192, path=binding.PATH_TF32X3)
+    st, plan = binding.plan(256, 256, 8192, lda=8192, path=binding.PATH_TF32X3, num_sms=0)
     assert plan["split_k"] > 1
     run_batch(2, 256, 256, 8192, binding.PATH_TF32X3, seed=41)
 

@@ -30,7 +30,7 @@ def test_dependent_launch_matches_normal_launch(monkeypatch, m, n, k, lda, beta)
     p = inputs.make_problem(m, n, k, alpha=1.25, beta=beta, seed=m + n + 3 * k, a="normal", b="uniform",
                             c="uniform" if beta else None, lda=lda)
     st, plan = binding.plan(p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, path=TC,
-                            num_sms=torch.cuda.get_device_properties(0).multi_processor_count)
+                            num_sms=0)
     assert st == 0 and plan["grid"] <= 152
     outs = []
     for pdl in ("1", "0"):

@@ -265,7 +265,10 @@ def test_split_k_clusters(monkeypatch, m, n, k, beta):
     their partial tiles through distributed shared memory (stream-K, which
     the plan may prefer for some of these shapes, is pinned off)."""
     monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
-    st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3)
+    st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3, num_sms=0)
+    if plan["split_k"] == 1:   # this device's cluster capacity favours whole tiles here: split anyway
+        monkeypatch.setenv("SGEMM_GB300_SPLIT_K", "3")
+        st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3, num_sms=0)
     assert st == 0 and plan["split_k"] > 1, plan
     p = inputs.make_problem(m, n, k, alpha=1.25, beta=beta, seed=m + n + k, a="normal", b="uniform",
                             c="uniform" if beta else None)
@@ -276,7 +279,10 @@ def test_split_k_clusters(monkeypatch, m, n, k, beta):
 def test_split_k_integer_twin_bit_exact(monkeypatch, m, n, k):
     """Partial sums of integers are exact, so the split result is too."""
     monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
-    st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3)
+    st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3, num_sms=0)
+    if plan["split_k"] == 1:   # as above
+        monkeypatch.setenv("SGEMM_GB300_SPLIT_K", "3")
+        st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3, num_sms=0)
     assert st == 0 and plan["split_k"] > 1
     p = inputs.make_problem(m, n, k, alpha=2.0, beta=0.5, seed=7 * k, a="int", b="int", c="int")
     run_and_check(p, binding.PATH_TF32X3, exact=True)

@@ -39,7 +39,7 @@ def _run(p, exact=False):
 
 
 def _plan(p):
-    st, plan = binding.plan(p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, path=TC)
+    st, plan = binding.plan(p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, path=TC, num_sms=0)
     assert st == 0
     return plan
 

@@ -34,7 +34,7 @@ def a_split(request, monkeypatch):
 
 
 def _plan(p):
-    st, plan = binding.plan(p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, path=TC)
+    st, plan = binding.plan(p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc, path=TC, num_sms=0)
     assert st == 0
     return plan
 
@@ -99,5 +99,5 @@ def test_trans_tiles_strided_batch():
 
 def test_plan_prefers_trans_for_the_skinny_workload(monkeypatch):
     monkeypatch.delenv("SGEMM_GB300_TRANS")
-    st, plan = binding.plan(16384, 128, 8192, path=TC)
+    st, plan = binding.plan(16384, 128, 8192, path=TC, num_sms=0)
     assert st == 0 and plan["trans"] == 1 and plan["grid"] >= 128, plan
