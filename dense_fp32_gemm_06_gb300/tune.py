@@ -1,6 +1,7 @@
-"""Tile-width x split-K sweep of the tensor-core GEMM for given shapes.
+"""Sweeps of the tensor-core path's plan choices for given shapes.
 
     python -m dense_fp32_gemm_06_gb300.tune --shapes 1000,1500,777 256,256,8192 ...
+    python -m dense_fp32_gemm_06_gb300.tune --policy --shapes 2048,2048,2048 ...
 
 For each shape the operands are split once; then the GEMM kernel alone
 (``sgemm_tf32x3_split_gemm``) is timed with CUDA events, after an L2 flush,
@@ -9,6 +10,15 @@ pinned through the library's tuning variables ``SGEMM_GB300_TILE_N`` and
 ``SGEMM_GB300_SPLIT_K``, and once more with the library's own choice.  One
 line per shape: the automatic choice's time, the best configuration, and
 every configuration's median time in microseconds.
+
+--policy: whole calls (sgemm, splits included) under each setting of the
+plan's other choices -- stream-K (SGEMM_GB300_STREAM_K), the transposed
+tile for n <= 128 (SGEMM_GB300_TRANS), A split inside the GEMM
+(SGEMM_GB300_SPLIT_A_IN) -- and under the library's own plan.  The settings
+take turns within each repetition (L2 flushed before every call, CUDA-event
+timed) so that clock and power drift falls on all of them alike; one line
+per shape with the plan the device made, every setting's median time, and
+the plan of each setting that differs from it.
 """
 from __future__ import annotations
 
@@ -82,6 +92,79 @@ def sweep(m, n, k, reps=20, widths=(256, 128), splits=(1, 2, 3, 4, 6, 8), max_ct
     return auto, results
 
 
+POLICY_VARS = ("SGEMM_GB300_STREAM_K", "SGEMM_GB300_TRANS", "SGEMM_GB300_SPLIT_A_IN")
+
+
+def policy(m, n, k, reps=20):
+    """({setting: median us}, {setting: plan}) of whole tensor-core calls;
+    setting "auto" is the library's own plan, the others pin one tuning
+    variable to 0 or 1."""
+    import torch
+    from . import binding
+    stream = torch.cuda.current_stream()
+    flush_buf = torch.empty(2 * L2_BYTES // 4, device="cuda")
+    A = torch.randn(m, k, device="cuda")
+    B = torch.randn(k, n, device="cuda")
+    C = torch.zeros(m, n, device="cuda")
+
+    def call():
+        st = binding.sgemm_raw(m, n, k, 1.0, A.data_ptr(), k, B.data_ptr(), n, 0.0, C.data_ptr(), n,
+                               stream.cuda_stream, binding.PATH_TF32X3)
+        if st:
+            raise RuntimeError(binding.status_string(st))
+
+    def use(var, val):
+        for v in POLICY_VARS:
+            os.environ.pop(v, None)
+        if var is not None:
+            os.environ[var] = val
+
+    settings = [("auto", None, None)]
+    for var in POLICY_VARS:
+        if var == "SGEMM_GB300_TRANS" and n > 128:
+            continue
+        settings += [(f"{var[12:].lower()}={val}", var, val) for val in ("0", "1")]
+    saved = {v: os.environ.get(v) for v in POLICY_VARS}
+    times, plans = {name: [] for name, _, _ in settings}, {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        for name, var, val in settings:
+            use(var, val)
+            st, pl = binding.plan(m, n, k, 1.0, A.data_ptr(), k, B.data_ptr(), n, 0.0, C.data_ptr(), n,
+                                  path=binding.PATH_TF32X3, num_sms=0)
+            plans[name] = pl
+            for _ in range(3):
+                call()
+        for _ in range(reps):
+            for name, var, val in settings:
+                use(var, val)
+                flush_buf.fill_(1.0)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                e1.synchronize()
+                times[name].append(e0.elapsed_time(e1) * 1e3)
+    finally:
+        for v, old in saved.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+    return {name: statistics.median(ts) for name, ts in times.items()}, plans
+
+
+def plan_text(pl):
+    t = f"{pl['bm']}x{pl['bn']}"
+    if pl["trans"]:
+        t += " transposed"
+    if pl["stream_k"]:
+        t += " stream-K"
+    elif pl["split_k"] > 1:
+        t += f" split-K {pl['split_k']}"
+    t += ", A split " + ("in the GEMM" if pl["a_in_kernel"] else "pass (lo only)" if pl["a_lo_only"] else "pass")
+    return t
+
+
 def reduce_bandwidth(n=1 << 28, reps=50):
     """GB/s of reduce_sum_f32 on n floats (4n bytes read per call), CUDA
     events, median of `reps` calls (n = 2^28: 1 GiB, far larger than L2)."""
@@ -104,7 +187,18 @@ def main(argv=None):
                                                     "2048,1024,8192"])
     ap.add_argument("--reps", type=int, default=20)
     ap.add_argument("--reduce", type=int, default=0, help="measure reduce_sum_f32 on this many floats instead")
+    ap.add_argument("--policy", action="store_true", help="whole calls under each plan choice (see above)")
     args = ap.parse_args(argv)
+    if args.policy:
+        for spec in args.shapes:
+            m, n, k = (int(x) for x in spec.split(","))
+            res, plans = policy(m, n, k, reps=args.reps)
+            best = min(res, key=res.get)
+            cells = " ".join(f"{name}:{us:.1f}" + ("" if plans[name] == plans["auto"] else
+                                                   f"[{plan_text(plans[name])}]") for name, us in res.items())
+            print(f"{(m, n, k)} auto={res['auto']:.1f}us [{plan_text(plans['auto'])}] best={best} "
+                  f"{2 * m * n * k / res[best] / 1e6:.1f}TF | {cells}", flush=True)
+        return
     if args.reduce:
         gbs, us = reduce_bandwidth(args.reduce)
         print(f"reduce_sum_f32 n={args.reduce} {us:.1f} us {gbs:.1f} GB/s", flush=True)

@@ -284,3 +284,16 @@ def test_device_plan_needs_a_device():
         pytest.skip("a device is present")
     st, _ = binding.plan(2048, 2048, 2048, num_sms=0)
     assert st == 100
+
+
+def test_tune_plan_text_names_the_plan():
+    """The policy sweep's plan labels follow the host plan's fields."""
+    from dense_fp32_gemm_06_gb300 import tune
+    st, thin = binding.plan(16384, 128, 8192, path=binding.PATH_TF32X3, num_sms=152)
+    assert st == 0
+    text = tune.plan_text(thin)
+    assert text.startswith(f"{thin['bm']}x{thin['bn']}")
+    assert ("transposed" in text) == bool(thin["trans"])
+    assert ("stream-K" in text) == bool(thin["stream_k"])
+    st, square = binding.plan(2048, 2048, 2048, lda=2048, path=binding.PATH_TF32X3, num_sms=152)
+    assert st == 0 and "transposed" not in tune.plan_text(square)
