@@ -320,27 +320,30 @@ def time_e2e(p, world, host, step_on, steps):
     """End-to-end steps through the C ABI from pinned host memory: each step
     copies its A and B (and C0 when beta != 0) host -> device, runs the
     GEMM and copies C device -> host.  Steps are pipelined the way a
-    streaming caller would run them: two device buffer sets, one stream for
-    host -> device copies, one for the GEMM, one for device -> host copies,
-    so step i+1's inputs and step i-1's result move while step i computes.
+    streaming caller would run them: three device buffer sets, one stream
+    for host -> device copies, one for the GEMM, one for device -> host
+    copies, so step i+1's inputs and step i-1's result move while step i
+    computes (with two sets, step i+1's upload would also wait for step
+    i-1's download, which puts both copies of a step on one chain).
     Returns the metric over the whole run (first copy in to last copy out)."""
     import torch
     A_h, B_h, C_h, out_h = host
     up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    nsets = 3
     sets = [(torch.empty_like(A_h, device="cuda"), torch.empty_like(B_h, device="cuda"),
-             torch.empty_like(C_h, device="cuda")) for _ in range(2)]
-    outs = [torch.empty_like(C_h).pin_memory() for _ in range(2)]
-    done_compute = [None, None]
-    done_down = [None, None]
+             torch.empty_like(C_h, device="cuda")) for _ in range(nsets)]
+    outs = [torch.empty_like(C_h).pin_memory() for _ in range(nsets)]
+    done_compute = [None] * nsets
+    done_down = [None] * nsets
 
     def run(n):
         for i in range(n):
-            A, B, C = sets[i % 2]
+            A, B, C = sets[i % nsets]
             with torch.cuda.stream(up):
-                if done_compute[i % 2] is not None:
-                    up.wait_event(done_compute[i % 2])      # the GEMM of step i-2 has read A, B
-                if done_down[i % 2] is not None:
-                    up.wait_event(done_down[i % 2])         # and its result has left C
+                if done_compute[i % nsets] is not None:
+                    up.wait_event(done_compute[i % nsets])      # the GEMM of step i-3 has read A, B
+                if done_down[i % nsets] is not None:
+                    up.wait_event(done_down[i % nsets])         # and its result has left C
                 A.copy_(A_h, non_blocking=True)
                 B.copy_(B_h, non_blocking=True)
                 if p.beta != 0:
@@ -350,18 +353,18 @@ def time_e2e(p, world, host, step_on, steps):
             with torch.cuda.stream(comp):
                 comp.wait_event(ready)
                 step_on(A, B, C, comp.cuda_stream)
-                done_compute[i % 2] = torch.cuda.Event()
-                done_compute[i % 2].record(comp)
+                done_compute[i % nsets] = torch.cuda.Event()
+                done_compute[i % nsets].record(comp)
             with torch.cuda.stream(down):
-                down.wait_event(done_compute[i % 2])
-                outs[i % 2].copy_(C, non_blocking=True)
-                done_down[i % 2] = torch.cuda.Event()
-                done_down[i % 2].record(down)
+                down.wait_event(done_compute[i % nsets])
+                outs[i % nsets].copy_(C, non_blocking=True)
+                done_down[i % nsets] = torch.cuda.Event()
+                done_down[i % nsets].record(down)
 
-    run(2)
+    run(nsets)
     torch.cuda.synchronize()
-    done_compute[:] = [None, None]
-    done_down[:] = [None, None]
+    done_compute[:] = [None] * nsets
+    done_down[:] = [None] * nsets
     t = time.perf_counter()
     run(steps)
     torch.cuda.synchronize()
@@ -369,7 +372,7 @@ def time_e2e(p, world, host, step_on, steps):
     h2d = A_h.numel() * 4 + B_h.numel() * 4 + (C_h.numel() * 4 if p.beta != 0 else 0)
     return {"value": tflops(p, ms, world), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": C_h.numel() * 4, "ms_per_step": ms, "steps": steps,
-            "pipelining": "2 device buffer sets; copies in, GEMM, copies out on three streams"}
+            "pipelining": f"{nsets} device buffer sets; copies in, GEMM, copies out on three streams"}
 
 
 def run_ours(args, rank, world):
