@@ -107,7 +107,8 @@ struct Config {
     static constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;   // A_hi, A_lo, B_hi, B_lo
     static constexpr int TMEM_COLS = 2 * BN;                      // two accumulators
     static constexpr int COLS_PER_THREAD = BN / 2;                // two warps per 32-lane group
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_REGION;
+    static constexpr int EPI_BYTES = ACC_WARPS * 32 * 32 * 4;     // a 32 x 32 staging block per accumulator warp
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_REGION + EPI_BYTES;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "power-of-two TMEM allocation");
     static_assert(COLS_PER_THREAD % 16 == 0, "accumulator warps load 16 columns at a time");
@@ -354,6 +355,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 8);
     volatile int *const sk_last = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 12);
     const uint32_t bar_conv = bar_done + 24;             // [STAGES] A slab split in place (A_IN)
+    float4 *const epi = reinterpret_cast<float4 *>(bars + BAR_REGION);   // [ACC_WARPS][32 rows][8 float4]
     static_assert(8 * (3 * STAGES + 7) <= BAR_REGION, "barrier region");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -596,73 +598,117 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
         float acc[COLS_PER_THREAD];
         bool ok = true;
 
-        // Quad q of this thread's part of the tile at (m0, n0): columns
-        // n0 + half*COLS_PER_THREAD + 4q .. +3 of its row of C, or (TRANS)
-        // rows m0 + half*COLS_PER_THREAD + 4q .. +3 of its column of C (the
-        // 32 lanes of a warp then cover 128 contiguous bytes of a C row).
-        // Stores go in blocks: the block's C values (beta != 0) are loaded
-        // first, so the loads are in flight together instead of each waiting
-        // behind the previous store to the same array.
-        auto load_c = [&](int m0, int n0, int q) -> float4 {
+        // Writing C.  TRANS: quad q of this thread's part of the tile at
+        // (m0, n0) is rows m0 + half*COLS_PER_THREAD + 4q .. +3 of its column
+        // n0 + trow of C; the 32 lanes of a warp cover 128 contiguous bytes of
+        // a C row, so these go straight to C.  Stores go in blocks: the
+        // block's C values (beta != 0) are loaded first, so the loads are in
+        // flight together instead of each waiting behind the previous store.
+        auto load_c_t = [&](int m0, int n0, int q) -> float4 {
             float c[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (TRANS) {
-                const int col = n0 + trow, r = m0 + half * COLS_PER_THREAD + 4 * q;
-                if (col < p.n) {
+            const int col = n0 + trow, r = m0 + half * COLS_PER_THREAD + 4 * q;
+            if (col < p.n) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (r + e < p.m) c[e] = Cb[(long long)(r + e) * p.ldc + col];
-                }
-            } else {
-                const int row = m0 + trow, col = n0 + half * COLS_PER_THREAD + 4 * q;
-                if (row < p.m) {
-                    const float *crow = Cb + (long long)row * p.ldc;
-                    if (C_VEC && col + 3 < p.n) return *reinterpret_cast<const float4 *>(crow + col);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (col + e < p.n) c[e] = crow[col + e];
-                }
+                for (int e = 0; e < 4; ++e)
+                    if (r + e < p.m) c[e] = Cb[(long long)(r + e) * p.ldc + col];
             }
             return make_float4(c[0], c[1], c[2], c[3]);
         };
         // C = alpha * v + beta * c for quad q (c: its C values, read when beta != 0)
-        auto put_quad = [&](int m0, int n0, int q, float4 v, float4 c4) {
+        auto put_quad_t = [&](int m0, int n0, int q, float4 v, float4 c4) {
             const float alpha = p.alpha, beta = p.beta;
             const float a[4] = {v.x, v.y, v.z, v.w}, c[4] = {c4.x, c4.y, c4.z, c4.w};
-            float o[4];
+            const int col = n0 + trow, r = m0 + half * COLS_PER_THREAD + 4 * q;
+            if (col >= p.n) return;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[e] = beta != 0.f ? fmaf(alpha, a[e], beta * c[e]) : alpha * a[e];
-            if constexpr (TRANS) {
-                const int col = n0 + trow, r = m0 + half * COLS_PER_THREAD + 4 * q;
-                if (col >= p.n) return;
+            for (int e = 0; e < 4; ++e)
+                if (r + e < p.m)
+                    Cb[(long long)(r + e) * p.ldc + col] = beta != 0.f ? fmaf(alpha, a[e], beta * c[e]) : alpha * a[e];
+        };
+        // Otherwise a thread's row holds 4 consecutive columns per quad, and
+        // direct stores from a warp would touch 32 rows with 16 bytes each.
+        // A block of 32 columns of the warp's 32 rows goes through the warp's
+        // staging buffer instead and leaves as 4 rows x 128 contiguous bytes
+        // per store (C, when beta != 0, is read the same way).  Chunk j of
+        // row r is kept at chunk j ^ (r & 7): the row-wise writes and the
+        // chunk-wise reads both touch every bank once per 128 bytes.
+        auto c_at = [&](int row, int col) -> float4 {
+            const float *crow = Cb + (long long)row * p.ldc;
+            if (C_VEC && col + 3 < p.n) return *reinterpret_cast<const float4 *>(crow + col);
+            float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (col + e < p.n) c[e] = crow[col + e];
+            return make_float4(c[0], c[1], c[2], c[3]);
+        };
+        auto put_at = [&](int row, int col, float4 v, float4 c) {
+            const float alpha = p.alpha, beta = p.beta;
+            const float4 o = beta != 0.f ? make_float4(fmaf(alpha, v.x, beta * c.x), fmaf(alpha, v.y, beta * c.y),
+                                                       fmaf(alpha, v.z, beta * c.z), fmaf(alpha, v.w, beta * c.w))
+                                         : make_float4(alpha * v.x, alpha * v.y, alpha * v.z, alpha * v.w);
+            float *crow = Cb + (long long)row * p.ldc;
+            if (C_VEC && col + 3 < p.n) {
+                *reinterpret_cast<float4 *>(crow + col) = o;
+            } else {
+                const float a[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (r + e < p.m) Cb[(long long)(r + e) * p.ldc + col] = o[e];
-            } else {
-                const int row = m0 + trow, col = n0 + half * COLS_PER_THREAD + 4 * q;
-                if (row >= p.m) return;
-                float *crow = Cb + (long long)row * p.ldc;
-                if (C_VEC && col + 3 < p.n) {
-                    *reinterpret_cast<float4 *>(crow + col) = make_float4(o[0], o[1], o[2], o[3]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (col + e < p.n) crow[col + e] = o[e];
-                }
+                    if (col + e < p.n) crow[col + e] = a[e];
             }
         };
-        auto store_tile = [&](int m0, int n0) {
-            constexpr int EB = 4;   // quads per block
+        float4 *const stg = epi + (warp - 2) * 256;
+        // v: this thread's columns half*COLS_PER_THREAD + 32*blk .. +31 of its row
+        auto store_block32 = [&](int m0, int n0, int blk, const float4 (&v)[8]) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) stg[lane * 8 + (j ^ (lane & 7))] = v[j];
+            __syncwarp();
+            const int c = lane & 7;
+            const int col = n0 + half * COLS_PER_THREAD + 32 * blk + 4 * c;
+            const int row0 = m0 + lane_grp * 32 + (lane >> 3);   // + 4i for read i
             const bool read_c = p.beta != 0.f;
 #pragma unroll
-            for (int qb = 0; qb < COLS_PER_THREAD / 4; qb += EB) {
-                float4 c[EB];
+            for (int i0 = 0; i0 < 8; i0 += 4) {
+                float4 cv[4];
 #pragma unroll
-                for (int u = 0; u < EB; ++u)
-                    c[u] = read_c ? load_c(m0, n0, qb + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int u = 0; u < 4; ++u)
+                    cv[u] = read_c && row0 + 4 * (i0 + u) < p.m ? c_at(row0 + 4 * (i0 + u), col)
+                                                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int u = 0; u < EB; ++u) {
-                    const int q = qb + u;
-                    put_quad(m0, n0, q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]), c[u]);
+                for (int u = 0; u < 4; ++u) {
+                    const int rr = 4 * (i0 + u) + (lane >> 3);
+                    const float4 a = stg[rr * 8 + (c ^ (rr & 7))];
+                    if (row0 + 4 * (i0 + u) < p.m) put_at(row0 + 4 * (i0 + u), col, a, cv[u]);
+                }
+            }
+            __syncwarp();   // the buffer is read before the next block overwrites it
+        };
+        auto store_tile = [&](int m0, int n0) {
+            if constexpr (TRANS) {
+                constexpr int EB = 4;   // quads per block
+                const bool read_c = p.beta != 0.f;
+#pragma unroll
+                for (int qb = 0; qb < COLS_PER_THREAD / 4; qb += EB) {
+                    float4 c[EB];
+#pragma unroll
+                    for (int u = 0; u < EB; ++u)
+                        c[u] = read_c ? load_c_t(m0, n0, qb + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int u = 0; u < EB; ++u) {
+                        const int q = qb + u;
+                        put_quad_t(m0, n0, q, make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]),
+                                   c[u]);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int blk = 0; blk < COLS_PER_THREAD / 32; ++blk) {
+                    float4 v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int q = 8 * blk + j;
+                        v[j] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                    }
+                    store_block32(m0, n0, blk, v);
                 }
             }
         };
@@ -699,7 +745,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
             __threadfence();
             // blocks of QB quads: each contributor's QB loads are in flight
             // together (one L2 round trip per block and contributor)
-            constexpr int QB = 8;
+            constexpr int QB = 8;   // = one 32-column block of store_block32
             const float4 *first = ws + ((size_t)g_first * 2 + first_slot) * SLOT;
 #pragma unroll 1
             for (int qb = 0; qb < COLS_PER_THREAD / 4; qb += QB) {
@@ -721,13 +767,17 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                         sum[u].w += v[u].w;
                     }
                 }
-                const bool read_c = p.beta != 0.f;
-                float4 c[QB];
+                if constexpr (TRANS) {
+                    const bool read_c = p.beta != 0.f;
+                    float4 c[QB];
 #pragma unroll
-                for (int u = 0; u < QB; ++u)
-                    c[u] = read_c ? load_c(m0, n0, qb + u) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int u = 0; u < QB; ++u)
+                        c[u] = read_c ? load_c_t(m0, n0, qb + u) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int u = 0; u < QB; ++u) put_quad(m0, n0, qb + u, sum[u], c[u]);
+                    for (int u = 0; u < QB; ++u) put_quad_t(m0, n0, qb + u, sum[u], c[u]);
+                } else {
+                    store_block32(m0, n0, qb / QB, sum);
+                }
             }
         };
 
