@@ -481,7 +481,9 @@ def run_ours(args, rank, world):
         b_hi = torch.empty(p.n * ka, device="cuda")
         b_lo = torch.empty_like(b_hi)
         a_in = bool(plan["a_in_kernel"])
-        launches_per_step = 2 if a_in else 3
+        # one split launch (split_pair_kernel, for B alone or for both
+        # operands) and the GEMM
+        launches_per_step = 2
         if a_in or plan["stream_k"] > 0:
             # the GEMM kernel splits A itself, or runs stream-K with a
             # workspace only the whole call provides: its time is the
@@ -500,7 +502,9 @@ def run_ours(args, rank, world):
                 splits_only()
             split_ms = device_time_ms(splits_only, stream, 20, flush=flush)
             gemm_ms = mean_ms - split_ms
-            gemm_timing = ("whole call minus " + ("split_bt_kernel" if a_in else "split_a_kernel + split_bt_kernel")
+            gemm_timing = ("whole call minus " + ("the split pass over B" if a_in else
+                                                  "the split passes over A and B (timed as two launches; the call "
+                                                  "runs both in one)")
                            + " timed alone (device time of 20 back-to-back launches, CUDA events)")
             del a_hi, a_lo
         else:

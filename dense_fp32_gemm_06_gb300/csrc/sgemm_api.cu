@@ -411,10 +411,9 @@ int ka_of(int k) { return (k + 3) & ~3; }
 // looping over its share (they are HBM-bound).
 constexpr int kSplitBlocks = 8 * 160;
 
-int launch_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream,
-                   int batch = 1, long long src_batch = 0, long long dst_batch = 0) {
-    if (m == 0 || k == 0 || batch == 0) return SGEMM_STATUS_OK;
-    const bool vec = aligned(A, 16) && (lda % 4) == 0;
+tf32x3::SplitJob split_a_job(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, int batch,
+                             long long src_batch, long long dst_batch) {
+    const bool vec = aligned(A, 16) && (lda % 4) == 0 && (src_batch % 4) == 0;
     const int per_row = vec ? (k / 4 > 0 ? k / 4 : 1) : k;
     int gx = (per_row + 255) / 256;
     if (gx > 16) gx = 16;
@@ -424,26 +423,44 @@ int launch_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_
     if (gy > 65535) gy = 65535;
     // with a batch, fewer rows per problem in flight
     if (batch > 1) gy = gy / batch > 0 ? gy / batch : 1;
-    const dim3 grid(gx, gy, batch);
-    if (vec && (src_batch % 4) == 0)
-        tf32x3::split_a_kernel<true><<<grid, 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k), src_batch,
-                                                               dst_batch);
-    else
-        tf32x3::split_a_kernel<false><<<grid, 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, ka_of(k), src_batch,
-                                                                dst_batch);
-    return SGEMM_STATUS_OK;
+    return tf32x3::SplitJob{A, lda, m, k, a_hi, a_lo, ka_of(k), src_batch, dst_batch, gx, gy, vec ? 1 : 0};
 }
 
 // B (k x n, ldb) -> bt_hi, bt_lo (B^T, n x ka).
-int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, cudaStream_t stream,
-                   int batch = 1, long long src_batch = 0, long long dst_batch = 0) {
-    if (n == 0 || k == 0 || batch == 0) return SGEMM_STATUS_OK;
+tf32x3::SplitJob split_b_job(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, int batch,
+                             long long src_batch, long long dst_batch) {
     long long gx = (n + 63) / 64, gy = (k + 31) / 32;
     const long long budget = batch > 1 ? (kSplitBlocks / batch > 0 ? kSplitBlocks / batch : 1) : kSplitBlocks;
     if (gx > budget) gx = budget;
     if (gy > budget / gx) gy = budget / gx > 0 ? budget / gx : 1;
-    tf32x3::split_bt_kernel<<<dim3((unsigned)gx, (unsigned)gy, (unsigned)batch), 256, 0, stream>>>(
-        B, ldb, k, n, bt_hi, bt_lo, ka_of(k), src_batch, dst_batch);
+    return tf32x3::SplitJob{B, ldb, k, n, bt_hi, bt_lo, ka_of(k), src_batch, dst_batch, (int)gx, (int)gy, 2};
+}
+
+// Split passes in one launch (split_pair_kernel): j0, then j1 (none when j1.gx = 0).
+void launch_split_pair(const tf32x3::SplitJob &j0, const tf32x3::SplitJob &j1, int batch, cudaStream_t stream) {
+    const unsigned blocks = (unsigned)(j0.gx * j0.gy + j1.gx * j1.gy);
+    tf32x3::split_pair_kernel<<<dim3(blocks, 1, (unsigned)batch), 256, 0, stream>>>(j0, j1);
+}
+
+int launch_split_a(int m, int k, const float *A, int lda, float *a_hi, float *a_lo, cudaStream_t stream,
+                   int batch = 1, long long src_batch = 0, long long dst_batch = 0) {
+    if (m == 0 || k == 0 || batch == 0) return SGEMM_STATUS_OK;
+    const tf32x3::SplitJob j = split_a_job(m, k, A, lda, a_hi, a_lo, batch, src_batch, dst_batch);
+    const dim3 grid(j.gx, j.gy, batch);
+    if (j.kind == 1)
+        tf32x3::split_a_kernel<true><<<grid, 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, j.ka, src_batch, dst_batch);
+    else
+        tf32x3::split_a_kernel<false><<<grid, 256, 0, stream>>>(A, lda, m, k, a_hi, a_lo, j.ka, src_batch,
+                                                                dst_batch);
+    return SGEMM_STATUS_OK;
+}
+
+int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *bt_lo, cudaStream_t stream,
+                   int batch = 1, long long src_batch = 0, long long dst_batch = 0) {
+    if (n == 0 || k == 0 || batch == 0) return SGEMM_STATUS_OK;
+    tf32x3::SplitJob j = split_b_job(k, n, B, ldb, bt_hi, bt_lo, batch, src_batch, dst_batch), none = j;
+    none.gx = none.gy = 0;
+    launch_split_pair(j, none, batch, stream);
     return SGEMM_STATUS_OK;
 }
 
@@ -571,19 +588,27 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
     }
     // both split operands are k-contiguous (K-major): an operand stored with
     // k contiguous is split in place order, one stored k-major is transposed
+    // one launch splits both operands (only B's pass when the GEMM splits A)
+    const tf32x3::SplitJob jb =
+        pl.op_b == SGEMM_OP_N ? split_b_job(k, n, B, ldb, b_hi, b_lo, bt.count, bt.sb, (long long)b_elems)
+                              : split_a_job(n, k, B, ldb, b_hi, b_lo, bt.count, bt.sb, (long long)b_elems);
     if (pl.a_in_kernel) {
         a_hi = const_cast<float *>(A);   // the GEMM reads A itself and splits it in shared memory
         a_lo = nullptr;
-    } else if (pl.a_lo_only) {
-        a_hi = const_cast<float *>(A);   // the GEMM reads A itself as its hi operand
-        launch_split_a(m, k, A, lda, nullptr, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
-    } else if (pl.op_a == SGEMM_OP_N) {
-        launch_split_a(m, k, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
+        if (pl.op_b == SGEMM_OP_N) launch_split_b(k, n, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
+        else launch_split_a(n, k, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
     } else {
-        launch_split_b(k, m, A, lda, a_hi, a_lo, stream, bt.count, bt.sa, (long long)a_elems);
+        tf32x3::SplitJob ja;
+        if (pl.a_lo_only) {
+            a_hi = const_cast<float *>(A);   // the GEMM reads A itself as its hi operand
+            ja = split_a_job(m, k, A, lda, nullptr, a_lo, bt.count, bt.sa, (long long)a_elems);
+        } else if (pl.op_a == SGEMM_OP_N) {
+            ja = split_a_job(m, k, A, lda, a_hi, a_lo, bt.count, bt.sa, (long long)a_elems);
+        } else {
+            ja = split_b_job(k, m, A, lda, a_hi, a_lo, bt.count, bt.sa, (long long)a_elems);
+        }
+        launch_split_pair(ja, jb, bt.count, stream);
     }
-    if (pl.op_b == SGEMM_OP_N) launch_split_b(k, n, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
-    else launch_split_a(n, k, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
     // the GEMM starts its set-up while the split kernels finish when it runs
     // in one wave (measured: 2048^3 +2.4 %, 1024^3 +7 %, 512^3 +14 %; a
     // many-wave GEMM gains nothing from it: 8192^3 -3 %)
@@ -839,13 +864,9 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
         // left in the array by an earlier call is ever used
         const size_t a_elems = (size_t)m * ka, b_elems = (size_t)n * ka;
         float *a_hi = ws, *a_lo = ws + a_elems, *b_hi = a_lo + a_elems, *b_lo = b_hi + b_elems;
-        if (pl.a_lo_only) {
-            launch_split_a(m, k, A, lda, nullptr, a_lo, stream);
-            a_hi = const_cast<float *>(A);
-        } else {
-            launch_split_a(m, k, A, lda, a_hi, a_lo, stream);
-        }
-        launch_split_b(k, n, B, ldb, b_hi, b_lo, stream);
+        const tf32x3::SplitJob ja = split_a_job(m, k, A, lda, pl.a_lo_only ? nullptr : a_hi, a_lo, 1, 0, 0);
+        if (pl.a_lo_only) a_hi = const_cast<float *>(A);
+        launch_split_pair(ja, split_b_job(k, n, B, ldb, b_hi, b_lo, 1, 0, 0), 1, stream);
         if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream, 1, 0, lda)))
             return st;
     }

@@ -232,22 +232,25 @@ __device__ __forceinline__ float lo_of_raw(float x) {
 // (read element by element: the bytes past k may lie outside A).
 // hi == nullptr: only lo, for a GEMM that reads A itself as its hi operand
 // (hi = A with its low 13 bits dropped, lo = tf32(A - hi); see lo_of_raw).
+// The work of block (bx, by) of a gx x gy grid, on problem bz of a strided
+// batch (split_a_kernel runs it on its own grid, split_pair_kernel on part
+// of a shared one).
 template <bool VEC>
-__global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ A, long long lda, int m, int k,
-                                                      float *__restrict__ hi, float *__restrict__ lo, int ka,
-                                                      long long src_batch, long long dst_batch) {
-    griddep_launch_dependents();   // the GEMM may start its set-up meanwhile
-    // problem blockIdx.z of a strided batch
-    A += blockIdx.z * src_batch;
-    if (hi != nullptr) hi += blockIdx.z * dst_batch;
-    lo += blockIdx.z * dst_batch;
+__device__ __forceinline__ void split_rows(const float *__restrict__ A, long long lda, int m, int k,
+                                           float *__restrict__ hi, float *__restrict__ lo, int ka,
+                                           long long src_batch, long long dst_batch, int bx, int by, int bz, int gx,
+                                           int gy) {
+    A += bz * src_batch;
+    if (hi != nullptr) hi += bz * dst_batch;
+    lo += bz * dst_batch;
     const int full4 = VEC ? k / 4 : 0;               // float4 chunks entirely inside the row
     const int scal0 = 4 * full4;                      // first element done one at a time
-    for (int row = blockIdx.y; row < m; row += gridDim.y) {
+    const int stride = gx * (int)blockDim.x;
+    for (int row = by; row < m; row += gy) {
         const float *src = A + (long long)row * lda;
         float *h = hi != nullptr ? hi + (long long)row * ka : nullptr;
         float *l = lo + (long long)row * ka;
-        for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < full4; c += gridDim.x * blockDim.x) {
+        for (int c = bx * (int)blockDim.x + (int)threadIdx.x; c < full4; c += stride) {
             const float4 x = __ldg(reinterpret_cast<const float4 *>(src) + c);
             if (hi == nullptr) {
                 reinterpret_cast<float4 *>(l)[c] =
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ 
             reinterpret_cast<float4 *>(h)[c] = xh;
             reinterpret_cast<float4 *>(l)[c] = xl;
         }
-        for (int t = scal0 + blockIdx.x * blockDim.x + threadIdx.x; t < k; t += gridDim.x * blockDim.x) {
+        for (int t = scal0 + bx * (int)blockDim.x + (int)threadIdx.x; t < k; t += stride) {
             if (hi == nullptr) {
                 l[t] = lo_of_raw(__ldg(src + t));
                 continue;
@@ -275,39 +278,81 @@ __global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ 
     }
 }
 
-// B (k x n, row pitch ldb) -> hi, lo of B^T (n x ka, row pitch ka), through
-// a 32 (k) x 64 (n) shared tile padded to 65 columns: reads of B and writes
-// of B^T are both 128-byte coalesced per warp, and the column reads of the
-// tile hit 32 different banks.
-__global__ void __launch_bounds__(256) split_bt_kernel(const float *__restrict__ B, long long ldb, int k, int n,
-                                                       float *__restrict__ hi, float *__restrict__ lo, int ka,
-                                                       long long src_batch, long long dst_batch) {
+template <bool VEC>
+__global__ void __launch_bounds__(256) split_a_kernel(const float *__restrict__ A, long long lda, int m, int k,
+                                                      float *__restrict__ hi, float *__restrict__ lo, int ka,
+                                                      long long src_batch, long long dst_batch) {
     griddep_launch_dependents();   // the GEMM may start its set-up meanwhile
-    B += blockIdx.z * src_batch;
-    hi += blockIdx.z * dst_batch;
-    lo += blockIdx.z * dst_batch;
+    split_rows<VEC>(A, lda, m, k, hi, lo, ka, src_batch, dst_batch, (int)blockIdx.x, (int)blockIdx.y,
+                    (int)blockIdx.z, (int)gridDim.x, (int)gridDim.y);
+}
+
+// One split pass of a GEMM call: a k-contiguous operand is split row by row
+// (split_rows; kind 1 with float4 loads when its rows are 16-byte aligned);
+// a k-major one (B, k x n, row pitch ld) becomes hi, lo of its transpose
+// (n x ka, row pitch ka) through a 32 (k) x 64 (n) shared tile padded to 65
+// columns: reads of B and writes of B^T are both 128-byte coalesced per
+// warp, and the column reads of the tile hit 32 different banks.  gx x gy
+// blocks per problem.
+struct SplitJob {
+    const float *src;
+    long long ld;
+    int rows, cols;   // rows x k (kinds 0, 1), or k x n (transpose)
+    float *hi, *lo;
+    int ka;
+    long long src_batch, dst_batch;
+    int gx, gy;
+    int kind;         // 0: split_rows, 1: split_rows with float4 loads, 2: transpose
+};
+
+// The split passes of a GEMM call in one launch (one launch gap fewer before
+// the GEMM when both operands are split): blocks [0, j0.gx * j0.gy) of each
+// batch slice run job j0, the rest job j1 (none when j1.gx = 0).  The branch
+// is uniform per block.  The transpose is written out here rather than in a
+// device function: that form measured ~19 % slower on GB300 (B of 8192 x
+// 8192: 209.6 against 176.8 us).
+__global__ void __launch_bounds__(256) split_pair_kernel(SplitJob j0, SplitJob j1) {
+    griddep_launch_dependents();   // the GEMM may start its set-up meanwhile
+    const int n0 = j0.gx * j0.gy;
+    const bool first = (int)blockIdx.x < n0;
+    const SplitJob j = first ? j0 : j1;
+    const int b = first ? (int)blockIdx.x : (int)blockIdx.x - n0;
+    const int bx = b % j.gx, by = b / j.gx, bz = (int)blockIdx.z;
+    if (j.kind != 2) {
+        if (j.kind == 1)
+            split_rows<true>(j.src, j.ld, j.rows, j.cols, j.hi, j.lo, j.ka, j.src_batch, j.dst_batch, bx, by, bz,
+                             j.gx, j.gy);
+        else
+            split_rows<false>(j.src, j.ld, j.rows, j.cols, j.hi, j.lo, j.ka, j.src_batch, j.dst_batch, bx, by, bz,
+                              j.gx, j.gy);
+        return;
+    }
     __shared__ float tile[32][65];
+    const float *B = j.src + bz * j.src_batch;
+    float *hi = j.hi + bz * j.dst_batch, *lo = j.lo + bz * j.dst_batch;
+    const int k = j.rows, n = j.cols, ka = j.ka;
+    const long long ldb = j.ld;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
-    for (int t0 = blockIdx.y * 32; t0 < k; t0 += gridDim.y * 32) {
-        for (int j0 = blockIdx.x * 64; j0 < n; j0 += gridDim.x * 64) {
+    for (int t0 = by * 32; t0 < k; t0 += j.gy * 32) {
+        for (int j0_ = bx * 64; j0_ < n; j0_ += j.gx * 64) {
 #pragma unroll
             for (int r = ty; r < 32; r += 8) {
                 const int t = t0 + r;
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const int j = j0 + 32 * q + tx;
-                    tile[r][32 * q + tx] = (t < k && j < n) ? __ldg(B + (long long)t * ldb + j) : 0.f;
+                    const int jj = j0_ + 32 * q + tx;
+                    tile[r][32 * q + tx] = (t < k && jj < n) ? __ldg(B + (long long)t * ldb + jj) : 0.f;
                 }
             }
             __syncthreads();
 #pragma unroll
             for (int r = ty; r < 64; r += 8) {
-                const int j = j0 + r, t = t0 + tx;
-                if (j < n && t < k) {
+                const int jj = j0_ + r, t = t0 + tx;
+                if (jj < n && t < k) {
                     float xh, xl;
                     split_one(tile[tx][r], xh, xl);
-                    hi[(long long)j * ka + t] = xh;
-                    lo[(long long)j * ka + t] = xl;
+                    hi[(long long)jj * ka + t] = xh;
+                    lo[(long long)jj * ka + t] = xl;
                 }
             }
             __syncthreads();
