@@ -211,12 +211,17 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
     if (num_sms <= 0) num_sms = 1;
     pl->op_a = op_a;
     pl->op_b = op_b;
-    // AUTO: the tensor-core path for every problem with enough work to fill
-    // the GPU (it is ~5x the FFMA rate at 2048^3 and beyond) and for long k
-    // (its chunked accumulation holds the bound where a plain sequential
-    // FP32 sum over k drifts); the FFMA path for small problems.
+    // AUTO: the tensor-core path from 2^20 multiply-adds with k >= 64 (it is
+    // ~5x the FFMA rate at 2048^3 and beyond, and its two launches already
+    // beat the FFMA kernel's 128 x 128 tiles at 128^3: 16 against 19 us,
+    // whole call, L2 flushed) and for long k (its chunked accumulation holds
+    // the bound where a plain sequential FP32 sum over k drifts); the FFMA
+    // path for tiny problems (64^3: 13 against 14 us) and for k < 64, where
+    // the split passes cost more than they save (4096 x 4096 x 32: 35.5
+    // against 40.6 us).
+    const long long mnk = (long long)m * n * k;
     const bool use_tc = path == SGEMM_PATH_TF32X3 ||
-                        (path == SGEMM_PATH_AUTO && ((long long)m * n * k >= (1LL << 27) || k > 8192));
+                        (path == SGEMM_PATH_AUTO && ((mnk >= (1LL << 20) && k >= 64) || k > 8192));
     pl->path = use_tc ? SGEMM_PATH_TF32X3 : SGEMM_PATH_FFMA;
     pl->split_k = 1;
     pl->c_vec = aligned(C, 16) && (ldc % 4) == 0;

@@ -82,7 +82,7 @@ extern "C" {
 
 /* Kernel families sgemm_ex() can be asked for. */
 #define SGEMM_PATH_AUTO 0   /* the library's choice (what sgemm() runs): TF32X3 when
-                               m*n*k >= 2^27 or k > 8192, else FFMA              */
+                               m*n*k >= 2^20 and k >= 64, or k > 8192; else FFMA */
 #define SGEMM_PATH_FFMA 1   /* CUDA-core FP32 FFMA, exact FP32 products        */
 #define SGEMM_PATH_TF32X3 2 /* tcgen05 tensor cores, 3xTF32 split precision    */
 

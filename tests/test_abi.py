@@ -147,9 +147,15 @@ def test_split_api_arguments(fn, over, status):
 
 
 def test_auto_policy():
-    """AUTO takes the tensor-core path from 2^27 multiply-adds or k > 8192,
-    the FFMA path below."""
-    assert binding.plan(256, 256, 256)[1]["path"] == binding.PATH_FFMA
+    """AUTO takes the tensor-core path from 2^20 multiply-adds with k >= 64,
+    or for k > 8192; the FFMA path for smaller problems and shorter k."""
+    assert binding.plan(64, 64, 64)[1]["path"] == binding.PATH_FFMA
+    assert binding.plan(100, 100, 100)[1]["path"] == binding.PATH_FFMA       # 10^6 < 2^20
+    assert binding.plan(128, 128, 64)[1]["path"] == binding.PATH_TF32X3      # 2^20
+    assert binding.plan(256, 256, 256)[1]["path"] == binding.PATH_TF32X3
+    assert binding.plan(4096, 4096, 32)[1]["path"] == binding.PATH_FFMA     # k < 64
+    assert binding.plan(4096, 4096, 63)[1]["path"] == binding.PATH_FFMA
+    assert binding.plan(4096, 4096, 64)[1]["path"] == binding.PATH_TF32X3
     assert binding.plan(512, 512, 512)[1]["path"] == binding.PATH_TF32X3
     assert binding.plan(8192, 8192, 8192)[1]["path"] == binding.PATH_TF32X3
     assert binding.plan(16, 16, 8193)[1]["path"] == binding.PATH_TF32X3
