@@ -94,7 +94,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 # Exported symbols, in the order the header declares them.
 EXPORTS = ["sgemm", "sgemm_ex", "sgemm_op", "sgemm_strided_batched", "sgemm_tf32x3_split_a", "sgemm_tf32x3_split_b", "sgemm_tf32x3_split_gemm",
            "sgemm_tf32x3_noalloc", "reduce_sum_f32", "sgemm_status_string", "sgemm_last_cuda_error", "sgemm_plan_for", "sgemm_device_status",
-           "sgemm_version"]
+           "sgemm_selftest_wait", "sgemm_version"]
 
 
 class Plan(ctypes.Structure):
@@ -134,6 +134,8 @@ def _declare(lib):
     lib.sgemm_plan_for.restype = i
     lib.sgemm_device_status.argtypes = [ctypes.POINTER(i), i]
     lib.sgemm_device_status.restype = i
+    lib.sgemm_selftest_wait.argtypes = [ctypes.c_ulonglong, ctypes.POINTER(i)]
+    lib.sgemm_selftest_wait.restype = i
     lib.sgemm_version.argtypes = []
     lib.sgemm_version.restype = ctypes.c_char_p
     return lib

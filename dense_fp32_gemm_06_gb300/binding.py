@@ -261,3 +261,31 @@ def reduce_tree_depth(n: int, num_sms: int = 152, vec: bool = True) -> int:
     # 4-byte loads (misaligned x) all go to one; +1 for the tail
     per_acc = -(-n // (blocks * threads * (4 if vec else 1))) + 1
     return per_acc + 2 + 5 + 5 + blocks
+
+
+def last_cuda_error() -> int:
+    """The CUDA error code behind the calling thread's last status 100."""
+    return int(_native.load().sgemm_last_cuda_error())
+
+
+def device_status(clear: bool = False) -> int:
+    """The device-side status word of the tensor-core path (0: no bounded
+    wait has run out); synchronises the device; resets it when `clear`."""
+    flag = ctypes.c_int(0)
+    _check(_native.load().sgemm_device_status(ctypes.byref(flag), int(bool(clear))))
+    return flag.value
+
+
+def selftest_wait_raw(limit_ns: int, gave_up=None) -> int:
+    """sgemm_selftest_wait: one bounded wait on a barrier nothing signals;
+    returns the status (`gave_up`, a ctypes.c_int, receives the outcome)."""
+    return _native.load().sgemm_selftest_wait(ctypes.c_ulonglong(int(limit_ns)),
+                                              ctypes.byref(gave_up) if gave_up is not None else None)
+
+
+def selftest_wait(limit_ns: int = 1_000_000) -> bool:
+    """Runs the bounded-wait self-test; True when the wait ran out (it
+    should: nothing signals its barrier)."""
+    flag = ctypes.c_int(0)
+    _check(selftest_wait_raw(limit_ns, flag))
+    return flag.value == 1

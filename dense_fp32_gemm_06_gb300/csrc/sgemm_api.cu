@@ -580,9 +580,15 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
     const size_t sk_ws_floats =
         pl.stream_k > 0 ? (size_t)pl.stream_k * 2 * tf32x3::BM * (pl.trans ? tf32x3::Wide::BN : pl.bn) : 0;
     float *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(
-        reinterpret_cast<void **>(&ws),
-        (cnt * (a_hi_elems + a_lo_elems + 2 * b_elems) + sk_cnt_floats + sk_ws_floats) * sizeof(float), pool, stream);
+    // SGEMM_GB300_FAIL_ALLOC (fault injection for tests): the allocation
+    // reports out-of-memory without being attempted
+    cudaError_t e = std::getenv("SGEMM_GB300_FAIL_ALLOC") != nullptr
+                        ? cudaErrorMemoryAllocation
+                        : cudaMallocFromPoolAsync(
+                              reinterpret_cast<void **>(&ws),
+                              (cnt * (a_hi_elems + a_lo_elems + 2 * b_elems) + sk_cnt_floats + sk_ws_floats) *
+                                  sizeof(float),
+                              pool, stream);
     if (e != cudaSuccess) return fail_cuda(e);
     float *a_hi = ws, *a_lo = ws + cnt * a_hi_elems, *b_hi = a_lo + cnt * a_lo_elems, *b_lo = b_hi + cnt * b_elems;
     int *sk_cnt = pl.stream_k > 0 ? reinterpret_cast<int *>(b_lo + cnt * b_elems) : nullptr;
@@ -674,6 +680,22 @@ void launch_ffma(const sgemm_plan &pl, const GemmArgs &a, int batch, cudaStream_
     if (akind == 0) launch_ffma_b<ALoadScatter>(bkind, a, grid, s);
     else if (akind == 1) launch_ffma_b<ALoadVec>(bkind, a, grid, s);
     else launch_ffma_b<ALoadScalar>(bkind, a, grid, s);
+}
+
+// Status code of the bounded-wait self-test (sgemm_selftest_wait).
+constexpr int kStatusSelfTest = 0x207;
+
+// One bounded wait on an mbarrier that nothing arrives at: it runs out after
+// limit_ns, records kStatusSelfTest in the status word (through the same
+// mbar_wait every pipeline wait of the GEMM uses) and returns; *gave_up
+// tells the host that it did.  Exercises the failure-reporting path without
+// a real stall.
+__global__ void selftest_wait_kernel(unsigned long long limit_ns, int *gave_up) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    *gave_up = mbar_wait(smem_u32(&bar), 0, kStatusSelfTest, limit_ns) ? 0 : 1;
 }
 
 }  // namespace
@@ -951,6 +973,22 @@ int sgemm_device_status(int *flag, int clear) {
         const int zero = 0;
         if ((e = cudaMemcpyToSymbol(g_sgemm_status, &zero, sizeof(int))) != cudaSuccess) return fail_cuda(e);
     }
+    return SGEMM_STATUS_OK;
+}
+
+int sgemm_selftest_wait(unsigned long long limit_ns, int *gave_up) {
+    if (limit_ns == 0 || limit_ns > 10000000000ull) return 1;
+    if (gave_up == nullptr) return 2;
+    int *d = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&d), sizeof(int));
+    if (e != cudaSuccess) return fail_cuda(e);
+    selftest_wait_kernel<<<1, 32>>>(limit_ns, d);
+    if ((e = cudaGetLastError()) == cudaSuccess) e = cudaDeviceSynchronize();
+    int v = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&v, d, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    if (e != cudaSuccess) return fail_cuda(e);
+    *gave_up = v;
     return SGEMM_STATUS_OK;
 }
 

@@ -277,9 +277,25 @@ int sgemm_plan_for(int m, int n, int k, float alpha,
  * accumulator warps for a finished chunk, 0x204 a wait while draining after
  * an earlier timeout, 0x205 the MMA issuer for a free TMEM buffer, 0x206 the
  * splitter warps for a loaded slab.  Each means the result of that call is
- * not valid.
+ * not valid.  0x207 is recorded only by sgemm_selftest_wait.
  */
 int sgemm_device_status(int *flag, int clear);
+
+/*
+ * Diagnostic for the failure-reporting path: runs one bounded wait on a
+ * shared-memory barrier that nothing signals, through the same bounded-wait
+ * routine as the GEMM's pipeline waits.  It gives up after `limit_ns`
+ * nanoseconds (1 .. 10^10), records 0x207 in the device status word (unless
+ * an earlier code is kept there) and returns; the context stays usable.
+ * Synchronises the device; *gave_up (host pointer) = 1 when the wait ran
+ * out.  Status 1: limit_ns out of range; 2: gave_up is NULL; 100: CUDA error.
+ *
+ * Fault injection for tests: with the environment variable
+ * SGEMM_GB300_FAIL_ALLOC set, the tensor-core path's scratch allocation
+ * reports cudaErrorMemoryAllocation without being attempted, so the call
+ * returns 100 before launching anything (C is not written).
+ */
+int sgemm_selftest_wait(unsigned long long limit_ns, int *gave_up);
 
 /* Library version string, e.g. "sgemm_gb300 0.1 (sm_103a)". */
 const char *sgemm_version(void);

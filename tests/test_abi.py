@@ -303,3 +303,13 @@ def test_tune_plan_text_names_the_plan():
     assert ("stream-K" in text) == bool(thin["stream_k"])
     st, square = binding.plan(2048, 2048, 2048, lda=2048, path=binding.PATH_TF32X3, num_sms=152)
     assert st == 0 and "transposed" not in tune.plan_text(square)
+
+
+def test_selftest_wait_argument_checks():
+    """The bounded-wait self-test rejects its arguments before any CUDA call."""
+    import ctypes
+    flag = ctypes.c_int(-1)
+    assert binding.selftest_wait_raw(0, flag) == 1                  # no limit
+    assert binding.selftest_wait_raw(10_000_000_001, flag) == 1     # over 10 s
+    assert binding.selftest_wait_raw(1_000_000, None) == 2          # no result pointer
+    assert flag.value == -1
