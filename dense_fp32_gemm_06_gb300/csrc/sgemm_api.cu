@@ -246,10 +246,12 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         // 256-wide slab ~0.5 us, a 128-wide one ~0.375 us (1.5x the time per
         // FLOP), a transposed 256 x 128 one ~0.66 us (split-K cases: its
         // 16 KB of A to split and its column-wise stores); a split adds
-        // ~5 us + 0.9 us per CTA of the cluster.  Units below: 1/32 us.
+        // ~2 us + 0.5 us per CTA of the cluster (fitted to whole calls and
+        // split-K sweeps: 256 x 256 x 8192 over S = 1..8, 384^3, 500 x 500
+        // x 300).  Units below: 1/32 us.
         // Waves count CTAs against the SMs (S = 1) or
         // clusters against the clusters that fit at once (S > 1); a split
-        // must fit in one wave and leave each CTA >= 8 slabs (128 k).
+        // must fit in one wave and leave each CTA >= 4 slabs (64 k).
         const int tiles_m = (m + pl->bm - 1) / pl->bm;
         const long long KT = (k + tf32x3::BK - 1) / tf32x3::BK;
         // tuning overrides for benchmarks and tests: SGEMM_GB300_TILE_N (128
@@ -306,7 +308,7 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
             for (int S = 1; S <= 8; ++S) {
                 if (force_s >= 1 && force_s <= 8) {
                     if (S != force_s) continue;
-                } else if (S > 1 && KT / S < 8) {
+                } else if (S > 1 && KT / S < 4) {
                     break;
                 }
                 long long slots = num_sms;   // CTAs (S = 1) or clusters (S > 1) resident at once
@@ -316,7 +318,7 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
                     if (slots <= 0 || (tiles > slots && !(force_s >= 1 && force_s <= 8))) continue;
                 }
                 const long long waves = (tiles + slots - 1) / slots;
-                const long long cost = waves * ((KT + S - 1) / S) * slab + (S > 1 ? 160 + 28 * S : 0);
+                const long long cost = waves * ((KT + S - 1) / S) * slab + (S > 1 ? 64 + 16 * S : 0);
                 consider(cost, bn, S, tr, false);
             }
             // stream-K: W = tiles / G full waves of whole tiles, then the R
