@@ -516,7 +516,7 @@ def run_ours(args, rank, world):
                            + " timed alone (device time of 20 back-to-back launches, CUDA events)")
             del a_hi, a_lo
         else:
-            # the step is split_a + split_bt + the tcgen05 GEMM; the GEMM
+            # the step is the split launch + the tcgen05 GEMM; the GEMM
             # kernel alone is timed on operands split once, through the
             # split-GEMM call
             a_hi = torch.empty(p.m * ka, device="cuda")
