@@ -313,3 +313,17 @@ def test_selftest_wait_argument_checks():
     assert binding.selftest_wait_raw(10_000_000_001, flag) == 1     # over 10 s
     assert binding.selftest_wait_raw(1_000_000, None) == 2          # no result pointer
     assert flag.value == -1
+
+
+def test_split_k_policy_small_and_large_shapes():
+    """Host plan (152 SMs, no device): small problems with few tiles split k
+    over clusters (a split costs ~2 us + 0.5 us per CTA and leaves each CTA
+    >= 4 slabs); problems that fill the GPU with whole tiles do not."""
+    TC = binding.PATH_TF32X3
+    expect = {(256, 256, 256): 4, (384, 384, 384): 4, (500, 500, 300): 4, (256, 256, 8192): 8,
+              (128, 128, 128): 1, (2048, 2048, 2048): 1, (8192, 8192, 8192): 1}
+    for (m, n, k), s in expect.items():
+        st, p = binding.plan(m, n, k, lda=k, path=TC, num_sms=152)
+        assert st == 0 and p["split_k"] == s and p["stream_k"] == 0, ((m, n, k), p)
+        assert p["grid"] == p["tiles"] * s
+        assert p["k_tiles"] // p["split_k"] >= 4 or s == 1
