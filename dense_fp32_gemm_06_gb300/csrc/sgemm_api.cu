@@ -544,10 +544,10 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
-    // right after this call's split kernels (after_split): launch as their
-    // dependent, so the GEMM's set-up overlaps their tail (its producer
-    // waits for them before reading the split operands; nothing else it
-    // reads is written by them).  SGEMM_GB300_PDL=0 turns it off.
+    // right after this call's split launch (after_split): launch as its
+    // dependent, so the GEMM's set-up overlaps its tail (the producer waits
+    // for it before reading the split operands; nothing else the GEMM reads
+    // is written by it).  SGEMM_GB300_PDL=0 turns it off.
     if (after_split) {
         const char *env = std::getenv("SGEMM_GB300_PDL");
         if (!(env && env[0] == '0')) {
@@ -622,7 +622,7 @@ int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, con
         }
         launch_split_pair(ja, jb, bt.count, stream);
     }
-    // the GEMM starts its set-up while the split kernels finish when it runs
+    // the GEMM starts its set-up while the split launch finishes when it runs
     // in one wave (measured: 2048^3 +2.4 %, 1024^3 +7 %, 512^3 +14 %; a
     // many-wave GEMM gains nothing from it: 8192^3 -3 %)
     const bool pdl = (long long)pl.grid * bt.count <= num_sms;

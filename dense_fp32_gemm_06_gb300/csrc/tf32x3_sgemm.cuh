@@ -12,8 +12,9 @@
 // reads A's hi part straight from A (the MMA drops the low 13 bits: hi =
 // trunc(x), |lo| < 2^-10 |x|), the bound per product is ~2^-20 |a||b|.
 //
-// Two steps per call:
-//  1. split kernels (HBM-bound): A (any lda, any 4-byte alignment) becomes
+// Two launches per call:
+//  1. the split pass (split_pair_kernel, HBM-bound, both operands in one
+//     grid): A (any lda, any 4-byte alignment) becomes
 //     A_hi, A_lo, m x ka row-major (ka = k rounded up to 4, 16-byte rows);
 //     B becomes B^T_hi, B^T_lo, n x ka, transposed through a 32 x 64 shared
 //     tile padded to 65 columns (coalesced reads and writes).  Both operands
@@ -42,7 +43,9 @@
 //       with tcgen05.ld and add it into FP32 registers with round-to-nearest
 //       adds, then release the TMEM buffer.  After the last chunk they write
 //       alpha*acc + beta*C for rows < m, columns < n (C not read when
-//       beta == 0).
+//       beta == 0), 32 columns of each warp's 32 rows at a time through the
+//       warp's 4 KB staging buffer in shared memory, so that every store
+//       covers 4 rows x 128 contiguous bytes.
 //     Split-K for problems with too few tiles to fill the GPU: the grid is
 //     launched in clusters of S CTAs (S <= 8) that share one tile, CTA r
 //     taking k slabs [r*KT/S, (r+1)*KT/S).  Each parks its FP32 partial
@@ -61,8 +64,8 @@
 //     waves and share the last wave's tiles out by slabs, a shared tile
 //     being finished by the last of its CTAs from partials in a workspace.
 //     A GEMM that runs in one wave is launched as a programmatic dependent
-//     of the split kernels: it sets up while they finish, and its producer
-//     waits for them before the first load.
+//     of the split launch: it sets up while the split finishes, and its
+//     producer waits for it before the first load.
 //     TMA zero-fills rows past m, columns past n and k past the end, so the
 //     MMA never sees an index test.  Every mbarrier wait is bounded (2 s):
 //     a wait that runs out records a code in the library status word,
@@ -461,9 +464,9 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            // launched as the dependent of the split kernels, the CTA set
-            // itself up while they ran; the operands they write are read
-            // only after they have completed
+            // launched as the dependent of the split launch, the CTA set
+            // itself up while it ran; the operands it writes are read only
+            // after it has completed
             griddep_wait();
             int tile, k0, nk, g = 0;   // g: slabs issued so far (ring position)
             bool stop = false;
