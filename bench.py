@@ -63,6 +63,8 @@ def parse(argv=None):
                     help="target CPU time of the oracle sample")
     ap.add_argument("--shape", default=None,
                     help="m,n,k of a smaller stand-in of the 8192^3 workload (profiling captures)")
+    ap.add_argument("--reduce", type=int, default=0, metavar="N",
+                    help="time reduce_sum_f32 on N floats instead of the GEMM (its own JSON line)")
     return ap.parse_args(argv)
 
 
@@ -98,8 +100,72 @@ def load_problem(args):
 
 # ----------------------------------------------------------------------------- clocks
 
-class ClockSampler:
-    """nvidia-smi sampled every 100 ms in the background."""
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (the
+    driver's libnvidia-ml, by ctypes) every `period_s` seconds on a
+    background thread, so that even a timed region of a few tens of
+    milliseconds gets many samples.  Reads only; changes no setting."""
+
+    # nvmlClocksEventReasons bits
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+
+    def __init__(self, device_index, period_s=0.005):
+        import ctypes
+        import threading
+        self.ok = False
+        self.rows = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint(0)
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))   # NVML_CLOCK_SM
+            get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:
+            return
+        self.nv, self.h, self.max_mhz = nv, h, float(mx.value)
+        self.ok = True
+        self.stop_flag = threading.Event()
+
+        def loop():
+            clk, pw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+            while not self.stop_flag.is_set():
+                t = time.time()
+                if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                    nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+                    get_reasons(h, ctypes.byref(rs))
+                    self.rows.append((t, float(clk.value), pw.value / 1000.0, int(rs.value)))
+                time.sleep(period_s)
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        if self.ok:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        inside = [r for r in self.rows if t0 <= r[0] <= t1]
+        if not inside:
+            return None
+        reasons = sorted({name for r in inside for bit, name in self.REASONS.items() if r[3] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(r[1] for r in inside), "reasons": reasons, "samples": len(inside),
+                "power_w_median": statistics.median(r[2] for r in inside),
+                "source": "NVML every 5 ms during the timed region"}
+
+
+class SmiClockSampler:
+    """nvidia-smi sampled every 100 ms in the background (used when NVML
+    cannot be opened directly)."""
 
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -159,7 +225,31 @@ class ClockSampler:
                 "sm_max_mhz": max(r[2] for r in inside),
                 "reasons": reasons,
                 "samples": len(inside),
-                "power_w_median": statistics.median(power) if power else None}
+                "power_w_median": statistics.median(power) if power else None,
+                "source": "nvidia-smi every 100 ms"}
+
+
+class ClockSampler:
+    """Clocks during a timed region: NVML every 5 ms, falling back to
+    nvidia-smi every 100 ms when NVML cannot be opened."""
+
+    def __init__(self, device_index):
+        self.nvml = NvmlClockSampler(device_index)
+        self.smi = None if self.nvml.ok else SmiClockSampler(device_index)
+
+    def stop(self):
+        self.nvml.stop()
+        if self.smi is not None:
+            self.smi.stop()
+
+    def summary(self, t0, t1):
+        if self.smi is None:
+            got = self.nvml.summary(t0, t1)
+            if got is not None:
+                return got
+            return {"sm_mhz": None, "sm_max_mhz": self.nvml.max_mhz, "reasons": [], "samples": 0,
+                    "note": "no NVML sample inside the timed region"}
+        return self.smi.summary(t0, t1)
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -226,6 +316,50 @@ def oracle_sample(p, seconds):
     oracle.problem_f64(p, rows=(0, rows))
     dt = time.perf_counter() - t
     return 2.0 * rows * p.n * p.k / dt / 1e12, rows, dt, threads
+
+
+def oracle_full_small():
+    """The whole FP64 oracle (every output) on the three configurations it
+    finishes in about a second, on all host cores: the CPU baseline of those
+    workloads, timed once each."""
+    import oracle
+    from dense_fp32_gemm_06_gb300 import inputs
+    oracle.build()
+    out = []
+    for name in ("256^3", "2048^3", "1000x1500x777"):
+        q = inputs.workload(name)
+        oracle.problem_f64(q, rows=(0, min(q.m, 8)))   # warm (threads, pages)
+        t = time.perf_counter()
+        oracle.problem_f64(q)
+        dt = time.perf_counter() - t
+        out.append({"workload": WORKLOAD_TEXT[name], "seconds": dt, "value": flops(q) / dt / 1e12,
+                    "unit": "TFLOPS", "cores": oracle.max_threads(), "kind": "oracle",
+                    "sample": "every output (full run)"})
+    return out
+
+
+def cublas_side_reference(p, A, B, C, stream, flush, sms):
+    """cuBLAS FP32 SGEMM (torch.matmul, TF32 off, so FP32 FFMA) on the same
+    operands and stream, CUDA events per launch: context for the library's
+    numbers, not a path the library takes."""
+    import torch
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        Av = A[:, :p.k]
+        Bv = B[:, :p.n]
+        out = torch.empty(p.m, p.n, device="cuda")
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                torch.matmul(Av, Bv, out=out)
+            count = max(10, int(1.0 / max(1e-6, flops(p) / 60e12)))
+            ms = time_launches(lambda: torch.matmul(Av, Bv, out=out), stream, count, flush=flush)
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    med = statistics.median(ms)
+    return {"value": tflops(p, med), "unit": "TFLOPS", "median_ms": med, "launches": len(ms),
+            "what": "cuBLAS FP32 SGEMM via torch.matmul (allow_tf32 = False), same operands and stream; "
+                    "side reference only, not on the library's path"}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -620,6 +754,12 @@ def run_ours(args, rank, world):
         ffma = {"value": tflops(p, f_ms), "unit": "TFLOPS", "ms": f_ms, "launches": len(fm),
                 "frac_of_ffma_peak": tflops(p, f_ms) / fpeak, "ffma_peak_tflops": fpeak, "clocks": fclk}
 
+    # ---- side reference: cuBLAS FP32 SGEMM (torch.matmul with TF32 off) on
+    # the same operands; never on the library's path, reported for context
+    cublas = None
+    if not args.no_secondary and not args.shape:
+        cublas = cublas_side_reference(p, A, B, C, stream, flush, sms)
+
     # ---- CPU baseline: the oracle on a bounded slab of the same workload
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -627,6 +767,11 @@ def run_ours(args, rank, world):
         cpu = {"value": tf, "unit": "TFLOPS", "cores": threads, "kind": "oracle",
                "sample": f"output rows 0..{nrows - 1} of the workload ({nrows} x {p.n} outputs, "
                          f"k = {p.k}, FP64), {secs:.1f} s"}
+
+    # ---- CPU baseline on the small configurations: the whole oracle, timed
+    cpu_configs = None
+    if rank == 0 and not args.no_cpu_baseline and not args.shape:
+        cpu_configs = oracle_full_small()
 
     if rank == 0:
         path_name = {binding.PATH_FFMA: "ffma", binding.PATH_TF32X3: "tf32x3"}.get(plan["path"], "?")
@@ -648,9 +793,61 @@ def run_ours(args, rank, world):
             "e2e": e2e,
             "gpu_launches": args.steps * launches_per_step,
             "cpu_baseline": cpu,
+            "cpu_baseline_full": cpu_configs,
             "secondary": secondary,
             "ffma_path": ffma,
+            "cublas_side_reference": cublas,
         }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reduce(args, rank, world):
+    """reduce_sum_f32 on N uniform[-1, 1) floats resident in HBM: CUDA events
+    over `steps` launches on the launching stream after `warmup`; HBM-bound
+    (4N bytes read per call), against the measured copy bandwidth."""
+    import torch
+    from dense_fp32_gemm_06_gb300 import binding
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    n = args.reduce
+    stream = torch.cuda.current_stream()
+    x = torch.empty(n, device="cuda").uniform_(-1, 1)
+    out = torch.empty(1, device="cuda")
+
+    def step():
+        st = binding.reduce_sum_raw(x.data_ptr(), n, out.data_ptr(), stream.cuda_stream)
+        if st:
+            raise SystemExit(f"reduce failed: {binding.status_string(st)}")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dev)
+    time.sleep(0.1)
+    t0 = time.time()
+    ms = time_launches(step, stream, args.steps)
+    t1 = time.time()
+    time.sleep(0.05)
+    sampler.stop()
+    mean = sum(ms) / len(ms)
+    s64 = x.double().sum().item()
+    gbs = 4.0 * n / (mean * 1e-3) / 1e9
+    world_gbs = gbs * world
+    mp = measured_peaks()
+    peak = (mp or {}).get("hbm_gbs", 6800.0)
+    line = {"metric": "reduce_sum_f32 GB/s (HBM read of x)", "value": world_gbs, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean, "median_ms": statistics.median(ms),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (torch uniform[-1,1))",
+            "config": {"workload": f"reduce_sum_f32 of {n} floats ({4 * n / 2**20:.0f} MiB, larger than L2)",
+                       "relative_difference_to_fp64_sum": abs(out.item() - s64) / max(1e-30, x.abs().double().sum().item())},
+            "roofline": {"bound": "hbm", "kernel": "reduce_sum_kernel", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_basis": ("measured copy bandwidth (MEASURED_PEAKS.json), of measured"
+                                                             if mp else "fallback 6800 GB/s, of fallback"),
+                         "traffic": None},
+            "clocks": sampler.summary(t0, t1), "gpu_launches": args.steps}
+    if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
 
@@ -661,6 +858,8 @@ def main(argv=None):
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.reduce:
+        return run_reduce(args, rank, world)
     if world > 1:
         import torch
         import torch.distributed as dist

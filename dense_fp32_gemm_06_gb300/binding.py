@@ -40,10 +40,11 @@ def sgemm_raw(m, n, k, alpha, A_ptr, lda, B_ptr, ldb, beta, C_ptr, ldc, stream=0
 
 
 def plan(m, n, k, alpha=1.0, A_ptr=16, lda=None, B_ptr=16, ldb=None, beta=0.0, C_ptr=16, ldc=None,
-         path=PATH_AUTO, num_sms=152):
+         path=PATH_AUTO, num_sms=0):
     """The launch plan the library would use; returns (status, dict).
-    num_sms > 0: host only (no GPU needed) for a device with that many SMs;
-    num_sms=0: the plan a call on the current device would use."""
+    num_sms=0 (default): the plan a call on the current device would use (its
+    SM count and measured cluster capacity); num_sms > 0: host only (no GPU
+    needed) for a device with that many SMs."""
     lib = _native.load()
     lda = max(1, k) if lda is None else lda
     ldb = max(1, n) if ldb is None else ldb
@@ -226,10 +227,6 @@ def bmm(A, B, C, alpha=1.0, beta=0.0, *, path=PATH_AUTO, stream=None):
     return C
 
 
-REDUCE_THREADS = 512          # threads per block of the reduction kernel
-REDUCE_BLOCKS_PER_SM = 4
-
-
 def reduce_sum_raw(x_ptr, n, out_ptr, stream=0) -> int:
     """*out = sum of the n floats at x (device pointers); returns the status."""
     return _native.load().reduce_sum_f32(ctypes.c_void_p(x_ptr or None), int(n), ctypes.c_void_p(out_ptr or None),
@@ -248,19 +245,6 @@ def reduce_sum(x, out=None, *, stream=None):
     with torch.cuda.device(x.device):
         _check(reduce_sum_raw(x.data_ptr(), x.numel(), out.data_ptr(), stream))
     return out
-
-
-def reduce_tree_depth(n: int, num_sms: int = 152, vec: bool = True) -> int:
-    """Depth of the summation tree the reduction kernel uses for n values:
-    the longest chain of additions any partial sum goes through (per-thread
-    sequential sums, the 4-accumulator and shuffle combines, the per-block
-    combine, and the block commits to *out), for the bound gamma_h sum|x|."""
-    threads = REDUCE_THREADS
-    blocks = max(1, min(-(-n // (16 * threads)), num_sms * REDUCE_BLOCKS_PER_SM)) if n else 1
-    # one accumulator's sequential adds: 16-byte loads feed 4 accumulators,
-    # 4-byte loads (misaligned x) all go to one; +1 for the tail
-    per_acc = -(-n // (blocks * threads * (4 if vec else 1))) + 1
-    return per_acc + 2 + 5 + 5 + blocks
 
 
 def last_cuda_error() -> int:

@@ -14,12 +14,16 @@
 #pragma once
 #include <cstdint>
 
+#include "../../include/sgemm_gb300.h"
+
 namespace sgemm_gb300 {
 namespace reduce {
 
-constexpr int THREADS = 512;
+// the launch shape the header states (its error bound depends on it)
+constexpr int THREADS = SGEMM_REDUCE_THREADS;
 constexpr int WARPS = THREADS / 32;
-constexpr int BLOCKS_PER_SM = 4;
+constexpr int BLOCKS_PER_SM = SGEMM_REDUCE_BLOCKS_PER_SM;
+static_assert(WARPS <= 32, "one warp combines the block's warp sums");
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -943,19 +943,33 @@ int reduce_sum_f32(const float *x, long long n, float *out, cudaStream_t stream)
 }
 
 const char *sgemm_status_string(int status) {
+    // Argument errors name the 1-based position in the call that returned
+    // them; the entry points number their arguments differently (the header
+    // lists each one's positions), so the text names only the position.
+    static const char *const kArg[18] = {
+        "success",
+        "invalid argument 1 (1-based position in the call's argument list)",
+        "invalid argument 2 (1-based position in the call's argument list)",
+        "invalid argument 3 (1-based position in the call's argument list)",
+        "invalid argument 4 (1-based position in the call's argument list)",
+        "invalid argument 5 (1-based position in the call's argument list)",
+        "invalid argument 6 (1-based position in the call's argument list)",
+        "invalid argument 7 (1-based position in the call's argument list)",
+        "invalid argument 8 (1-based position in the call's argument list)",
+        "invalid argument 9 (1-based position in the call's argument list)",
+        "invalid argument 10 (1-based position in the call's argument list)",
+        "invalid argument 11 (1-based position in the call's argument list)",
+        "invalid argument 12 (1-based position in the call's argument list)",
+        "invalid argument 13 (1-based position in the call's argument list)",
+        "invalid argument 14 (1-based position in the call's argument list)",
+        "invalid argument 15 (1-based position in the call's argument list)",
+        "invalid argument 16 (1-based position in the call's argument list)",
+        "invalid argument 17 (1-based position in the call's argument list)",
+    };
+    if (status >= 0 && status <= 17) return kArg[status];
     switch (status) {
-        case SGEMM_STATUS_OK: return "success";
-        case 1: return "invalid argument 1: m < 0";
-        case 2: return "invalid argument 2: n < 0";
-        case 3: return "invalid argument 3: k < 0";
-        case 5: return "invalid argument 5: A is NULL or not 4-byte aligned";
-        case 6: return "invalid argument 6: lda < max(1, k)";
-        case 7: return "invalid argument 7: B is NULL or not 4-byte aligned";
-        case 8: return "invalid argument 8: ldb < max(1, n)";
-        case 10: return "invalid argument 10: C is NULL or not 4-byte aligned";
-        case 11: return "invalid argument 11: ldc < max(1, n)";
         case SGEMM_STATUS_TOO_LARGE:
-            return "problem too large for the fixed no-allocation scratch (2*(m+n)*ka > SGEMM_NOALLOC_SCRATCH_FLOATS)";
+            return "problem too large for the fixed no-allocation scratch (SGEMM_NOALLOC_SCRATCH_FLOATS)";
         case SGEMM_STATUS_BAD_PATH: return "unknown kernel path";
         case SGEMM_STATUS_UNSUPPORTED: return "no plan structure given";
         case SGEMM_STATUS_CUDA_ERROR: return "CUDA runtime error (see sgemm_last_cuda_error)";

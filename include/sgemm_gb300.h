@@ -44,7 +44,11 @@
  * or sgemm_strided_batched may be captured into a CUDA graph once an earlier
  * call has done the device's one-time set-up (kernel attributes, the
  * scratch pool): its pool allocation, the counter reset of stream-K and its
- * launches become graph nodes.
+ * launches become graph nodes.  The library keeps per-device state from
+ * its first call on a device (kernel attributes, cluster capacity, the
+ * scratch pool, the device address of the no-allocation scratch); calls
+ * made after cudaDeviceReset() on a device it has already used are not
+ * supported.
  *
  * Errors.  The return value is a status:
  *     0                      success;
@@ -215,12 +219,29 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha,
  * register sums over a grid-stride loop, warp shuffles, a shared-memory
  * combine per block and one atomic add per block into *out (which the call
  * zeroes first on `stream`).  x and out are device pointers (x 4-byte
- * aligned; 16-byte aligned x takes 16-byte loads).  The order in which
- * blocks commit is not fixed, so the last bits of the sum may differ
- * between runs; the error is within gamma_h * sum|x_i| for the summation
- * tree depth h.  Status: 1 x NULL / misaligned while n > 0, 2 n < 0,
- * 3 out NULL / misaligned, SGEMM_STATUS_CUDA_ERROR.  n == 0 gives 0.
+ * aligned).
+ *
+ * Launch shape: B = min(ceil(n / (16 * SGEMM_REDUCE_THREADS)),
+ * SGEMM_REDUCE_BLOCKS_PER_SM * SMs) blocks (at least 1) of
+ * SGEMM_REDUCE_THREADS threads, G = B * SGEMM_REDUCE_THREADS threads in all.
+ * With x 16-byte aligned, thread g reads float4 g, g + G, g + 2G, ... and
+ * adds component c of each into accumulator c (four FP32 accumulators),
+ * the n % 4 values after the last whole float4 going one each into the
+ * first accumulator of threads 0 .. n%4-1; otherwise every value goes
+ * through 4-byte loads into the first accumulator.  Then
+ * (a0 + a1) + (a2 + a3), a 5-level shuffle tree over the warp, the same
+ * tree over the block's warp sums, and the B block sums are added into *out
+ * one after another.  The longest chain of additions is therefore
+ *     h = ceil(floor(n/4) / G) + (n % 4 != 0) + 12 + B   (x 16-byte aligned)
+ *     h = ceil(n / G) + 12 + B                            (otherwise)
+ * and the result is within gamma_h * sum|x_i| of the exact sum
+ * (gamma_h = h u / (1 - h u), u = 2^-24).  The order in which blocks commit
+ * is not fixed, so the last bits of the sum may differ between runs.
+ * Status: 1 x NULL / misaligned while n > 0, 2 n < 0, 3 out NULL /
+ * misaligned, SGEMM_STATUS_CUDA_ERROR.  n == 0 gives 0.
  */
+#define SGEMM_REDUCE_THREADS 512
+#define SGEMM_REDUCE_BLOCKS_PER_SM 4
 int reduce_sum_f32(const float *x, long long n, float *out, cudaStream_t stream);
 
 /* Static, NUL-terminated description of a status code. */

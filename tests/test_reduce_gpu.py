@@ -1,11 +1,13 @@
 """GPU parity of reduce_sum_f32 against the FP64 sum oracle: within the
-gamma_h bound of the kernel's summation tree on real values, exact on small
-integers (every partial sum an integer below 2^24)."""
+gamma_h bound of the summation tree of the launch shape the header states
+(tests/reduce_model.py) on real values, exact on small integers (every
+partial sum an integer below 2^24)."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
+import reduce_model
 from dense_fp32_gemm_06_gb300 import binding, inputs
 
 pytestmark = pytest.mark.gpu
@@ -29,8 +31,8 @@ def test_reduce_real_values(n, offset):
     x = inputs.draw_matrix("normal", n + offset, 0, 1, n)[0] if n else np.zeros(0, np.float32)
     got = run(x, offset)
     s, a = oracle.sum_f64(x)
-    depth = binding.reduce_tree_depth(n, torch.cuda.get_device_properties(0).multi_processor_count,
-                                      vec=offset % 4 == 0)
+    depth = reduce_model.tree_depth(n, torch.cuda.get_device_properties(0).multi_processor_count,
+                                    vec=offset % 4 == 0)
     assert oracle.sum_within_tolerance(got, s, a, depth), (got, s, oracle.sum_tolerance(a, depth))
 
 
@@ -47,7 +49,7 @@ def test_reduce_full_size():
     got = binding.reduce_sum(x).item()
     xh = x.cpu().numpy()
     s, a = oracle.sum_f64(xh)
-    depth = binding.reduce_tree_depth(n, torch.cuda.get_device_properties(0).multi_processor_count)
+    depth = reduce_model.tree_depth(n, torch.cuda.get_device_properties(0).multi_processor_count, vec=True)
     assert oracle.sum_within_tolerance(got, s, a, depth)
 
 

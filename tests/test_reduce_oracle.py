@@ -74,9 +74,29 @@ def test_sum_tolerance_formula():
     assert not oracle.sum_within_tolerance(float("nan"), 1.0, 1.0, 10)
 
 
-def test_tree_depth_of_the_kernel_launch():
-    from dense_fp32_gemm_06_gb300 import binding
-    # 2^28 values on 152 SMs: 608 blocks of 512 threads, 16-byte loads
-    d = binding.reduce_tree_depth(1 << 28)
-    assert d == -(-(1 << 28) // (608 * 512 * 4)) + 1 + 2 + 5 + 5 + 608
-    assert binding.reduce_tree_depth(5) == (1 + 1) + 2 + 5 + 5 + 1
+def test_tree_depth_of_three_launches_by_hand():
+    """Depths worked out by hand from the launch shape the header states.
+    2^28 aligned values on 152 SMs: min(2^28 / 8192, 4 * 152) = 608 blocks,
+    608 * 512 = 311296 threads; 2^26 float4 loads over them is 215.6, so a
+    thread's accumulator takes 216 values, no tail; 216 + 2 + 5 + 5 + 608 =
+    836.  4099 values, 4-byte loads: one block of 512 threads, 9 values per
+    thread (4099 / 512 = 8.006), 9 + 12 + 1 = 22.  5 aligned values: one
+    block, one float4 and the one-value tail in thread 0's first
+    accumulator, 2 + 12 + 1 = 15."""
+    import reduce_model
+    assert reduce_model.tree_depth(1 << 28, 152, vec=True) == 836
+    assert reduce_model.tree_depth(4099, 152, vec=False) == 22
+    assert reduce_model.tree_depth(5, 152, vec=True) == 15
+
+
+def test_reduce_model_matches_the_header():
+    """The launch constants the depth model assumes are the ones the header
+    declares (a change of the kernel's launch shape must change both)."""
+    import os
+    import re
+    import reduce_model
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "sgemm_gb300.h")).read()
+    got = dict(re.findall(r"#define (SGEMM_REDUCE_\w+) (\d+)", text))
+    assert int(got["SGEMM_REDUCE_THREADS"]) == reduce_model.THREADS
+    assert int(got["SGEMM_REDUCE_BLOCKS_PER_SM"]) == reduce_model.BLOCKS_PER_SM
