@@ -254,12 +254,22 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- helpers
 
-# sources that define each kernel family (a traffic figure is void once any changes)
+# sources that define each kernel family (a traffic figure is void once any
+# changes); the tensor-core families differ in which operands the GEMM reads
+# as stored (raw) and which come split by the split pass
+_TC_SOURCES = ["tf32x3_sgemm.cuh", "tcgen05.cuh", "ptx.cuh", "raster.cuh"]
 KERNEL_SOURCES = {
     "ffma": ["ffma_sgemm.cuh", "ptx.cuh", "raster.cuh"],
-    "tf32x3": ["tf32x3_sgemm.cuh", "tcgen05.cuh", "ptx.cuh", "raster.cuh"],
-    "tf32x3_a_in": ["tf32x3_sgemm.cuh", "tcgen05.cuh", "ptx.cuh", "raster.cuh"],
+    "tf32x3_raw_ab": _TC_SOURCES,
+    "tf32x3_raw_a": _TC_SOURCES,
+    "tf32x3_raw_b": _TC_SOURCES,
+    "tf32x3_presplit": _TC_SOURCES,
 }
+
+
+def tc_family(a_raw, b_raw):
+    return {(True, True): "tf32x3_raw_ab", (True, False): "tf32x3_raw_a", (False, True): "tf32x3_raw_b",
+            (False, False): "tf32x3_presplit"}[(bool(a_raw), bool(b_raw))]
 
 
 def kernel_source_hash(family):
@@ -620,65 +630,46 @@ def run_ours(args, rank, world):
                 "traffic": traffic_record("ffma", p.m * p.n * p.k)}
     else:
         ka = binding.ka_of(p.k)
-        b_hi = torch.empty(p.n * ka, device="cuda")
-        b_lo = torch.empty_like(b_hi)
-        a_in = bool(plan["a_in_kernel"])
-        # one split launch (split_pair_kernel, for B alone or for both
-        # operands) and the GEMM
-        launches_per_step = 2
-        if a_in or plan["stream_k"] > 0:
-            # the GEMM kernel splits A itself, or runs stream-K with a
-            # workspace only the whole call provides: its time is the
-            # call's minus the split kernels timed alone
-            a_hi = a_lo = None
-            if not a_in:
+        a_raw, b_raw = bool(plan["a_in_kernel"]), bool(plan["b_in_kernel"])
+        # the GEMM, plus one split launch when an operand cannot be read as stored
+        launches_per_step = 1 if (a_raw and b_raw) else 2
+        if a_raw and b_raw:
+            # the call is the GEMM kernel alone (no split pass, no scratch)
+            gemm_ms = mean_ms
+            gemm_timing = "the whole call: one launch of the GEMM kernel (CUDA events per launch)"
+        else:
+            # the GEMM's time is the call's minus the split passes it runs,
+            # timed alone through the public split entry points
+            a_hi = a_lo = b_hi = b_lo = None
+            if not a_raw:
                 a_hi = torch.empty(p.m * ka, device="cuda")
                 a_lo = torch.empty_like(a_hi)
+            if not b_raw:
+                b_hi = torch.empty(p.n * ka, device="cuda")
+                b_lo = torch.empty_like(b_hi)
 
             def splits_only():
-                if not a_in:
+                if not a_raw:
                     binding.tf32x3_split_a(A[:, :p.k], a_hi, a_lo)
-                binding.tf32x3_split_b(B[:, :p.n], b_hi, b_lo)
+                if not b_raw:
+                    binding.tf32x3_split_b(B[:, :p.n], b_hi, b_lo)
 
             for _ in range(3):
                 splits_only()
             split_ms = device_time_ms(splits_only, stream, 20, flush=flush)
             gemm_ms = mean_ms - split_ms
-            gemm_timing = ("whole call minus " + ("the split pass over B" if a_in else
-                                                  "the split passes over A and B (timed as two launches; the call "
-                                                  "runs both in one)")
-                           + " timed alone (device time of 20 back-to-back launches, CUDA events)")
-            del a_hi, a_lo
-        else:
-            # the step is the split launch + the tcgen05 GEMM; the GEMM
-            # kernel alone is timed on operands split once, through the
-            # split-GEMM call
-            a_hi = torch.empty(p.m * ka, device="cuda")
-            a_lo = torch.empty_like(a_hi)
-            binding.tf32x3_split_a(A[:, :p.k], a_hi, a_lo)
-            binding.tf32x3_split_b(B[:, :p.n], b_hi, b_lo)
-
-            def gemm_only():
-                s = binding.tf32x3_split_gemm_raw(p.m, p.n, p.k, p.alpha, a_hi.data_ptr(), a_lo.data_ptr(),
-                                                   b_hi.data_ptr(), b_lo.data_ptr(), p.beta, C.data_ptr(),
-                                                   p.ldc, sptr)
-                if s:
-                    raise SystemExit(f"split gemm failed: {binding.status_string(s)}")
-
-            for _ in range(3):
-                gemm_only()
-            gm = time_launches(gemm_only, stream, min(args.steps, 100), flush=flush)
-            gemm_ms = sum(gm) / len(gm)
-            gemm_timing = "split-GEMM call on operands split once (CUDA events)"
-            del a_hi, a_lo
-        del b_hi, b_lo
+            gemm_timing = ("whole call minus the split pass over " +
+                           " and ".join(x for x, raw in (("A", a_raw), ("B", b_raw)) if not raw) +
+                           " timed alone (device time of 20 back-to-back launches, CUDA events)")
+            del a_hi, a_lo, b_hi, b_lo
         achieved = tflops(p, gemm_ms)
         mp = measured_peaks()
         bf16 = (mp or {}).get("bf16_tflops", 1900.0)
         tf32 = bf16 * NOMINAL_TF32_OVER_BF16
-        family = "tf32x3_a_in" if a_in else "tf32x3"
-        traits = [t for t, on in (("A split in kernel", a_in), ("transposed tiles", plan["trans"]),
-                                  ("stream-K", plan["stream_k"] > 0)) if on]
+        family = tc_family(a_raw, b_raw)
+        traits = [t for t, on in (("A read raw", a_raw), ("B read raw", b_raw), ("transposed tiles", plan["trans"]),
+                                  ("stream-K", plan["stream_k"] > 0), (f"split-K {plan['split_k']}",
+                                                                       plan["split_k"] > 1)) if on]
         roof = {"bound": "tensor", "kernel": "tf32x3_gemm_kernel" + (f"<{', '.join(traits)}>" if traits else ""),
                 "achieved": achieved, "peak": tf32 / 3,
                 "unit": "TFLOP/s", "frac": achieved / (tf32 / 3),

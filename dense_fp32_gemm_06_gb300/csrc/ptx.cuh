@@ -103,6 +103,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *desc, int 
         : "memory");
 }
 
+// 3-D tiled TMA load of the box at (x, y, z) (x innermost).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *desc, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // Programmatic dependent launch: a kernel launched as the dependent of the
 // previous kernel in its stream may start before that kernel completes;
 // griddep_wait() blocks the calling thread until the previous kernel has

@@ -86,13 +86,20 @@ int ffma_smem_bytes(int akind, int bkind) {
                       : akind == 1 ? ffma_smem_b<ALoadVec>(bkind) : ffma_smem_b<ALoadScalar>(bkind);
 }
 
-template <class Cfg, bool CV, bool TRANS = false>
+template <class Cfg, bool TRANS, bool XM, bool YM>
+cudaError_t set_tc_attr_one() {
+    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+}
+
+// The four operand-layout variants of one tile shape (X and Y each K-major
+// or MN-major).
+template <class Cfg, bool TRANS>
 cudaError_t set_tc_attr() {
-    cudaError_t e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV, false, TRANS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, CV, true, TRANS>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+    cudaError_t e = set_tc_attr_one<Cfg, TRANS, false, false>();
+    if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, false, true>();
+    if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, true, false>();
+    if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, true, true>();
     return e;
 }
 
@@ -112,7 +119,7 @@ cudaError_t max_clusters_of(int S, int *out) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     *out = 0;
-    return cudaOccupancyMaxActiveClusters(out, tf32x3::tf32x3_gemm_kernel<Cfg, true, false>, &cfg);
+    return cudaOccupancyMaxActiveClusters(out, tf32x3::tf32x3_gemm_kernel<Cfg, false, false, true>, &cfg);
 }
 
 // One-time per-device set-up: SM count and kernel attributes.
@@ -129,11 +136,9 @@ int device_state(DeviceState **out) {
         if ((e = set_ffma_attr_all_b<ALoadScatter>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_ffma_attr_all_b<ALoadVec>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_ffma_attr_all_b<ALoadScalar>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_tc_attr<tf32x3::Wide, true>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Wide, false>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_tc_attr<tf32x3::Narrow, true>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Narrow, false>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_tc_attr<tf32x3::Wide, false, true>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_tc_attr<tf32x3::Wide, true>()) != cudaSuccess) return fail_cuda(e);
         for (int S = 2; S <= 8; ++S) {
             if ((e = max_clusters_of<tf32x3::Wide>(S, &d.max_clusters[0][S])) != cudaSuccess) return fail_cuda(e);
             if ((e = max_clusters_of<tf32x3::Narrow>(S, &d.max_clusters[1][S])) != cudaSuccess) return fail_cuda(e);
@@ -199,9 +204,20 @@ int check_args(int m, int n, int k, float alpha, const float *A, int lda, const 
 
 // max_clusters: the device's cluster capacity table (DeviceState), or NULL
 // for a host-only plan, which assumes 8 GPCs of num_sms / 8 SMs.
+// Whether the tensor-core GEMM can read an operand as stored, by TMA: a
+// 16-byte aligned base and 16-byte rows, and in a batch either one matrix
+// for all problems (stride 0) or problems that do not overlap, 16 bytes apart.
+// `outer` x `ld` is the stored matrix (rows x row pitch).
+bool tma_readable(const void *X, long long ld, long long outer, int batch, long long stride) {
+    if (!aligned(X, 16) || ld % 4 != 0) return false;
+    if (batch > 1 && stride != 0 && (stride % 4 != 0 || stride < outer * ld)) return false;
+    return true;
+}
+
 int plan(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
          const float *C, int ldc, int path, int num_sms, sgemm_plan *pl, const int (*max_clusters)[9] = nullptr,
-         int op_a = SGEMM_OP_N, int op_b = SGEMM_OP_N, int batch = 1, bool allow_sk = true) {
+         int op_a = SGEMM_OP_N, int op_b = SGEMM_OP_N, int batch = 1, bool allow_sk = true,
+         long long stride_a = 0, long long stride_b = 0) {
     (void)beta;
     std::memset(pl, 0, sizeof(*pl));
     if (path != SGEMM_PATH_AUTO && path != SGEMM_PATH_FFMA && path != SGEMM_PATH_TF32X3)
@@ -336,27 +352,30 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
                 consider(W * KT * slab + share * slab + (share < KT ? 640 : 320), bn, 1, tr, true);
             }
         }
-        // A is split inside the GEMM (two extra warps split each raw slab in
-        // shared memory, no pass over A through HBM) when the kernel can read
-        // A itself by TMA (untransposed, 16-byte rows, one problem).  The
-        // pre-pass moves 12 bytes per element of A (read 4, write 8) and the
-        // GEMM then reads 8 more; the in-kernel split reads 4 bytes per
-        // element per tile column but re-splits A once per tile column, which
-        // costs shared-memory bandwidth next to the MMA.  Measured on GB300
-        // (whole call, m = k = 8192): 2.4x faster at n = 512, 1.65x at 1024,
-        // 1.27x at 2048, 1.10x at 4096, even at 8192; so n <= 4096.
-        // SGEMM_GB300_SPLIT_A_IN (0 / 1) pins it.
+        // Each operand is read by the GEMM as the caller stored it whenever
+        // TMA can read it (tma_readable): the GEMM's two splitter warps turn
+        // each raw slab into its TF32 lo part in shared memory and the MMA
+        // reads the raw slab as the hi part, so the call needs no split pass
+        // and no scratch memory for that operand.  Otherwise the split pass
+        // writes the operand's hi and lo parts into scratch first.
+        // SGEMM_GB300_SPLIT_A_IN / SGEMM_GB300_SPLIT_B_IN = 0 force the split
+        // pass (tests and measurements).
+        // B's split, though, is ~1.6x the work of A's per slab (the tile's
+        // 256 n-rows against 128 m-rows), and on 128 x 256 tiles the
+        // splitter warps' shared-memory traffic then holds up the tensor
+        // core (measured, whole call, L2 flushed: 8192^3 5.8 against 3.7 ms
+        // with B split by the split pass; 2048^3 118 against 82 us), while
+        // for small problems the split pass's launch and round trip cost
+        // more (256^3 14.7 against 16.3 us; 1000 x 1500 x 780 35.8 against
+        // 36.6).  So B is read as stored for m*n*k <= 2^31 only.
         const char *env_ain = std::getenv("SGEMM_GB300_SPLIT_A_IN");
-        const bool a_tma = op_a == SGEMM_OP_N && aligned(A, 16) && (lda % 4) == 0 && batch == 1;
-        if (env_ain && (env_ain[0] == '0' || env_ain[0] == '1'))
-            pl->a_in_kernel = a_tma && env_ain[0] == '1';
-        else
-            pl->a_in_kernel = a_tma && n <= 4096;
-        // otherwise, when the GEMM can still read A by TMA, it reads A's hi
-        // part from A itself too and the split pass writes only A's lo part
-        // (8 bytes per element of A through HBM instead of 12)
-        pl->a_lo_only = a_tma && !pl->a_in_kernel;
-        pl->threads = tf32x3::threads_for(pl->a_in_kernel != 0);
+        const char *env_bin = std::getenv("SGEMM_GB300_SPLIT_B_IN");
+        const bool a_tma = tma_readable(A, lda, op_a == SGEMM_OP_N ? m : k, batch, stride_a);
+        const bool b_tma = tma_readable(B, ldb, op_b == SGEMM_OP_N ? k : n, batch, stride_b);
+        const bool b_small = (long long)m * n * k * (batch > 0 ? batch : 1) <= (1LL << 31);
+        pl->a_in_kernel = a_tma && !(env_ain && env_ain[0] == '0');
+        pl->b_in_kernel = b_tma && (env_bin && (env_bin[0] == '0' || env_bin[0] == '1') ? env_bin[0] == '1' : b_small);
+        pl->threads = tf32x3::THREADS;
         const bool narrow = best_bn == tf32x3::Narrow::BN;
         pl->trans = best_tr;
         // bm x bn: the tile of C (256 x 128 when transposed)
@@ -396,19 +415,64 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
     return SGEMM_STATUS_OK;
 }
 
-// 2-D row-major FP32 tensor map: `rows` x `cols` with a row pitch of `ld`
-// floats, copied in boxes of box_rows x box_cols.
-int make_tensor_map(CUtensorMap *map, const float *base, int rows, int cols, int ld, int box_rows, int box_cols,
-                    CUtensorMapSwizzle swizzle) {
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides,
+// 3-D FP32 tensor map: `nb` matrices of `rows` x `cols` (row pitch `ld`
+// floats, `bstride` floats from one matrix to the next), copied in boxes of
+// box_rows x box_cols of one matrix.
+int make_tensor_map(CUtensorMap *map, const float *base, long long rows, long long cols, long long ld, int nb,
+                    long long bstride, int box_rows, int box_cols, CUtensorMapSwizzle swizzle) {
+    // a single matrix still gets a legal (16-byte multiple) batch stride
+    if (nb <= 1) bstride = (rows * ld + 3) / 4 * 4;
+    const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)(nb > 1 ? nb : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)bstride * 4};
+    const cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides,
                                 box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail_cuda(cudaErrorInvalidValue);
     return SGEMM_STATUS_OK;
+}
+
+// One MMA operand of the tensor-core GEMM as the kernel reads it.  `rows` is
+// its extent along the tile (m for A, n for B), k its depth.
+//   raw: the caller's matrix, read by TMA as stored -- kmajor: stored
+//     rows x k (row pitch ld); otherwise stored k x rows (MN-major);
+//   pre-split: hi / lo arrays of rows x ka per problem (pitch ka), problems
+//     rows * ka apart.
+struct Operand {
+    bool raw = false, kmajor = true;
+    const float *hi = nullptr, *lo = nullptr;
+    long long ld = 0, bstride = 0;
+    int rows = 0;
+};
+
+// The operand's two tensor maps (hi / raw, and lo), boxes of box_rows of it
+// by 16 k: K-major in 64-byte swizzled rows, MN-major in 32-row boxes with
+// the 128-byte swizzle of 32-byte atoms (the layout the MMA reads an
+// MN-major TF32 operand in).  `z` is set when the kernel should address problem
+// blockIdx.y of the map (a batch of distinct matrices).
+int encode_operand(const Operand &o, int k, int box_rows, int batch, CUtensorMap *hi, CUtensorMap *lo, int *z) {
+    int st;
+    if (o.raw) {
+        const int nb = batch > 1 && o.bstride != 0 ? batch : 1;
+        *z = nb > 1;
+        if (o.kmajor)
+            st = make_tensor_map(hi, o.hi, o.rows, k, o.ld, nb, o.bstride, box_rows, tf32x3::BK,
+                                 CU_TENSOR_MAP_SWIZZLE_64B);
+        else
+            st = make_tensor_map(hi, o.hi, k, o.rows, o.ld, nb, o.bstride, tf32x3::BK, 32,
+                                 CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B);
+        if (!st) *lo = *hi;   // not read
+        return st;
+    }
+    const long long ka = (k + 3) & ~3;
+    *z = batch > 1;
+    st = make_tensor_map(hi, o.hi, o.rows, k, ka, batch, (long long)o.rows * ka, box_rows, tf32x3::BK,
+                         CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!st)
+        st = make_tensor_map(lo, o.lo, o.rows, k, ka, batch, (long long)o.rows * ka, box_rows, tf32x3::BK,
+                             CU_TENSOR_MAP_SWIZZLE_64B);
+    return st;
 }
 
 int ka_of(int k) { return (k + 3) & ~3; }
@@ -471,68 +535,73 @@ int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *b
     return SGEMM_STATUS_OK;
 }
 
-// The tcgen05 GEMM on split operands (row pitch ka).
-template <class Cfg>
-cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, const sgemm_plan &pl, const CUtensorMap &ahi,
-                      const CUtensorMap &alo, const CUtensorMap &bhi, const CUtensorMap &blo,
-                      const tf32x3::Params &a) {
-    if constexpr (Cfg::BN == tf32x3::Wide::BN) {
-        if (pl.trans)   // C^T tiles (256-wide only): scalar stores along n, C_VEC unused
-            return pl.a_in_kernel ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, true, true>, ahi,
-                                                       alo, bhi, blo, a)
-                                  : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, false, true>, ahi,
-                                                       alo, bhi, blo, a);
-    }
-    if (pl.a_in_kernel)
-        return pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, true, true>, ahi, alo, bhi, blo, a)
-                        : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, true>, ahi, alo, bhi, blo,
-                                             a);
-    return pl.c_vec ? cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, true, false>, ahi, alo, bhi, blo, a)
-                    : cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, false, false>, ahi, alo, bhi, blo, a);
+template <class Cfg, bool TRANS, bool XM, bool YM>
+cudaError_t launch_tc_one(const cudaLaunchConfig_t &cfg, const CUtensorMap *maps, const tf32x3::Params &a) {
+    return cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM>, maps[0], maps[1], maps[2],
+                              maps[3], a);
 }
 
-// batch > 1: the split operands of the batch's problems are stacked, problem
-// b's A rows at b*m and B^T rows at b*n (tiles overhanging m or n read the
-// next problem's rows, which only reach outputs that are never stored).
-int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const float *a_lo, const float *bt_hi,
-                      const float *bt_lo, float beta, float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream,
-                      int batch = 1, long long stride_c = 0, int a_ld = 0, float *sk_ws = nullptr,
-                      int *sk_cnt = nullptr, bool after_split = false) {
-    const int ka = ka_of(k);
+template <class Cfg, bool TRANS>
+cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, bool xm, bool ym, const CUtensorMap *maps,
+                      const tf32x3::Params &a) {
+    if (xm) return ym ? launch_tc_one<Cfg, TRANS, true, true>(cfg, maps, a) : launch_tc_one<Cfg, TRANS, true, false>(cfg, maps, a);
+    return ym ? launch_tc_one<Cfg, TRANS, false, true>(cfg, maps, a) : launch_tc_one<Cfg, TRANS, false, false>(cfg, maps, a);
+}
+
+// Everything a tensor-core GEMM launch needs, prepared before anything is
+// enqueued (so that a failure here leaves the stream untouched).
+struct GemmLaunch {
+    CUtensorMap maps[4];   // X hi, X lo, Y hi, Y lo
+    tf32x3::Params prm;
+    bool xm = false, ym = false;
+};
+
+// Builds the launch of the GEMM for operands a (m side) and b (n side):
+// untransposed tiles take X = a, Y = b; TRANS tiles X = b, Y = a.
+int prepare_gemm(int m, int n, int k, float alpha, const Operand &a, const Operand &b, float beta, float *C,
+                 int ldc, const sgemm_plan &pl, int batch, long long stride_c, float *sk_ws, int *sk_cnt,
+                 GemmLaunch *L) {
     // stream-K needs its workspace (callers that allocate nothing plan without it)
     if (pl.stream_k > 0 && (sk_ws == nullptr || sk_cnt == nullptr || batch != 1)) return SGEMM_STATUS_UNSUPPORTED;
-    CUtensorMap t_ahi, t_alo, t_bhi, t_blo;
-    const int am = m * batch, bn = n * batch;
-    // a_hi is the caller's A (row pitch a_ld) when the GEMM splits A itself
-    // (a_lo is then not read) or when the split pass wrote only A's lo part
-    const int hi_pitch = pl.a_in_kernel || pl.a_lo_only ? a_ld : ka;
-    // boxes: a tile's rows of A (pl.bm) and of B^T (pl.bn)
-    int st = make_tensor_map(&t_ahi, a_hi, am, k, hi_pitch, pl.bm, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st)
-        st = pl.a_in_kernel ? make_tensor_map(&t_alo, a_hi, am, k, hi_pitch, pl.bm, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B)
-                            : make_tensor_map(&t_alo, a_lo, am, k, ka, pl.bm, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st) st = make_tensor_map(&t_bhi, bt_hi, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (!st) st = make_tensor_map(&t_blo, bt_lo, bn, k, ka, pl.bn, tf32x3::BK, CU_TENSOR_MAP_SWIZZLE_64B);
+    const Operand &x = pl.trans ? b : a, &y = pl.trans ? a : b;
+    // boxes: 128 rows of X (the MMA's M), BN rows of Y (its N)
+    const int y_rows = pl.trans ? pl.bm : pl.bn;
+    tf32x3::Params &p = L->prm;
+    int st = encode_operand(x, k, tf32x3::BM, batch, &L->maps[0], &L->maps[1], &p.x_z);
+    if (!st) st = encode_operand(y, k, y_rows, batch, &L->maps[2], &L->maps[3], &p.y_z);
     if (st) return st;
-    tf32x3::Params a;
-    a.m = m;
-    a.n = n;
-    a.k = k;
-    a.alpha = alpha;
-    a.beta = beta;
-    a.C = C;
-    a.ldc = ldc;
-    a.tiles_m = (m + pl.bm - 1) / pl.bm;
-    a.tiles_n = (n + pl.bn - 1) / pl.bn;
-    a.group_m = pl.group_m;
-    a.stride_c = stride_c;
-    a.sk_ctas = pl.stream_k;
-    a.sk_ws = sk_ws;
-    a.sk_cnt = sk_cnt;
-    // clusters of split_k CTAs (consecutive in x) share a tile; y = batch
+    L->xm = x.raw && !x.kmajor;
+    L->ym = y.raw && !y.kmajor;
+    p.m = m;
+    p.n = n;
+    p.k = k;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.C = C;
+    p.ldc = ldc;
+    p.tiles_m = (m + pl.bm - 1) / pl.bm;
+    p.tiles_n = (n + pl.bn - 1) / pl.bn;
+    p.group_m = pl.group_m;
+    p.stride_c = stride_c;
+    p.x_src = x.raw ? tf32x3::kRaw : tf32x3::kPreSplit;
+    p.y_src = y.raw ? tf32x3::kRaw : tf32x3::kPreSplit;
+    p.c_vec = pl.c_vec;
+    p.sk_ctas = pl.stream_k;
+    p.sk_ws = sk_ws;
+    p.sk_cnt = sk_cnt;
+    return SGEMM_STATUS_OK;
+}
+
+// Enqueues a prepared GEMM: clusters of split_k CTAs (consecutive in x)
+// share a tile, grid y = problem.  after_split: launched right after this
+// call's split pass, as its programmatic dependent, so the GEMM's set-up
+// overlaps the split's tail (its producer waits for the split before the
+// first load; nothing else the GEMM reads is written by it).
+// SGEMM_GB300_PDL=0 turns that off.
+int launch_gemm(const GemmLaunch &L, const sgemm_plan &pl, int batch, cudaStream_t stream, bool after_split) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid, (unsigned)batch, 1);
-    cfg.blockDim = dim3((unsigned)pl.threads, 1, 1);
+    cfg.blockDim = dim3((unsigned)tf32x3::THREADS, 1, 1);
     cfg.dynamicSmemBytes = (size_t)pl.smem_bytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -544,10 +613,6 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
-    // right after this call's split launch (after_split): launch as its
-    // dependent, so the GEMM's set-up overlaps its tail (the producer waits
-    // for it before reading the split operands; nothing else the GEMM reads
-    // is written by it).  SGEMM_GB300_PDL=0 turns it off.
     if (after_split) {
         const char *env = std::getenv("SGEMM_GB300_PDL");
         if (!(env && env[0] == '0')) {
@@ -559,79 +624,122 @@ int launch_split_gemm(int m, int n, int k, float alpha, const float *a_hi, const
     cfg.attrs = attr;
     cfg.numAttrs = na;
     cudaError_t e;
-    if (pl.bn == tf32x3::Narrow::BN && !pl.trans)
-        e = launch_tc<tf32x3::Narrow>(cfg, pl, t_ahi, t_alo, t_bhi, t_blo, a);
+    if (pl.trans)
+        e = launch_tc<tf32x3::Wide, true>(cfg, L.xm, L.ym, L.maps, L.prm);
+    else if (pl.bn == tf32x3::Narrow::BN)
+        e = launch_tc<tf32x3::Narrow, false>(cfg, L.xm, L.ym, L.maps, L.prm);
     else
-        e = launch_tc<tf32x3::Wide>(cfg, pl, t_ahi, t_alo, t_bhi, t_blo, a);
+        e = launch_tc<tf32x3::Wide, false>(cfg, L.xm, L.ym, L.maps, L.prm);
     if (e != cudaSuccess) return fail_cuda(e);
     return SGEMM_STATUS_OK;
 }
 
-// 3xTF32 path of sgemm: split A and B^T into a stream-ordered scratch
-// buffer, run the tcgen05 GEMM, release the scratch.
+// Scratch of a tensor-core call (floats): the hi and lo parts of each
+// operand the GEMM cannot read as stored (2 * rows * ka per problem), then
+// stream-K's per-tile counters and two partial tiles per CTA.
+struct Scratch {
+    size_t a = 0, b = 0, sk_cnt = 0, sk_ws = 0;
+    size_t total() const { return a + b + sk_cnt + sk_ws; }
+};
+
+Scratch scratch_of(int m, int n, int k, const sgemm_plan &pl, int batch) {
+    Scratch sc;
+    const size_t ka = (size_t)ka_of(k), cnt = (size_t)batch;
+    if (!pl.a_in_kernel) sc.a = 2 * cnt * (size_t)m * ka;
+    if (!pl.b_in_kernel) sc.b = 2 * cnt * (size_t)n * ka;
+    if (pl.stream_k > 0) {
+        sc.sk_cnt = ((size_t)pl.tiles + 3) / 4 * 4;
+        sc.sk_ws = (size_t)pl.stream_k * 2 * tf32x3::BM * (pl.trans ? tf32x3::Wide::BN : pl.bn);
+    }
+    return sc;
+}
+
+// The tensor-core path of one call (a strided batch of `bt.count`
+// problems): operands the GEMM can read as stored go to it as they are; the
+// others are split into scratch first by one split_pair_kernel launch.
+// `ws` is the call's scratch (scratch_of(...).total() floats), NULL when
+// it needs none.  Everything is prepared before the first launch.
+int run_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
+               float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream, int num_sms, const Batch &bt, float *ws) {
+    const Scratch sc = scratch_of(m, n, k, pl, bt.count);
+    const size_t a_elems = (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
+    float *a_hi = ws, *a_lo = ws + sc.a / 2, *b_hi = ws + sc.a, *b_lo = ws + sc.a + sc.b / 2;
+    int *sk_cnt = pl.stream_k > 0 ? reinterpret_cast<int *>(ws + sc.a + sc.b) : nullptr;
+    float *sk_ws = pl.stream_k > 0 ? ws + sc.a + sc.b + sc.sk_cnt : nullptr;
+    Operand oa, ob;
+    oa.rows = m;
+    ob.rows = n;
+    if (pl.a_in_kernel) {
+        oa.raw = true;
+        oa.kmajor = pl.op_a == SGEMM_OP_N;   // stored m x k; else k x m
+        oa.hi = A;
+        oa.ld = lda;
+        oa.bstride = bt.sa;
+    } else {
+        oa.hi = a_hi;
+        oa.lo = a_lo;
+    }
+    if (pl.b_in_kernel) {
+        ob.raw = true;
+        ob.kmajor = pl.op_b == SGEMM_OP_T;   // stored n x k; else k x n
+        ob.hi = B;
+        ob.ld = ldb;
+        ob.bstride = bt.sb;
+    } else {
+        ob.hi = b_hi;
+        ob.lo = b_lo;
+    }
+    GemmLaunch L;
+    int st = prepare_gemm(m, n, k, alpha, oa, ob, beta, C, ldc, pl, bt.count, bt.sc, sk_ws, sk_cnt, &L);
+    if (st) return st;
+    cudaError_t e;
+    if (sk_cnt != nullptr && (e = cudaMemsetAsync(sk_cnt, 0, (size_t)pl.tiles * sizeof(int), stream)) != cudaSuccess)
+        return fail_cuda(e);
+    // split pass for the operands the GEMM cannot read as stored: an operand
+    // stored with k contiguous is split row by row, one stored k-major
+    // through the transposing split; both in one launch
+    tf32x3::SplitJob jobs[2];
+    int nj = 0;
+    if (!pl.a_in_kernel)
+        jobs[nj++] = pl.op_a == SGEMM_OP_N ? split_a_job(m, k, A, lda, a_hi, a_lo, bt.count, bt.sa, (long long)a_elems)
+                                           : split_b_job(k, m, A, lda, a_hi, a_lo, bt.count, bt.sa, (long long)a_elems);
+    if (!pl.b_in_kernel)
+        jobs[nj++] = pl.op_b == SGEMM_OP_N ? split_b_job(k, n, B, ldb, b_hi, b_lo, bt.count, bt.sb, (long long)b_elems)
+                                           : split_a_job(n, k, B, ldb, b_hi, b_lo, bt.count, bt.sb, (long long)b_elems);
+    if (nj > 0) {
+        tf32x3::SplitJob none = jobs[0];
+        none.gx = none.gy = 0;
+        launch_split_pair(jobs[0], nj > 1 ? jobs[1] : none, bt.count, stream);
+    }
+    // after a split pass the GEMM starts its set-up while the split finishes
+    // when it runs in one wave (measured: 2048^3 +2.4 %, 1024^3 +7 %, 512^3
+    // +14 %; a many-wave GEMM gains nothing from it: 8192^3 -3 %)
+    const bool pdl = nj > 0 && (long long)pl.grid * bt.count <= num_sms;
+    return launch_gemm(L, pl, bt.count, stream, pdl);
+}
+
+// run_tf32x3 with the call's scratch taken from the device's stream-ordered
+// pool for the duration of the call (nothing is allocated when the call
+// needs no scratch).  SGEMM_GB300_FAIL_ALLOC (fault injection for tests):
+// the allocation reports out-of-memory without being attempted.
 int launch_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
                   float *C, int ldc, const sgemm_plan &pl, cudaStream_t stream, cudaMemPool_t pool, int num_sms,
                   const Batch &bt = Batch()) {
-    // scratch per problem: A's hi and lo parts (A's lo part only when
-    // a_lo_only, nothing when the GEMM splits A itself), B^T's hi and lo
-    const size_t a_elems = (size_t)m * ka_of(k), b_elems = (size_t)n * ka_of(k);
-    const size_t a_hi_elems = pl.a_in_kernel || pl.a_lo_only ? 0 : a_elems, a_lo_elems = pl.a_in_kernel ? 0 : a_elems;
-    const size_t cnt = (size_t)bt.count;
-    // stream-K: per-tile arrival counters, then two partial-tile slots per CTA
-    const size_t sk_cnt_floats = pl.stream_k > 0 ? ((size_t)pl.tiles + 3) / 4 * 4 : 0;
-    const size_t sk_ws_floats =
-        pl.stream_k > 0 ? (size_t)pl.stream_k * 2 * tf32x3::BM * (pl.trans ? tf32x3::Wide::BN : pl.bn) : 0;
+    const size_t need = scratch_of(m, n, k, pl, bt.count).total();
     float *ws = nullptr;
-    // SGEMM_GB300_FAIL_ALLOC (fault injection for tests): the allocation
-    // reports out-of-memory without being attempted
-    cudaError_t e = std::getenv("SGEMM_GB300_FAIL_ALLOC") != nullptr
-                        ? cudaErrorMemoryAllocation
-                        : cudaMallocFromPoolAsync(
-                              reinterpret_cast<void **>(&ws),
-                              (cnt * (a_hi_elems + a_lo_elems + 2 * b_elems) + sk_cnt_floats + sk_ws_floats) *
-                                  sizeof(float),
-                              pool, stream);
-    if (e != cudaSuccess) return fail_cuda(e);
-    float *a_hi = ws, *a_lo = ws + cnt * a_hi_elems, *b_hi = a_lo + cnt * a_lo_elems, *b_lo = b_hi + cnt * b_elems;
-    int *sk_cnt = pl.stream_k > 0 ? reinterpret_cast<int *>(b_lo + cnt * b_elems) : nullptr;
-    float *sk_ws = pl.stream_k > 0 ? b_lo + cnt * b_elems + sk_cnt_floats : nullptr;
-    if (sk_cnt != nullptr && (e = cudaMemsetAsync(sk_cnt, 0, (size_t)pl.tiles * sizeof(int), stream)) != cudaSuccess) {
-        cudaFreeAsync(ws, stream);
-        return fail_cuda(e);
+    if (need > 0) {
+        const cudaError_t e = std::getenv("SGEMM_GB300_FAIL_ALLOC") != nullptr
+                                  ? cudaErrorMemoryAllocation
+                                  : cudaMallocFromPoolAsync(reinterpret_cast<void **>(&ws), need * sizeof(float),
+                                                            pool, stream);
+        if (e != cudaSuccess) return fail_cuda(e);
     }
-    // both split operands are k-contiguous (K-major): an operand stored with
-    // k contiguous is split in place order, one stored k-major is transposed
-    // one launch splits both operands (only B's pass when the GEMM splits A)
-    const tf32x3::SplitJob jb =
-        pl.op_b == SGEMM_OP_N ? split_b_job(k, n, B, ldb, b_hi, b_lo, bt.count, bt.sb, (long long)b_elems)
-                              : split_a_job(n, k, B, ldb, b_hi, b_lo, bt.count, bt.sb, (long long)b_elems);
-    if (pl.a_in_kernel) {
-        a_hi = const_cast<float *>(A);   // the GEMM reads A itself and splits it in shared memory
-        a_lo = nullptr;
-        if (pl.op_b == SGEMM_OP_N) launch_split_b(k, n, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
-        else launch_split_a(n, k, B, ldb, b_hi, b_lo, stream, bt.count, bt.sb, (long long)b_elems);
-    } else {
-        tf32x3::SplitJob ja;
-        if (pl.a_lo_only) {
-            a_hi = const_cast<float *>(A);   // the GEMM reads A itself as its hi operand
-            ja = split_a_job(m, k, A, lda, nullptr, a_lo, bt.count, bt.sa, (long long)a_elems);
-        } else if (pl.op_a == SGEMM_OP_N) {
-            ja = split_a_job(m, k, A, lda, a_hi, a_lo, bt.count, bt.sa, (long long)a_elems);
-        } else {
-            ja = split_b_job(k, m, A, lda, a_hi, a_lo, bt.count, bt.sa, (long long)a_elems);
-        }
-        launch_split_pair(ja, jb, bt.count, stream);
+    const int st = run_tf32x3(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, pl, stream, num_sms, bt, ws);
+    if (ws != nullptr) {
+        const cudaError_t e = cudaFreeAsync(ws, stream);
+        if (!st && e != cudaSuccess) return fail_cuda(e);
     }
-    // the GEMM starts its set-up while the split launch finishes when it runs
-    // in one wave (measured: 2048^3 +2.4 %, 1024^3 +7 %, 512^3 +14 %; a
-    // many-wave GEMM gains nothing from it: 8192^3 -3 %)
-    const bool pdl = (long long)pl.grid * bt.count <= num_sms;
-    const int st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream, bt.count,
-                                     bt.sc, lda, sk_ws, sk_cnt, pdl);
-    e = cudaFreeAsync(ws, stream);
-    if (st) return st;
-    if (e != cudaSuccess) return fail_cuda(e);
-    return SGEMM_STATUS_OK;
+    return st;
 }
 
 // ---------------------------------------------------------------- no-allocation variant
@@ -731,11 +839,8 @@ int sgemm_strided_batched(int op_a, int op_b, int m, int n, int k, float alpha, 
     DeviceState *dev = nullptr;
     int st = device_state(&dev);
     if (st != SGEMM_STATUS_OK) return st;
-    // grid.y carries the batch (<= 65535 per launch) and the stacked split
-    // operands need 32-bit TMA row coordinates: larger batches go in chunks
-    long long chunk = 65535;
-    const long long mn = m > n ? m : n;
-    if (chunk * mn > 2147483647LL) chunk = 2147483647LL / mn;
+    // grid.y carries the batch (<= 65535 per launch): larger batches go in chunks
+    const long long chunk = 65535;
     for (long long b0 = 0; b0 < batch; b0 += chunk) {
         const int cnt = (int)(batch - b0 < chunk ? batch - b0 : chunk);
         const float *Ab = A ? A + b0 * stride_a : A;
@@ -743,7 +848,7 @@ int sgemm_strided_batched(int op_a, int op_b, int m, int n, int k, float alpha, 
         float *Cb = C + b0 * stride_c;
         sgemm_plan pl;
         st = plan(m, n, k, alpha, Ab, lda, Bb, ldb, beta, Cb, ldc, path, dev->sms, &pl, dev->max_clusters, op_a, op_b,
-                  cnt);
+                  cnt, true, stride_a, stride_b);
         if (st != SGEMM_STATUS_OK) return st;
         // 16-byte accesses need every problem's base aligned, not only the first
         if (stride_c % 4) pl.c_vec = 0;
@@ -857,12 +962,20 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
                   dev->max_clusters, SGEMM_OP_N, SGEMM_OP_N, 1, false);   // allocates nothing: no stream-K
     if (st) return st;
     pl.a_in_kernel = 0;   // the operands are split already
-    pl.a_lo_only = 0;
-    pl.threads = tf32x3::threads_for(false);
+    pl.b_in_kernel = 0;
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
-    } else if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, bt_hi, bt_lo, beta, C, ldc, pl, stream))) {
-        return st;
+    } else {
+        Operand oa, ob;
+        oa.rows = m;
+        oa.hi = a_hi;
+        oa.lo = a_lo;
+        ob.rows = n;
+        ob.hi = bt_hi;
+        ob.lo = bt_lo;
+        GemmLaunch L;
+        if ((st = prepare_gemm(m, n, k, alpha, oa, ob, beta, C, ldc, pl, 1, 0, nullptr, nullptr, &L))) return st;
+        if ((st = launch_gemm(L, pl, 1, stream, false))) return st;
     }
     const cudaError_t e = cudaGetLastError();
     return e == cudaSuccess ? SGEMM_STATUS_OK : fail_cuda(e);
@@ -872,8 +985,6 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
                          float beta, float *C, int ldc, cudaStream_t stream) {
     if (int bad = check_args(m, n, k, alpha, A, lda, B, ldb, C, ldc)) return bad;
     if (m == 0 || n == 0) return SGEMM_STATUS_OK;
-    const long long ka = (long long)ka_of(k);
-    if (2 * ((long long)m + n) * ka > (long long)SGEMM_NOALLOC_SCRATCH_FLOATS) return SGEMM_STATUS_TOO_LARGE;
     DeviceState *dev = nullptr;
     int st = device_state(&dev);
     if (st != SGEMM_STATUS_OK) return st;
@@ -881,22 +992,22 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
     st = plan(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, SGEMM_PATH_TF32X3, dev->sms, &pl, dev->max_clusters,
               SGEMM_OP_N, SGEMM_OP_N, 1, false);   // no stream-K workspace in the fixed scratch
     if (st != SGEMM_STATUS_OK) return st;
-    pl.a_in_kernel = 0;   // this entry point splits A into its fixed scratch
-    pl.a_lo_only = aligned(A, 16) && (lda % 4) == 0;   // then only A's lo part (the GEMM reads hi from A)
-    pl.threads = tf32x3::threads_for(false);
+    // read every operand TMA can read as stored, whatever the size (the
+    // plan splits a large B with the split pass, which is faster there):
+    // scratch only for operands whose rows are not 16 bytes apart
+    if (tma_readable(B, ldb, k, 1, 0)) pl.b_in_kernel = 1;
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
     } else {
+        // only operands the GEMM cannot read as stored need scratch: their
+        // split parts go into the fixed array instead of the pool
+        const size_t need = scratch_of(m, n, k, pl, 1).total();
+        if (need > (size_t)SGEMM_NOALLOC_SCRATCH_FLOATS) return SGEMM_STATUS_TOO_LARGE;
         float *ws = nullptr;
-        if ((st = noalloc_scratch(&ws))) return st;
-        // the split kernels write every element the GEMM reads, so nothing
+        if (need > 0 && (st = noalloc_scratch(&ws))) return st;
+        // the split pass writes every element the GEMM reads, so nothing
         // left in the array by an earlier call is ever used
-        const size_t a_elems = (size_t)m * ka, b_elems = (size_t)n * ka;
-        float *a_hi = ws, *a_lo = ws + a_elems, *b_hi = a_lo + a_elems, *b_lo = b_hi + b_elems;
-        const tf32x3::SplitJob ja = split_a_job(m, k, A, lda, pl.a_lo_only ? nullptr : a_hi, a_lo, 1, 0, 0);
-        if (pl.a_lo_only) a_hi = const_cast<float *>(A);
-        launch_split_pair(ja, split_b_job(k, n, B, ldb, b_hi, b_lo, 1, 0, 0), 1, stream);
-        if ((st = launch_split_gemm(m, n, k, alpha, a_hi, a_lo, b_hi, b_lo, beta, C, ldc, pl, stream, 1, 0, lda)))
+        if ((st = run_tf32x3(m, n, k, alpha, A, lda, B, ldb, beta, C, ldc, pl, stream, dev->sms, Batch(), ws)))
             return st;
     }
     const cudaError_t e = cudaGetLastError();

@@ -62,15 +62,16 @@ __device__ __forceinline__ void commit(uint32_t bar) {
                  : "memory");
 }
 
-// Instruction descriptor of kind::tf32 with FP32 accumulation; both operands
-// K-major.  Bit fields: [4,6) D format (1 = F32), [7,10) A format and
-// [10,13) B format (2 = TF32), 15 / 16 A / B major (0 = K-major),
-// [17,23) N >> 3, [24,29) M >> 4.
-template <int M, int N>
+// Instruction descriptor of kind::tf32 with FP32 accumulation.  Bit fields:
+// [4,6) D format (1 = F32), [7,10) A format and [10,13) B format (2 = TF32),
+// 15 / 16 A / B major (0 = K-major: rows of the operand hold consecutive k;
+// 1 = MN-major: rows hold consecutive m / n), [17,23) N >> 3, [24,29) M >> 4.
+template <int M, int N, bool A_MN = false, bool B_MN = false>
 __host__ __device__ constexpr uint32_t idesc_tf32_f32() {
     static_assert(M == 64 || M == 128, "cta_group::1 M");
     static_assert(N % 16 == 0 && N >= 16 && N <= 256, "N");
-    return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+    return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(A_MN) << 15) | (uint32_t(B_MN) << 16) |
+           (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor of a K-major operand stored as rows of
@@ -78,12 +79,34 @@ __host__ __device__ constexpr uint32_t idesc_tf32_f32() {
 // 512 bytes apart (stride byte offset); the leading byte offset is unused
 // for swizzled K-major layouts.  Bits: [0,14) start >> 4, [16,30) LBO >> 4,
 // [32,46) SBO >> 4, [46,48) version 1, [61,64) layout (4 = 64B swizzle).
+// The k step of 8 values inside a row is a 32-byte advance of the start.
 __device__ __forceinline__ uint64_t desc_kmajor_sw64(uint32_t smem_addr) {
     uint64_t d = (uint64_t)((smem_addr >> 4) & 0x3FFFu);
     d |= (uint64_t)1u << 16;
     d |= (uint64_t)((512u >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1u << 46;
     d |= (uint64_t)4u << 61;
+    return d;
+}
+
+// Descriptor of an MN-major operand (rows of the operand = consecutive m or
+// n in memory) as TMA writes it with the 128-byte swizzle of 32-byte atoms
+// (CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B: 32-byte chunks permuted within each
+// 128-byte line), layout code 1 here.  A slab is stored as boxes of
+// 32 operand rows (one 128-byte line per k) by 16 k, box j of the tile at
+// j * 2048 bytes.  Fields, as measured on GB300 with identity products
+// whose every output names the element it was read from: the leading byte
+// offset is the distance between 32-row atoms along m / n (2048 here), the
+// stride byte offset the distance between groups of 4 k lines (512); the k
+// step of 8 values is a 1024-byte advance of the start.  (With the 16-byte
+// 128-byte swizzle, layout code 2, an MN-major TF32 operand multiplied as
+// zeros, whatever the offsets.)
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128_32b(uint32_t smem_addr) {
+    uint64_t d = (uint64_t)((smem_addr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((2048u >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((512u >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1u << 46;
+    d |= (uint64_t)1u << 61;
     return d;
 }
 

@@ -91,13 +91,11 @@ constexpr int CHUNK_STAGES = KC / BK;
 constexpr int A_TILE = BM * BK * 4;                       // 8 KB
 constexpr int ACC_WARPS = 8;
 constexpr int ACC_THREADS = 32 * ACC_WARPS;
-constexpr int THREADS = 64 + ACC_THREADS;                 // producer warp, MMA warp, 8 accumulator warps
-constexpr int CONV_WARPS = 2;                             // A splitters when A is split in the kernel
+constexpr int CONV_WARPS = 2;                             // splitters of raw operands
 constexpr int CONV_THREADS = 32 * CONV_WARPS;
-// Threads per CTA: 10 warps, or 12 with the A splitters.  Either way three
-// warps share a sub-partition's register file, so the per-thread register
-// cap (168) is the same.
-__host__ __device__ constexpr int threads_for(bool a_in) { return a_in ? THREADS + CONV_THREADS : THREADS; }
+// producer warp, MMA warp, 8 accumulator warps, 2 splitter warps: three
+// warps per sub-partition, a cap of 168 registers per thread
+constexpr int THREADS = 64 + ACC_THREADS + CONV_THREADS;
 constexpr int BAR_REGION = 256;
 static_assert(BK * 4 == 64, "one 64-byte swizzle row per operand row");
 static_assert(KC % BK == 0, "chunks are whole slabs");
@@ -132,10 +130,15 @@ struct Params {
     float *C;
     long long ldc;
     int tiles_m, tiles_n, group_m;
-    // strided batch: problem blockIdx.y reads rows y*m .. of the split A and
-    // y*n .. of the split B^T (the batch's operands stacked as one tall
-    // matrix) and writes C + y*stride_c
+    // strided batch: problem blockIdx.y writes C + y*stride_c and reads its
+    // operands at TMA coordinate z = y (x_z, y_z set: the operand's tensor
+    // map has a batch dimension) or z = 0 (one operand shared by the batch)
     long long stride_c;
+    int x_z, y_z;
+    // where each MMA operand comes from (kPreSplit or kRaw, see the kernel)
+    int x_src, y_src;
+    // C rows 16-byte aligned (ldc % 4 == 0, C 16-byte aligned): float4 access
+    int c_vec;
     // stream-K (sk_ctas > 0, grid = G = sk_ctas persistent CTAs, one
     // problem): with tiles = W G + R, CTA g first takes whole tiles g,
     // g + G, ..., g + (W - 1) G (the full waves, in raster order, so CTAs
@@ -223,11 +226,16 @@ __device__ __forceinline__ void split_one(float x, float &h, float &l) {
 // The lo part of x when x itself is the MMA's hi operand: a kind::tf32 MMA
 // reads an FP32 operand with its low 13 mantissa bits dropped (measured on
 // GB300: every output of x * I equals x truncated to TF32, ties and all), so
-// hi = trunc(x); x - hi is exact in FP32 and lo = tf32(x - hi), rounded to
-// nearest, with |x - hi - lo| <= 2^-11 |x - hi| < 2^-21 |x|.
+// hi = trunc(x); r = x - hi is exact in FP32 and lo = tf32(r), rounded to
+// nearest with ties away from zero, with |x - hi - lo| <= 2^-11 |r| <
+// 2^-21 |x|.  The rounding is done on the bits (add half of the dropped
+// range to the magnitude, then drop it): the same result as cvt.rna.tf32
+// for every finite r (|r| < 2^-10 |x| cannot round up to infinity),
+// at two integer operations, which measured ~6 % faster than the
+// conversion instruction in the GEMM's splitter warps at 8192^3.
 __device__ __forceinline__ float lo_of_raw(float x) {
     const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    return tc::round_tf32(x - h);
+    return __uint_as_float((__float_as_uint(x - h) + 0x1000u) & 0xFFFFE000u);
 }
 
 // A (m x k, row pitch lda) -> hi, lo (m x ka, row pitch ka).  VEC: A and
@@ -365,30 +373,95 @@ __global__ void __launch_bounds__(256) split_pair_kernel(SplitJob j0, SplitJob j
 
 // ---------------------------------------------------------------- GEMM kernel
 
-// A_IN: A is split here instead of by split_a_kernel -- TMA loads the raw
-// FP32 A slab into A's hi slot and the MMA reads it as it is (hi = x with
-// the low 13 mantissa bits dropped, which is how a kind::tf32 MMA reads an
-// FP32 operand).  Two extra warps (10, 11) compute lo = tf32(x - hi) into
-// A's lo slot as soon as the slab lands, make the writes visible to the
-// tensor core's proxy and arrive on the slot's "converted" barrier.  The MMA
-// issuer sends the two products that do not need A's lo as soon as the slab
-// lands and waits for "converted" only before the third, so the split
-// overlaps the tensor core instead of costing an HBM round trip of A.
-// Error: |x - hi - lo| < 2^-21 |x| and |lo| < 2^-10 |x| (against 2^-22 and
-// 2^-11 for a round-to-nearest hi), so each product stays
-// within ~2^-20 |a b| of exact, far inside the FP32 acceptance bound.
-template <class Cfg, bool C_VEC, bool A_IN = false, bool TRANS = false>
-__global__ void __launch_bounds__(threads_for(A_IN), 1)
-    tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmAhi, const __grid_constant__ CUtensorMap tmAlo,
-                       const __grid_constant__ CUtensorMap tmBhi, const __grid_constant__ CUtensorMap tmBlo,
+// The MMA's two operands: X, its 128-row A operand, and Y, its BN-row B
+// operand.  Untransposed tiles: X = rows of A (m side), Y = columns of B
+// (n side).  TRANS tiles: X = columns of B, Y = rows of A.
+//
+// Each operand reaches a stage slot in one of two ways (Params::x_src,
+// y_src):
+//   kPreSplit: its hi and lo parts were written by the split pass (K-major,
+//     row pitch ka) and TMA loads both;
+//   kRaw: TMA loads the operand as the caller stored it into the hi slot --
+//     K-major (rows of consecutive k: A stored m x k, B stored n x k) in
+//     64-byte rows with the 64-byte swizzle, or MN-major (X_MN / Y_MN: rows
+//     of consecutive m or n: A stored k x m, B stored k x n) in boxes of
+//     32 rows x 16 k with the 128-byte swizzle of 32-byte atoms.  The MMA reads that FP32 slab as
+//     its hi part (a kind::tf32 MMA drops the low 13 mantissa bits), and the
+//     two splitter warps (10, 11) write lo = tf32(x - hi) into the lo slot
+//     at the same (swizzled) position, make the writes visible to the tensor
+//     core's proxy and arrive on the slot's "converted" barrier of that
+//     operand.  The MMA issuer sends hi x hi as soon as the slab lands and
+//     waits for an operand's lo only before the product that reads it.
+// Error of a raw operand: hi = trunc(x), |x - hi - lo| < 2^-21 |x| and
+// |lo| < 2^-10 |x| (against 2^-22 and 2^-11 for the split pass's
+// round-to-nearest hi), so each product stays within ~2^-19 |a b| of exact
+// even with both operands raw, far inside the FP32 acceptance bound.
+constexpr int kPreSplit = 0;
+constexpr int kRaw = 1;
+
+// Loads one operand's part of a slab: `rows` rows starting at row0 and 16 k
+// starting at kx, of problem z.  K-major: one box (16 k x rows); MN-major:
+// rows / 32 boxes (32 rows x 16 k, 2 KB each) side by side.
+template <bool MN, int ROWS>
+__device__ __forceinline__ void load_operand(uint32_t hi_slot, uint32_t lo_slot, const CUtensorMap *map_hi,
+                                             const CUtensorMap *map_lo, bool raw, int row0, int kx, int z,
+                                             uint32_t bar) {
+    if constexpr (MN) {
+#pragma unroll
+        for (int j = 0; j < ROWS / 32; ++j) tma_load_3d(hi_slot + j * 2048, map_hi, row0 + 32 * j, kx, z, bar);
+    } else {
+        tma_load_3d(hi_slot, map_hi, kx, row0, z, bar);
+        if (!raw) tma_load_3d(lo_slot, map_lo, kx, row0, z, bar);
+    }
+}
+
+// Descriptor of k step kk (8 values) of an operand slot.
+template <bool MN>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t slot, int kk) {
+    if constexpr (MN)
+        return tc::desc_mnmajor_sw128_32b(slot + (uint32_t)kk * 1024u);
+    else
+        return tc::desc_kmajor_sw64(slot + (uint32_t)kk * (UMMA_K * 4));
+}
+
+// lo = tf32(x - trunc(x)) of every value of a raw slot, in place order,
+// by `cw` threads (this one is `ct`), eight 16-byte loads in flight each.
+template <int BYTES, int CW>
+__device__ __forceinline__ void split_slot_lo(const uint8_t *raw_slot, uint8_t *lo_slot, int ct) {
+    constexpr int PER = BYTES / 16 / CW;   // float4 per thread
+    static_assert(BYTES % (16 * CW) == 0, "whole float4s per thread");
+    const float4 *raw = reinterpret_cast<const float4 *>(raw_slot);
+    float4 *lo = reinterpret_cast<float4 *>(lo_slot);
+    constexpr int G = PER < 8 ? PER : 8;
+#pragma unroll
+    for (int j0 = 0; j0 < PER; j0 += G) {
+        float4 x[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) x[j] = raw[ct + (j0 + j) * CW];
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            lo[ct + (j0 + j) * CW] =
+                make_float4(lo_of_raw(x[j].x), lo_of_raw(x[j].y), lo_of_raw(x[j].z), lo_of_raw(x[j].w));
+    }
+}
+
+template <class Cfg, bool TRANS = false, bool X_MN = false, bool Y_MN = false>
+__global__ void __launch_bounds__(THREADS, 1)
+    tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmXhi, const __grid_constant__ CUtensorMap tmXlo,
+                       const __grid_constant__ CUtensorMap tmYhi, const __grid_constant__ CUtensorMap tmYlo,
                        const Params p) {
-    constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, B_TILE = Cfg::B_TILE, STAGE_BYTES = Cfg::STAGE_BYTES;
+    constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, Y_TILE = Cfg::B_TILE, STAGE_BYTES = Cfg::STAGE_BYTES;
+    constexpr int X_TILE = A_TILE;
     constexpr int TMEM_COLS = Cfg::TMEM_COLS, COLS_PER_THREAD = Cfg::COLS_PER_THREAD;
     constexpr int PART_PITCH = BN + 4;   // floats per row of a parked split-K partial tile
-    constexpr int NTHREADS = threads_for(A_IN);
-    constexpr bool CONV_PER_WARP = BN == 128;   // A splitters: one warp per slab (see there)
-    // where A sits in a stage (the MMA's A operand, or its B operand when TRANS)
-    constexpr int SPLIT_OFF = TRANS ? 2 * A_TILE : 0, SPLIT_BYTES = TRANS ? B_TILE : A_TILE;
+    constexpr int NTHREADS = THREADS;
+    constexpr bool CONV_PER_WARP = BN == 128;   // splitters: one warp per slab (see there)
+    // slots of a stage: [X hi | X lo | Y hi | Y lo]
+    constexpr int X_HI = 0, X_LO = X_TILE, Y_HI = 2 * X_TILE, Y_LO = 2 * X_TILE + Y_TILE;
+    static_assert(X_LO % 1024 == 0 && Y_HI % 1024 == 0 && Y_LO % 1024 == 0 && STAGE_BYTES % 1024 == 0,
+                  "slots on 1 KB boundaries (128-byte swizzle atoms)");
+    static_assert(!X_MN || X_TILE == (BM / 32) * 2048, "MN-major X: 32-row boxes of 2 KB");
+    static_assert(!Y_MN || Y_TILE == (BN / 32) * 2048, "MN-major Y: 32-row boxes of 2 KB");
     static_assert(BM * PART_PITCH * 4 <= STAGES * STAGE_BYTES, "partial tile fits the stage memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *const smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -402,11 +475,14 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     uint32_t *const tmem_slot = reinterpret_cast<uint32_t *>(bars + 8 * (2 * STAGES + 5));
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 8);
     volatile int *const sk_last = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 12);
-    const uint32_t bar_conv = bar_done + 24;             // [STAGES] A slab split in place (A_IN)
+    const uint32_t bar_conv_x = bar_done + 24;           // [STAGES] X's lo written (raw X)
+    const uint32_t bar_conv_y = bar_conv_x + 8 * STAGES; // [STAGES] Y's lo written (raw Y)
     float4 *const epi = reinterpret_cast<float4 *>(bars + BAR_REGION);   // [ACC_WARPS][32 rows][8 float4]
-    static_assert(8 * (3 * STAGES + 7) <= BAR_REGION, "barrier region");
+    static_assert(8 * (4 * STAGES + 7) <= BAR_REGION, "barrier region");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool x_raw = p.x_src == kRaw, y_raw = p.y_src == kRaw;
+    const bool c_vec = p.c_vec != 0;
     // split-K: the CTAs of a cluster share one output tile and take
     // consecutive ranges of its k slabs (a cluster of one without split-K)
     const uint32_t nsplit = tc::cluster_nctarank(), rank = tc::cluster_ctarank();
@@ -421,8 +497,6 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     // remaining tiles' slabs (stream-K), a consecutive range of one tile's
     // slabs (split-K cluster rank `rank`), or one whole tile
     // (cta_segment above walks it)
-    // origin in C of tile t, and rows of its operands inside the (stacked,
-    // when batched) operand arrays
     auto tile_origin = [&](int t, int &m0, int &n0) {
         int tm, tn;
         raster_tile(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
@@ -443,14 +517,16 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
             mbar_init(bar_tempty + 8 * b, ACC_THREADS);
         }
         mbar_init(bar_done, 1);
-        if (A_IN)
-            for (int s = 0; s < STAGES; ++s) mbar_init(bar_conv + 8 * s, CONV_PER_WARP ? 32 : CONV_THREADS);
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_conv_x + 8 * s, CONV_PER_WARP ? 32 : CONV_THREADS);
+            mbar_init(bar_conv_y + 8 * s, CONV_PER_WARP ? 32 : CONV_THREADS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tmAhi);
-        tma_prefetch_desc(&tmAlo);
-        tma_prefetch_desc(&tmBhi);
-        tma_prefetch_desc(&tmBlo);
+        tma_prefetch_desc(&tmXhi);
+        tma_prefetch_desc(&tmXlo);
+        tma_prefetch_desc(&tmYhi);
+        tma_prefetch_desc(&tmYlo);
     }
     if (warp == 1) {
         tc::tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -473,7 +549,9 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
             for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
                 int m0, n0;
                 tile_origin(tile, m0, n0);
-                const int arow0 = (int)blockIdx.y * p.m + m0, brow0 = (int)blockIdx.y * p.n + n0;
+                const int x0 = TRANS ? n0 : m0, y0 = TRANS ? m0 : n0;
+                const int zx = p.x_z ? (int)blockIdx.y : 0, zy = p.y_z ? (int)blockIdx.y : 0;
+                const uint32_t tx_bytes = (x_raw ? 1 : 2) * X_TILE + (y_raw ? 1 : 2) * Y_TILE;
                 for (int kt = 0; kt < nk; ++kt, ++g) {
                     const int s = g % STAGES;
                     if (g >= STAGES && !mbar_wait(bar_empty + 8 * s, ((g / STAGES) - 1) & 1, kStatusProducer)) {
@@ -487,21 +565,10 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                     }
                     const uint32_t st = stage0 + s * STAGE_BYTES;
                     const uint32_t fb = bar_full + 8 * s;
-                    mbar_arrive_expect_tx(fb, A_IN ? STAGE_BYTES - SPLIT_BYTES : STAGE_BYTES);
+                    mbar_arrive_expect_tx(fb, tx_bytes);
                     const int kx = (k0 + kt) * BK;
-                    // slots [MMA A hi | MMA A lo | MMA B hi | MMA B lo]; raw A
-                    // into A's hi slot and nothing into its lo slot when A_IN
-                    if constexpr (!TRANS) {
-                        tma_load_2d(st, &tmAhi, kx, arow0, fb);
-                        if (!A_IN) tma_load_2d(st + A_TILE, &tmAlo, kx, arow0, fb);
-                        tma_load_2d(st + 2 * A_TILE, &tmBhi, kx, brow0, fb);
-                        tma_load_2d(st + 2 * A_TILE + B_TILE, &tmBlo, kx, brow0, fb);
-                    } else {
-                        tma_load_2d(st, &tmBhi, kx, brow0, fb);
-                        tma_load_2d(st + A_TILE, &tmBlo, kx, brow0, fb);
-                        tma_load_2d(st + 2 * A_TILE, &tmAhi, kx, arow0, fb);
-                        if (!A_IN) tma_load_2d(st + 2 * A_TILE + B_TILE, &tmAlo, kx, arow0, fb);
-                    }
+                    load_operand<X_MN, BM>(st + X_HI, st + X_LO, &tmXhi, &tmXlo, x_raw, x0, kx, zx, fb);
+                    load_operand<Y_MN, BN>(st + Y_HI, st + Y_LO, &tmYhi, &tmYlo, y_raw, y0, kx, zy, fb);
                 }
             }
             if (*abort_flag) {
@@ -513,7 +580,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_tf32_f32<BM, BN>();
+            constexpr uint32_t idesc = tc::idesc_tf32_f32<BM, BN, X_MN, Y_MN>();
             int tile, k0, nk, g = 0, cg = 0;   // g: slabs consumed, cg: chunks started
             bool stop = false;
             for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
@@ -531,7 +598,8 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                     break;
                 }
                 const int s = g % STAGES;
-                if (!mbar_wait(bar_full + 8 * s, (g / STAGES) & 1, kStatusMma)) {
+                const uint32_t ph = (g / STAGES) & 1;
+                if (!mbar_wait(bar_full + 8 * s, ph, kStatusMma)) {
                     *abort_flag = 1;
                     stop = true;
                     break;
@@ -539,52 +607,34 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                 tc::fence_after_sync();
                 const uint32_t st = stage0 + s * STAGE_BYTES;
                 const uint32_t d = tmem + (uint32_t)(b * BN);
-                if constexpr (!A_IN) {
+                // hi x hi needs only what TMA loaded; each product with a lo
+                // part of a raw operand waits for the splitters to write it
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint32_t off = kk * UMMA_K * 4;   // 32 bytes along the 64-byte row
-                        const uint64_t a_hi = tc::desc_kmajor_sw64(st + off);
-                        const uint64_t a_lo = tc::desc_kmajor_sw64(st + A_TILE + off);
-                        const uint64_t b_hi = tc::desc_kmajor_sw64(st + 2 * A_TILE + off);
-                        const uint64_t b_lo = tc::desc_kmajor_sw64(st + 2 * A_TILE + B_TILE + off);
-                        tc::mma_tf32(d, a_hi, b_hi, idesc, (chunk_first && kk == 0) ? 0u : 1u);
-                        tc::mma_tf32(d, a_hi, b_lo, idesc, 1u);
-                        tc::mma_tf32(d, a_lo, b_hi, idesc, 1u);
-                    }
-                } else {
-                    // A's hi slot holds raw A (read as hi = A with its low 13
-                    // bits dropped): the two products without A's lo go first,
-                    // the third once the splitters have written A's lo
-#pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint32_t off = kk * UMMA_K * 4;
-                        const uint64_t a_hi = tc::desc_kmajor_sw64(st + off);
-                        const uint64_t a_lo = tc::desc_kmajor_sw64(st + A_TILE + off);
-                        const uint64_t b_hi = tc::desc_kmajor_sw64(st + 2 * A_TILE + off);
-                        const uint64_t b_lo = tc::desc_kmajor_sw64(st + 2 * A_TILE + B_TILE + off);
-                        tc::mma_tf32(d, a_hi, b_hi, idesc, (chunk_first && kk == 0) ? 0u : 1u);
-                        if (TRANS)
-                            tc::mma_tf32(d, a_lo, b_hi, idesc, 1u);   // B^T lo x raw A
-                        else
-                            tc::mma_tf32(d, a_hi, b_lo, idesc, 1u);   // raw A x B^T lo
-                    }
-                    if (!mbar_wait(bar_conv + 8 * s, (g / STAGES) & 1, kStatusMma)) {
+                for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                    tc::mma_tf32(d, operand_desc<X_MN>(st + X_HI, kk), operand_desc<Y_MN>(st + Y_HI, kk), idesc,
+                                 (chunk_first && kk == 0) ? 0u : 1u);
+                if (x_raw) {
+                    if (!mbar_wait(bar_conv_x + 8 * s, ph, kStatusMma)) {
                         *abort_flag = 1;
                         stop = true;
                         break;
                     }
                     tc::fence_after_sync();
-#pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint32_t off = kk * UMMA_K * 4;
-                        if (TRANS)   // B^T hi x A lo
-                            tc::mma_tf32(d, tc::desc_kmajor_sw64(st + off),
-                                         tc::desc_kmajor_sw64(st + 2 * A_TILE + B_TILE + off), idesc, 1u);
-                        else         // A lo x B^T hi
-                            tc::mma_tf32(d, tc::desc_kmajor_sw64(st + A_TILE + off),
-                                         tc::desc_kmajor_sw64(st + 2 * A_TILE + off), idesc, 1u);
-                    }
                 }
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                    tc::mma_tf32(d, operand_desc<X_MN>(st + X_LO, kk), operand_desc<Y_MN>(st + Y_HI, kk), idesc, 1u);
+                if (y_raw) {
+                    if (!mbar_wait(bar_conv_y + 8 * s, ph, kStatusMma)) {
+                        *abort_flag = 1;
+                        stop = true;
+                        break;
+                    }
+                    tc::fence_after_sync();
+                }
+#pragma unroll
+                for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                    tc::mma_tf32(d, operand_desc<X_MN>(st + X_HI, kk), operand_desc<Y_MN>(st + Y_LO, kk), idesc, 1u);
                 tc::commit(bar_empty + 8 * s);
                 if (chunk_last) {
                     tc::commit(bar_tfull + 8 * b);
@@ -597,8 +647,8 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
             mbar_wait(bar_done, 0, kStatusDrain);
         }
         __syncwarp();
-    } else if (A_IN && warp >= 2 + ACC_WARPS) {
-        // ------------------------------------------------------------ A splitters (warps 10, 11)
+    } else if (warp >= 2 + ACC_WARPS) {
+        // ------------------------------------------------------------ splitters (warps 10, 11)
         // 128-wide tiles give the tensor core ~400 cycles per slab, less
         // than one slab's split takes end to end, so there each warp splits
         // whole slabs, alternating (two in flight); 256-wide tiles leave
@@ -607,7 +657,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
         const int ct = CONV_PER_WARP ? lane : (int)threadIdx.x - (64 + ACC_THREADS);
         const int mine = CONV_PER_WARP ? warp - (2 + ACC_WARPS) : 0;
         int tile, k0, nk, g = 0;   // g: slab sequence position (ring position)
-        bool stop = false;
+        bool stop = !x_raw && !y_raw;   // nothing to split: both operands come split
         for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
           for (int kt = 0; kt < nk; ++kt, ++g) {
             if (CONV_PER_WARP && (g % CONV_WARPS) != mine) continue;
@@ -621,20 +671,22 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                 stop = true;
                 break;
             }
-            // the raw slab stays as A's hi (the MMA reads it as hi = x with
-            // its low 13 bits dropped); lo = tf32(x - hi) goes into A's lo
-            // slot at the same swizzled position (the split is elementwise)
-            const float4 *raw = reinterpret_cast<const float4 *>(smem + s * STAGE_BYTES + SPLIT_OFF);
-            float4 *lo = reinterpret_cast<float4 *>(smem + s * STAGE_BYTES + SPLIT_OFF + SPLIT_BYTES);
-            float4 x[SPLIT_BYTES / 16 / CW];
-#pragma unroll
-            for (int j = 0; j < SPLIT_BYTES / 16 / CW; ++j) x[j] = raw[ct + j * CW];
-#pragma unroll
-            for (int j = 0; j < SPLIT_BYTES / 16 / CW; ++j)
-                lo[ct + j * CW] = make_float4(lo_of_raw(x[j].x), lo_of_raw(x[j].y), lo_of_raw(x[j].z),
-                                              lo_of_raw(x[j].w));
-            tc::fence_proxy_async_smem();
-            mbar_arrive(bar_conv + 8 * s);
+            // the raw slab stays as the operand's hi part (the MMA reads it
+            // as hi = x with its low 13 bits dropped); lo = tf32(x - hi) goes
+            // into the lo slot at the same position (the split is elementwise,
+            // so the swizzled layout does not matter); X first, whose lo the
+            // MMA needs first
+            uint8_t *const st = smem + s * STAGE_BYTES;
+            if (x_raw) {
+                split_slot_lo<X_TILE, CW>(st + X_HI, st + X_LO, ct);
+                tc::fence_proxy_async_smem();
+                mbar_arrive(bar_conv_x + 8 * s);
+            }
+            if (y_raw) {
+                split_slot_lo<Y_TILE, CW>(st + Y_HI, st + Y_LO, ct);
+                tc::fence_proxy_async_smem();
+                mbar_arrive(bar_conv_y + 8 * s);
+            }
           }
         }
     } else {
@@ -682,7 +734,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
         // chunk-wise reads both touch every bank once per 128 bytes.
         auto c_at = [&](int row, int col) -> float4 {
             const float *crow = Cb + (long long)row * p.ldc;
-            if (C_VEC && col + 3 < p.n) return *reinterpret_cast<const float4 *>(crow + col);
+            if (c_vec && col + 3 < p.n) return *reinterpret_cast<const float4 *>(crow + col);
             float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
@@ -695,7 +747,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                                                        fmaf(alpha, v.z, beta * c.z), fmaf(alpha, v.w, beta * c.w))
                                          : make_float4(alpha * v.x, alpha * v.y, alpha * v.z, alpha * v.w);
             float *crow = Cb + (long long)row * p.ldc;
-            if (C_VEC && col + 3 < p.n) {
+            if (c_vec && col + 3 < p.n) {
                 *reinterpret_cast<float4 *>(crow + col) = o;
             } else {
                 const float a[4] = {o.x, o.y, o.z, o.w};
@@ -928,7 +980,7 @@ __global__ void __launch_bounds__(threads_for(A_IN), 1)
                 }
                 if (row >= p.m) continue;
                 float *crow = Cb + (long long)row * p.ldc;
-                if (C_VEC && col + 3 < p.n) {
+                if (c_vec && col + 3 < p.n) {
                     float4 o;
                     if (beta != 0.f) {
                         const float4 c = *reinterpret_cast<const float4 *>(crow + col);

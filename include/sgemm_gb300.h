@@ -24,16 +24,25 @@
  *
  * Ownership.  A, B and C are device pointers owned by the caller (any memory
  * the current device can address).  The library keeps no pointer after the
- * call returns.  Per device it lazily caches kernel attributes.  The FFMA
- * path allocates nothing; the tensor-core path takes its split operands
- * (8 * (m + n) * ka bytes, ka = k rounded up to 4; 8 * n * ka when the GEMM
- * splits A itself) for the duration of the call from a stream-ordered
- * memory pool that the library creates per device on first use
- * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`).  The pool keeps up
- * to 2 GiB mapped between calls (environment variable
- * SGEMM_GB300_POOL_KEEP_MB overrides it, read once per device), so repeated
- * calls do not map and unmap device memory; it is released when the process
- * exits.  C must not overlap A or B.
+ * call returns.  Per device it lazily caches kernel attributes and its
+ * cluster capacity.  The FFMA path allocates nothing.  The tensor-core GEMM
+ * reads an operand as stored (by TMA) and splits it into TF32 parts itself
+ * when the operand's base is 16-byte aligned and its rows are 16 bytes
+ * apart (lda, ldb multiples of 4; in a batch also a stride of 0 or of whole
+ * non-overlapping matrices, a multiple of 4) -- always for A, and for B
+ * when m*n*k <= 2^31 (larger problems split B with a separate pass, which
+ * is faster there).  Only the other operands, and stream-K's partial tiles
+ * (plans with sgemm_plan.stream_k > 0), take scratch: 8 * rows * ka bytes
+ * per split operand (ka = k rounded up to 4) and 2 * stream_k tiles of
+ * 128 * bn floats, for the duration of the call, from a stream-ordered
+ * memory pool the library creates per device on first use
+ * (cudaMallocFromPoolAsync / cudaFreeAsync on `stream`).  A call that needs
+ * no scratch allocates nothing.  The pool keeps up to 2 GiB mapped between
+ * calls (environment variable SGEMM_GB300_POOL_KEEP_MB overrides it, read
+ * once per device), so repeated calls do not map and unmap device memory;
+ * it is released when the process exits.  sgemm_plan_for() tells which
+ * case a problem is (a_in_kernel, b_in_kernel, stream_k).  C must not
+ * overlap A or B.
  *
  * Execution.  Every entry point that takes a stream enqueues its kernels on
  * `stream` (0 = the legacy default stream) of the current device and returns
@@ -66,7 +75,12 @@
  *     SGEMM_STATUS_CUDA_ERROR  a CUDA runtime call or launch failed; the CUDA
  *                            error code is kept per thread and returned by
  *                            sgemm_last_cuda_error().
- * On any non-zero status nothing has been enqueued.
+ * Argument errors, a failed scratch allocation and a failed tensor-map
+ * encoding return before anything is enqueued.  A launch that fails
+ * (status SGEMM_STATUS_CUDA_ERROR from the launch itself) may leave earlier
+ * kernels of the same call enqueued; sgemm_strided_batched with more than
+ * 65535 problems runs one chunk of 65535 after another and stops at the
+ * first chunk that fails.
  */
 #ifndef SGEMM_GB300_H
 #define SGEMM_GB300_H
@@ -276,11 +290,11 @@ typedef struct sgemm_plan {
     int split_k;       /* CTAs sharing one tile along k (a thread-block cluster; 1 = no split) */
     int op_a, op_b;    /* SGEMM_OP_N / SGEMM_OP_T of the problem planned                      */
     int a_vec;         /* 1: A (stored k x m) loaded 16 bytes at a time (FFMA path)            */
-    int a_in_kernel;   /* 1: the tensor-core GEMM splits A itself (no split pass over A)       */
+    int a_in_kernel;   /* 1: the tensor-core GEMM reads A as stored (TMA) and splits it itself */
     int trans;         /* 1: tensor-core tiles of C^T = B^T A^T (n <= 128; bm = 256, bn = 128) */
     int stream_k;      /* > 0: stream-K over this many CTAs (grid); each takes an equal share  */
                        /*      of all tiles' k slabs, partial tiles meet in a workspace        */
-    int a_lo_only;     /* 1: the split pass writes only A's lo part; the GEMM reads hi from A  */
+    int b_in_kernel;   /* 1: the same for B (no split pass, no scratch for that operand)       */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

@@ -208,38 +208,45 @@ def test_stream_k_policy(monkeypatch):
 
 
 def test_in_kernel_split_policy(monkeypatch):
-    """The tensor-core GEMM splits A itself (12 warps) when it can load A by
-    TMA -- untransposed, 16-byte aligned rows, one problem -- and n <= 4096;
-    otherwise a pre-pass splits A and the kernel runs 10 warps.  The tuning
-    variable pins the choice but cannot make an unaligned A eligible."""
-    monkeypatch.delenv("SGEMM_GB300_SPLIT_A_IN", raising=False)
+    """The tensor-core GEMM reads an operand as stored and splits it itself
+    when TMA can load it -- a 16-byte aligned base, rows a multiple of 16
+    bytes and, in a batch, a stride of 0 or of whole non-overlapping matrices
+    16 bytes apart; otherwise a split pass writes that operand's hi and lo
+    parts into scratch.  A is read as stored whenever it can be; B (whose
+    split costs the GEMM more per slab) only for m*n*k <= 2^31.  The tuning
+    variables pin the choice but cannot make an unaligned operand eligible.
+    Every tensor-core plan runs 12 warps."""
+    for v in ("SGEMM_GB300_SPLIT_A_IN", "SGEMM_GB300_SPLIT_B_IN"):
+        monkeypatch.delenv(v, raising=False)
     TC = binding.PATH_TF32X3
 
-    def ain(m, n, k, **kw):
+    def raw(m, n, k, **kw):
         st, p = hplan(m, n, k, path=TC, **kw)
         assert st == 0
-        assert p["threads"] == (384 if p["a_in_kernel"] else 320)
-        return p["a_in_kernel"]
+        assert p["threads"] == 384
+        return p["a_in_kernel"], p["b_in_kernel"]
 
-    assert ain(16384, 128, 8192) == 1
-    assert ain(8192, 4096, 8192) == 1
-    assert ain(8192, 4097, 8192) == 0
-    assert ain(8192, 8192, 8192) == 0
-    assert ain(1000, 1500, 777) == 0                 # lda = 777: rows not 16-byte aligned
-    assert ain(1000, 1500, 777, lda=780) == 1
-    assert ain(1000, 1500, 780, A_ptr=20) == 0       # A not 16-byte aligned
-    # n > 4096: a split pass, which writes only A's lo part when TMA can read A
-    st, p = hplan(8192, 8192, 8192, path=TC)
-    assert (p["a_in_kernel"], p["a_lo_only"]) == (0, 1)
-    st, p = hplan(8192, 8192, 8190, path=TC)  # lda = 8190: rows not 16-byte aligned
-    assert (p["a_in_kernel"], p["a_lo_only"]) == (0, 0)
-    st, p = hplan(2048, 2048, 2048, path=TC)
-    assert (p["a_in_kernel"], p["a_lo_only"]) == (1, 0)
+    assert raw(16384, 128, 8192) == (1, 0)
+    assert raw(8192, 8192, 8192) == (1, 0)
+    assert raw(2048, 2048, 2048) == (1, 0)
+    assert raw(1024, 1024, 2048) == (1, 1)                # 2^31 multiply-adds
+    assert raw(1024, 1024, 2049, lda=2052) == (1, 0)      # one k more
+    assert raw(256, 256, 256) == (1, 1)
+    assert raw(1000, 1500, 777) == (0, 1)                 # lda = 777: A's rows not 16-byte aligned
+    assert raw(1000, 1500, 777, lda=780) == (1, 1)
+    assert raw(1000, 1500, 780, A_ptr=20) == (0, 1)       # A not 16-byte aligned
+    assert raw(1000, 1500, 780, B_ptr=24) == (1, 0)       # B not 16-byte aligned
+    assert raw(1000, 1498, 780) == (1, 0)                 # ldb = 1498: B's rows not 16-byte aligned
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "1")
+    assert raw(16384, 128, 8192) == (1, 1)
+    assert raw(1000, 1498, 780) == (1, 0)
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "0")
-    assert ain(16384, 128, 8192) == 0
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "0")
+    assert raw(256, 256, 256) == (0, 0)
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "1")
-    assert ain(8192, 8192, 8192) == 1
-    assert ain(1000, 1500, 777) == 0
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "1")
+    assert raw(8192, 8192, 8192) == (1, 1)
+    assert raw(1000, 1500, 777) == (0, 1)
 
 
 def test_op_argument_checks():

@@ -105,13 +105,13 @@ def test_traffic_record_matches_size_and_sources(tmp_path, monkeypatch):
     and only while the kernel's sources are unchanged."""
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     (tmp_path / "profiles").mkdir()
-    h = bench.kernel_source_hash("tf32x3_a_in")
-    recs = {"tf32x3_a_in": [{"units": 10, "source_hash": h, "dram_bytes_per_launch": 111},
+    h = bench.kernel_source_hash("tf32x3_raw_ab")
+    recs = {"tf32x3_raw_ab": [{"units": 10, "source_hash": h, "dram_bytes_per_launch": 111},
                             {"units": 20, "source_hash": "stale", "dram_bytes_per_launch": 222}],
             "ffma": {"units": 30, "source_hash": bench.kernel_source_hash("ffma"), "dram_bytes_per_launch": 333}}
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(recs))
-    assert bench.traffic_record("tf32x3_a_in", 10) == 111
-    assert bench.traffic_record("tf32x3_a_in", 20) is None      # sources changed since the capture
-    assert bench.traffic_record("tf32x3_a_in", 30) is None      # never captured at this size
+    assert bench.traffic_record("tf32x3_raw_ab", 10) == 111
+    assert bench.traffic_record("tf32x3_raw_ab", 20) is None      # sources changed since the capture
+    assert bench.traffic_record("tf32x3_raw_ab", 30) is None      # never captured at this size
     assert bench.traffic_record("ffma", 30) == 333              # single-record form
-    assert bench.traffic_record("tf32x3", 10) is None
+    assert bench.traffic_record("tf32x3_presplit", 10) is None

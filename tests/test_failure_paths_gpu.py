@@ -45,7 +45,10 @@ def test_bounded_wait_runs_out_and_is_reported():
 
 
 def test_forced_allocation_failure(monkeypatch):
-    p = inputs.make_problem(512, 384, 256, alpha=1.0, beta=0.5, seed=11, a="uniform", b="uniform", c="uniform")
+    # lda = 257: A's rows are not 16-byte aligned, so the tensor-core call
+    # splits A into scratch from the pool -- the allocation the fake fails
+    p = inputs.make_problem(512, 384, 256, alpha=1.0, beta=0.5, seed=11, a="uniform", b="uniform", c="uniform",
+                            lda=257)
     A = torch.from_numpy(p.A).cuda()
     B = torch.from_numpy(p.B).cuda()
     C = torch.from_numpy(p.C0).cuda()
@@ -55,18 +58,37 @@ def test_forced_allocation_failure(monkeypatch):
                            p.ldc, torch.cuda.current_stream().cuda_stream, binding.PATH_TF32X3)
     assert st == 100 and binding.last_cuda_error() == CUDA_ERROR_MEMORY_ALLOCATION
     with pytest.raises(binding.SgemmError) as err:
-        binding.sgemm_ex(A, B, C, p.alpha, p.beta, path=binding.PATH_TF32X3)
+        binding.sgemm_ex(A[:, :p.k], B, C, p.alpha, p.beta, path=binding.PATH_TF32X3)
     assert err.value.status == 100
     torch.cuda.synchronize()
     assert torch.equal(C, C0), "C was written although the call failed before launching"
     # the FFMA path allocates nothing and is unaffected
-    binding.sgemm_ex(A, B, C, p.alpha, p.beta, path=binding.PATH_FFMA)
+    binding.sgemm_ex(A[:, :p.k], B, C, p.alpha, p.beta, path=binding.PATH_FFMA)
     R, E, _ = oracle.problem_f64(p)
     ok, worst, _ = oracle.within_tolerance(C.cpu().numpy(), R, E, p.beta, p.C0)
     assert ok, worst
     monkeypatch.delenv("SGEMM_GB300_FAIL_ALLOC")
     C.copy_(C0)
+    binding.sgemm_ex(A[:, :p.k], B, C, p.alpha, p.beta, path=binding.PATH_TF32X3)
+    ok, worst, _ = oracle.within_tolerance(C.cpu().numpy(), R, E, p.beta, p.C0)
+    assert ok, worst
+    assert binding.device_status() == 0
+
+
+def test_aligned_tensor_core_call_allocates_nothing(monkeypatch):
+    """With 16-byte rows the tensor-core GEMM reads A and B as stored and the
+    call takes no scratch: it succeeds while every pool allocation is made to
+    fail, and matches the oracle."""
+    p = inputs.make_problem(1024, 512, 768, alpha=1.5, beta=0.5, seed=12, a="normal", b="uniform", c="uniform")
+    st, plan = binding.plan(p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc,
+                            path=binding.PATH_TF32X3)
+    assert st == 0 and plan["a_in_kernel"] == 1 and plan["b_in_kernel"] == 1 and plan["stream_k"] == 0, plan
+    A = torch.from_numpy(p.A).cuda()
+    B = torch.from_numpy(p.B).cuda()
+    C = torch.from_numpy(p.C0).cuda()
+    monkeypatch.setenv("SGEMM_GB300_FAIL_ALLOC", "1")
     binding.sgemm_ex(A, B, C, p.alpha, p.beta, path=binding.PATH_TF32X3)
+    R, E, _ = oracle.problem_f64(p)
     ok, worst, _ = oracle.within_tolerance(C.cpu().numpy(), R, E, p.beta, p.C0)
     assert ok, worst
     assert binding.device_status() == 0

@@ -210,11 +210,14 @@ def test_stream_ordering():
 
 # ---------------------------------------------------------------- 3xTF32 split operands
 
-def test_tf32x3_split_operands():
+def test_tf32x3_split_operands(monkeypatch):
     """The split calls produce hi = TF32(x) (low 13 mantissa bits zero),
     lo = TF32(x - hi), with |x - hi - lo| <= 2^-22 |x| and |lo| <= 2^-11 |x|;
     B comes out transposed; the split GEMM equals the one-call path bit for
-    bit (same kernels, same operands)."""
+    bit when that path splits both operands with the split pass too (same
+    kernels, same operands)."""
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "0")
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "0")
     p = inputs.make_problem(300, 260, 150, alpha=1.25, beta=0.5, seed=31, a="normal", b="uniform", c="uniform")
     ka = binding.ka_of(p.k)
     A = torch.from_numpy(p.A).cuda()

@@ -1,10 +1,13 @@
-"""GPU parity of the tensor-core path with A split inside the GEMM kernel
-(raw FP32 A loaded by TMA and read as its own hi part, lo computed in
-shared memory) and with A split by the separate pre-pass, each pinned
-through the library's tuning variable SGEMM_GB300_SPLIT_A_IN and checked
-against the FP64 oracle:
-ragged tiles, k tails that are not a multiple of the 16-deep slab, split-K
-clusters, beta != 0, padded lda, and bit-exact integer twins."""
+"""GPU parity of the tensor-core path with each operand split inside the
+GEMM kernel (the raw FP32 operand loaded by TMA as stored -- A K-major, B
+MN-major -- and read as its own hi part, lo computed in shared memory) or
+by the separate split pass, pinned through the library's tuning variables
+SGEMM_GB300_SPLIT_A_IN / SGEMM_GB300_SPLIT_B_IN and checked against the FP64
+oracle: ragged tiles, k tails that are not a multiple of the 16-deep slab,
+split-K clusters, beta != 0, padded leading dimensions, and bit-exact
+integer twins.  Also the property the in-kernel split rests on: the tensor
+core reads an FP32 operand, K-major or MN-major, with its low 13 mantissa
+bits dropped."""
 import pytest
 import torch
 
@@ -21,10 +24,21 @@ def _gpu():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-@pytest.fixture(params=["1", "0"], ids=["in_kernel", "pre_pass"])
-def a_split(request, monkeypatch):
-    monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", request.param)
-    return request.param == "1"
+@pytest.fixture(params=[("1", "1"), ("1", "0"), ("0", "1"), ("0", "0")],
+                ids=["both_in_kernel", "a_in_kernel", "b_in_kernel", "pre_pass"])
+def split(request, monkeypatch):
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", request.param[0])
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", request.param[1])
+    return request.param[0] == "1", request.param[1] == "1"
+
+
+def _expect_plan(p, split):
+    """The requested in-kernel splits, where TMA can read the operand (its
+    rows 16-byte aligned; the guarded buffers start 16-byte aligned)."""
+    plan = _plan(p)
+    assert plan["a_in_kernel"] == int(split[0] and p.lda % 4 == 0), plan
+    assert plan["b_in_kernel"] == int(split[1] and p.ldb % 4 == 0), plan
+    assert plan["threads"] == 384, plan
 
 
 def _run(p, exact=False):
@@ -53,31 +67,36 @@ def _plan(p):
     (640, 1024, 2048, None, 2.0),    # wide tiles
     (128, 128, 4, None, 0.0),        # one slab, k = 4
 ])
-def test_in_kernel_and_pre_pass_split_match_oracle(a_split, m, n, k, lda, beta):
+def test_in_kernel_and_pre_pass_split_match_oracle(split, m, n, k, lda, beta):
     p = inputs.make_problem(m, n, k, alpha=1.25, beta=beta, seed=m * 7 + n + k, a="normal", b="uniform",
                             c="uniform" if beta else None, lda=lda)
-    plan = _plan(p)
-    assert plan["a_in_kernel"] == int(a_split), plan
-    assert plan["threads"] == (384 if a_split else 320), plan
+    _expect_plan(p, split)
     _run(p)
 
 
 @pytest.mark.parametrize("m,n,k", [(1000, 300, 777), (129, 257, 4096), (512, 512, 2048)])
-def test_in_kernel_split_integer_twin_bit_exact(a_split, m, n, k):
+def test_in_kernel_split_integer_twin_bit_exact(split, m, n, k):
     """hi(x) = x and lo(x) = 0 for small integers, so every product and
-    partial sum is exact whichever side splits A."""
+    partial sum is exact whichever side splits A and B."""
     lda = (k + 3) // 4 * 4
-    p = inputs.make_problem(m, n, k, alpha=2.0, beta=0.5, seed=3 * k + n, a="int", b="int", c="int", lda=lda)
-    assert _plan(p)["a_in_kernel"] == int(a_split)
+    ldb = (n + 3) // 4 * 4
+    p = inputs.make_problem(m, n, k, alpha=2.0, beta=0.5, seed=3 * k + n, a="int", b="int", c="int", lda=lda,
+                            ldb=ldb)
+    _expect_plan(p, split)
     _run(p, exact=True)
 
 
-def test_unaligned_lda_falls_back_to_pre_pass(monkeypatch):
-    """TMA needs 16-byte rows: with lda % 4 != 0 A is split by the pre-pass
-    even when the in-kernel split is requested."""
+def test_unaligned_rows_fall_back_to_pre_pass(monkeypatch):
+    """TMA needs 16-byte rows: with lda % 4 != 0 (or ldb % 4 != 0) that
+    operand is split by the split pass even when the in-kernel split is
+    requested; the other one is still read as stored."""
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "1")
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "1")
     p = inputs.make_problem(300, 200, 777, alpha=1.0, beta=0.0, seed=5, a="normal", b="normal")
-    assert p.lda == 777 and _plan(p)["a_in_kernel"] == 0
+    assert p.lda == 777 and (_plan(p)["a_in_kernel"], _plan(p)["b_in_kernel"]) == (0, 1)
+    _run(p)
+    p = inputs.make_problem(300, 203, 776, alpha=1.0, beta=0.0, seed=6, a="normal", b="normal")
+    assert p.ldb == 203 and (_plan(p)["a_in_kernel"], _plan(p)["b_in_kernel"]) == (1, 0)
     _run(p)
 
 
@@ -86,6 +105,7 @@ def test_in_kernel_split_is_deterministic(monkeypatch):
     fixed); the in-kernel and pre-pass splits differ only in how hi is
     rounded, both within the bound."""
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "1")
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "1")
     p = inputs.make_problem(700, 384, 1500, alpha=1.0, beta=0.0, seed=11, a="normal", b="normal", lda=1500)
     A = torch.from_numpy(p.A).cuda()
     B = torch.from_numpy(p.B).cuda()
@@ -122,3 +142,61 @@ def test_tensor_core_reads_fp32_operands_truncated_to_tf32():
     torch.cuda.synchronize()
     truncated = (X.view(np.uint32) & ~np.uint32(0x1FFF)).view(np.float32)
     assert np.array_equal(C.cpu().numpy(), truncated)
+
+
+def _hi_plus_lo(X):
+    """What the GEMM makes of a raw operand value x: hi = x with its low 13
+    mantissa bits dropped (how the MMA reads FP32), lo = x - hi rounded to
+    TF32 to nearest, ties away from zero (exact in FP32 arithmetic), and
+    their sum, exact in FP32 (hi has 11 significant bits, lo at most 11
+    more, 11 or more binary places below)."""
+    import numpy as np
+    bits = X.view(np.uint32)
+    hi = (bits & ~np.uint32(0x1FFF)).view(np.float32)
+    r = (X - hi).astype(np.float32)
+    rb = r.view(np.uint32)
+    lo = ((rb + np.uint32(0x1000)) & ~np.uint32(0x1FFF)).view(np.float32)   # |r| < 2^-10 |x|: no overflow
+    return (hi.astype(np.float64) + lo.astype(np.float64)).astype(np.float32)
+
+
+def _boundary_values(rows, cols, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((rows, cols)).astype(np.float32)
+    bits = X.view(np.uint32)
+    pats = np.array([0x1000, 0x0FFF, 0x1001, 0x1FFF, 1, 0, 0x17FF, 0x0800], np.uint32)
+    bits[:, :8] = (bits[:, :8] & ~np.uint32(0x1FFF)) | pats
+    return X
+
+
+@pytest.mark.parametrize("op_a,op_b", [(0, 0), (0, 1), (1, 0)], ids=["B_mn_major", "B_k_major", "A_mn_major"])
+def test_raw_operands_read_as_truncated_hi_plus_lo(monkeypatch, op_a, op_b):
+    """With the identity as the other operand, every output is a single
+    product: C = X exactly as the GEMM splits a raw X, hi = trunc(x) plus
+    lo = tf32(x - hi), for X read MN-major (B stored k x n, or A stored
+    k x m) or K-major (B stored n x k); values on the rounding boundaries
+    included.  A tensor core that rounded an MN-major FP32 operand instead
+    of truncating it would miss by up to 2^-11 |x|."""
+    import numpy as np
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "1")
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "1")
+    n = k = m = 256
+    X = _boundary_values(256, 256, 7 + op_a + 2 * op_b)
+    eye = np.eye(256, dtype=np.float32)
+    if op_a == 0:
+        # C = I * op(B): op(B) = X, stored as X (k x n) or as X^T (n x k)
+        A, B, want = eye, (X if op_b == 0 else np.ascontiguousarray(X.T)), _hi_plus_lo(X)
+    else:
+        # C = op(A) * I with op(A) = X stored as X^T (k x m)
+        A, B, want = np.ascontiguousarray(X.T), eye, _hi_plus_lo(X)
+    st, plan = binding.plan(m, n, k, 1.0, 256, 256, 256, 256, 0.0, 256, 256, path=TC)
+    assert st == 0 and plan["a_in_kernel"] == 1 and plan["b_in_kernel"] == 1
+    Ad = torch.from_numpy(A).cuda()
+    Bd = torch.from_numpy(B).cuda()
+    C = torch.zeros(m, n, device="cuda")
+    st = binding.sgemm_op_raw(op_a, op_b, m, n, k, 1.0, Ad.data_ptr(), 256, Bd.data_ptr(), 256, 0.0, C.data_ptr(),
+                              n, torch.cuda.current_stream().cuda_stream, TC)
+    assert st == 0, binding.status_string(st)
+    torch.cuda.synchronize()
+    got = C.cpu().numpy()
+    assert np.array_equal(got, want), np.argwhere(got != want)[:5]

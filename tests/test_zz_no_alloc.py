@@ -1,15 +1,24 @@
 """The allocation-free tensor-core entry point, sgemm_tf32x3_noalloc.
 
-Some callers must not allocate device memory while they run (allocator
-callbacks, out-of-memory handlers, processes that reserve all device memory
-up front, latency-critical loops that cannot risk cudaMalloc's
-synchronisation or failure).  For them the library offers one entry point
-whose scratch is a fixed 64 MiB device array instead of the stream-ordered
-pool.  These tests call it through the C ABI and hold its output to the
-same bound as every other parity test, against the regular entry point
-(sgemm_ex with the tensor-core path) on the same inputs -- twice in a row,
-the second time on a smaller problem, so that whatever the first call left
-in the shared array must not leak into the second result.
+Some callers must not allocate device memory while they run: code inside an
+allocator callback or an out-of-memory handler (an allocation there can
+recurse or deadlock on the allocator's own lock), processes that reserve all
+of their device memory up front and leave none to a library, and
+latency-critical loops that cannot risk cudaMalloc's implicit
+synchronisation or its failure under memory pressure.  The regular entry
+point takes scratch from a stream-ordered pool when an operand cannot be
+read by TMA as stored (rows not 16 bytes apart, a misaligned base) or when
+its plan uses stream-K; this entry point instead puts the split operands in
+one fixed 64 MiB device array and plans without stream-K.
+
+These tests call it through the C ABI and hold its output to the FP64
+oracle within the bound every parity test uses, twice in a row (the second
+time on a smaller problem, so that whatever the first call left in the
+shared array must not leak into the second result), with the regular entry
+point's result as a second reference.  They also check the property the
+entry point exists for: with every pool allocation made to fail, it still
+succeeds while the regular entry point on the same problem reports the
+failed allocation.
 
 This file is collected last on purpose: if it fails, a run that stops at
 the first failure has already run every other test.
@@ -28,47 +37,95 @@ def _device(arr):
     return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
 
 
+def _noalloc(p, A, B, C, stream):
+    return binding.tf32x3_noalloc_raw(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                                      C.data_ptr(), p.ldc, stream)
+
+
+def _regular(p, A, B, C, stream):
+    return binding.sgemm_raw(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
+                             C.data_ptr(), p.ldc, stream, binding.PATH_TF32X3)
+
+
+def _check_oracle(p, got):
+    R, E, _ = oracle.problem_f64(p)
+    ok, worst, where = oracle.within_tolerance(got, R, E, p.beta, p.C0[:, :p.n])
+    assert ok, f"|C - r| / tol = {worst} at {where}"
+    return R, E
+
+
+# (m, n, k, seed, lda pad): odd pads make A's rows misaligned (A split into
+# the fixed scratch), even ones leave A readable as stored
 @pytest.mark.parametrize("shapes", [
-    [(1000, 1500, 777, 2), (300, 200, 150, 3)],
-    [(2048, 2048, 2048, 5), (129, 257, 1000, 6)],
+    [(1000, 1500, 777, 2, 0), (300, 200, 150, 3, 1)],
+    [(2048, 2048, 2048, 5, 1), (129, 257, 1000, 6, 0)],
 ])
-def test_noalloc_matches_regular_entry_point_twice(shapes, monkeypatch):
-    # the no-allocation entry point splits A with the pre-pass and runs
-    # without stream-K (no workspace); the regular call is pinned to the
-    # same (it may otherwise split A inside the GEMM, which rounds hi
-    # differently, or add stream-K partial tiles in another order) so both
-    # run the same kernels
-    monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "0")
+def test_noalloc_matches_oracle_twice(shapes, monkeypatch):
+    # the regular call is planned without stream-K, as this entry point is,
+    # so that both run the same kernels
     monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
     stream = torch.cuda.current_stream().cuda_stream
-    for m, n, k, seed in shapes:
+    for m, n, k, seed, pad in shapes:
         p = inputs.make_problem(m, n, k, alpha=1.5, beta=0.5, seed=seed, a="normal", b="uniform", c="uniform",
-                                lda=k + (1 if seed % 2 else 0))
+                                lda=k + pad)
         A, B = _device(p.A), _device(p.B)
-        C_ref, C_na = _device(p.C0), _device(p.C0)
-        st = binding.sgemm_raw(m, n, k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
-                               C_ref.data_ptr(), p.ldc, stream, binding.PATH_TF32X3)
+        C_na, C_ref = _device(p.C0), _device(p.C0)
+        st = _noalloc(p, A, B, C_na, stream)
         assert st == 0, binding.status_string(st)
-        st = binding.tf32x3_noalloc_raw(m, n, k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta,
-                                        C_na.data_ptr(), p.ldc, stream)
+        st = _regular(p, A, B, C_ref, stream)
         assert st == 0, binding.status_string(st)
         torch.cuda.synchronize()
-        ref = C_ref.cpu().numpy()[:, :n].astype(np.float64)
-        got = C_na.cpu().numpy()[:, :n].astype(np.float64)
-        # the bound of every parity test, with the regular entry point's result
-        # standing in for r; E from the oracle's error scale
-        _, E, _ = oracle.problem_f64(p)
-        bound = oracle.tolerance(E, p.beta, p.C0[:, :n])
+        got = C_na.cpu().numpy()[:, :p.n]
         assert np.all(np.isfinite(got))
-        assert np.all(np.abs(got - ref) <= bound)
-        # same kernels on the same operands: in practice bit-identical
-        assert np.array_equal(got, ref)
+        R, E = _check_oracle(p, got)
+        # the regular entry point's result, within the same bound of it
+        ref = C_ref.cpu().numpy()[:, :p.n].astype(np.float64)
+        assert np.all(np.abs(got - ref) <= oracle.tolerance(E, p.beta, p.C0[:, :p.n]))
+
+
+def test_noalloc_needs_no_allocation(monkeypatch):
+    """With SGEMM_GB300_FAIL_ALLOC set every pool allocation of the library
+    reports out-of-memory.  On a problem whose A must be split into scratch
+    (lda = 777: rows not 16 bytes apart) the regular entry point then fails
+    with status 100 and leaves C alone; the allocation-free one succeeds,
+    twice in a row, and matches the oracle."""
+    stream = torch.cuda.current_stream().cuda_stream
+    p = inputs.workload("1000x1500x777")
+    assert p.lda == 777
+    A, B = _device(p.A), _device(p.B)
+    monkeypatch.setenv("SGEMM_GB300_FAIL_ALLOC", "1")
+    C_ref = _device(p.C0)
+    assert _regular(p, A, B, C_ref, stream) == 100
+    for _ in range(2):
+        C = _device(p.C0)
+        st = _noalloc(p, A, B, C, stream)
+        assert st == 0, binding.status_string(st)
+        torch.cuda.synchronize()
+        _check_oracle(p, C.cpu().numpy())
+    assert np.array_equal(C_ref.cpu().numpy(), p.C0, equal_nan=True)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    # 2 * (m + n) * ka floats are needed; 2048^3 fills the array exactly,
-    # one more row does not fit.  Rejected before anything is enqueued.
+    """Only operands that cannot be read as stored take scratch: 2 * rows *
+    ka floats each (ka = k rounded up to 4).  With both operands' rows
+    misaligned (lda = ldb = 2049), m = n = 2048 and k = 2048 fill the array
+    exactly; k = 2049 (ka = 2052) does not fit and is rejected before
+    anything is enqueued, while the same shape with 16-byte rows needs no
+    scratch at all."""
     assert binding.NOALLOC_SCRATCH_FLOATS == 2 * (2048 + 2048) * 2048
-    st = binding.tf32x3_noalloc_raw(2049, 2048, 2048, 1.0, 256, 2048, 512, 2048, 0.0, 1024, 2048, 0)
+    st = binding.tf32x3_noalloc_raw(2048, 2048, 2049, 1.0, 256, 2049, 512, 2049, 0.0, 1024, 2048, 0)
     assert st == 97
     assert "scratch" in binding.status_string(st)
+    # a problem that fits exactly, and one that needs no scratch, both run
+    stream = torch.cuda.current_stream().cuda_stream
+    for k, ld in ((2048, 2049), (2049, 2052)):
+        p = inputs.make_problem(2048, 2048, k, alpha=1.0, beta=0.0, seed=k, a="uniform", b="uniform",
+                                lda=ld, ldb=ld)
+        A, B, C = _device(p.A), _device(p.B), _device(p.C0)
+        st = _noalloc(p, A, B, C, stream)
+        assert st == 0, binding.status_string(st)
+        torch.cuda.synchronize()
+        rows, cols = inputs.sample_indices(p.m, p.n, 512, seed=k)
+        R, E = oracle.problem_f64_sampled(p, rows, cols)
+        ok, worst, _ = oracle.within_tolerance(C.cpu().numpy()[rows, cols], R, E, 0.0, None)
+        assert ok, worst
