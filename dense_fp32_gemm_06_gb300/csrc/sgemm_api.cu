@@ -139,6 +139,7 @@ int device_state(DeviceState **out) {
         if ((e = set_tc_attr<tf32x3::Wide, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Narrow, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Wide, true>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_tc_attr<tf32x3::Pair, false>()) != cudaSuccess) return fail_cuda(e);
         for (int S = 2; S <= 8; ++S) {
             if ((e = max_clusters_of<tf32x3::Wide>(S, &d.max_clusters[0][S])) != cudaSuccess) return fail_cuda(e);
             if ((e = max_clusters_of<tf32x3::Narrow>(S, &d.max_clusters[1][S])) != cudaSuccess) return fail_cuda(e);
@@ -212,6 +213,23 @@ bool tma_readable(const void *X, long long ld, long long outer, int batch, long 
     if (!aligned(X, 16) || ld % 4 != 0) return false;
     if (batch > 1 && stride != 0 && (stride % 4 != 0 || stride < outer * ld)) return false;
     return true;
+}
+
+// The tensor-core plan on CTA pairs: 256 x 256 tiles of two CTAs each, whole
+// tiles (no split-K, no stream-K); the operand sources stay as planned.
+void set_pair_plan(int m, int n, int k, sgemm_plan *pl) {
+    pl->pair = 1;
+    pl->trans = 0;
+    pl->bm = pl->bn = tf32x3::Pair::BN;
+    pl->split_k = 1;
+    pl->stream_k = 0;
+    pl->stages = tf32x3::Pair::STAGES;
+    pl->smem_bytes = tf32x3::Pair::SMEM_BYTES;
+    const int tm = (m + pl->bm - 1) / pl->bm, tn = (n + pl->bn - 1) / pl->bn;
+    pl->tiles = tm * tn;
+    pl->grid = 2 * pl->tiles;
+    pl->k_tiles = (k + tf32x3::BK - 1) / tf32x3::BK;
+    pl->group_m = tm < 8 ? tm : 8;
 }
 
 int plan(int m, int n, int k, float alpha, const float *A, int lda, const float *B, int ldb, float beta,
@@ -376,6 +394,15 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         pl->a_in_kernel = a_tma && !(env_ain && env_ain[0] == '0');
         pl->b_in_kernel = b_tma && (env_bin && (env_bin[0] == '0' || env_bin[0] == '1') ? env_bin[0] == '1' : b_small);
         pl->threads = tf32x3::THREADS;
+        // CTA pairs (cta_group::2): 256 x 256 tiles, each CTA staging (and,
+        // for operands read as stored, splitting) 128 rows of A and 128 of
+        // B; whole tiles only (no split-K, no stream-K).
+        // SGEMM_GB300_PAIR = 1 asks for it where it applies.
+        const char *env_pair = std::getenv("SGEMM_GB300_PAIR");
+        if (env_pair && env_pair[0] == '1' && !best_tr) {
+            set_pair_plan(m, n, k, pl);
+            return SGEMM_STATUS_OK;
+        }
         const bool narrow = best_bn == tf32x3::Narrow::BN;
         pl->trans = best_tr;
         // bm x bn: the tile of C (256 x 128 when transposed)
@@ -564,8 +591,9 @@ int prepare_gemm(int m, int n, int k, float alpha, const Operand &a, const Opera
     // stream-K needs its workspace (callers that allocate nothing plan without it)
     if (pl.stream_k > 0 && (sk_ws == nullptr || sk_cnt == nullptr || batch != 1)) return SGEMM_STATUS_UNSUPPORTED;
     const Operand &x = pl.trans ? b : a, &y = pl.trans ? a : b;
-    // boxes: 128 rows of X (the MMA's M), BN rows of Y (its N)
-    const int y_rows = pl.trans ? pl.bm : pl.bn;
+    // boxes: 128 rows of X (the MMA's M, per CTA), BN rows of Y (its N;
+    // half of them per CTA of a pair)
+    const int y_rows = pl.trans ? pl.bm : (pl.pair ? pl.bn / 2 : pl.bn);
     tf32x3::Params &p = L->prm;
     int st = encode_operand(x, k, tf32x3::BM, batch, &L->maps[0], &L->maps[1], &p.x_z);
     if (!st) st = encode_operand(y, k, y_rows, batch, &L->maps[2], &L->maps[3], &p.y_z);
@@ -606,9 +634,9 @@ int launch_gemm(const GemmLaunch &L, const sgemm_plan &pl, int batch, cudaStream
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
     unsigned na = 0;
-    if (pl.split_k > 1) {
+    if (pl.split_k > 1 || pl.pair) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = (unsigned)pl.split_k;
+        attr[na].val.clusterDim.x = pl.pair ? 2u : (unsigned)pl.split_k;
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -624,7 +652,9 @@ int launch_gemm(const GemmLaunch &L, const sgemm_plan &pl, int batch, cudaStream
     cfg.attrs = attr;
     cfg.numAttrs = na;
     cudaError_t e;
-    if (pl.trans)
+    if (pl.pair)
+        e = launch_tc<tf32x3::Pair, false>(cfg, L.xm, L.ym, L.maps, L.prm);
+    else if (pl.trans)
         e = launch_tc<tf32x3::Wide, true>(cfg, L.xm, L.ym, L.maps, L.prm);
     else if (pl.bn == tf32x3::Narrow::BN)
         e = launch_tc<tf32x3::Narrow, false>(cfg, L.xm, L.ym, L.maps, L.prm);
@@ -994,8 +1024,14 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
     if (st != SGEMM_STATUS_OK) return st;
     // read every operand TMA can read as stored, whatever the size (the
     // plan splits a large B with the split pass, which is faster there):
-    // scratch only for operands whose rows are not 16 bytes apart
-    if (tma_readable(B, ldb, k, 1, 0)) pl.b_in_kernel = 1;
+    // scratch only for operands whose rows are not 16 bytes apart.  With
+    // both read as stored, large problems run on CTA pairs, which split B
+    // in half the shared-memory traffic per SM (measured, whole call:
+    // 8192^3 4.29 ms against 5.8 ms on single-CTA 128 x 256 tiles)
+    if (pl.kernel != kKernelScale && tma_readable(B, ldb, k, 1, 0)) {
+        pl.b_in_kernel = 1;
+        if (pl.a_in_kernel && !pl.trans && (long long)m * n * k > (1LL << 31)) set_pair_plan(m, n, k, &pl);
+    }
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);
     } else {

@@ -25,6 +25,22 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// The same for a CTA pair (cta_group::2): one warp of each of the two peer
+// CTAs executes it, and the columns are allocated (freed) in both CTAs'
+// tensor memory at the same address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
 __device__ __forceinline__ void fence_before_sync() {
     asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
 }
@@ -55,6 +71,32 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint6
         : "memory");
 }
 
+// The CTA pair's MMA (cta_group::2), issued by one thread of the even CTA:
+// A's rows are split between the two CTAs (M / 2 in each, same shared-memory
+// offset), B's between them likewise (N / 2 in each), and each CTA's tensor
+// memory receives its M / 2 rows of D, all N columns.
+__device__ __forceinline__ void mma_tf32_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::tf32 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// One arrival on the mbarrier at shared-memory offset `bar` in every CTA of
+// `cta_mask` (bit i = cluster rank i) once the pair MMAs this thread issued
+// have completed.
+__device__ __forceinline__ void commit_pair(uint32_t bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(bar),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // The mbarrier at `bar` (shared, 32-bit address) receives one arrival when
 // every tcgen05 operation this thread issued before has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {
@@ -68,7 +110,7 @@ __device__ __forceinline__ void commit(uint32_t bar) {
 // 1 = MN-major: rows hold consecutive m / n), [17,23) N >> 3, [24,29) M >> 4.
 template <int M, int N, bool A_MN = false, bool B_MN = false>
 __host__ __device__ constexpr uint32_t idesc_tf32_f32() {
-    static_assert(M == 64 || M == 128, "cta_group::1 M");
+    static_assert(M == 64 || M == 128 || M == 256, "M: 64 or 128 (one CTA), 128 or 256 (a CTA pair)");
     static_assert(N % 16 == 0 && N >= 16 && N <= 256, "N");
     return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(A_MN) << 15) | (uint32_t(B_MN) << 16) |
            (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);

@@ -96,15 +96,20 @@ constexpr int CONV_THREADS = 32 * CONV_WARPS;
 // producer warp, MMA warp, 8 accumulator warps, 2 splitter warps: three
 // warps per sub-partition, a cap of 168 registers per thread
 constexpr int THREADS = 64 + ACC_THREADS + CONV_THREADS;
-constexpr int BAR_REGION = 256;
+constexpr int BAR_REGION = 512;
 static_assert(BK * 4 == 64, "one 64-byte swizzle row per operand row");
 static_assert(KC % BK == 0, "chunks are whole slabs");
 
 // Tile width BN (256, or 128 for narrow / few-tile problems) and ring depth.
-template <int BN_, int STAGES_>
+// PAIR: a CTA pair (cta_group::2) computes a 256 x BN tile with one MMA of
+// M = 256; each CTA holds 128 rows of the MMA's A operand and BN / 2 rows of
+// its B operand, and receives 128 rows x BN columns of D.
+template <int BN_, int STAGES_, bool PAIR_ = false>
 struct Config {
     static constexpr int BN = BN_, STAGES = STAGES_;
-    static constexpr int B_TILE = BN * BK * 4;
+    static constexpr bool PAIR = PAIR_;
+    static constexpr int Y_ROWS = PAIR ? BN / 2 : BN;             // rows of the MMA's B operand in this CTA
+    static constexpr int B_TILE = Y_ROWS * BK * 4;
     static constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;   // A_hi, A_lo, B_hi, B_lo
     static constexpr int TMEM_COLS = 2 * BN;                      // two accumulators
     static constexpr int COLS_PER_THREAD = BN / 2;                // two warps per 32-lane group
@@ -116,6 +121,7 @@ struct Config {
 };
 using Wide = Config<256, 4>;     // 48 KB stages
 using Narrow = Config<128, 6>;   // 32 KB stages
+using Pair = Config<256, 6, true>;   // 32 KB stages per CTA, 256 x 256 tiles per CTA pair
 
 constexpr int kStatusProducer = 0x201;
 constexpr int kStatusMma = 0x202;
@@ -159,11 +165,12 @@ struct Params {
 // [k0, k0 + nk) of its kt_all slabs; false past the last.  Stream-K (see
 // Params): the whole tiles blockIdx.x + w G first, then the CTA's run of
 // the remaining tiles' slab sequence cut at tile boundaries.  Otherwise one
-// segment: split-K cluster rank `rank`'s share of tile blockIdx.x / nsplit
-// (possibly empty), or the whole tile.  Recomputed on demand so that no
+// segment of tile blockIdx.x / ctas_per_tile (nsplit for a split-K cluster,
+// 2 for a CTA pair, else 1): split-K cluster rank `rank`'s share of its
+// slabs (possibly empty), or all of them.  Recomputed on demand so that no
 // role keeps iteration state next to its accumulators.
 __device__ __forceinline__ bool cta_segment(const Params &p, int kt_all, int tiles, uint32_t nsplit, uint32_t rank,
-                                            int si, int &tile, int &k0, int &nk) {
+                                            int si, int &tile, int &k0, int &nk, int ctas_per_tile) {
     long long it0, it1;
     if (p.sk_ctas > 0) {
         const int whole = tiles / p.sk_ctas;
@@ -180,7 +187,7 @@ __device__ __forceinline__ bool cta_segment(const Params &p, int kt_all, int til
         it1 = base + T * (blockIdx.x + 1) / p.sk_ctas;
     } else {
         if (si > 0) return false;
-        tile = (int)(blockIdx.x / nsplit);
+        tile = (int)blockIdx.x / ctas_per_tile;
         k0 = (int)((long long)kt_all * rank / nsplit);
         nk = (int)((long long)kt_all * (rank + 1) / nsplit) - k0;
         return true;
@@ -445,6 +452,28 @@ __device__ __forceinline__ void split_slot_lo(const uint8_t *raw_slot, uint8_t *
     }
 }
 
+// Both lo parts of a slab at once: every thread's 16-byte loads of X and Y
+// in flight together, then the conversions and the stores.
+template <int XBYTES, int YBYTES, int CW>
+__device__ __forceinline__ void split_slots_lo(const uint8_t *x_raw, uint8_t *x_lo, const uint8_t *y_raw,
+                                               uint8_t *y_lo, int ct) {
+    constexpr int PX = XBYTES / 16 / CW, PY = YBYTES / 16 / CW;
+    static_assert(XBYTES % (16 * CW) == 0 && YBYTES % (16 * CW) == 0, "whole float4s per thread");
+    const float4 *xr = reinterpret_cast<const float4 *>(x_raw), *yr = reinterpret_cast<const float4 *>(y_raw);
+    float4 *xl = reinterpret_cast<float4 *>(x_lo), *yl = reinterpret_cast<float4 *>(y_lo);
+    float4 v[PX + PY];
+#pragma unroll
+    for (int j = 0; j < PX; ++j) v[j] = xr[ct + j * CW];
+#pragma unroll
+    for (int j = 0; j < PY; ++j) v[PX + j] = yr[ct + j * CW];
+#pragma unroll
+    for (int j = 0; j < PX + PY; ++j) v[j] = make_float4(lo_of_raw(v[j].x), lo_of_raw(v[j].y), lo_of_raw(v[j].z), lo_of_raw(v[j].w));
+#pragma unroll
+    for (int j = 0; j < PX; ++j) xl[ct + j * CW] = v[j];
+#pragma unroll
+    for (int j = 0; j < PY; ++j) yl[ct + j * CW] = v[PX + j];
+}
+
 template <class Cfg, bool TRANS = false, bool X_MN = false, bool Y_MN = false>
 __global__ void __launch_bounds__(THREADS, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmXhi, const __grid_constant__ CUtensorMap tmXlo,
@@ -452,16 +481,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                        const Params p) {
     constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, Y_TILE = Cfg::B_TILE, STAGE_BYTES = Cfg::STAGE_BYTES;
     constexpr int X_TILE = A_TILE;
+    constexpr bool PAIR = Cfg::PAIR;
+    constexpr int Y_ROWS = Cfg::Y_ROWS;
+    static_assert(!PAIR || !TRANS, "CTA pairs compute untransposed tiles");
     constexpr int TMEM_COLS = Cfg::TMEM_COLS, COLS_PER_THREAD = Cfg::COLS_PER_THREAD;
     constexpr int PART_PITCH = BN + 4;   // floats per row of a parked split-K partial tile
     constexpr int NTHREADS = THREADS;
     constexpr bool CONV_PER_WARP = BN == 128;   // splitters: one warp per slab (see there)
+    static_assert(!PAIR || !CONV_PER_WARP, "PAIR: both splitter warps take every slab (they meet at a barrier)");
     // slots of a stage: [X hi | X lo | Y hi | Y lo]
     constexpr int X_HI = 0, X_LO = X_TILE, Y_HI = 2 * X_TILE, Y_LO = 2 * X_TILE + Y_TILE;
     static_assert(X_LO % 1024 == 0 && Y_HI % 1024 == 0 && Y_LO % 1024 == 0 && STAGE_BYTES % 1024 == 0,
                   "slots on 1 KB boundaries (128-byte swizzle atoms)");
     static_assert(!X_MN || X_TILE == (BM / 32) * 2048, "MN-major X: 32-row boxes of 2 KB");
-    static_assert(!Y_MN || Y_TILE == (BN / 32) * 2048, "MN-major Y: 32-row boxes of 2 KB");
+    static_assert(!Y_MN || Y_TILE == (Y_ROWS / 32) * 2048, "MN-major Y: 32-row boxes of 2 KB");
     static_assert(BM * PART_PITCH * 4 <= STAGES * STAGE_BYTES, "partial tile fits the stage memory");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *const smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -477,18 +510,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     volatile int *const sk_last = reinterpret_cast<volatile int *>(bars + 8 * (2 * STAGES + 5) + 12);
     const uint32_t bar_conv_x = bar_done + 24;           // [STAGES] X's lo written (raw X)
     const uint32_t bar_conv_y = bar_conv_x + 8 * STAGES; // [STAGES] Y's lo written (raw Y)
+    // PAIR: [STAGES] the peer's slab landed and its lo parts are written
+    // (transaction bytes of a 16-byte signal copy the peer sends), and the
+    // 16-byte landing / source pad of that copy
+    const uint32_t bar_peer = bar_conv_y + 8 * STAGES;
+    const uint32_t sig_pad = (bar_peer + 8 * STAGES + 15) & ~15u;
     float4 *const epi = reinterpret_cast<float4 *>(bars + BAR_REGION);   // [ACC_WARPS][32 rows][8 float4]
-    static_assert(8 * (4 * STAGES + 7) <= BAR_REGION, "barrier region");
+    static_assert(8 * (5 * STAGES + 7) + 32 <= BAR_REGION, "barrier region");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool x_raw = p.x_src == kRaw, y_raw = p.y_src == kRaw;
     const bool c_vec = p.c_vec != 0;
     // split-K: the CTAs of a cluster share one output tile and take
-    // consecutive ranges of its k slabs (a cluster of one without split-K)
-    const uint32_t nsplit = tc::cluster_nctarank(), rank = tc::cluster_ctarank();
+    // consecutive ranges of its k slabs (a cluster of one without split-K).
+    // PAIR: the cluster is the CTA pair, which shares one tile and all of k;
+    // its even CTA (the leader) issues the MMAs, and `prank` (0 / 1) picks
+    // this CTA's half of the tile's rows and of its B operand
+    const uint32_t crank = tc::cluster_ctarank();
+    const uint32_t nsplit = PAIR ? 1u : tc::cluster_nctarank(), rank = PAIR ? 0u : crank;
+    const uint32_t prank = PAIR ? (crank & 1u) : 0u, leader = crank & ~1u;
+    constexpr int CTAS_PER_TILE_PAIR = PAIR ? 2 : 1;
+    const int CTAS_PER_TILE = PAIR ? CTAS_PER_TILE_PAIR : (int)nsplit;
     // TRANS: the tile is BN rows of C by BM columns (C^T = B^T A^T: the
-    // MMA's 128-row operand is B^T, its BN-row operand is A)
-    constexpr int TILE_M = TRANS ? BN : BM, TILE_N = TRANS ? BM : BN;
+    // MMA's 128-row operand is B^T, its BN-row operand is A).  PAIR: 256 x BN
+    constexpr int TILE_M = TRANS ? BN : (PAIR ? 2 * BM : BM), TILE_N = TRANS ? BM : BN;
     float *const Cb = p.C + (long long)blockIdx.y * p.stride_c;
     const int KT_ALL = (p.k + BK - 1) / BK;
     const int tiles = p.tiles_m * p.tiles_n;
@@ -506,20 +551,33 @@ __global__ void __launch_bounds__(THREADS, 1)
     // the split-K cluster's tile (its reduction below writes it)
     int cl_m0 = 0, cl_n0 = 0;
     if (nsplit > 1) tile_origin((int)(blockIdx.x / nsplit), cl_m0, cl_n0);
+    // PAIR: one arrival at barrier `bar` of the pair's leader -- a plain
+    // arrival in the leader itself, a cluster-scope release from its peer
+    auto arrive_leader = [&](uint32_t bar) {
+        if (prank == 0)
+            mbar_arrive(bar);
+        else
+            mbar_arrive_cluster(tc::map_shared_rank(bar, leader));
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
+        // PAIR: each CTA's accumulator warps arrive once at the leader's
+        // "drained" barrier (an elected thread after their named barrier);
+        // the per-slab signal from the peer is the transaction bytes of its
+        // signal copy, expected by the leader's MMA thread (one arrival)
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_tfull + 8 * b, 1);
-            mbar_init(bar_tempty + 8 * b, ACC_THREADS);
+            mbar_init(bar_tempty + 8 * b, PAIR ? 2 : ACC_THREADS);
         }
         mbar_init(bar_done, 1);
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_conv_x + 8 * s, CONV_PER_WARP ? 32 : CONV_THREADS);
             mbar_init(bar_conv_y + 8 * s, CONV_PER_WARP ? 32 : CONV_THREADS);
+            mbar_init(bar_peer + 8 * s, 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -529,11 +587,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tmYlo);
     }
     if (warp == 1) {
-        tc::tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-        tc::tmem_relinquish();
+        if constexpr (PAIR) {
+            tc::tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+            tc::tmem_relinquish_pair();
+        } else {
+            tc::tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+            tc::tmem_relinquish();
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
+    // PAIR: both CTAs' barriers are initialised before either arrives at
+    // the other's
+    if constexpr (PAIR) tc::cluster_sync();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
@@ -546,10 +612,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             griddep_wait();
             int tile, k0, nk, g = 0;   // g: slabs issued so far (ring position)
             bool stop = false;
-            for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
+            for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
                 int m0, n0;
                 tile_origin(tile, m0, n0);
-                const int x0 = TRANS ? n0 : m0, y0 = TRANS ? m0 : n0;
+                // PAIR: this CTA's 128 rows of A and Y_ROWS rows of B
+                const int x0 = TRANS ? n0 : m0 + (int)prank * BM, y0 = TRANS ? m0 : n0 + (int)prank * Y_ROWS;
                 const int zx = p.x_z ? (int)blockIdx.y : 0, zy = p.y_z ? (int)blockIdx.y : 0;
                 const uint32_t tx_bytes = (x_raw ? 1 : 2) * X_TILE + (y_raw ? 1 : 2) * Y_TILE;
                 for (int kt = 0; kt < nk; ++kt, ++g) {
@@ -568,7 +635,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     mbar_arrive_expect_tx(fb, tx_bytes);
                     const int kx = (k0 + kt) * BK;
                     load_operand<X_MN, BM>(st + X_HI, st + X_LO, &tmXhi, &tmXlo, x_raw, x0, kx, zx, fb);
-                    load_operand<Y_MN, BN>(st + Y_HI, st + Y_LO, &tmYhi, &tmYlo, y_raw, y0, kx, zy, fb);
+                    load_operand<Y_MN, Y_ROWS>(st + Y_HI, st + Y_LO, &tmYhi, &tmYlo, y_raw, y0, kx, zy, fb);
                 }
             }
             if (*abort_flag) {
@@ -579,11 +646,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_tf32_f32<BM, BN, X_MN, Y_MN>();
+        // PAIR: the leader issues the pair's MMAs (M = 256) and its commits
+        // arrive at the barrier of the same offset in both CTAs; it waits on
+        // its own barriers only
+        const uint16_t pair_mask = (uint16_t)(3u << leader);
+        auto commit_to = [&](uint32_t bar) {
+            if constexpr (PAIR)
+                tc::commit_pair(bar, pair_mask);
+            else
+                tc::commit(bar);
+        };
+        auto mma = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+            if constexpr (PAIR)
+                tc::mma_tf32_pair(d, a, b, idesc, acc);
+            else
+                tc::mma_tf32(d, a, b, idesc, acc);
+        };
+        if (lane == 0 && prank == 0) {
+            constexpr uint32_t idesc = tc::idesc_tf32_f32<PAIR ? 2 * BM : BM, BN, X_MN, Y_MN>();
             int tile, k0, nk, g = 0, cg = 0;   // g: slabs consumed, cg: chunks started
             bool stop = false;
-            for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
+            for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
               for (int kt = 0; kt < nk; ++kt, ++g) {
                 // each segment's slabs accumulate in chunks of CHUNK_STAGES
                 // slabs, alternating between the two TMEM buffers
@@ -592,7 +675,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool chunk_last = kt % CHUNK_STAGES == CHUNK_STAGES - 1 || kt == nk - 1;
                 // TMEM buffer b is reused once the accumulator warps drained chunk cg - 2
                 if (chunk_first && cg >= 2 &&
-                    !mbar_wait(bar_tempty + 8 * b, ((cg >> 1) - 1) & 1, kStatusMmaBuffer)) {
+                    !(PAIR ? mbar_wait_cluster(bar_tempty + 8 * b, ((cg >> 1) - 1) & 1, kStatusMmaBuffer)
+                           : mbar_wait(bar_tempty + 8 * b, ((cg >> 1) - 1) & 1, kStatusMmaBuffer))) {
                     *abort_flag = 1;
                     stop = true;
                     break;
@@ -604,6 +688,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     stop = true;
                     break;
                 }
+                // PAIR: and the peer's slab has landed and been split (its
+                // signal copy's 16 bytes; they may arrive before this expect)
+                if constexpr (PAIR) {
+                    mbar_arrive_expect_tx(bar_peer + 8 * s, 16);
+                    if (!mbar_wait(bar_peer + 8 * s, ph, kStatusMma)) {
+                        *abort_flag = 1;
+                        stop = true;
+                        break;
+                    }
+                }
                 tc::fence_after_sync();
                 const uint32_t st = stage0 + s * STAGE_BYTES;
                 const uint32_t d = tmem + (uint32_t)(b * BN);
@@ -611,8 +705,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // part of a raw operand waits for the splitters to write it
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                    tc::mma_tf32(d, operand_desc<X_MN>(st + X_HI, kk), operand_desc<Y_MN>(st + Y_HI, kk), idesc,
-                                 (chunk_first && kk == 0) ? 0u : 1u);
+                    mma(d, operand_desc<X_MN>(st + X_HI, kk), operand_desc<Y_MN>(st + Y_HI, kk), idesc,
+                        (chunk_first && kk == 0) ? 0u : 1u);
                 if (x_raw) {
                     if (!mbar_wait(bar_conv_x + 8 * s, ph, kStatusMma)) {
                         *abort_flag = 1;
@@ -623,7 +717,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                    tc::mma_tf32(d, operand_desc<X_MN>(st + X_LO, kk), operand_desc<Y_MN>(st + Y_HI, kk), idesc, 1u);
+                    mma(d, operand_desc<X_MN>(st + X_LO, kk), operand_desc<Y_MN>(st + Y_HI, kk), idesc, 1u);
                 if (y_raw) {
                     if (!mbar_wait(bar_conv_y + 8 * s, ph, kStatusMma)) {
                         *abort_flag = 1;
@@ -634,18 +728,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                    tc::mma_tf32(d, operand_desc<X_MN>(st + X_HI, kk), operand_desc<Y_MN>(st + Y_LO, kk), idesc, 1u);
-                tc::commit(bar_empty + 8 * s);
+                    mma(d, operand_desc<X_MN>(st + X_HI, kk), operand_desc<Y_MN>(st + Y_LO, kk), idesc, 1u);
+                commit_to(bar_empty + 8 * s);
                 if (chunk_last) {
-                    tc::commit(bar_tfull + 8 * b);
+                    commit_to(bar_tfull + 8 * b);
                     ++cg;
                 }
               }
             }
             // fires once every MMA issued has completed (TMEM may then be freed)
-            tc::commit(bar_done);
-            mbar_wait(bar_done, 0, kStatusDrain);
+            commit_to(bar_done);
         }
+        // both CTAs of a pair: the MMAs writing this CTA's tensor memory
+        // (and reading its shared memory) have completed
+        if (lane == 0) mbar_wait(bar_done, 0, kStatusDrain);
         __syncwarp();
     } else if (warp >= 2 + ACC_WARPS) {
         // ------------------------------------------------------------ splitters (warps 10, 11)
@@ -657,17 +753,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int ct = CONV_PER_WARP ? lane : (int)threadIdx.x - (64 + ACC_THREADS);
         const int mine = CONV_PER_WARP ? warp - (2 + ACC_WARPS) : 0;
         int tile, k0, nk, g = 0;   // g: slab sequence position (ring position)
-        bool stop = !x_raw && !y_raw;   // nothing to split: both operands come split
-        for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
+        // nothing to split (both operands come split), except that the odd
+        // CTA of a pair still tells the leader when its slab has landed
+        bool stop = !x_raw && !y_raw && !(PAIR && prank == 1);
+        for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
           for (int kt = 0; kt < nk; ++kt, ++g) {
             if (CONV_PER_WARP && (g % CONV_WARPS) != mine) continue;
             const int s = g % STAGES;
-            if (!mbar_wait(bar_full + 8 * s, (g / STAGES) & 1, kStatusSplit)) {
-                *abort_flag = 1;
-                stop = true;
-                break;
-            }
-            if (*abort_flag) {
+            const bool got = mbar_wait(bar_full + 8 * s, (g / STAGES) & 1, kStatusSplit);
+            if (!got) *abort_flag = 1;
+            bool quit = !got || *abort_flag != 0;
+            // the odd CTA of a pair: both splitter warps meet at a named
+            // barrier below on every slab, so they agree here whether to go
+            // on (a wait that ran out in one warp must not leave the other
+            // at that barrier)
+            if (PAIR && prank == 1) quit = named_barrier_or(2, CONV_THREADS, quit);
+            if (quit) {
                 stop = true;
                 break;
             }
@@ -677,15 +778,52 @@ __global__ void __launch_bounds__(THREADS, 1)
             // so the swizzled layout does not matter); X first, whose lo the
             // MMA needs first
             uint8_t *const st = smem + s * STAGE_BYTES;
-            if (x_raw) {
-                split_slot_lo<X_TILE, CW>(st + X_HI, st + X_LO, ct);
+            if (PAIR && prank == 0) {
+                // both lo parts together (one fence), then both signals
+                if (x_raw && y_raw) {
+                    split_slots_lo<X_TILE, Y_TILE, CW>(st + X_HI, st + X_LO, st + Y_HI, st + Y_LO, ct);
+                    tc::fence_proxy_async_smem();
+                    mbar_arrive(bar_conv_x + 8 * s);
+                    mbar_arrive(bar_conv_y + 8 * s);
+                } else if (x_raw || y_raw) {
+                    if (x_raw) split_slot_lo<X_TILE, CW>(st + X_HI, st + X_LO, ct);
+                    if (y_raw) split_slot_lo<Y_TILE, CW>(st + Y_HI, st + Y_LO, ct);
+                    tc::fence_proxy_async_smem();
+                    mbar_arrive(x_raw ? bar_conv_x + 8 * s : bar_conv_y + 8 * s);
+                }
+            } else if (!PAIR) {
+                // each lo part signalled to this CTA's MMA issuer as soon as
+                // it is written
+                if (x_raw) {
+                    split_slot_lo<X_TILE, CW>(st + X_HI, st + X_LO, ct);
+                    tc::fence_proxy_async_smem();
+                    mbar_arrive(bar_conv_x + 8 * s);
+                }
+                if (y_raw) {
+                    split_slot_lo<Y_TILE, CW>(st + Y_HI, st + Y_LO, ct);
+                    tc::fence_proxy_async_smem();
+                    mbar_arrive(bar_conv_y + 8 * s);
+                }
+            } else {
+                // PAIR, the odd CTA: split both halves, then one signal to the
+                // leader's MMA issuer -- a 16-byte copy into the leader's
+                // shared memory that completes on its barrier.  An arrival
+                // from here would release at cluster scope and hold this
+                // thread for ~800 cycles (measured) per slab; the copy is
+                // issued and left to complete on its own.  Every writer
+                // fences its lo values for the tensor core's proxy before the
+                // barrier that precedes the copy.
+                if (x_raw && y_raw) {
+                    split_slots_lo<X_TILE, Y_TILE, CW>(st + X_HI, st + X_LO, st + Y_HI, st + Y_LO, ct);
+                } else {
+                    if (x_raw) split_slot_lo<X_TILE, CW>(st + X_HI, st + X_LO, ct);
+                    if (y_raw) split_slot_lo<Y_TILE, CW>(st + Y_HI, st + Y_LO, ct);
+                }
                 tc::fence_proxy_async_smem();
-                mbar_arrive(bar_conv_x + 8 * s);
-            }
-            if (y_raw) {
-                split_slot_lo<Y_TILE, CW>(st + Y_HI, st + Y_LO, ct);
-                tc::fence_proxy_async_smem();
-                mbar_arrive(bar_conv_y + 8 * s);
+                named_barrier_sync(2, CONV_THREADS);
+                if (ct == 0)
+                    bulk_copy_to_peer(tc::map_shared_rank(sig_pad, leader), sig_pad, 16,
+                                      tc::map_shared_rank(bar_peer + 8 * s, leader));
             }
           }
         }
@@ -882,15 +1020,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         };
 
         int tile, k0, nk, cg = 0;   // cg: chunks drained so far
-        for (int si = 0; cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk); ++si) {
+        for (int si = 0; cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
 #pragma unroll
             for (int j = 0; j < COLS_PER_THREAD; ++j) acc[j] = 0.f;
             const int nc = (nk + CHUNK_STAGES - 1) / CHUNK_STAGES;
             for (int c = 0; c < nc && ok; ++c, ++cg) {
                 const int b = cg & 1;
-                if (!mbar_wait(bar_tfull + 8 * b, (cg >> 1) & 1, kStatusAccumulate)) {
+                const bool got = mbar_wait(bar_tfull + 8 * b, (cg >> 1) & 1, kStatusAccumulate);
+                if (!got) *abort_flag = 1;
+                // PAIR: the accumulator threads meet at a named barrier below
+                // on every chunk, so they agree here whether to go on
+                const bool quit = PAIR ? named_barrier_or(3, ACC_THREADS, !got) : !got;
+                if (quit) {
                     ok = false;
-                    *abort_flag = 1;
                     break;
                 }
                 tc::fence_after_sync();
@@ -903,7 +1045,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int i = 0; i < 16; ++i) acc[q * 16 + i] += __uint_as_float(v[i]);
                 }
                 tc::fence_before_sync();
-                mbar_arrive(bar_tempty + 8 * b);
+                if constexpr (PAIR) {
+                    // one arrival per CTA at the leader's barrier, after every
+                    // accumulator thread's loads of the buffer have completed
+                    named_barrier_sync(4, ACC_THREADS);
+                    if (threadIdx.x == 64) arrive_leader(bar_tempty + 8 * b);
+                } else {
+                    mbar_arrive(bar_tempty + 8 * b);
+                }
             }
             // leave together (the stream-K hand-off below synchronises
             // these 256 threads, and a wait that ran out may have stopped
@@ -911,6 +1060,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (named_barrier_or(1, ACC_THREADS, !ok || *abort_flag != 0)) break;
             int m0, n0;
             tile_origin(tile, m0, n0);
+            m0 += (int)prank * BM;   // PAIR: this CTA's 128 rows of the 256-row tile
             if (nsplit > 1) {
                 // park the partial tile in this CTA's (now idle) stage memory,
                 // rows PART_PITCH floats apart (4 banks apart: conflict-free)
@@ -1003,9 +1153,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
         tc::cluster_sync();
     }
+    // PAIR: neither CTA leaves (or frees its tensor memory) while the other
+    // may still arrive at its barriers
+    if constexpr (PAIR) tc::cluster_sync();
     if (warp == 1) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem, TMEM_COLS);
+        if constexpr (PAIR)
+            tc::tmem_dealloc_pair(tmem, TMEM_COLS);
+        else
+            tc::tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 

@@ -295,6 +295,7 @@ typedef struct sgemm_plan {
     int stream_k;      /* > 0: stream-K over this many CTAs (grid); each takes an equal share  */
                        /*      of all tiles' k slabs, partial tiles meet in a workspace        */
     int b_in_kernel;   /* 1: the same for B (no split pass, no scratch for that operand)       */
+    int pair;          /* 1: CTA pairs (cta_group::2) compute 256 x 256 tiles, 2 CTAs per tile */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,
