@@ -204,6 +204,22 @@ struct Layout {
     static constexpr int SMEM_BYTES = Cfg::STAGES * (A_STAGE + B_STAGE) * 4;
 };
 
+// d0 += a0 * b0, d1 += a1 * b1 as one packed instruction (fma.rn.f32x2 of
+// sm_100-class GPUs): each half is an IEEE round-to-nearest fused
+// multiply-add, the same result as fmaf, but one issue slot does two of them.
+__device__ __forceinline__ void fma2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n"
+        ".reg .b64 ra, rb, rd;\n"
+        "mov.b64 ra, {%2, %3};\n"
+        "mov.b64 rb, {%4, %5};\n"
+        "mov.b64 rd, {%0, %1};\n"
+        "fma.rn.f32x2 rd, ra, rb, rd;\n"
+        "mov.b64 {%0, %1}, rd;\n"
+        "}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 template <class Cfg, class AL, class BL>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kernel(const GemmArgs p) {
     constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
@@ -296,10 +312,13 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
                 b[4 * h + 2] = fb[cur][h].z;
                 b[4 * h + 3] = fb[cur][h].w;
             }
+            // the outer product as packed pairs of neighbouring columns:
+            // TM * TN / 2 instructions instead of TM * TN (per output still
+            // one rounded fused multiply-add per k, in increasing k)
 #pragma unroll
             for (int i = 0; i < TM; ++i)
 #pragma unroll
-                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < TN; j += 2) fma2(acc[i][j], acc[i][j + 1], a[i], a[i], b[j], b[j + 1]);
         }
     }
     cp_async_wait<0>();
