@@ -20,6 +20,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -272,13 +273,22 @@ def tc_family(a_raw, b_raw):
             (False, False): "tf32x3_presplit"}[(bool(a_raw), bool(b_raw))]
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines, so that a kernel's
+    hash changes with its code only (string literals in these sources hold
+    no comment markers)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash(family):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "dense_fp32_gemm_06_gb300", "csrc")
     for name in KERNEL_SOURCES[family]:
         try:
-            with open(os.path.join(csrc, name), "rb") as fh:
-                h.update(name.encode() + fh.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as fh:
+                h.update(name.encode() + strip_comments(fh.read()).encode())
         except OSError:
             h.update(name.encode() + b"<missing>")
     return h.hexdigest()[:16]

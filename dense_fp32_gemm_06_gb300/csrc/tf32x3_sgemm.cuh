@@ -2,37 +2,42 @@
 //
 // Not on the pages (they only describe CUDA-core FFMA kernels); this is the
 // tensor-core path for the same C = alpha*A*B + beta*C.  Each FP32 operand
-// x is split into two TF32 numbers, hi = tf32(x) and lo = tf32(x - hi), and
+// x is split into two TF32 numbers, hi and lo = tf32(x - hi), and
 //     a*b ~= a_hi*b_hi + a_hi*b_lo + a_lo*b_hi,
 // every product exact in the tensor core and accumulated in FP32 in tensor
-// memory.  With round-to-nearest splits |a_lo| <= 2^-11 |a|, the dropped
-// a_lo*b_lo term and the rounding of the lo parts stay below ~3 * 2^-22
-// |a||b| per product, well inside the FP32 acceptance bound
-// |C - r| <= 1e-5 * sum_t |A_it||B_tj| + 1e-6 |beta C0|.  When the GEMM
-// reads A's hi part straight from A (the MMA drops the low 13 bits: hi =
-// trunc(x), |lo| < 2^-10 |x|), the bound per product is ~2^-20 |a||b|.
+// memory.  With the split pass's round-to-nearest hi, |a_lo| <= 2^-11 |a|
+// and the dropped a_lo*b_lo term plus the rounding of the lo parts stay
+// below ~3 * 2^-22 |a||b| per product; with an operand read as stored (hi =
+// x with its low 13 mantissa bits dropped, how the MMA reads FP32), below
+// ~2^-19 |a||b|: far inside the FP32 acceptance bound
+// |C - r| <= 1e-5 * sum_t |A_it||B_tj| + 1e-6 |beta C0|.
 //
-// Two launches per call:
-//  1. the split pass (split_pair_kernel, HBM-bound, both operands in one
-//     grid): A (any lda, any 4-byte alignment) becomes
-//     A_hi, A_lo, m x ka row-major (ka = k rounded up to 4, 16-byte rows);
-//     B becomes B^T_hi, B^T_lo, n x ka, transposed through a 32 x 64 shared
-//     tile padded to 65 columns (coalesced reads and writes).  Both operands
-//     of the MMA are then K-major.  When TMA can read A as it is, A skips
-//     this pass -- the GEMM kernel splits it from a raw TMA load (A_IN, at
-//     the kernel) -- or, for wide problems, the pass writes only A's lo part
-//     and the GEMM reads A's hi part from A;
-//  2. the GEMM kernel: one CTA per 128 x BN tile of C (BN = 256, or 128 for
-//     narrow or few-tile problems; the rest of this comment says 256), 10 warps
-//     (12 when the kernel splits A itself, below).
-//     warp 0 lane 0: TMA producer -- per 16-deep k slab, four boxes (A_hi,
-//       A_lo 128 x 16; B_hi, B_lo 256 x 16, 64-byte rows with the 64-byte
-//       swizzle) into a 4-stage ring, completing on the slot's "full"
-//       mbarrier; a slot is refilled after the MMA commit for it arrives on
-//       its "empty" mbarrier;
+// One launch per call, or two:
+//  0. (only for an operand TMA cannot read as stored -- rows not 16 bytes
+//     apart, a misaligned base -- or, for B, problems above 2^31
+//     multiply-adds) the split pass, split_pair_kernel: the operand becomes
+//     hi, lo row-major with k contiguous (row pitch ka = k rounded up to 4);
+//     a k-major operand (B stored k x n) is transposed through a 32 x 64
+//     shared tile padded to 65 columns;
+//  1. the GEMM kernel, 12 warps, one CTA per 128 x BN tile of C (BN = 256,
+//     or 128 for narrow or few-tile problems; the rest says 256):
+//     warp 0 lane 0: TMA producer -- per 16-deep k slab, the MMA's 128-row
+//       operand X and its 256-row operand Y into a 4-stage ring (48 KB per
+//       stage: [X hi | X lo | Y hi | Y lo]), completing on the slot's "full"
+//       mbarrier; an operand read as stored is one raw box (K-major: 64-byte
+//       rows, 64-byte swizzle) or 32-row boxes (MN-major: 128-byte swizzle
+//       of 32-byte atoms) into its hi slot; a split operand is two boxes;
+//       a slot is refilled after the MMA commit for it arrives on its
+//       "empty" mbarrier;
+//     warps 10, 11: splitters -- for each operand read as stored, lo =
+//       tf32(x - trunc(x)) of the raw slab into its lo slot (elementwise, so
+//       the swizzle does not matter), a proxy fence, and an arrival on the
+//       slot's "converted" barrier of that operand;
 //     warp 1: allocates 512 TMEM columns (two 128 x 256 FP32 accumulators);
 //       lane 0 issues, per 8-deep k step, the three tcgen05.mma kind::tf32
-//       (128 x 256 x 8) and commits each slab back to its "empty" barrier;
+//       (128 x 256 x 8): hi x hi as soon as the slab lands, each product
+//       with a lo part of a raw operand once it is converted; it commits
+//       each slab back to its "empty" barrier;
 //     warps 2-9: FP32 accumulation on the CUDA cores.  The tensor core's
 //       own FP32 accumulation is not round-to-nearest: its error is biased
 //       and grows with the number of accumulation steps (measured: 0.31 of
@@ -63,8 +68,11 @@
 //     Stream-K (Params): persistent CTAs that take whole tiles for the full
 //     waves and share the last wave's tiles out by slabs, a shared tile
 //     being finished by the last of its CTAs from partials in a workspace.
-//     A GEMM that runs in one wave is launched as a programmatic dependent
-//     of the split launch: it sets up while the split finishes, and its
+//     CTA pairs (Pair config, cta_group::2): two CTAs of a cluster compute a
+//     256 x 256 tile with M = 256 MMAs issued by the even CTA; each stages
+//     and splits its 128 rows of A and of B (6 stages of 32 KB).
+//     After a split pass, a GEMM that runs in one wave is launched as its
+//     programmatic dependent: it sets up while the split finishes, and its
 //     producer waits for it before the first load.
 //     TMA zero-fills rows past m, columns past n and k past the end, so the
 //     MMA never sees an index test.  Every mbarrier wait is bounded (2 s):

@@ -165,10 +165,12 @@ int sgemm_strided_batched(int op_a, int op_b, int m, int n, int k, float alpha,
  * lo = tf32(x - hi) (both rounded to nearest), and summing
  * a_hi*b_hi + a_hi*b_lo + a_lo*b_hi on the tensor cores in 128-deep chunks
  * whose sums are added in FP32 on the CUDA cores.  sgemm_ex(...,
- * SGEMM_PATH_TF32X3) does all of it with a stream-ordered scratch buffer
- * (from the library's pool, on `stream`); a caller that multiplies
- * the same operand many times can split it once with these calls and reuse
- * it.
+ * SGEMM_PATH_TF32X3) does all of it: an operand TMA can read as stored is
+ * split inside the GEMM kernel (hi = x with its low 13 mantissa bits
+ * dropped, which is how the tensor core reads an FP32 operand, and
+ * lo = tf32(x - hi) rounded to nearest), the others by a split pass into
+ * scratch (see Ownership above).  A caller that multiplies the same operand
+ * many times can split it once with these calls and reuse it.
  *
  * Split layout: ka = k rounded up to a multiple of 4.  a_hi, a_lo are
  * m x ka row-major (row pitch ka floats); bt_hi, bt_lo hold B TRANSPOSED,
@@ -204,14 +206,20 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
  * caller already holds).
  *
  * Arguments, layout, results and status codes are those of sgemm() with the
- * tensor-core path, plus SGEMM_STATUS_TOO_LARGE.  The split operands live in
- * one fixed array of SGEMM_NOALLOC_SCRATCH_FLOATS floats (64 MiB) in device
- * memory that every GPU which loads this library holds until the process
- * exits; a problem needs 2 * (m + n) * ka of them (ka = k rounded up to 4),
- * and a larger one is rejected with SGEMM_STATUS_TOO_LARGE before anything
- * is enqueued (for m = n = k = 2048 it needs 8 * 2^20 * 2 = exactly the
- * capacity).  No cudaMalloc, cudaMallocAsync, cudaFree or allocating library
- * routine is called.
+ * tensor-core path, plus SGEMM_STATUS_TOO_LARGE.  Every operand whose rows
+ * are 16 bytes apart and whose base is 16-byte aligned is read as stored
+ * and split inside the GEMM, whatever the problem's size (problems above
+ * 2^31 multiply-adds with both operands so run on CTA pairs: 256 x 256
+ * tiles, cta_group::2), so such calls need no scratch at all.  The split
+ * parts of the other operands live in one fixed array of
+ * SGEMM_NOALLOC_SCRATCH_FLOATS floats (64 MiB) in device memory that every
+ * GPU which loads this library holds until the process exits: 2 * rows * ka
+ * floats per such operand (rows = m for A, n for B; ka = k rounded up to
+ * 4); a problem that needs more is rejected with SGEMM_STATUS_TOO_LARGE
+ * before anything is enqueued (with both operands' rows misaligned,
+ * m = n = k = 2048 needs exactly the capacity).  No stream-K.  No
+ * cudaMalloc, cudaMallocAsync, cudaFree or allocating library routine is
+ * called.
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with the device current) and keeps it; make
@@ -275,12 +283,12 @@ int sgemm_last_cuda_error(void);
 typedef struct sgemm_plan {
     int path;          /* SGEMM_PATH_FFMA or SGEMM_PATH_TF32X3; 0 = no kernel (m or n is 0) */
     int kernel;        /* 0 FFMA GEMM kernel, 1 C = beta*C scale kernel, 2 3xTF32 tensor-core
-                          GEMM (launched after the two split kernels)                          */
+                          GEMM (after one split launch when an operand is not read as stored) */
     int bm, bn, bk;    /* CTA tile (rows of C, columns of C, k per pipeline stage)             */
     int rm, rn;        /* per-thread register tile of C (FFMA path; 0 otherwise)               */
     int threads;       /* threads per CTA                                                      */
     int stages;        /* shared-memory pipeline depth                                         */
-    int grid;          /* CTAs launched (tiles * split_k)                                      */
+    int grid;          /* CTAs launched (tiles * split_k; 2 * tiles for CTA pairs)             */
     int tiles;         /* output tiles = ceil(m/bm) * ceil(n/bn)                               */
     int k_tiles;       /* pipeline stages consumed per tile = ceil(k/bk)                       */
     int smem_bytes;    /* dynamic shared memory per CTA                                        */
@@ -328,8 +336,9 @@ int sgemm_device_status(int *flag, int clear);
  *
  * Fault injection for tests: with the environment variable
  * SGEMM_GB300_FAIL_ALLOC set, the tensor-core path's scratch allocation
- * reports cudaErrorMemoryAllocation without being attempted, so the call
- * returns 100 before launching anything (C is not written).
+ * reports cudaErrorMemoryAllocation without being attempted, so a call that
+ * needs scratch returns 100 before launching anything (C is not written);
+ * a call that needs none runs as usual.
  */
 int sgemm_selftest_wait(unsigned long long limit_ns, int *gave_up);
 

@@ -115,3 +115,12 @@ def test_traffic_record_matches_size_and_sources(tmp_path, monkeypatch):
     assert bench.traffic_record("tf32x3_raw_ab", 30) is None      # never captured at this size
     assert bench.traffic_record("ffma", 30) == 333              # single-record form
     assert bench.traffic_record("tf32x3_presplit", 10) is None
+
+
+def test_kernel_hash_ignores_comments_only():
+    """A traffic figure is void once the kernel's code changes, not when only
+    its comments do."""
+    code = "int f(int x) {\n    return x + 1;   // one more\n}\n/* a note */\n"
+    assert bench.strip_comments(code) == bench.strip_comments(code.replace("one more", "plus one"))
+    assert bench.strip_comments(code) != bench.strip_comments(code.replace("x + 1", "x + 2"))
+    assert "note" not in bench.strip_comments(code) and "return x + 1;" in bench.strip_comments(code)

@@ -105,6 +105,27 @@ def test_noalloc_needs_no_allocation(monkeypatch):
     assert np.array_equal(C_ref.cpu().numpy(), p.C0, equal_nan=True)
 
 
+@pytest.mark.parametrize("name", ["8192^3", "16384x128x8192"])
+def test_noalloc_large_workloads_with_allocations_failing(name, monkeypatch):
+    """The two large workloads need no scratch at all through this entry
+    point (both operands read as stored: CTA pairs at 8192^3, transposed
+    tiles at n = 128), so they run with every pool allocation made to fail;
+    checked on 4096 sampled outputs plus every tile edge."""
+    monkeypatch.setenv("SGEMM_GB300_FAIL_ALLOC", "1")
+    stream = torch.cuda.current_stream().cuda_stream
+    p = inputs.workload(name)
+    A, B, C = _device(p.A), _device(p.B), _device(p.C0)
+    st = _noalloc(p, A, B, C, stream)
+    assert st == 0, binding.status_string(st)
+    torch.cuda.synchronize()
+    rows, cols = inputs.sample_indices(p.m, p.n, 4096, seed=p.seed + 1000)
+    R, E = oracle.problem_f64_sampled(p, rows, cols)
+    got = C.cpu().numpy()[rows, cols]
+    ok, worst, where = oracle.within_tolerance(got, R, E, p.beta, p.C0[rows, cols] if p.beta else None)
+    assert ok, (worst, where)
+    assert binding.device_status() == 0
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     """Only operands that cannot be read as stored take scratch: 2 * rows *
     ka floats each (ka = k rounded up to 4).  With both operands' rows
