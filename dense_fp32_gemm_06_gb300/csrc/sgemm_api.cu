@@ -26,8 +26,9 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     // clusters of S CTAs (S = 2..8) of the tensor-core kernel that fit on the
-    // device at once, for the 256- and 128-wide tiles ([0] and [1])
-    int max_clusters[2][9] = {};
+    // device at once, for the 256- and 128-wide tiles ([0] and [1]); [2][2]:
+    // CTA pairs of the Pair configuration
+    int max_clusters[3][9] = {};
     // stream-ordered pool of the tensor-core path's scratch; keeps up to
     // its release threshold mapped between calls (the default pool's
     // threshold is 0: every synchronize would unmap the scratch and the next
@@ -144,6 +145,7 @@ int device_state(DeviceState **out) {
             if ((e = max_clusters_of<tf32x3::Wide>(S, &d.max_clusters[0][S])) != cudaSuccess) return fail_cuda(e);
             if ((e = max_clusters_of<tf32x3::Narrow>(S, &d.max_clusters[1][S])) != cudaSuccess) return fail_cuda(e);
         }
+        if ((e = max_clusters_of<tf32x3::Pair>(2, &d.max_clusters[2][2])) != cudaSuccess) return fail_cuda(e);
         if (d.pool == nullptr) {
             cudaMemPoolProps props = {};
             props.allocType = cudaMemAllocationTypePinned;
@@ -213,6 +215,15 @@ bool tma_readable(const void *X, long long ld, long long outer, int batch, long 
     if (!aligned(X, 16) || ld % 4 != 0) return false;
     if (batch > 1 && stride != 0 && (stride % 4 != 0 || stride < outer * ld)) return false;
     return true;
+}
+
+// Whether a K-major operand TMA cannot read as stored can be read in row
+// phases (rows j, j + 4, ...: 4 * ld floats apart, a multiple of 16 bytes):
+// always for one matrix; in a batch, one matrix for all problems or
+// problems that do not overlap, a multiple of 4 floats apart (each phase
+// then has the same shift in every problem).
+bool phase_readable(long long outer, long long ld, int batch, long long stride) {
+    return !(batch > 1 && stride != 0 && (stride % 4 != 0 || stride < outer * ld));
 }
 
 // The tensor-core plan on CTA pairs: 256 x 256 tiles of two CTAs each, whole
@@ -391,15 +402,38 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         const bool a_tma = tma_readable(A, lda, op_a == SGEMM_OP_N ? m : k, batch, stride_a);
         const bool b_tma = tma_readable(B, ldb, op_b == SGEMM_OP_N ? k : n, batch, stride_b);
         const bool b_small = (long long)m * n * k * (batch > 0 ? batch : 1) <= (1LL << 31);
-        pl->a_in_kernel = a_tma && !(env_ain && env_ain[0] == '0');
+        // an A that TMA cannot read as one tensor (rows not 16 bytes apart,
+        // a misaligned base) on untransposed tiles is read in four row
+        // phases, each of which TMA can read, and put in place and split by
+        // the GEMM's splitter warps
+        const bool a_phased = !a_tma && op_a == SGEMM_OP_N && !best_tr && phase_readable(m, lda, batch, stride_a);
+        pl->a_in_kernel = (a_tma || a_phased) && !(env_ain && env_ain[0] == '0');
         pl->b_in_kernel = b_tma && (env_bin && (env_bin[0] == '0' || env_bin[0] == '1') ? env_bin[0] == '1' : b_small);
         pl->threads = tf32x3::THREADS;
         // CTA pairs (cta_group::2): 256 x 256 tiles, each CTA staging (and,
         // for operands read as stored, splitting) 128 rows of A and 128 of
         // B; whole tiles only (no split-K, no stream-K).
         // SGEMM_GB300_PAIR = 1 asks for it where it applies.
+        // The default takes pairs where they are the faster plan and spare
+        // B's split pass: above 2^31 multiply-adds (where B would be split
+        // first), both operands read as stored, and 256 x 256 tiles that fill
+        // at least three quarters of the device's pair slots in one wave
+        // (measured, whole call, L2 flushed: 2048^3 81.9 against 83.9 us; at
+        // 8192^3, many waves, 4.02 against 3.71 ms, and at 4096^3 against
+        // stream-K 622 against 527 us, so those keep single CTAs).
+        // SGEMM_GB300_PAIR = 1 / 0 pins the choice (1: wherever the tiles are
+        // not transposed).
         const char *env_pair = std::getenv("SGEMM_GB300_PAIR");
-        if (env_pair && env_pair[0] == '1' && !best_tr) {
+        const long long pair_tiles = (long long)((m + 255) / 256) * ((n + 255) / 256) * (batch > 0 ? batch : 1);
+        const long long pair_slots = max_clusters ? max_clusters[2][2] : num_sms / 2;
+        // (any pin of the single-CTA plan -- tile width, split-K, transposed
+        // tiles, stream-K -- keeps that plan)
+        const bool pinned = force_bn != 0 || (force_s >= 1 && force_s <= 8) || force_tr != -1 || force_sk != -1;
+        const bool pair_auto = a_tma && b_tma && !b_small && pl->a_in_kernel && !(env_bin && env_bin[0] == '0') &&
+                               !pinned && pair_tiles <= pair_slots && 4 * pair_tiles >= 3 * pair_slots;
+        if (!best_tr && (env_pair ? env_pair[0] == '1' : pair_auto)) {
+            if (!env_pair) pl->b_in_kernel = 1;
+            if (!a_tma) pl->a_in_kernel = 0;   // pairs read A by TMA or take it split
             set_pair_plan(m, n, k, pl);
             return SGEMM_STATUS_OK;
         }
@@ -466,8 +500,11 @@ int make_tensor_map(CUtensorMap *map, const float *base, long long rows, long lo
 //     rows x k (row pitch ld); otherwise stored k x rows (MN-major);
 //   pre-split: hi / lo arrays of rows x ka per problem (pitch ka), problems
 //     rows * ka apart.
+//   phased: raw and K-major, but with rows TMA cannot read as one tensor:
+//     read in four row phases (X on untransposed single-CTA tiles only).
 struct Operand {
     bool raw = false, kmajor = true;
+    bool phased = false;
     const float *hi = nullptr, *lo = nullptr;
     long long ld = 0, bstride = 0;
     int rows = 0;
@@ -500,6 +537,36 @@ int encode_operand(const Operand &o, int k, int box_rows, int batch, CUtensorMap
         st = make_tensor_map(lo, o.lo, o.rows, k, ka, batch, (long long)o.rows * ka, box_rows, tf32x3::BK,
                              CU_TENSOR_MAP_SWIZZLE_64B);
     return st;
+}
+
+// The four row-phase tensor maps of a phased operand (see kPhased in the
+// kernel): phase j = rows j, j + 4, j + 8, ... (a row pitch of 4 * ld
+// floats, a multiple of 16 bytes), based at its first row rounded down to
+// 16 bytes, each row of the view extended at the front by the shift sh_j
+// (0..3 floats) so that it holds k + sh_j columns: the TMA box (20 columns
+// from a slab's first k, 32 row groups) then covers the slab's 16 values
+// of every row, and whatever lies past k + sh_j reads as zero.  The bytes
+// in front of a row (its shift) lie in the 16-byte granule of the row's
+// first value.  A phase with no rows (rows < 4) repeats phase 0, whose
+// values then land in tile rows that are never stored.  Its shifts go into
+// *shifts (2 bits per phase).  Needs problems 16 bytes apart (bstride % 4
+// == 0) in a batch.
+int encode_phased(const Operand &o, int k, int batch, CUtensorMap *maps[4], int *shifts, int *z) {
+    const int nb = batch > 1 && o.bstride != 0 ? batch : 1;
+    *z = nb > 1;
+    *shifts = 0;
+    for (int j = 0; j < 4; ++j) {
+        const int jj = j < o.rows ? j : 0;
+        const uintptr_t first = reinterpret_cast<uintptr_t>(o.hi + (long long)jj * o.ld);
+        const int sh = (int)((first & 15) / 4);
+        const float *base = reinterpret_cast<const float *>(first - (first & 15));
+        const long long rows_j = (o.rows - jj + 3) / 4;
+        const int st = make_tensor_map(maps[j], base, rows_j, (long long)k + sh, 4 * o.ld, nb, o.bstride,
+                                       tf32x3::BM / 4, tf32x3::PHASE_COLS, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st) return st;
+        *shifts |= sh << (2 * j);
+    }
+    return SGEMM_STATUS_OK;
 }
 
 int ka_of(int k) { return (k + 3) & ~3; }
@@ -565,7 +632,7 @@ int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *b
 template <class Cfg, bool TRANS, bool XM, bool YM>
 cudaError_t launch_tc_one(const cudaLaunchConfig_t &cfg, const CUtensorMap *maps, const tf32x3::Params &a) {
     return cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM>, maps[0], maps[1], maps[2],
-                              maps[3], a);
+                              maps[3], maps[4], maps[5], a);
 }
 
 template <class Cfg, bool TRANS>
@@ -578,7 +645,7 @@ cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, bool xm, bool ym, const CUt
 // Everything a tensor-core GEMM launch needs, prepared before anything is
 // enqueued (so that a failure here leaves the stream untouched).
 struct GemmLaunch {
-    CUtensorMap maps[4];   // X hi, X lo, Y hi, Y lo
+    CUtensorMap maps[6];   // X hi, X lo, Y hi, Y lo; a phased X: phases 0..3 in 0, 1, 4, 5
     tf32x3::Params prm;
     bool xm = false, ym = false;
 };
@@ -595,7 +662,19 @@ int prepare_gemm(int m, int n, int k, float alpha, const Operand &a, const Opera
     // half of them per CTA of a pair)
     const int y_rows = pl.trans ? pl.bm : (pl.pair ? pl.bn / 2 : pl.bn);
     tf32x3::Params &p = L->prm;
-    int st = encode_operand(x, k, tf32x3::BM, batch, &L->maps[0], &L->maps[1], &p.x_z);
+    if (y.phased || (x.phased && (pl.trans || pl.pair || !x.kmajor))) return SGEMM_STATUS_UNSUPPORTED;   // plans never ask for these
+    int st;
+    p.x_shift = 0;
+    if (x.phased) {
+        CUtensorMap *ph[4] = {&L->maps[0], &L->maps[1], &L->maps[4], &L->maps[5]};
+        st = encode_phased(x, k, batch, ph, &p.x_shift, &p.x_z);
+    } else {
+        st = encode_operand(x, k, tf32x3::BM, batch, &L->maps[0], &L->maps[1], &p.x_z);
+        if (!st) {   // not read
+            L->maps[4] = L->maps[0];
+            L->maps[5] = L->maps[0];
+        }
+    }
     if (!st) st = encode_operand(y, k, y_rows, batch, &L->maps[2], &L->maps[3], &p.y_z);
     if (st) return st;
     L->xm = x.raw && !x.kmajor;
@@ -611,7 +690,7 @@ int prepare_gemm(int m, int n, int k, float alpha, const Operand &a, const Opera
     p.tiles_n = (n + pl.bn - 1) / pl.bn;
     p.group_m = pl.group_m;
     p.stride_c = stride_c;
-    p.x_src = x.raw ? tf32x3::kRaw : tf32x3::kPreSplit;
+    p.x_src = x.phased ? tf32x3::kPhased : x.raw ? tf32x3::kRaw : tf32x3::kPreSplit;
     p.y_src = y.raw ? tf32x3::kRaw : tf32x3::kPreSplit;
     p.c_vec = pl.c_vec;
     p.sk_ctas = pl.stream_k;
@@ -702,6 +781,7 @@ int run_tf32x3(int m, int n, int k, float alpha, const float *A, int lda, const 
     if (pl.a_in_kernel) {
         oa.raw = true;
         oa.kmajor = pl.op_a == SGEMM_OP_N;   // stored m x k; else k x m
+        oa.phased = !tma_readable(A, lda, pl.op_a == SGEMM_OP_N ? m : k, bt.count, bt.sa);
         oa.hi = A;
         oa.ld = lda;
         oa.bstride = bt.sa;
@@ -1024,13 +1104,16 @@ int sgemm_tf32x3_noalloc(int m, int n, int k, float alpha, const float *A, int l
     if (st != SGEMM_STATUS_OK) return st;
     // read every operand TMA can read as stored, whatever the size (the
     // plan splits a large B with the split pass, which is faster there):
-    // scratch only for operands whose rows are not 16 bytes apart.  With
-    // both read as stored, large problems run on CTA pairs, which split B
-    // in half the shared-memory traffic per SM (measured, whole call:
-    // 8192^3 4.29 ms against 5.8 ms on single-CTA 128 x 256 tiles)
+    // scratch only for a B whose rows TMA cannot read, and for such an A on
+    // transposed tiles (elsewhere the GEMM reads it in row phases).  With
+    // both read by TMA as stored, large problems run on CTA pairs, which
+    // split B in half the shared-memory traffic per SM (measured, whole
+    // call: 8192^3 4.29 ms against 5.8 ms on single-CTA 128 x 256 tiles);
+    // pairs take no phased A
     if (pl.kernel != kKernelScale && tma_readable(B, ldb, k, 1, 0)) {
         pl.b_in_kernel = 1;
-        if (pl.a_in_kernel && !pl.trans && (long long)m * n * k > (1LL << 31)) set_pair_plan(m, n, k, &pl);
+        if (pl.a_in_kernel && tma_readable(A, lda, m, 1, 0) && !pl.trans && (long long)m * n * k > (1LL << 31))
+            set_pair_plan(m, n, k, &pl);
     }
     if (pl.kernel == kKernelScale) {
         scale_c_kernel<<<pl.grid, pl.threads, 0, stream>>>(C, ldc, m, n, beta, 0);

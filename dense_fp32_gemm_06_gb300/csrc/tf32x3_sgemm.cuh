@@ -70,7 +70,8 @@
 //     being finished by the last of its CTAs from partials in a workspace.
 //     CTA pairs (Pair config, cta_group::2): two CTAs of a cluster compute a
 //     256 x 256 tile with M = 256 MMAs issued by the even CTA; each stages
-//     and splits its 128 rows of A and of B (6 stages of 32 KB).
+//     and splits its 128 rows of A and of B (7 stages of 32 KB; C staged in
+//     the ring once the tile's last slab is done).
 //     After a split pass, a GEMM that runs in one wave is launched as its
 //     programmatic dependent: it sets up while the split finishes, and its
 //     producer waits for it before the first load.
@@ -121,7 +122,12 @@ struct Config {
     static constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;   // A_hi, A_lo, B_hi, B_lo
     static constexpr int TMEM_COLS = 2 * BN;                      // two accumulators
     static constexpr int COLS_PER_THREAD = BN / 2;                // two warps per 32-lane group
-    static constexpr int EPI_BYTES = ACC_WARPS * 32 * 32 * 4;     // a 32 x 32 staging block per accumulator warp
+    // C's staging blocks (a 32 x 32 block per accumulator warp, 32 KB): in
+    // their own region, or -- for CTA pairs, which never run stream-K, so a
+    // CTA stores its one tile only after its last slab -- at the start of
+    // the then idle stage ring, which leaves room for a seventh stage
+    static constexpr bool EPI_IN_RING = PAIR;
+    static constexpr int EPI_BYTES = EPI_IN_RING ? 0 : ACC_WARPS * 32 * 32 * 4;
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_REGION + EPI_BYTES;
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
     static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "power-of-two TMEM allocation");
@@ -129,7 +135,7 @@ struct Config {
 };
 using Wide = Config<256, 4>;     // 48 KB stages
 using Narrow = Config<128, 6>;   // 32 KB stages
-using Pair = Config<256, 6, true>;   // 32 KB stages per CTA, 256 x 256 tiles per CTA pair
+using Pair = Config<256, 7, true>;   // 32 KB stages per CTA, 256 x 256 tiles per CTA pair
 
 constexpr int kStatusProducer = 0x201;
 constexpr int kStatusMma = 0x202;
@@ -149,8 +155,10 @@ struct Params {
     // map has a batch dimension) or z = 0 (one operand shared by the batch)
     long long stride_c;
     int x_z, y_z;
-    // where each MMA operand comes from (kPreSplit or kRaw, see the kernel)
+    // where each MMA operand comes from (kPreSplit, kRaw or kPhased, see the
+    // kernel); kPhased: bits 2j..2j+1 of x_shift = row phase j's shift
     int x_src, y_src;
+    int x_shift;
     // C rows 16-byte aligned (ldc % 4 == 0, C 16-byte aligned): float4 access
     int c_vec;
     // stream-K (sk_ctas > 0, grid = G = sk_ctas persistent CTAs, one
@@ -168,31 +176,34 @@ struct Params {
     float *sk_ws;
     int *sk_cnt;
 };
+// (a parameter block above 128 bytes measurably raised the GEMM kernel's
+// register spills)
+static_assert(sizeof(Params) <= 128, "kernel parameter block");
 
 // Segment `si` of the work of CTA blockIdx.x -- one tile and a range
-// [k0, k0 + nk) of its kt_all slabs; false past the last.  Stream-K (see
-// Params): the whole tiles blockIdx.x + w G first, then the CTA's run of
+// [k0, k0 + nk) of its kt_all slabs; false past the last.  Stream-K over
+// sk_ctas > 0 CTAs (see Params): the whole tiles blockIdx.x + w G first, then the CTA's run of
 // the remaining tiles' slab sequence cut at tile boundaries.  Otherwise one
 // segment of tile blockIdx.x / ctas_per_tile (nsplit for a split-K cluster,
 // 2 for a CTA pair, else 1): split-K cluster rank `rank`'s share of its
 // slabs (possibly empty), or all of them.  Recomputed on demand so that no
 // role keeps iteration state next to its accumulators.
-__device__ __forceinline__ bool cta_segment(const Params &p, int kt_all, int tiles, uint32_t nsplit, uint32_t rank,
+__device__ __forceinline__ bool cta_segment(int sk_ctas, int kt_all, int tiles, uint32_t nsplit, uint32_t rank,
                                             int si, int &tile, int &k0, int &nk, int ctas_per_tile) {
     long long it0, it1;
-    if (p.sk_ctas > 0) {
-        const int whole = tiles / p.sk_ctas;
+    if (sk_ctas > 0) {
+        const int whole = tiles / sk_ctas;
         if (si < whole) {
-            tile = (int)blockIdx.x + si * p.sk_ctas;
+            tile = (int)blockIdx.x + si * sk_ctas;
             k0 = 0;
             nk = kt_all;
             return true;
         }
         si -= whole;
-        const long long base = (long long)whole * p.sk_ctas * kt_all;
-        const long long T = (long long)(tiles - whole * p.sk_ctas) * kt_all;
-        it0 = base + T * blockIdx.x / p.sk_ctas;
-        it1 = base + T * (blockIdx.x + 1) / p.sk_ctas;
+        const long long base = (long long)whole * sk_ctas * kt_all;
+        const long long T = (long long)(tiles - whole * sk_ctas) * kt_all;
+        it0 = base + T * blockIdx.x / sk_ctas;
+        it1 = base + T * (blockIdx.x + 1) / sk_ctas;
     } else {
         if (si > 0) return false;
         tile = (int)blockIdx.x / ctas_per_tile;
@@ -243,21 +254,46 @@ __device__ __forceinline__ void split_one(float x, float &h, float &l) {
 // GB300: every output of x * I equals x truncated to TF32, ties and all), so
 // hi = trunc(x); r = x - hi is exact in FP32 and lo = tf32(r), rounded to
 // nearest with ties away from zero, with |x - hi - lo| <= 2^-11 |r| <
-// 2^-21 |x|.  The rounding is done on the bits (add half of the dropped
-// range to the magnitude, then drop it): the same result as cvt.rna.tf32
-// for every finite r (|r| < 2^-10 |x| cannot round up to infinity),
-// at two integer operations, which measured ~6 % faster than the
-// conversion instruction in the GEMM's splitter warps at 8192^3.
+// 2^-21 |x|.  The rounding is done on the bits: add half of the dropped
+// range to the magnitude (|r| < 2^-10 |x| cannot round up to infinity).
+// Dropping the low 13 bits afterwards is left to the MMA, which reads them
+// that way -- the product is the same as with cvt.rna.tf32 -- so a value
+// costs three operations (the conversion instruction measured ~6 % slower
+// in the splitter warps at 8192^3).  The result is meant for the MMA only.
 __device__ __forceinline__ float lo_of_raw(float x) {
     const float h = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
-    return __uint_as_float((__float_as_uint(x - h) + 0x1000u) & 0xFFFFE000u);
+    return __uint_as_float(__float_as_uint(x - h) + 0x1000u);
+}
+
+// d0 = a0 - b0, d1 = a1 - b1 as one packed instruction (sub.rn.f32x2).
+__device__ __forceinline__ void sub2(float &d0, float &d1, float a0, float a1, float b0, float b1) {
+    asm("{\n"
+        ".reg .b64 ra, rb, rd;\n"
+        "mov.b64 ra, {%2, %3};\n"
+        "mov.b64 rb, {%4, %5};\n"
+        "sub.rn.f32x2 rd, ra, rb;\n"
+        "mov.b64 {%0, %1}, rd;\n"
+        "}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// lo_of_raw of four values, the subtractions as two packed instructions.
+__device__ __forceinline__ float4 lo4_of_raw(float4 x) {
+    const float hx = __uint_as_float(__float_as_uint(x.x) & 0xFFFFE000u);
+    const float hy = __uint_as_float(__float_as_uint(x.y) & 0xFFFFE000u);
+    const float hz = __uint_as_float(__float_as_uint(x.z) & 0xFFFFE000u);
+    const float hw = __uint_as_float(__float_as_uint(x.w) & 0xFFFFE000u);
+    float4 r;
+    sub2(r.x, r.y, x.x, x.y, hx, hy);
+    sub2(r.z, r.w, x.z, x.w, hz, hw);
+    return make_float4(__uint_as_float(__float_as_uint(r.x) + 0x1000u), __uint_as_float(__float_as_uint(r.y) + 0x1000u),
+                       __uint_as_float(__float_as_uint(r.z) + 0x1000u), __uint_as_float(__float_as_uint(r.w) + 0x1000u));
 }
 
 // A (m x k, row pitch lda) -> hi, lo (m x ka, row pitch ka).  VEC: A and
 // lda 16-byte aligned, so every row is read as float4 except a k % 4 tail
 // (read element by element: the bytes past k may lie outside A).
-// hi == nullptr: only lo, for a GEMM that reads A itself as its hi operand
-// (hi = A with its low 13 bits dropped, lo = tf32(A - hi); see lo_of_raw).
 // The work of block (bx, by) of a gx x gy grid, on problem bz of a strided
 // batch (split_a_kernel runs it on its own grid, split_pair_kernel on part
 // of a shared one).
@@ -267,22 +303,17 @@ __device__ __forceinline__ void split_rows(const float *__restrict__ A, long lon
                                            long long src_batch, long long dst_batch, int bx, int by, int bz, int gx,
                                            int gy) {
     A += bz * src_batch;
-    if (hi != nullptr) hi += bz * dst_batch;
+    hi += bz * dst_batch;
     lo += bz * dst_batch;
     const int full4 = VEC ? k / 4 : 0;               // float4 chunks entirely inside the row
     const int scal0 = 4 * full4;                      // first element done one at a time
     const int stride = gx * (int)blockDim.x;
     for (int row = by; row < m; row += gy) {
         const float *src = A + (long long)row * lda;
-        float *h = hi != nullptr ? hi + (long long)row * ka : nullptr;
+        float *h = hi + (long long)row * ka;
         float *l = lo + (long long)row * ka;
         for (int c = bx * (int)blockDim.x + (int)threadIdx.x; c < full4; c += stride) {
             const float4 x = __ldg(reinterpret_cast<const float4 *>(src) + c);
-            if (hi == nullptr) {
-                reinterpret_cast<float4 *>(l)[c] =
-                    make_float4(lo_of_raw(x.x), lo_of_raw(x.y), lo_of_raw(x.z), lo_of_raw(x.w));
-                continue;
-            }
             float4 xh, xl;
             split_one(x.x, xh.x, xl.x);
             split_one(x.y, xh.y, xl.y);
@@ -292,10 +323,6 @@ __device__ __forceinline__ void split_rows(const float *__restrict__ A, long lon
             reinterpret_cast<float4 *>(l)[c] = xl;
         }
         for (int t = scal0 + bx * (int)blockDim.x + (int)threadIdx.x; t < k; t += stride) {
-            if (hi == nullptr) {
-                l[t] = lo_of_raw(__ldg(src + t));
-                continue;
-            }
             float xh, xl;
             split_one(__ldg(src + t), xh, xl);
             h[t] = xh;
@@ -392,8 +419,8 @@ __global__ void __launch_bounds__(256) split_pair_kernel(SplitJob j0, SplitJob j
 // operand.  Untransposed tiles: X = rows of A (m side), Y = columns of B
 // (n side).  TRANS tiles: X = columns of B, Y = rows of A.
 //
-// Each operand reaches a stage slot in one of two ways (Params::x_src,
-// y_src):
+// Each operand reaches a stage slot in one of these ways (Params::x_src,
+// y_src; kPhased below for X only):
 //   kPreSplit: its hi and lo parts were written by the split pass (K-major,
 //     row pitch ka) and TMA loads both;
 //   kRaw: TMA loads the operand as the caller stored it into the hi slot --
@@ -413,6 +440,22 @@ __global__ void __launch_bounds__(256) split_pair_kernel(SplitJob j0, SplitJob j
 // even with both operands raw, far inside the FP32 acceptance bound.
 constexpr int kPreSplit = 0;
 constexpr int kRaw = 1;
+// kPhased: X (K-major A on untransposed single-CTA tiles) whose rows TMA
+// cannot read as one tensor -- rows not 16 bytes apart, or a misaligned
+// base.  Every fourth row is, though: the rows 4i + j of row phase j
+// (j = 0..3) are 4 * lda floats apart, a multiple of 16 bytes, so each
+// phase is a tensor of its own, based at its first row rounded down to 16
+// bytes, where each row starts sh_j (0..3) floats into its own row of the
+// view.  TMA loads the four phases' 32-row boxes of PHASE_COLS = 20 columns
+// (16 k and the shift) into a staging area over the X hi and lo slots; the
+// splitter warps read each row's 16 values from sh_j on, then write hi
+// (the value as stored) and lo into the swizzled slots, where the MMA takes
+// them like a raw operand's -- hi x hi too only after that.
+constexpr int kPhased = 2;
+constexpr int PHASE_COLS = 20;
+constexpr int PHASE_BOX = (BM / 4) * PHASE_COLS * 4;   // one phase's 32 rows, bytes
+constexpr int PHASE_BYTES = 4 * PHASE_BOX;
+static_assert(PHASE_BYTES <= 2 * A_TILE, "staging fits over the X hi and lo slots");
 
 // Loads one operand's part of a slab: `rows` rows starting at row0 and 16 k
 // starting at kx, of problem z.  K-major: one box (16 k x rows); MN-major:
@@ -455,8 +498,7 @@ __device__ __forceinline__ void split_slot_lo(const uint8_t *raw_slot, uint8_t *
         for (int j = 0; j < G; ++j) x[j] = raw[ct + (j0 + j) * CW];
 #pragma unroll
         for (int j = 0; j < G; ++j)
-            lo[ct + (j0 + j) * CW] =
-                make_float4(lo_of_raw(x[j].x), lo_of_raw(x[j].y), lo_of_raw(x[j].z), lo_of_raw(x[j].w));
+            lo[ct + (j0 + j) * CW] = lo4_of_raw(x[j]);
     }
 }
 
@@ -475,17 +517,55 @@ __device__ __forceinline__ void split_slots_lo(const uint8_t *x_raw, uint8_t *x_
 #pragma unroll
     for (int j = 0; j < PY; ++j) v[PX + j] = yr[ct + j * CW];
 #pragma unroll
-    for (int j = 0; j < PX + PY; ++j) v[j] = make_float4(lo_of_raw(v[j].x), lo_of_raw(v[j].y), lo_of_raw(v[j].z), lo_of_raw(v[j].w));
+    for (int j = 0; j < PX + PY; ++j) v[j] = lo4_of_raw(v[j]);
 #pragma unroll
     for (int j = 0; j < PX; ++j) xl[ct + j * CW] = v[j];
 #pragma unroll
     for (int j = 0; j < PY; ++j) yl[ct + j * CW] = v[PX + j];
 }
 
+// A phased X slab (kPhased): the four phases' staged boxes at hi_slot
+// (phase j's 32 rows of PHASE_COLS floats at j * PHASE_BOX; its rows start
+// sh_j = bits 2j..2j+1 of `shifts` floats in) -> hi (the value as stored)
+// and lo, K-major in the 64-byte swizzle (16-byte chunk q of row r at chunk
+// q ^ ((r >> 1) & 3)).  The staging lies over both slots, so the CW threads
+// (this one is ct) read all of their values first and meet at a barrier
+// (named barrier 2 for two warps) before writing.  A warp reads one
+// 16-byte chunk q of rows 4i + j and 4(i + 4) + j (j = 0..3) per lane:
+// its 32 loads fall in 32 distinct banks when the four shifts differ (lda
+// odd).
+template <int CW>
+__device__ __forceinline__ void split_phased(uint8_t *hi_slot, uint8_t *lo_slot, uint32_t shifts, int ct) {
+    constexpr int UNITS = 16 / (CW / 32);   // warp-wide reads of 32 chunks per thread
+    const int lane = ct & 31, q = lane & 3, j = (lane >> 2) & 3;
+    const float *stg = reinterpret_cast<const float *>(hi_slot) + j * (PHASE_BOX / 4) + ((shifts >> (2 * j)) & 3) + 4 * q;
+    float4 v[UNITS];
+#pragma unroll
+    for (int t = 0; t < UNITS; ++t) {
+        const int u = (ct >> 5) + (CW / 32) * t;
+        const int i = (u & 3) + 8 * (u >> 2) + 4 * (lane >> 4);
+        const float *x = stg + i * PHASE_COLS;
+        v[t] = make_float4(x[0], x[1], x[2], x[3]);
+    }
+    if constexpr (CW == 32)
+        __syncwarp();
+    else
+        named_barrier_sync(2, CW);
+#pragma unroll
+    for (int t = 0; t < UNITS; ++t) {
+        const int u = (ct >> 5) + (CW / 32) * t;
+        const int r = 4 * ((u & 3) + 8 * (u >> 2) + 4 * (lane >> 4)) + j;
+        const int off = r * 64 + ((q ^ ((r >> 1) & 3)) << 4);
+        *reinterpret_cast<float4 *>(hi_slot + off) = v[t];
+        *reinterpret_cast<float4 *>(lo_slot + off) = lo4_of_raw(v[t]);
+    }
+}
+
 template <class Cfg, bool TRANS = false, bool X_MN = false, bool Y_MN = false>
 __global__ void __launch_bounds__(THREADS, 1)
     tf32x3_gemm_kernel(const __grid_constant__ CUtensorMap tmXhi, const __grid_constant__ CUtensorMap tmXlo,
                        const __grid_constant__ CUtensorMap tmYhi, const __grid_constant__ CUtensorMap tmYlo,
+                       const __grid_constant__ CUtensorMap tmX2, const __grid_constant__ CUtensorMap tmX3,
                        const Params p) {
     constexpr int BN = Cfg::BN, STAGES = Cfg::STAGES, Y_TILE = Cfg::B_TILE, STAGE_BYTES = Cfg::STAGE_BYTES;
     constexpr int X_TILE = A_TILE;
@@ -523,11 +603,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     // 16-byte landing / source pad of that copy
     const uint32_t bar_peer = bar_conv_y + 8 * STAGES;
     const uint32_t sig_pad = (bar_peer + 8 * STAGES + 15) & ~15u;
-    float4 *const epi = reinterpret_cast<float4 *>(bars + BAR_REGION);   // [ACC_WARPS][32 rows][8 float4]
+    // [ACC_WARPS][32 rows][8 float4]
+    float4 *const epi = reinterpret_cast<float4 *>(Cfg::EPI_IN_RING ? smem : bars + BAR_REGION);
+    static_assert(!Cfg::EPI_IN_RING || ACC_WARPS * 32 * 32 * 4 <= STAGES * STAGE_BYTES, "staging fits the ring");
     static_assert(8 * (5 * STAGES + 7) + 32 <= BAR_REGION, "barrier region");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool x_raw = p.x_src == kRaw, y_raw = p.y_src == kRaw;
+    const bool x_ph = !TRANS && !X_MN && !PAIR && p.x_src == kPhased;   // X loaded in row phases
+    const bool x_raw = p.x_src == kRaw || x_ph, y_raw = p.y_src == kRaw;
     const bool c_vec = p.c_vec != 0;
     // split-K: the CTAs of a cluster share one output tile and take
     // consecutive ranges of its k slabs (a cluster of one without split-K).
@@ -545,7 +628,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     float *const Cb = p.C + (long long)blockIdx.y * p.stride_c;
     const int KT_ALL = (p.k + BK - 1) / BK;
     const int tiles = p.tiles_m * p.tiles_n;
-    const bool sk = p.sk_ctas > 0;
+    // stream-K's CTA count (CTA pairs never run stream-K: a constant 0 lets
+    // the compiler drop those paths)
+    const int SK_CTAS = PAIR ? 0 : p.sk_ctas;
+    const bool sk = SK_CTAS > 0;
     // this CTA's work: whole tiles of the full waves and a share of the
     // remaining tiles' slabs (stream-K), a consecutive range of one tile's
     // slabs (split-K cluster rank `rank`), or one whole tile
@@ -593,6 +679,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tmXlo);
         tma_prefetch_desc(&tmYhi);
         tma_prefetch_desc(&tmYlo);
+        if (x_ph) {
+            tma_prefetch_desc(&tmX2);
+            tma_prefetch_desc(&tmX3);
+        }
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -620,13 +710,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             griddep_wait();
             int tile, k0, nk, g = 0;   // g: slabs issued so far (ring position)
             bool stop = false;
-            for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
+            for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
                 int m0, n0;
                 tile_origin(tile, m0, n0);
                 // PAIR: this CTA's 128 rows of A and Y_ROWS rows of B
                 const int x0 = TRANS ? n0 : m0 + (int)prank * BM, y0 = TRANS ? m0 : n0 + (int)prank * Y_ROWS;
                 const int zx = p.x_z ? (int)blockIdx.y : 0, zy = p.y_z ? (int)blockIdx.y : 0;
-                const uint32_t tx_bytes = (x_raw ? 1 : 2) * X_TILE + (y_raw ? 1 : 2) * Y_TILE;
+                const uint32_t tx_bytes = (x_ph ? PHASE_BYTES : (x_raw ? 1 : 2) * X_TILE) + (y_raw ? 1 : 2) * Y_TILE;
                 for (int kt = 0; kt < nk; ++kt, ++g) {
                     const int s = g % STAGES;
                     if (g >= STAGES && !mbar_wait(bar_empty + 8 * s, ((g / STAGES) - 1) & 1, kStatusProducer)) {
@@ -642,7 +732,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t fb = bar_full + 8 * s;
                     mbar_arrive_expect_tx(fb, tx_bytes);
                     const int kx = (k0 + kt) * BK;
-                    load_operand<X_MN, BM>(st + X_HI, st + X_LO, &tmXhi, &tmXlo, x_raw, x0, kx, zx, fb);
+                    if (x_ph) {
+                        // the four row phases of the tile's 128 rows (32 row
+                        // groups from x0 / 4), PHASE_COLS columns from kx
+                        tma_load_3d(st + X_HI + 0 * PHASE_BOX, &tmXhi, kx, x0 / 4, zx, fb);
+                        tma_load_3d(st + X_HI + 1 * PHASE_BOX, &tmXlo, kx, x0 / 4, zx, fb);
+                        tma_load_3d(st + X_HI + 2 * PHASE_BOX, &tmX2, kx, x0 / 4, zx, fb);
+                        tma_load_3d(st + X_HI + 3 * PHASE_BOX, &tmX3, kx, x0 / 4, zx, fb);
+                    } else {
+                        load_operand<X_MN, BM>(st + X_HI, st + X_LO, &tmXhi, &tmXlo, x_raw, x0, kx, zx, fb);
+                    }
                     load_operand<Y_MN, Y_ROWS>(st + Y_HI, st + Y_LO, &tmYhi, &tmYlo, y_raw, y0, kx, zy, fb);
                 }
             }
@@ -674,7 +773,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr uint32_t idesc = tc::idesc_tf32_f32<PAIR ? 2 * BM : BM, BN, X_MN, Y_MN>();
             int tile, k0, nk, g = 0, cg = 0;   // g: slabs consumed, cg: chunks started
             bool stop = false;
-            for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
+            for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
               for (int kt = 0; kt < nk; ++kt, ++g) {
                 // each segment's slabs accumulate in chunks of CHUNK_STAGES
                 // slabs, alternating between the two TMEM buffers
@@ -706,16 +805,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                 }
+                // hi x hi needs only what TMA loaded; each product with a lo
+                // part of a raw operand waits for the splitters to write it
+                // (a phased X's hi part too)
+                if (x_ph && !mbar_wait(bar_conv_x + 8 * s, ph, kStatusMma)) {
+                    *abort_flag = 1;
+                    stop = true;
+                    break;
+                }
                 tc::fence_after_sync();
                 const uint32_t st = stage0 + s * STAGE_BYTES;
                 const uint32_t d = tmem + (uint32_t)(b * BN);
-                // hi x hi needs only what TMA loaded; each product with a lo
-                // part of a raw operand waits for the splitters to write it
 #pragma unroll
                 for (int kk = 0; kk < BK / UMMA_K; ++kk)
                     mma(d, operand_desc<X_MN>(st + X_HI, kk), operand_desc<Y_MN>(st + Y_HI, kk), idesc,
                         (chunk_first && kk == 0) ? 0u : 1u);
-                if (x_raw) {
+                if (x_raw && !x_ph) {
                     if (!mbar_wait(bar_conv_x + 8 * s, ph, kStatusMma)) {
                         *abort_flag = 1;
                         stop = true;
@@ -764,7 +869,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // nothing to split (both operands come split), except that the odd
         // CTA of a pair still tells the leader when its slab has landed
         bool stop = !x_raw && !y_raw && !(PAIR && prank == 1);
-        for (int si = 0; !stop && cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
+        for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
           for (int kt = 0; kt < nk; ++kt, ++g) {
             if (CONV_PER_WARP && (g % CONV_WARPS) != mine) continue;
             const int s = g % STAGES;
@@ -775,7 +880,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             // barrier below on every slab, so they agree here whether to go
             // on (a wait that ran out in one warp must not leave the other
             // at that barrier)
-            if (PAIR && prank == 1) quit = named_barrier_or(2, CONV_THREADS, quit);
+            // so do both splitter warps of a phased X (split_phased)
+            if ((PAIR && prank == 1) || (!CONV_PER_WARP && x_ph)) quit = named_barrier_or(2, CONV_THREADS, quit);
             if (quit) {
                 stop = true;
                 break;
@@ -803,7 +909,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // each lo part signalled to this CTA's MMA issuer as soon as
                 // it is written
                 if (x_raw) {
-                    split_slot_lo<X_TILE, CW>(st + X_HI, st + X_LO, ct);
+                    if (x_ph)
+                        split_phased<CW>(st + X_HI, st + X_LO, (uint32_t)p.x_shift, ct);
+                    else
+                        split_slot_lo<X_TILE, CW>(st + X_HI, st + X_LO, ct);
                     tc::fence_proxy_async_smem();
                     mbar_arrive(bar_conv_x + 8 * s);
                 }
@@ -1028,7 +1137,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         };
 
         int tile, k0, nk, cg = 0;   // cg: chunks drained so far
-        for (int si = 0; cta_segment(p, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
+        for (int si = 0; cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
 #pragma unroll
             for (int j = 0; j < COLS_PER_THREAD; ++j) acc[j] = 0.f;
             const int nc = (nk + CHUNK_STAGES - 1) / CHUNK_STAGES;

@@ -171,9 +171,11 @@ def test_auto_policy():
     assert hplan(8192, 8192, 8192)[1]["path"] == binding.PATH_TF32X3
     assert hplan(16, 16, 8193)[1]["path"] == binding.PATH_TF32X3
     assert hplan(1000, 1500, 777, lda=777)[1]["path"] == binding.PATH_TF32X3
-    st, p = hplan(2048, 2048, 2048, path=binding.PATH_TF32X3)
-    assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"]) == (128, 256, 16, 384)
-    assert p["grid"] == p["tiles"] == 16 * 8 and p["k_tiles"] == 128 and p["stream_k"] == 0
+    st, p = hplan(2048, 2048, 2048, path=binding.PATH_TF32X3)     # CTA pairs: 8 x 8 tiles of 256 x 256
+    assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"], p["pair"]) == (256, 256, 16, 384, 1)
+    assert p["tiles"] == 8 * 8 and p["grid"] == 2 * p["tiles"] and p["k_tiles"] == 128 and p["stream_k"] == 0
+    st, p = hplan(8192, 8192, 8192, path=binding.PATH_TF32X3)     # many waves: single CTAs
+    assert st == 0 and (p["bm"], p["bn"], p["pair"]) == (128, 256, 0) and p["grid"] == p["tiles"] == 64 * 32
 
 
 def test_stream_k_policy(monkeypatch):
@@ -191,7 +193,7 @@ def test_stream_k_policy(monkeypatch):
     # 8192^3: 13.47 waves, 3.8 % of the last one idle; 2048^3: the estimate ties
     for shape in [(8192, 8192, 8192), (2048, 2048, 2048), (3072, 3072, 3072)]:
         st, p = hplan(*shape, path=TC)
-        assert p["stream_k"] == 0 and p["grid"] == p["tiles"] * p["split_k"], (shape, p)
+        assert p["stream_k"] == 0 and p["grid"] == p["tiles"] * p["split_k"] * (2 if p["pair"] else 1), (shape, p)
     st, p = hplan(256, 256, 8192, path=TC)          # 2 tiles: a split-K cluster instead
     assert p["stream_k"] == 0 and p["split_k"] > 1
     st, p = hplan(4096, 4096, 4096, path=TC, num_sms=64)
@@ -212,10 +214,13 @@ def test_in_kernel_split_policy(monkeypatch):
     when TMA can load it -- a 16-byte aligned base, rows a multiple of 16
     bytes and, in a batch, a stride of 0 or of whole non-overlapping matrices
     16 bytes apart; otherwise a split pass writes that operand's hi and lo
-    parts into scratch.  A is read as stored whenever it can be; B (whose
-    split costs the GEMM more per slab) only for m*n*k <= 2^31.  The tuning
-    variables pin the choice but cannot make an unaligned operand eligible.
-    Every tensor-core plan runs 12 warps."""
+    parts into scratch -- except an A that TMA cannot read on untransposed
+    single-CTA tiles, which the GEMM reads in four row phases.  A is
+    read as stored whenever it can be; B (whose split costs the GEMM more per
+    slab) for m*n*k <= 2^31, and above that on CTA pairs when their 256 x 256
+    tiles fill 3/4 to all of the pair slots in one wave.  The tuning variables
+    pin the choice but cannot make an unaligned B eligible.  Every
+    tensor-core plan runs 12 warps."""
     for v in ("SGEMM_GB300_SPLIT_A_IN", "SGEMM_GB300_SPLIT_B_IN"):
         monkeypatch.delenv(v, raising=False)
     TC = binding.PATH_TF32X3
@@ -228,13 +233,17 @@ def test_in_kernel_split_policy(monkeypatch):
 
     assert raw(16384, 128, 8192) == (1, 0)
     assert raw(8192, 8192, 8192) == (1, 0)
-    assert raw(2048, 2048, 2048) == (1, 0)
+    assert raw(2048, 2048, 2048) == (1, 1)                # one wave of CTA pairs, which read B as stored
+    assert raw(2048, 2048, 2048, B_ptr=24) == (1, 0)      # B not 16-byte aligned: single CTAs, B split first
+    assert raw(3072, 2048, 2048) == (1, 0)                # 96 pair tiles: more than one wave
     assert raw(1024, 1024, 2048) == (1, 1)                # 2^31 multiply-adds
     assert raw(1024, 1024, 2049, lda=2052) == (1, 0)      # one k more
     assert raw(256, 256, 256) == (1, 1)
-    assert raw(1000, 1500, 777) == (0, 1)                 # lda = 777: A's rows not 16-byte aligned
+    assert raw(1000, 1500, 777) == (1, 1)                 # lda = 777: A read in row phases
     assert raw(1000, 1500, 777, lda=780) == (1, 1)
-    assert raw(1000, 1500, 780, A_ptr=20) == (0, 1)       # A not 16-byte aligned
+    assert raw(1000, 1500, 780, A_ptr=20) == (1, 1)       # A not 16-byte aligned: row phases too
+    assert raw(16384, 128, 8191) == (0, 0)                # transposed tiles (A on the n side): A split first
+    assert raw(2048, 2048, 2048, lda=2049) == (1, 0)      # phased A: single CTAs, so B split first
     assert raw(1000, 1500, 780, B_ptr=24) == (1, 0)       # B not 16-byte aligned
     assert raw(1000, 1498, 780) == (1, 0)                 # ldb = 1498: B's rows not 16-byte aligned
     monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "1")
@@ -246,6 +255,8 @@ def test_in_kernel_split_policy(monkeypatch):
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "1")
     monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "1")
     assert raw(8192, 8192, 8192) == (1, 1)
+    assert raw(1000, 1500, 777) == (1, 1)
+    monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "0")
     assert raw(1000, 1500, 777) == (0, 1)
 
 
@@ -330,5 +341,5 @@ def test_split_k_policy_small_and_large_shapes():
     for (m, n, k), s in expect.items():
         st, p = hplan(m, n, k, lda=k, path=TC, num_sms=152)
         assert st == 0 and p["split_k"] == s and p["stream_k"] == 0, ((m, n, k), p)
-        assert p["grid"] == p["tiles"] * s
+        assert p["grid"] == p["tiles"] * s * (2 if p["pair"] else 1)
         assert p["k_tiles"] // p["split_k"] >= 4 or s == 1

@@ -98,6 +98,19 @@ def test_split_k_inside_a_batch():
     run_batch(2, 256, 256, 8192, binding.PATH_TF32X3, seed=41)
 
 
+@pytest.mark.parametrize("k,share_a,gap_a", [(77, True, 0), (96, False, 1), (77, False, 2)],
+                         ids=["lda77_shared", "stride_misaligned", "lda77_gap"])
+def test_phased_a_inside_a_batch(k, share_a, gap_a):
+    """An A that TMA cannot read -- rows 77 floats apart, or 16-byte rows
+    whose problems are 1 float further apart than a multiple of 4 -- is
+    read by the GEMM in row phases from problem blockIdx.y's matrix (or the
+    one shared matrix)."""
+    m, n = 200, 150
+    st, plan = binding.plan(m, n, k, lda=k, path=binding.PATH_TF32X3, num_sms=0)
+    assert st == 0 and plan["a_in_kernel"] == 1 and plan["trans"] == 0
+    run_batch(3, m, n, k, binding.PATH_TF32X3, share_a=share_a, gap=(gap_a, 0, 3), seed=61 + k)
+
+
 @pytest.mark.parametrize("path", PATHS.values(), ids=PATHS.keys())
 def test_many_small_problems(path):
     run_batch(300, 48, 40, 24, path, seed=53, check=[0, 1, 150, 298, 299])

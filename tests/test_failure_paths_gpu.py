@@ -45,10 +45,10 @@ def test_bounded_wait_runs_out_and_is_reported():
 
 
 def test_forced_allocation_failure(monkeypatch):
-    # lda = 257: A's rows are not 16-byte aligned, so the tensor-core call
-    # splits A into scratch from the pool -- the allocation the fake fails
+    # ldb = 386: B's rows are not 16-byte aligned, so the tensor-core call
+    # splits B into scratch from the pool -- the allocation the fake fails
     p = inputs.make_problem(512, 384, 256, alpha=1.0, beta=0.5, seed=11, a="uniform", b="uniform", c="uniform",
-                            lda=257)
+                            ldb=386)
     A = torch.from_numpy(p.A).cuda()
     B = torch.from_numpy(p.B).cuda()
     C = torch.from_numpy(p.C0).cuda()
@@ -58,28 +58,32 @@ def test_forced_allocation_failure(monkeypatch):
                            p.ldc, torch.cuda.current_stream().cuda_stream, binding.PATH_TF32X3)
     assert st == 100 and binding.last_cuda_error() == CUDA_ERROR_MEMORY_ALLOCATION
     with pytest.raises(binding.SgemmError) as err:
-        binding.sgemm_ex(A[:, :p.k], B, C, p.alpha, p.beta, path=binding.PATH_TF32X3)
+        binding.sgemm_ex(A, B[:, :p.n], C, p.alpha, p.beta, path=binding.PATH_TF32X3)
     assert err.value.status == 100
     torch.cuda.synchronize()
     assert torch.equal(C, C0), "C was written although the call failed before launching"
     # the FFMA path allocates nothing and is unaffected
-    binding.sgemm_ex(A[:, :p.k], B, C, p.alpha, p.beta, path=binding.PATH_FFMA)
+    binding.sgemm_ex(A, B[:, :p.n], C, p.alpha, p.beta, path=binding.PATH_FFMA)
     R, E, _ = oracle.problem_f64(p)
     ok, worst, _ = oracle.within_tolerance(C.cpu().numpy(), R, E, p.beta, p.C0)
     assert ok, worst
     monkeypatch.delenv("SGEMM_GB300_FAIL_ALLOC")
     C.copy_(C0)
-    binding.sgemm_ex(A[:, :p.k], B, C, p.alpha, p.beta, path=binding.PATH_TF32X3)
+    binding.sgemm_ex(A, B[:, :p.n], C, p.alpha, p.beta, path=binding.PATH_TF32X3)
     ok, worst, _ = oracle.within_tolerance(C.cpu().numpy(), R, E, p.beta, p.C0)
     assert ok, worst
     assert binding.device_status() == 0
 
 
-def test_aligned_tensor_core_call_allocates_nothing(monkeypatch):
-    """With 16-byte rows the tensor-core GEMM reads A and B as stored and the
-    call takes no scratch: it succeeds while every pool allocation is made to
-    fail, and matches the oracle."""
-    p = inputs.make_problem(1024, 512, 768, alpha=1.5, beta=0.5, seed=12, a="normal", b="uniform", c="uniform")
+@pytest.mark.parametrize("lda", [768, 769, 771])
+def test_tensor_core_call_with_readable_b_allocates_nothing(lda, monkeypatch):
+    """With B's rows 16 bytes apart the tensor-core GEMM reads B as stored,
+    and A as stored too -- by TMA when its rows are 16 bytes apart, else
+    (lda = 769, 771) in four row phases that TMA can read -- so the call takes
+    no scratch: it succeeds while every pool allocation is made to fail, and
+    matches the oracle."""
+    p = inputs.make_problem(1024, 512, 768, alpha=1.5, beta=0.5, seed=12, a="normal", b="uniform", c="uniform",
+                            lda=lda)
     st, plan = binding.plan(p.m, p.n, p.k, p.alpha, 256, p.lda, 256, p.ldb, p.beta, 256, p.ldc,
                             path=binding.PATH_TF32X3)
     assert st == 0 and plan["a_in_kernel"] == 1 and plan["b_in_kernel"] == 1 and plan["stream_k"] == 0, plan
@@ -87,7 +91,7 @@ def test_aligned_tensor_core_call_allocates_nothing(monkeypatch):
     B = torch.from_numpy(p.B).cuda()
     C = torch.from_numpy(p.C0).cuda()
     monkeypatch.setenv("SGEMM_GB300_FAIL_ALLOC", "1")
-    binding.sgemm_ex(A, B, C, p.alpha, p.beta, path=binding.PATH_TF32X3)
+    binding.sgemm_ex(A[:, :p.k], B, C, p.alpha, p.beta, path=binding.PATH_TF32X3)
     R, E, _ = oracle.problem_f64(p)
     ok, worst, _ = oracle.within_tolerance(C.cpu().numpy(), R, E, p.beta, p.C0)
     assert ok, worst

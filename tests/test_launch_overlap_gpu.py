@@ -23,7 +23,7 @@ def _gpu():
 
 @pytest.mark.parametrize("m,n,k,lda,beta,env", [
     (2048, 2048, 512, None, 0.0, {"SGEMM_GB300_SPLIT_B_IN": "0"}),   # 128 whole tiles, B split first
-    (1000, 1500, 777, None, 0.5, {}),                                # lda = 777: A split first, split-K cluster
+    (1000, 1500, 777, None, 0.5, {"SGEMM_GB300_SPLIT_A_IN": "0"}),   # lda = 777, A split first: split-K cluster
     (3000, 100, 2048, None, 1.0, {"SGEMM_GB300_SPLIT_B_IN": "0"}),   # transposed tiles
     (512, 512, 512, None, -2.0, {"SGEMM_GB300_SPLIT_A_IN": "0", "SGEMM_GB300_SPLIT_B_IN": "0"}),
 ])

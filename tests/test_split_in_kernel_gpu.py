@@ -8,6 +8,7 @@ split-K clusters, beta != 0, padded leading dimensions, and bit-exact
 integer twins.  Also the property the in-kernel split rests on: the tensor
 core reads an FP32 operand, K-major or MN-major, with its low 13 mantissa
 bits dropped."""
+import numpy as np
 import pytest
 import torch
 
@@ -86,18 +87,87 @@ def test_in_kernel_split_integer_twin_bit_exact(split, m, n, k):
     _run(p, exact=True)
 
 
-def test_unaligned_rows_fall_back_to_pre_pass(monkeypatch):
-    """TMA needs 16-byte rows: with lda % 4 != 0 (or ldb % 4 != 0) that
-    operand is split by the split pass even when the in-kernel split is
-    requested; the other one is still read as stored."""
+def test_unaligned_rows(monkeypatch):
+    """TMA needs 16-byte rows: with ldb % 4 != 0 B is split by the split
+    pass even when the in-kernel split is requested, while A is still read
+    as stored; with lda % 4 != 0 TMA reads A in four row phases (rows j,
+    j + 4, ...: 16-byte row pitch) and the splitter warps shift each row
+    into place and split it."""
     monkeypatch.setenv("SGEMM_GB300_SPLIT_A_IN", "1")
     monkeypatch.setenv("SGEMM_GB300_SPLIT_B_IN", "1")
     p = inputs.make_problem(300, 200, 777, alpha=1.0, beta=0.0, seed=5, a="normal", b="normal")
-    assert p.lda == 777 and (_plan(p)["a_in_kernel"], _plan(p)["b_in_kernel"]) == (0, 1)
+    assert p.lda == 777 and (_plan(p)["a_in_kernel"], _plan(p)["b_in_kernel"]) == (1, 1)
     _run(p)
     p = inputs.make_problem(300, 203, 776, alpha=1.0, beta=0.0, seed=6, a="normal", b="normal")
     assert p.ldb == 203 and (_plan(p)["a_in_kernel"], _plan(p)["b_in_kernel"]) == (1, 0)
     _run(p)
+
+
+# A whose rows TMA cannot read as one tensor, read in row phases and put
+# into the swizzled stage slots by the splitter warps: the plan each case
+# runs in a comment
+@pytest.mark.parametrize("m,n,k,lda,off_a,beta", [
+    (1000, 1500, 777, 777, 0, 0.5),      # the 1000 x 1500 x 777 workload's layout: split-K 3
+    (300, 200, 777, 777, 1, 0.0),        # base 4 bytes past 16-byte alignment too
+    (129, 257, 4096, 4097, 2, -1.0),     # split-K 8, B split first (ldb = 257)
+    (2048, 2048, 2048, 2049, 0, 0.0),    # 128 wide tiles, B split first (above 2^31)
+    (3000, 2000, 999, 999, 3, 1.0),      # stream-K over 152 CTAs
+    (128, 128, 5, 5, 0, 0.0),            # one slab, k = 5
+    (200, 300, 1, 1, 1, 0.5),            # k = 1
+    (640, 1024, 2047, 2047, 0, 2.0),     # split-K 6, k % 16 = 15
+    (1000, 300, 780, 780, 1, 0.0),       # 16-byte rows, base misaligned
+])
+def test_phased_a_matches_oracle(monkeypatch, m, n, k, lda, off_a, beta):
+    for v in ("SGEMM_GB300_SPLIT_A_IN", "SGEMM_GB300_SPLIT_B_IN"):
+        monkeypatch.delenv(v, raising=False)
+    p = inputs.make_problem(m, n, k, alpha=0.75, beta=beta, seed=m + n + 3 * k, a="normal", b="uniform",
+                            c="uniform" if beta else None, lda=lda)
+    st, plan = binding.plan(p.m, p.n, p.k, p.alpha, 256 + 4 * off_a, p.lda, 256, p.ldb, p.beta, 256, p.ldc,
+                            path=TC, num_sms=0)
+    assert st == 0 and plan["a_in_kernel"] == 1 and plan["trans"] == 0 and plan["pair"] == 0, plan
+    pl = Placed(p, off=(off_a, 0, 0))
+    st = pl.run(TC)
+    assert st == 0, binding.status_string(st)
+    C, guard_ok = pl.result()
+    assert guard_ok, "a write landed outside the m x n window of C"
+    assert pl.inputs_untouched(), "A or B was modified"
+    ok, worst, where = check_full(p, C)
+    assert ok, f"worst |C - r| / tol = {worst} at {where}"
+    assert binding.device_status() == 0
+
+
+@pytest.mark.parametrize("m,n,k,lda", [(1000, 1500, 777, 777), (700, 512, 1001, 1003), (129, 130, 33, 33)])
+def test_phased_a_integer_twin_bit_exact(monkeypatch, m, n, k, lda):
+    """Integer operands through the phased A: exact products and sums, so
+    any element put in the wrong place (a swizzle slip, a row, phase or
+    shift error) changes the result."""
+    for v in ("SGEMM_GB300_SPLIT_A_IN", "SGEMM_GB300_SPLIT_B_IN"):
+        monkeypatch.delenv(v, raising=False)
+    p = inputs.make_problem(m, n, k, alpha=2.0, beta=0.5, seed=k + 5 * n, a="int", b="int", c="int", lda=lda)
+    assert _plan(p)["a_in_kernel"] == 1
+    _run(p, exact=True)
+
+
+def test_phased_a_identity_names_every_element(monkeypatch):
+    """C = X * I with X[i][t] = i + 1024 t: every output is one element of A
+    exactly, so an element put in the wrong row, k position or swizzle
+    chunk shows as the wrong value (X has 1001 columns, lda = 1001)."""
+    for v in ("SGEMM_GB300_SPLIT_A_IN", "SGEMM_GB300_SPLIT_B_IN"):
+        monkeypatch.delenv(v, raising=False)
+    m, k, n = 300, 1001, 1001
+    X = (np.arange(m)[:, None] + 1024.0 * np.arange(k)[None, :]).astype(np.float32)
+    I = np.eye(k, n, dtype=np.float32)
+    Ad, Bd = torch.from_numpy(X).cuda(), torch.from_numpy(I).cuda()
+    st, plan = binding.plan(m, n, k, 1.0, Ad.data_ptr(), k, Bd.data_ptr(), n, 0.0, 256, n, path=TC)
+    assert st == 0 and plan["a_in_kernel"] == 1
+    C = torch.full((m, n), -1.0, device="cuda")
+    st = binding.sgemm_raw(m, n, k, 1.0, Ad.data_ptr(), k, Bd.data_ptr(), n, 0.0, C.data_ptr(), n,
+                           torch.cuda.current_stream().cuda_stream, TC)
+    assert st == 0, binding.status_string(st)
+    torch.cuda.synchronize()
+    got = C.cpu().numpy()
+    bad = np.argwhere(got != X)
+    assert bad.size == 0, [(int(i), int(j), float(got[i, j]), float(X[i, j])) for i, j in bad[:8]]
 
 
 def test_in_kernel_split_is_deterministic(monkeypatch):

@@ -6,10 +6,12 @@ recurse or deadlock on the allocator's own lock), processes that reserve all
 of their device memory up front and leave none to a library, and
 latency-critical loops that cannot risk cudaMalloc's implicit
 synchronisation or its failure under memory pressure.  The regular entry
-point takes scratch from a stream-ordered pool when an operand cannot be
-read by TMA as stored (rows not 16 bytes apart, a misaligned base) or when
-its plan uses stream-K; this entry point instead puts the split operands in
-one fixed 64 MiB device array and plans without stream-K.
+point takes scratch from a stream-ordered pool when B cannot be read by TMA
+as stored (rows not 16 bytes apart, a misaligned base), when a plan splits
+a large B first, or when its plan uses stream-K; this entry point reads
+every operand it can as stored (an A that TMA cannot read as one tensor is
+read in four row phases), puts a misaligned B's split parts in one fixed
+64 MiB device array, and plans without stream-K.
 
 These tests call it through the C ABI and hold its output to the FP64
 oracle within the bound every parity test uses, twice in a row (the second
@@ -54,20 +56,22 @@ def _check_oracle(p, got):
     return R, E
 
 
-# (m, n, k, seed, lda pad): odd pads make A's rows misaligned (A split into
-# the fixed scratch), even ones leave A readable as stored
+# (m, n, k, seed, lda pad, ldb pad): odd lda pads make A's rows misaligned
+# (A read in row phases), ldb pads that are not multiples of 4 B's (B split
+# into the fixed scratch)
 @pytest.mark.parametrize("shapes", [
-    [(1000, 1500, 777, 2, 0), (300, 200, 150, 3, 1)],
-    [(2048, 2048, 2048, 5, 1), (129, 257, 1000, 6, 0)],
+    [(1000, 1500, 777, 2, 0, 0), (300, 200, 150, 3, 1, 2)],
+    [(2048, 2048, 2048, 5, 1, 0), (129, 257, 1000, 6, 0, 3)],
+    [(700, 900, 500, 7, 3, 1), (2048, 2048, 2048, 8, 0, 0)],
 ])
 def test_noalloc_matches_oracle_twice(shapes, monkeypatch):
     # the regular call is planned without stream-K, as this entry point is,
-    # so that both run the same kernels
+    # so that both run the same kernels where their plans agree
     monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
     stream = torch.cuda.current_stream().cuda_stream
-    for m, n, k, seed, pad in shapes:
+    for m, n, k, seed, pad_a, pad_b in shapes:
         p = inputs.make_problem(m, n, k, alpha=1.5, beta=0.5, seed=seed, a="normal", b="uniform", c="uniform",
-                                lda=k + pad)
+                                lda=k + pad_a, ldb=n + pad_b)
         A, B = _device(p.A), _device(p.B)
         C_na, C_ref = _device(p.C0), _device(p.C0)
         st = _noalloc(p, A, B, C_na, stream)
@@ -85,12 +89,14 @@ def test_noalloc_matches_oracle_twice(shapes, monkeypatch):
 
 def test_noalloc_needs_no_allocation(monkeypatch):
     """With SGEMM_GB300_FAIL_ALLOC set every pool allocation of the library
-    reports out-of-memory.  On a problem whose A must be split into scratch
-    (lda = 777: rows not 16 bytes apart) the regular entry point then fails
-    with status 100 and leaves C alone; the allocation-free one succeeds,
-    twice in a row, and matches the oracle."""
+    reports out-of-memory.  On a problem whose B must be split into scratch
+    (ldb = 1501: rows not 16 bytes apart; A's rows misaligned too, lda = 777)
+    the regular entry point then fails with status 100 and leaves C alone;
+    the allocation-free one succeeds, twice in a row, and matches the
+    oracle."""
     stream = torch.cuda.current_stream().cuda_stream
-    p = inputs.workload("1000x1500x777")
+    p = inputs.make_problem(1000, 1500, 777, alpha=1.5, beta=0.5, seed=2, a="uniform", b="uniform", c="normal",
+                            ldb=1501)
     assert p.lda == 777
     A, B = _device(p.A), _device(p.B)
     monkeypatch.setenv("SGEMM_GB300_FAIL_ALLOC", "1")
@@ -105,12 +111,13 @@ def test_noalloc_needs_no_allocation(monkeypatch):
     assert np.array_equal(C_ref.cpu().numpy(), p.C0, equal_nan=True)
 
 
-@pytest.mark.parametrize("name", ["8192^3", "16384x128x8192"])
-def test_noalloc_large_workloads_with_allocations_failing(name, monkeypatch):
-    """The two large workloads need no scratch at all through this entry
-    point (both operands read as stored: CTA pairs at 8192^3, transposed
-    tiles at n = 128), so they run with every pool allocation made to fail;
-    checked on 4096 sampled outputs plus every tile edge."""
+@pytest.mark.parametrize("name", ["1000x1500x777", "8192^3", "16384x128x8192"])
+def test_noalloc_workloads_with_allocations_failing(name, monkeypatch):
+    """The workloads need no scratch at all through this entry point (both
+    operands read as stored: A in row phases at lda = 777, CTA pairs at
+    8192^3, transposed tiles at n = 128), so they run with every pool
+    allocation made to fail; checked on 4096 sampled outputs plus every tile
+    edge."""
     monkeypatch.setenv("SGEMM_GB300_FAIL_ALLOC", "1")
     stream = torch.cuda.current_stream().cuda_stream
     p = inputs.workload(name)
@@ -127,21 +134,19 @@ def test_noalloc_large_workloads_with_allocations_failing(name, monkeypatch):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
-    """Only operands that cannot be read as stored take scratch: 2 * rows *
-    ka floats each (ka = k rounded up to 4).  With both operands' rows
-    misaligned (lda = ldb = 2049), m = n = 2048 and k = 2048 fill the array
-    exactly; k = 2049 (ka = 2052) does not fit and is rejected before
-    anything is enqueued, while the same shape with 16-byte rows needs no
-    scratch at all."""
-    assert binding.NOALLOC_SCRATCH_FLOATS == 2 * (2048 + 2048) * 2048
-    st = binding.tf32x3_noalloc_raw(2048, 2048, 2049, 1.0, 256, 2049, 512, 2049, 0.0, 1024, 2048, 0)
+    """Only a B that TMA cannot read takes scratch: 2 * n * ka floats (ka = k
+    rounded up to 4).  With B's rows misaligned (ldb = 4097), n = 4096 and
+    k = 2048 fill the array exactly; k = 2049 (ka = 2052) does not fit and is
+    rejected before anything is enqueued, while the same shape with 16-byte
+    rows needs no scratch at all."""
+    assert binding.NOALLOC_SCRATCH_FLOATS == 2 * 4096 * 2048
+    st = binding.tf32x3_noalloc_raw(512, 4096, 2049, 1.0, 256, 2049, 512, 4097, 0.0, 1024, 4096, 0)
     assert st == 97
     assert "scratch" in binding.status_string(st)
     # a problem that fits exactly, and one that needs no scratch, both run
     stream = torch.cuda.current_stream().cuda_stream
-    for k, ld in ((2048, 2049), (2049, 2052)):
-        p = inputs.make_problem(2048, 2048, k, alpha=1.0, beta=0.0, seed=k, a="uniform", b="uniform",
-                                lda=ld, ldb=ld)
+    for k, ldb in ((2048, 4097), (2049, 4100)):
+        p = inputs.make_problem(512, 4096, k, alpha=1.0, beta=0.0, seed=k, a="uniform", b="uniform", ldb=ldb)
         A, B, C = _device(p.A), _device(p.B), _device(p.C0)
         st = _noalloc(p, A, B, C, stream)
         assert st == 0, binding.status_string(st)
