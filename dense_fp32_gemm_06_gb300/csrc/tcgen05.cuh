@@ -207,6 +207,15 @@ __device__ __forceinline__ void cluster_sync() {
             : "memory");
 }
 
+// The two halves of a cluster barrier: an arrival that orders nothing (for
+// a thread whose earlier accesses to other CTAs' shared memory are loads
+// whose values it has already used), and the wait for every thread of the
+// cluster to have arrived.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;\n" ::: "memory"); }
+
 // Address of the same shared-memory location in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
     uint32_t r;

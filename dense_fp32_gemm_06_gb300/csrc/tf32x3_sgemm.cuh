@@ -1011,6 +1011,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (col + e < p.n) crow[col + e] = a[e];
             }
         };
+        // the lines of C that this thread's part of tile t covers (TRANS:
+        // this warp's 32 columns of 128 rows, four rows per lane)
+        auto prefetch_c = [&](int t) {
+            int m0, n0;
+            tile_origin(t, m0, n0);
+            m0 += (int)prank * BM;
+            if constexpr (TRANS) {
+                const int col = n0 + lane_grp * 32;
+                if (col >= p.n) return;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int row = m0 + half * COLS_PER_THREAD + lane + 32 * i;
+                    if (row < p.m) prefetch_l2(Cb + (long long)row * p.ldc + col);
+                }
+            } else {
+                const int row = m0 + trow;
+                if (row >= p.m) return;
+#pragma unroll
+                for (int i = 0; i < COLS_PER_THREAD / 32; ++i) {
+                    const int col = n0 + half * COLS_PER_THREAD + 32 * i;
+                    if (col < p.n) prefetch_l2(Cb + (long long)row * p.ldc + col);
+                }
+            }
+        };
         float4 *const stg = epi + (warp - 2) * 256;
         // v: this thread's columns half*COLS_PER_THREAD + 32*blk .. +31 of its row
         auto store_block32 = [&](int m0, int n0, int blk, const float4 (&v)[8]) {
@@ -1142,6 +1166,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < COLS_PER_THREAD; ++j) acc[j] = 0.f;
             const int nc = (nk + CHUNK_STAGES - 1) / CHUNK_STAGES;
             for (int c = 0; c < nc && ok; ++c, ++cg) {
+                // beta != 0: while the tile's last chunk accumulates, bring
+                // the lines of C this warp will read (the old values) into
+                // L2, so the epilogue's loads of them do not go to DRAM
+                if (c == nc - 1 && p.beta != 0.f) prefetch_c(tile);
                 const int b = cg & 1;
                 const bool got = mbar_wait(bar_tfull + 8 * b, (cg >> 1) & 1, kStatusAccumulate);
                 if (!got) *abort_flag = 1;
@@ -1200,75 +1228,129 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------------ cluster reduction
         // every partial is parked; CTA `rank` sums rows [r0, r1) of the tile
         // over the cluster's CTAs in rank order (a fixed order: the result
-        // does not depend on timing) and writes them to C
+        // does not depend on timing) and writes them to C.  A thread's
+        // values (at most MAXIT float4 of the tile) are gathered rank by
+        // rank with all of a rank's remote loads in flight together (the
+        // abort flags with the first rank's), then C's values (beta != 0),
+        // also all at once: a few load latencies in all, not two per float4.
+        // Once its remote values are in registers a thread tells the cluster
+        // (the second barrier's arrival, which need not wait for the stores);
+        // it waits for the others only before leaving, so no CTA leaves
+        // while another may still read its partial.
         tc::cluster_sync();
         const uint32_t part0 = smem_u32(smem);
         const uint32_t abort_addr = smem_u32(const_cast<int *>(abort_flag));
-        int any_abort = 0;
-        for (uint32_t q = 0; q < nsplit; ++q) any_abort |= tc::ld_cluster_s32(tc::map_shared_rank(abort_addr, q));
         const int r0 = (int)(BM * rank / nsplit), r1 = (int)(BM * (rank + 1) / nsplit);
+        const int nrows = r1 - r0, total = nrows * (BN / 4);
+        constexpr int MAXIT = ((BM / 2) * (BN / 4) + NTHREADS - 1) / NTHREADS;   // nsplit >= 2
         const float alpha = p.alpha, beta = p.beta;
-        if (!any_abort) {
-            for (int idx = threadIdx.x; idx < (r1 - r0) * (BN / 4); idx += NTHREADS) {
-                // TRANS: consecutive threads take consecutive tile rows (=
-                // columns of C), so the stores below stay coalesced
-                const int r = TRANS ? r0 + idx % (r1 - r0) : r0 + idx / (BN / 4);
-                const int c4 = TRANS ? idx / (r1 - r0) : idx % (BN / 4);
-                const int row = cl_m0 + r, col = cl_n0 + 4 * c4;
-                const uint32_t off = part0 + (uint32_t)(r * PART_PITCH + 4 * c4) * 4u;
-                // all S remote loads first (in flight together), then the
-                // adds in rank order
-                float4 v[8];
+        // float4 `it` of this thread: tile row r, columns 4 c4 .. +3 (TRANS:
+        // consecutive threads take consecutive tile rows (= columns of C),
+        // so the stores below stay coalesced)
+        uint32_t off[MAXIT];
 #pragma unroll
-                for (uint32_t q = 0; q < 8; ++q)
-                    if (q < nsplit) v[q] = tc::ld_cluster_v4(tc::map_shared_rank(off, q));
-                float4 sum = v[0];
+        for (int it = 0; it < MAXIT; ++it) {
+            const int idx = (int)threadIdx.x + it * NTHREADS;
+            const int r = TRANS ? r0 + idx % nrows : r0 + idx / (BN / 4);
+            const int c4 = TRANS ? idx / nrows : idx % (BN / 4);
+            off[it] = part0 + (uint32_t)(r * PART_PITCH + 4 * c4) * 4u;
+        }
+        int flags[8];
 #pragma unroll
-                for (uint32_t q = 1; q < 8; ++q) {
-                    if (q < nsplit) {
-                        sum.x += v[q].x;
-                        sum.y += v[q].y;
-                        sum.z += v[q].z;
-                        sum.w += v[q].w;
-                    }
-                }
-                const float a[4] = {sum.x, sum.y, sum.z, sum.w};
-                if constexpr (TRANS) {
-                    const int cc = cl_n0 + r, rr = cl_m0 + 4 * c4;   // column of C, first of 4 rows
-                    if (cc >= p.n) continue;
+        for (uint32_t q = 0; q < 8; ++q) flags[q] = q < nsplit ? tc::ld_cluster_s32(tc::map_shared_rank(abort_addr, q)) : 0;
+        float4 sum[MAXIT], v[MAXIT];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (rr + e < p.m) {
-                            float *cp = Cb + (long long)(rr + e) * p.ldc + cc;
-                            *cp = beta != 0.f ? fmaf(alpha, a[e], beta * *cp) : alpha * a[e];
-                        }
-                    }
-                    continue;
-                }
-                if (row >= p.m) continue;
-                float *crow = Cb + (long long)row * p.ldc;
-                if (c_vec && col + 3 < p.n) {
-                    float4 o;
-                    if (beta != 0.f) {
-                        const float4 c = *reinterpret_cast<const float4 *>(crow + col);
-                        o = make_float4(fmaf(alpha, a[0], beta * c.x), fmaf(alpha, a[1], beta * c.y),
-                                        fmaf(alpha, a[2], beta * c.z), fmaf(alpha, a[3], beta * c.w));
-                    } else {
-                        o = make_float4(alpha * a[0], alpha * a[1], alpha * a[2], alpha * a[3]);
-                    }
-                    *reinterpret_cast<float4 *>(crow + col) = o;
-                } else {
+        for (int it = 0; it < MAXIT; ++it)
+            if ((int)threadIdx.x + it * NTHREADS < total) sum[it] = tc::ld_cluster_v4(tc::map_shared_rank(off[it], 0));
+        for (uint32_t q = 1; q < nsplit; ++q) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (col + e < p.n)
-                            crow[col + e] = beta != 0.f ? fmaf(alpha, a[e], beta * crow[col + e]) : alpha * a[e];
-                    }
+            for (int it = 0; it < MAXIT; ++it)
+                if ((int)threadIdx.x + it * NTHREADS < total) v[it] = tc::ld_cluster_v4(tc::map_shared_rank(off[it], q));
+#pragma unroll
+            for (int it = 0; it < MAXIT; ++it) {
+                if ((int)threadIdx.x + it * NTHREADS < total) {
+                    sum[it].x += v[it].x;
+                    sum[it].y += v[it].y;
+                    sum[it].z += v[it].z;
+                    sum[it].w += v[it].w;
                 }
             }
         }
-        // no CTA leaves while another may still read its partial
+        int any_abort = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) any_abort |= flags[q];
         __syncwarp();
-        tc::cluster_sync();
+        tc::cluster_arrive_relaxed();
+        if (!any_abort) {
+            // C's old values (beta != 0) into v: TRANS, four rows of one
+            // column of C; otherwise four columns of one row
+#pragma unroll
+            for (int it = 0; it < MAXIT; ++it) {
+                const int idx = (int)threadIdx.x + it * NTHREADS;
+                v[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (beta == 0.f || idx >= total) continue;
+                const int r = TRANS ? r0 + idx % nrows : r0 + idx / (BN / 4);
+                const int c4 = TRANS ? idx / nrows : idx % (BN / 4);
+                float c[4] = {0.f, 0.f, 0.f, 0.f};
+                if constexpr (TRANS) {
+                    const int cc = cl_n0 + r, rr = cl_m0 + 4 * c4;   // column of C, first of 4 rows
+                    if (cc < p.n) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (rr + e < p.m) c[e] = Cb[(long long)(rr + e) * p.ldc + cc];
+                    }
+                } else {
+                    const int row = cl_m0 + r, col = cl_n0 + 4 * c4;
+                    if (row < p.m) {
+                        const float *crow = Cb + (long long)row * p.ldc;
+                        if (c_vec && col + 3 < p.n) {
+                            const float4 c4v = *reinterpret_cast<const float4 *>(crow + col);
+                            c[0] = c4v.x;
+                            c[1] = c4v.y;
+                            c[2] = c4v.z;
+                            c[3] = c4v.w;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                if (col + e < p.n) c[e] = crow[col + e];
+                        }
+                    }
+                }
+                v[it] = make_float4(c[0], c[1], c[2], c[3]);
+            }
+#pragma unroll
+            for (int it = 0; it < MAXIT; ++it) {
+                const int idx = (int)threadIdx.x + it * NTHREADS;
+                if (idx >= total) continue;
+                const int r = TRANS ? r0 + idx % nrows : r0 + idx / (BN / 4);
+                const int c4 = TRANS ? idx / nrows : idx % (BN / 4);
+                const float a[4] = {sum[it].x, sum[it].y, sum[it].z, sum[it].w};
+                const float c[4] = {v[it].x, v[it].y, v[it].z, v[it].w};
+                float o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[e] = beta != 0.f ? fmaf(alpha, a[e], beta * c[e]) : alpha * a[e];
+                if constexpr (TRANS) {
+                    const int cc = cl_n0 + r, rr = cl_m0 + 4 * c4;
+                    if (cc >= p.n) continue;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (rr + e < p.m) Cb[(long long)(rr + e) * p.ldc + cc] = o[e];
+                    continue;
+                }
+                const int row = cl_m0 + r, col = cl_n0 + 4 * c4;
+                if (row >= p.m) continue;
+                float *crow = Cb + (long long)row * p.ldc;
+                if (c_vec && col + 3 < p.n) {
+                    *reinterpret_cast<float4 *>(crow + col) = make_float4(o[0], o[1], o[2], o[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (col + e < p.n) crow[col + e] = o[e];
+                }
+            }
+        }
+        __syncwarp();
+        tc::cluster_wait();
     }
     // PAIR: neither CTA leaves (or frees its tensor memory) while the other
     // may still arrive at its barriers

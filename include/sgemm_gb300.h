@@ -30,8 +30,14 @@
  * when the operand's base is 16-byte aligned and its rows are 16 bytes
  * apart (lda, ldb multiples of 4; in a batch also a stride of 0 or of whole
  * non-overlapping matrices, a multiple of 4) -- always for A, and for B
- * when m*n*k <= 2^31 (larger problems split B with a separate pass, which
- * is faster there).  Only the other operands, and stream-K's partial tiles
+ * when m*n*k <= 2^31 or the plan runs CTA pairs (other large problems
+ * split B with a separate pass, which is faster there).  An A (not
+ * transposed) whose rows are not 16 bytes apart, or whose base is not
+ * 16-byte aligned, the GEMM reads in four row phases (rows j, j + 4, ...
+ * are 4 * lda floats apart, which TMA can read) and needs no scratch for it
+ * either, except on transposed tiles (sgemm_plan.trans) and in a batch
+ * whose stride is not a multiple of 4.  Only the other operands, and
+ * stream-K's partial tiles
  * (plans with sgemm_plan.stream_k > 0), take scratch: 8 * rows * ka bytes
  * per split operand (ka = k rounded up to 4) and 2 * stream_k tiles of
  * 128 * bn floats, for the duration of the call, from a stream-ordered
@@ -210,16 +216,17 @@ int sgemm_tf32x3_split_gemm(int m, int n, int k, float alpha, const float *a_hi,
  * are 16 bytes apart and whose base is 16-byte aligned is read as stored
  * and split inside the GEMM, whatever the problem's size (problems above
  * 2^31 multiply-adds with both operands so run on CTA pairs: 256 x 256
- * tiles, cta_group::2), so such calls need no scratch at all.  The split
- * parts of the other operands live in one fixed array of
+ * tiles, cta_group::2), and an A that is not is read in row phases as in
+ * sgemm(), so such calls need no scratch at all.  The split parts of the
+ * other operands -- a B whose rows TMA cannot read, and such an A on
+ * transposed tiles (sgemm_plan.trans) -- live in one fixed array of
  * SGEMM_NOALLOC_SCRATCH_FLOATS floats (64 MiB) in device memory that every
  * GPU which loads this library holds until the process exits: 2 * rows * ka
  * floats per such operand (rows = m for A, n for B; ka = k rounded up to
  * 4); a problem that needs more is rejected with SGEMM_STATUS_TOO_LARGE
- * before anything is enqueued (with both operands' rows misaligned,
- * m = n = k = 2048 needs exactly the capacity).  No stream-K.  No
- * cudaMalloc, cudaMallocAsync, cudaFree or allocating library routine is
- * called.
+ * before anything is enqueued (with B's rows misaligned, n = 4096 and
+ * k = 2048 need exactly the capacity).  No stream-K.  No cudaMalloc,
+ * cudaMallocAsync, cudaFree or allocating library routine is called.
  *
  * The first call on a device looks up the array's device address on that
  * device (cudaGetSymbolAddress, with the device current) and keeps it; make
@@ -299,6 +306,7 @@ typedef struct sgemm_plan {
     int op_a, op_b;    /* SGEMM_OP_N / SGEMM_OP_T of the problem planned                      */
     int a_vec;         /* 1: A (stored k x m) loaded 16 bytes at a time (FFMA path)            */
     int a_in_kernel;   /* 1: the tensor-core GEMM reads A as stored (TMA) and splits it itself */
+                       /*    (in four row phases when its rows are not 16 bytes apart)      */
     int trans;         /* 1: tensor-core tiles of C^T = B^T A^T (n <= 128; bm = 256, bn = 128) */
     int stream_k;      /* > 0: stream-K over this many CTAs (grid); each takes an equal share  */
                        /*      of all tiles' k slabs, partial tiles meet in a workspace        */
