@@ -677,7 +677,10 @@ def run_ours(args, rank, world):
         bf16 = (mp or {}).get("bf16_tflops", 1900.0)
         tf32 = bf16 * NOMINAL_TF32_OVER_BF16
         family = tc_family(a_raw, b_raw)
-        traits = [t for t, on in (("A read raw", a_raw), ("B read raw", b_raw), ("transposed tiles", plan["trans"]),
+        # an A that TMA cannot read as one tensor is read in four row phases
+        a_phased = a_raw and not plan["trans"] and (p.lda % 4 != 0 or A.data_ptr() % 16 != 0)
+        traits = [t for t, on in (("A read raw" + (" in row phases" if a_phased else ""), a_raw), ("B read raw", b_raw),
+                                  ("CTA pairs", plan["pair"]), ("transposed tiles", plan["trans"]),
                                   ("stream-K", plan["stream_k"] > 0), (f"split-K {plan['split_k']}",
                                                                        plan["split_k"] > 1)) if on]
         roof = {"bound": "tensor", "kernel": "tf32x3_gemm_kernel" + (f"<{', '.join(traits)}>" if traits else ""),

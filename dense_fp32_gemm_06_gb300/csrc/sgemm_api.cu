@@ -87,20 +87,25 @@ int ffma_smem_bytes(int akind, int bkind) {
                       : akind == 1 ? ffma_smem_b<ALoadVec>(bkind) : ffma_smem_b<ALoadScalar>(bkind);
 }
 
-template <class Cfg, bool TRANS, bool XM, bool YM>
+template <class Cfg, bool TRANS, bool XM, bool YM, bool XP = false>
 cudaError_t set_tc_attr_one() {
-    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM>,
+    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM, XP>,
                                 cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
 }
 
 // The four operand-layout variants of one tile shape (X and Y each K-major
-// or MN-major).
+// or MN-major), and on untransposed single-CTA tiles the two with X read in
+// row phases.
 template <class Cfg, bool TRANS>
 cudaError_t set_tc_attr() {
     cudaError_t e = set_tc_attr_one<Cfg, TRANS, false, false>();
     if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, false, true>();
     if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, true, false>();
     if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, true, true>();
+    if constexpr (!TRANS && !Cfg::PAIR) {
+        if (e == cudaSuccess) e = set_tc_attr_one<Cfg, false, false, false, true>();
+        if (e == cudaSuccess) e = set_tc_attr_one<Cfg, false, false, true, true>();
+    }
     return e;
 }
 
@@ -629,15 +634,21 @@ int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *b
     return SGEMM_STATUS_OK;
 }
 
-template <class Cfg, bool TRANS, bool XM, bool YM>
+template <class Cfg, bool TRANS, bool XM, bool YM, bool XP = false>
 cudaError_t launch_tc_one(const cudaLaunchConfig_t &cfg, const CUtensorMap *maps, const tf32x3::Params &a) {
-    return cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM>, maps[0], maps[1], maps[2],
+    return cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM, XP>, maps[0], maps[1], maps[2],
                               maps[3], maps[4], maps[5], a);
 }
 
+// xm / ym: X / Y read MN-major; xp: X read in row phases (untransposed
+// single-CTA tiles only; prepare_gemm rejects the rest)
 template <class Cfg, bool TRANS>
-cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, bool xm, bool ym, const CUtensorMap *maps,
+cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, bool xm, bool ym, bool xp, const CUtensorMap *maps,
                       const tf32x3::Params &a) {
+    if constexpr (!TRANS && !Cfg::PAIR) {
+        if (xp) return ym ? launch_tc_one<Cfg, false, false, true, true>(cfg, maps, a)
+                          : launch_tc_one<Cfg, false, false, false, true>(cfg, maps, a);
+    }
     if (xm) return ym ? launch_tc_one<Cfg, TRANS, true, true>(cfg, maps, a) : launch_tc_one<Cfg, TRANS, true, false>(cfg, maps, a);
     return ym ? launch_tc_one<Cfg, TRANS, false, true>(cfg, maps, a) : launch_tc_one<Cfg, TRANS, false, false>(cfg, maps, a);
 }
@@ -647,7 +658,7 @@ cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, bool xm, bool ym, const CUt
 struct GemmLaunch {
     CUtensorMap maps[6];   // X hi, X lo, Y hi, Y lo; a phased X: phases 0..3 in 0, 1, 4, 5
     tf32x3::Params prm;
-    bool xm = false, ym = false;
+    bool xm = false, ym = false, xp = false;
 };
 
 // Builds the launch of the GEMM for operands a (m side) and b (n side):
@@ -679,6 +690,7 @@ int prepare_gemm(int m, int n, int k, float alpha, const Operand &a, const Opera
     if (st) return st;
     L->xm = x.raw && !x.kmajor;
     L->ym = y.raw && !y.kmajor;
+    L->xp = x.phased;
     p.m = m;
     p.n = n;
     p.k = k;
@@ -732,13 +744,13 @@ int launch_gemm(const GemmLaunch &L, const sgemm_plan &pl, int batch, cudaStream
     cfg.numAttrs = na;
     cudaError_t e;
     if (pl.pair)
-        e = launch_tc<tf32x3::Pair, false>(cfg, L.xm, L.ym, L.maps, L.prm);
+        e = launch_tc<tf32x3::Pair, false>(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
     else if (pl.trans)
-        e = launch_tc<tf32x3::Wide, true>(cfg, L.xm, L.ym, L.maps, L.prm);
+        e = launch_tc<tf32x3::Wide, true>(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
     else if (pl.bn == tf32x3::Narrow::BN)
-        e = launch_tc<tf32x3::Narrow, false>(cfg, L.xm, L.ym, L.maps, L.prm);
+        e = launch_tc<tf32x3::Narrow, false>(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
     else
-        e = launch_tc<tf32x3::Wide, false>(cfg, L.xm, L.ym, L.maps, L.prm);
+        e = launch_tc<tf32x3::Wide, false>(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
     if (e != cudaSuccess) return fail_cuda(e);
     return SGEMM_STATUS_OK;
 }
