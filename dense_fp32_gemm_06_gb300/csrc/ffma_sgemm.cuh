@@ -356,8 +356,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
     }
 }
 
-// The configuration the library launches.
+// The configurations the library launches: 128 x 128 tiles of 8 x 8 per
+// thread, two CTAs per SM (most problems), and 128 x 256 tiles of 8 x 16
+// per thread, one CTA per SM, for problems of many waves (6 LDS.128 per 128
+// FMA instead of 4 per 64; measured at 8192^3: 62.2 against 60.4 TFLOPS,
+// but 54.2 against 57.7 at 4096^3, where its 3.4 waves leave the last one a
+// third full at one CTA per SM).
 using Default = Config<128, 128, 32, 3, 8, 8, 2>;
+using Wide = Config<128, 256, 32, 3, 8, 16, 1>;
 
 }  // namespace ffma
 

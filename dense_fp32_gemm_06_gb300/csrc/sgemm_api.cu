@@ -53,38 +53,54 @@ int fail_cuda(cudaError_t e) {
 // FFMA operand loaders by storage: k contiguous -> ScatterLoader; rows
 // contiguous -> DirectLoader with 16-byte (rows 16-byte aligned) or 4-byte
 // copies.  Loader kinds: 0 scatter, 1 direct 16-byte, 2 direct 4-byte.
-using FCfg = ffma::Default;
-using ALoadScatter = ffma::ScatterLoader<FCfg::BM, FCfg::BK, FCfg::THREADS>;
-using ALoadVec = ffma::DirectLoader<FCfg::BM, FCfg::BK, FCfg::THREADS, true>;
-using ALoadScalar = ffma::DirectLoader<FCfg::BM, FCfg::BK, FCfg::THREADS, false>;
-using BLoadScatter = ffma::ScatterLoader<FCfg::BN, FCfg::BK, FCfg::THREADS>;
-using BLoadVec = ffma::DirectLoader<FCfg::BN, FCfg::BK, FCfg::THREADS, true>;
-using BLoadScalar = ffma::DirectLoader<FCfg::BN, FCfg::BK, FCfg::THREADS, false>;
+template <class FCfg>
+struct FfmaLoaders {
+    using AScatter = ffma::ScatterLoader<FCfg::BM, FCfg::BK, FCfg::THREADS>;
+    using AVec = ffma::DirectLoader<FCfg::BM, FCfg::BK, FCfg::THREADS, true>;
+    using AScalar = ffma::DirectLoader<FCfg::BM, FCfg::BK, FCfg::THREADS, false>;
+    using BScatter = ffma::ScatterLoader<FCfg::BN, FCfg::BK, FCfg::THREADS>;
+    using BVec = ffma::DirectLoader<FCfg::BN, FCfg::BK, FCfg::THREADS, true>;
+    using BScalar = ffma::DirectLoader<FCfg::BN, FCfg::BK, FCfg::THREADS, false>;
+};
 
-template <class AL, class BL>
+template <class FCfg, class AL, class BL>
 cudaError_t set_ffma_attr() {
     return cudaFuncSetAttribute(ffma::ffma_sgemm_kernel<FCfg, AL, BL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 ffma::Layout<FCfg, AL, BL>::SMEM_BYTES);
 }
 
-template <class AL>
+template <class FCfg, class AL>
 cudaError_t set_ffma_attr_all_b() {
-    cudaError_t e = set_ffma_attr<AL, BLoadScatter>();
-    if (e == cudaSuccess) e = set_ffma_attr<AL, BLoadVec>();
-    if (e == cudaSuccess) e = set_ffma_attr<AL, BLoadScalar>();
+    using L = FfmaLoaders<FCfg>;
+    cudaError_t e = set_ffma_attr<FCfg, AL, typename L::BScatter>();
+    if (e == cudaSuccess) e = set_ffma_attr<FCfg, AL, typename L::BVec>();
+    if (e == cudaSuccess) e = set_ffma_attr<FCfg, AL, typename L::BScalar>();
     return e;
 }
 
-template <class AL>
-int ffma_smem_b(int bkind) {
-    return bkind == 0 ? ffma::Layout<FCfg, AL, BLoadScatter>::SMEM_BYTES
-                      : bkind == 1 ? ffma::Layout<FCfg, AL, BLoadVec>::SMEM_BYTES
-                                   : ffma::Layout<FCfg, AL, BLoadScalar>::SMEM_BYTES;
+template <class FCfg>
+cudaError_t set_ffma_attr_all() {
+    using L = FfmaLoaders<FCfg>;
+    cudaError_t e = set_ffma_attr_all_b<FCfg, typename L::AScatter>();
+    if (e == cudaSuccess) e = set_ffma_attr_all_b<FCfg, typename L::AVec>();
+    if (e == cudaSuccess) e = set_ffma_attr_all_b<FCfg, typename L::AScalar>();
+    return e;
 }
 
+template <class FCfg, class AL>
+int ffma_smem_b(int bkind) {
+    using L = FfmaLoaders<FCfg>;
+    return bkind == 0 ? ffma::Layout<FCfg, AL, typename L::BScatter>::SMEM_BYTES
+                      : bkind == 1 ? ffma::Layout<FCfg, AL, typename L::BVec>::SMEM_BYTES
+                                   : ffma::Layout<FCfg, AL, typename L::BScalar>::SMEM_BYTES;
+}
+
+template <class FCfg>
 int ffma_smem_bytes(int akind, int bkind) {
-    return akind == 0 ? ffma_smem_b<ALoadScatter>(bkind)
-                      : akind == 1 ? ffma_smem_b<ALoadVec>(bkind) : ffma_smem_b<ALoadScalar>(bkind);
+    using L = FfmaLoaders<FCfg>;
+    return akind == 0 ? ffma_smem_b<FCfg, typename L::AScatter>(bkind)
+                      : akind == 1 ? ffma_smem_b<FCfg, typename L::AVec>(bkind)
+                                   : ffma_smem_b<FCfg, typename L::AScalar>(bkind);
 }
 
 template <class Cfg, bool TRANS, bool XM, bool YM, bool XP = false>
@@ -139,9 +155,8 @@ int device_state(DeviceState **out) {
     if (!d.ready) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr_all_b<ALoadScatter>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr_all_b<ALoadVec>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr_all_b<ALoadScalar>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_ffma_attr_all<ffma::Default>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = set_ffma_attr_all<ffma::Wide>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Wide, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Narrow, false>()) != cudaSuccess) return fail_cuda(e);
         if ((e = set_tc_attr<tf32x3::Wide, true>()) != cudaSuccess) return fail_cuda(e);
@@ -460,18 +475,25 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         return SGEMM_STATUS_OK;
     }
     pl->kernel = kKernelFfmaCpAsync;
-    pl->bm = ffma::Default::BM;
-    pl->bn = ffma::Default::BN;
-    pl->bk = ffma::Default::BK;
-    pl->rm = ffma::Default::TM;
-    pl->rn = ffma::Default::TN;
-    pl->threads = ffma::Default::THREADS;
-    pl->stages = ffma::Default::STAGES;
+    // 128 x 256 tiles (one CTA per SM) for problems of at least 8 waves of
+    // them, where the last wave's idle SMs cost little; 128 x 128 (two per
+    // SM) otherwise.  SGEMM_GB300_FFMA_TILE_N (128 / 256) pins the choice.
+    const char *env_fb = std::getenv("SGEMM_GB300_FFMA_TILE_N");
+    const long long wide_tiles = (long long)((m + ffma::Wide::BM - 1) / ffma::Wide::BM) *
+                                 ((n + ffma::Wide::BN - 1) / ffma::Wide::BN) * (batch > 0 ? batch : 1);
+    const bool fwide = env_fb ? std::atoi(env_fb) == ffma::Wide::BN : wide_tiles >= 8LL * num_sms;
+    pl->bm = fwide ? ffma::Wide::BM : ffma::Default::BM;
+    pl->bn = fwide ? ffma::Wide::BN : ffma::Default::BN;
+    pl->bk = fwide ? ffma::Wide::BK : ffma::Default::BK;
+    pl->rm = fwide ? ffma::Wide::TM : ffma::Default::TM;
+    pl->rn = fwide ? ffma::Wide::TN : ffma::Default::TN;
+    pl->threads = fwide ? ffma::Wide::THREADS : ffma::Default::THREADS;
+    pl->stages = fwide ? ffma::Wide::STAGES : ffma::Default::STAGES;
     // rows-contiguous operands take 16-byte copies when their rows are 16-byte aligned
     pl->a_vec = op_a == SGEMM_OP_T && aligned(A, 16) && (lda % 4) == 0;
     pl->b_vec = op_b == SGEMM_OP_N && aligned(B, 16) && (ldb % 4) == 0;
-    pl->smem_bytes = ffma_smem_bytes(op_a == SGEMM_OP_N ? 0 : (pl->a_vec ? 1 : 2),
-                                     op_b == SGEMM_OP_T ? 0 : (pl->b_vec ? 1 : 2));
+    const int akind = op_a == SGEMM_OP_N ? 0 : (pl->a_vec ? 1 : 2), bkind = op_b == SGEMM_OP_T ? 0 : (pl->b_vec ? 1 : 2);
+    pl->smem_bytes = fwide ? ffma_smem_bytes<ffma::Wide>(akind, bkind) : ffma_smem_bytes<ffma::Default>(akind, bkind);
     const int tiles_m = (m + pl->bm - 1) / pl->bm;
     const int tiles_n = (n + pl->bn - 1) / pl->bn;
     pl->tiles = tiles_m * tiles_n;
@@ -893,25 +915,35 @@ int noalloc_scratch(float **out) {
     return SGEMM_STATUS_OK;
 }
 
-template <class AL, class BL>
+template <class FCfg, class AL, class BL>
 void launch_ffma_t(const GemmArgs &a, dim3 grid, cudaStream_t s) {
     ffma::ffma_sgemm_kernel<FCfg, AL, BL><<<grid, FCfg::THREADS, ffma::Layout<FCfg, AL, BL>::SMEM_BYTES, s>>>(a);
 }
 
-template <class AL>
+template <class FCfg, class AL>
 void launch_ffma_b(int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s) {
-    if (bkind == 0) launch_ffma_t<AL, BLoadScatter>(a, grid, s);
-    else if (bkind == 1) launch_ffma_t<AL, BLoadVec>(a, grid, s);
-    else launch_ffma_t<AL, BLoadScalar>(a, grid, s);
+    using L = FfmaLoaders<FCfg>;
+    if (bkind == 0) launch_ffma_t<FCfg, AL, typename L::BScatter>(a, grid, s);
+    else if (bkind == 1) launch_ffma_t<FCfg, AL, typename L::BVec>(a, grid, s);
+    else launch_ffma_t<FCfg, AL, typename L::BScalar>(a, grid, s);
+}
+
+template <class FCfg>
+void launch_ffma_cfg(int akind, int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s) {
+    using L = FfmaLoaders<FCfg>;
+    if (akind == 0) launch_ffma_b<FCfg, typename L::AScatter>(bkind, a, grid, s);
+    else if (akind == 1) launch_ffma_b<FCfg, typename L::AVec>(bkind, a, grid, s);
+    else launch_ffma_b<FCfg, typename L::AScalar>(bkind, a, grid, s);
 }
 
 void launch_ffma(const sgemm_plan &pl, const GemmArgs &a, int batch, cudaStream_t s) {
     const int akind = pl.op_a == SGEMM_OP_N ? 0 : (pl.a_vec ? 1 : 2);
     const int bkind = pl.op_b == SGEMM_OP_T ? 0 : (pl.b_vec ? 1 : 2);
     const dim3 grid((unsigned)pl.grid, (unsigned)batch, 1);
-    if (akind == 0) launch_ffma_b<ALoadScatter>(bkind, a, grid, s);
-    else if (akind == 1) launch_ffma_b<ALoadVec>(bkind, a, grid, s);
-    else launch_ffma_b<ALoadScalar>(bkind, a, grid, s);
+    if (pl.bn == ffma::Wide::BN)
+        launch_ffma_cfg<ffma::Wide>(akind, bkind, a, grid, s);
+    else
+        launch_ffma_cfg<ffma::Default>(akind, bkind, a, grid, s);
 }
 
 // Status code of the bounded-wait self-test (sgemm_selftest_wait).

@@ -103,6 +103,28 @@ def test_plan_matches_blocking_model():
     assert p["smem_bytes"] <= 227 * 1024
 
 
+def test_ffma_tile_choice(monkeypatch):
+    """The FFMA path takes 128 x 256 tiles (8 x 16 per thread, 256 threads)
+    for at least 8 waves of them on the device's SMs, 128 x 128 (8 x 8)
+    otherwise; SGEMM_GB300_FFMA_TILE_N pins it."""
+    monkeypatch.delenv("SGEMM_GB300_FFMA_TILE_N", raising=False)
+    F = binding.PATH_FFMA
+
+    def tile(m, n, k):
+        st, p = hplan(m, n, k, path=F)
+        assert st == 0
+        return p["bm"], p["bn"], p["rm"], p["rn"], p["threads"]
+
+    assert tile(8192, 8192, 8192) == (128, 256, 8, 16, 256)   # 2048 tiles = 13.5 waves
+    assert tile(4096, 4096, 4096) == (128, 128, 8, 8, 256)     # 512 tiles = 3.4 waves
+    assert tile(6144, 6144, 64) == (128, 128, 8, 8, 256)       # 1152 tiles < 8 x 152 = 1216
+    assert tile(6400, 6400, 64) == (128, 256, 8, 16, 256)      # 1250 tiles
+    monkeypatch.setenv("SGEMM_GB300_FFMA_TILE_N", "256")
+    assert tile(64, 64, 64) == (128, 256, 8, 16, 256)
+    monkeypatch.setenv("SGEMM_GB300_FFMA_TILE_N", "128")
+    assert tile(8192, 8192, 8192) == (128, 128, 8, 8, 256)
+
+
 def test_plan_ragged_shapes_cover_the_output():
     for m, n, k in ((1000, 1500, 777), (1, 1, 1), (129, 257, 17), (16384, 128, 8192)):
         st, p = hplan(m, n, k, lda=k, path=binding.PATH_FFMA)
