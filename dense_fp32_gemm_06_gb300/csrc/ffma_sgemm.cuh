@@ -122,7 +122,9 @@ struct ScatterLoader {
         if (interior_r && k0 + BK <= o.k) {
             const float *a = src + k0;
 #pragma unroll
-            for (int j = 0; j < PER_THREAD; ++j, a += step) cp_async_4(slab + dst + j * ROW_STEP * 4, a, 4u);
+            for (int j = 0; j < PER_THREAD; ++j, a += step)
+                if (SG_IN(in_matrix(a, 1, o.ptr, o.ld, o.rows, o.k) && dst + j * ROW_STEP * 4 + 4 <= BK * LD * 4))
+                    cp_async_4(slab + dst + j * ROW_STEP * 4, a, 4u);
             return;
         }
         const bool k_ok = k0 + kc < o.k;
@@ -130,7 +132,9 @@ struct ScatterLoader {
 #pragma unroll
         for (int j = 0; j < PER_THREAD; ++j) {
             const bool ok = k_ok && r_base + row0 + j * ROW_STEP < o.rows;
-            cp_async_4(slab + dst + j * ROW_STEP * 4, ok ? a + j * step : o.ptr, ok ? 4u : 0u);
+            if (SG_IN((!ok || in_matrix(a + j * step, 1, o.ptr, o.ld, o.rows, o.k)) &&
+                      dst + j * ROW_STEP * 4 + 4 <= BK * LD * 4))
+                cp_async_4(slab + dst + j * ROW_STEP * 4, ok ? a + j * step : o.ptr, ok ? 4u : 0u);
         }
     }
 };
@@ -169,6 +173,9 @@ struct DirectLoader {
             const float *b = src + (long long)k0 * o.ld;
 #pragma unroll
             for (int j = 0; j < PER_THREAD; ++j, b += step) {
+                if (!SG_IN(in_matrix(b, W, o.ptr, o.ld, o.k, o.rows) &&
+                           dst + j * ROWS_PER_PASS * LD * 4 + W * 4 <= BK * LD * 4))
+                    continue;
                 if constexpr (VEC)
                     cp_async_16(slab + dst + j * ROWS_PER_PASS * LD * 4, b, 16u);
                 else
@@ -188,6 +195,9 @@ struct DirectLoader {
             const int kr = k0 + kk0 + j * ROWS_PER_PASS;
             const uint32_t nb = kr < o.k ? bytes : 0u;
             const float *b = nb ? src + (long long)(k0 + j * ROWS_PER_PASS) * o.ld : o.ptr;
+            if (!SG_IN((nb == 0 || in_matrix(b, (int)nb / 4, o.ptr, o.ld, o.k, o.rows)) &&
+                       dst + j * ROWS_PER_PASS * LD * 4 + W * 4 <= BK * LD * 4))
+                continue;
             if constexpr (VEC)
                 cp_async_16(slab + dst + j * ROWS_PER_PASS * LD * 4, b, nb);
             else
@@ -246,6 +256,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
     float *const Cb = p.C + bz * p.stride_c;
     const AL la(oa, m0, tid);
     const BL lb(ob, n0, tid);
+    // every fragment read below lies in its stage (the largest offsets of A's
+    // and B's reads; checked builds only)
+    const bool frag_ok = SG_IN(a_off + (BK - 1) * A_LD + 32 * (GM - 1) + 4 <= A_STAGE &&
+                               b_off + (BK - 1) * B_LD + 16 * (GN - 1) + 4 <= B_STAGE);
     const uint32_t As_u32 = smem_u32(As), Bs_u32 = smem_u32(Bs);
 
     // prologue: slabs 0 .. STAGES-2 in flight
@@ -282,9 +296,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
 
         float4 fa[2][GM], fb[2][GN];
 #pragma unroll
-        for (int g = 0; g < GM; ++g) fa[0][g] = *reinterpret_cast<const float4 *>(as + 32 * g);
+        for (int g = 0; g < GM; ++g) fa[0][g] = frag_ok ? *reinterpret_cast<const float4 *>(as + 32 * g) : float4{};
 #pragma unroll
-        for (int h = 0; h < GN; ++h) fb[0][h] = *reinterpret_cast<const float4 *>(bs + 16 * h);
+        for (int h = 0; h < GN; ++h) fb[0][h] = frag_ok ? *reinterpret_cast<const float4 *>(bs + 16 * h) : float4{};
 #pragma unroll
         for (int kk = 0; kk < BK; ++kk) {
             const int cur = kk & 1;
@@ -292,10 +306,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
                 const int nxt = cur ^ 1;
 #pragma unroll
                 for (int g = 0; g < GM; ++g)
-                    fa[nxt][g] = *reinterpret_cast<const float4 *>(as + (kk + 1) * A_LD + 32 * g);
+                    fa[nxt][g] = frag_ok ? *reinterpret_cast<const float4 *>(as + (kk + 1) * A_LD + 32 * g) : float4{};
 #pragma unroll
                 for (int h = 0; h < GN; ++h)
-                    fb[nxt][h] = *reinterpret_cast<const float4 *>(bs + (kk + 1) * B_LD + 16 * h);
+                    fb[nxt][h] = frag_ok ? *reinterpret_cast<const float4 *>(bs + (kk + 1) * B_LD + 16 * h) : float4{};
             }
             float a[TM], b[TN];
 #pragma unroll
@@ -335,6 +349,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
             const int col = n0 + b_off + 16 * h;
             const float *v = &acc[i][4 * h];
             if (p.c_vec && col + 3 < p.n) {
+                if (!SG_IN(in_matrix(crow + col, 4, Cb, p.ldc, p.m, p.n))) continue;
                 float4 o;
                 if (beta != 0.f) {
                     const float4 c = *reinterpret_cast<const float4 *>(crow + col);
@@ -347,7 +362,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
             } else {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    if (col + q < p.n) {
+                    if (col + q < p.n && SG_IN(in_matrix(crow + col + q, 1, Cb, p.ldc, p.m, p.n))) {
                         crow[col + q] = beta != 0.f ? fmaf(alpha, v[q], beta * crow[col + q]) : alpha * v[q];
                     }
                 }
@@ -365,18 +380,47 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
 using Default = Config<128, 128, 32, 3, 8, 8, 2>;
 using Wide = Config<128, 256, 32, 3, 8, 16, 1>;
 
+// Operand loaders of a configuration by storage: k contiguous ->
+// ScatterLoader; rows contiguous -> DirectLoader with 16-byte (rows 16-byte
+// aligned) or 4-byte copies.
+template <class Cfg>
+struct Loaders {
+    using AScatter = ScatterLoader<Cfg::BM, Cfg::BK, Cfg::THREADS>;
+    using AVec = DirectLoader<Cfg::BM, Cfg::BK, Cfg::THREADS, true>;
+    using AScalar = DirectLoader<Cfg::BM, Cfg::BK, Cfg::THREADS, false>;
+    using BScatter = ScatterLoader<Cfg::BN, Cfg::BK, Cfg::THREADS>;
+    using BVec = DirectLoader<Cfg::BN, Cfg::BK, Cfg::THREADS, true>;
+    using BScalar = DirectLoader<Cfg::BN, Cfg::BK, Cfg::THREADS, false>;
+};
+
+// Dynamic shared memory of the instance for loader kinds akind / bkind
+// (0 scatter, 1 direct 16-byte, 2 direct 4-byte).
+template <class Cfg>
+constexpr int smem_bytes(int akind, int bkind) {
+    using L = Loaders<Cfg>;
+    return akind == 0   ? (bkind == 0   ? Layout<Cfg, typename L::AScatter, typename L::BScatter>::SMEM_BYTES
+                           : bkind == 1 ? Layout<Cfg, typename L::AScatter, typename L::BVec>::SMEM_BYTES
+                                        : Layout<Cfg, typename L::AScatter, typename L::BScalar>::SMEM_BYTES)
+           : akind == 1 ? (bkind == 0   ? Layout<Cfg, typename L::AVec, typename L::BScatter>::SMEM_BYTES
+                           : bkind == 1 ? Layout<Cfg, typename L::AVec, typename L::BVec>::SMEM_BYTES
+                                        : Layout<Cfg, typename L::AVec, typename L::BScalar>::SMEM_BYTES)
+                        : (bkind == 0   ? Layout<Cfg, typename L::AScalar, typename L::BScatter>::SMEM_BYTES
+                           : bkind == 1 ? Layout<Cfg, typename L::AScalar, typename L::BVec>::SMEM_BYTES
+                                        : Layout<Cfg, typename L::AScalar, typename L::BScalar>::SMEM_BYTES);
+}
+
 }  // namespace ffma
 
 // C = beta * C over an m x n window (beta == 0 writes zeros without reading);
 // blockIdx.y selects the problem of a strided batch (C + y*stride_c).
-__global__ void scale_c_kernel(float *C, long long ldc, int m, int n, float beta, long long stride_c) {
+static __global__ void scale_c_kernel(float *C, long long ldc, int m, int n, float beta, long long stride_c) {
     C += blockIdx.y * stride_c;
     const long long total = (long long)m * n;
     for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
          idx += (long long)gridDim.x * blockDim.x) {
         const long long i = idx / n, j = idx - i * n;
         float *c = C + i * ldc + j;
-        *c = beta != 0.f ? beta * *c : 0.f;
+        if (SG_IN(in_matrix(c, 1, C, ldc, m, n))) *c = beta != 0.f ? beta * *c : 0.f;
     }
 }
 

@@ -2,6 +2,8 @@
 #pragma once
 #include <cstdint>
 
+#include <cuda_runtime.h>
+
 namespace sgemm_gb300 {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -111,8 +113,50 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Status word written by bounded waits that gave up (0 = never).
-__device__ int g_sgemm_status;
+// Status word written by bounded waits that gave up (0 = never).  Each
+// translation unit of the library has its own (internal linkage: the units
+// are compiled apart), read through unit_status below.
+static __device__ int g_sgemm_status;
+
+// ---------------------------------------------------------------- checked builds
+// Compiled with SGEMM_GB300_CHECKED, the kernels test each global and
+// shared-memory index they compute against its buffer before the access
+// (SG_IN(condition)): a failed test skips that access, records kStatusBounds
+// in the status word and the source line of the test in g_sgemm_bad_line,
+// and the call's results are then not valid.  No test traps or returns
+// early: barriers and waits run as usual, the context stays usable.
+// Without SGEMM_GB300_CHECKED, SG_IN(c) is `true` and the tests compile away.
+constexpr int kStatusBounds = 0x208;
+static __device__ int g_sgemm_bad_line;
+
+#ifdef SGEMM_GB300_CHECKED
+#define SG_CHECK_FN static __device__ __noinline__   // one copy of each test per unit: short compile times
+#else
+#define SG_CHECK_FN static __device__ __forceinline__
+#endif
+
+SG_CHECK_FN bool bounds_ok(bool ok, int line) {
+    if (!ok) {
+        atomicCAS(&g_sgemm_status, 0, kStatusBounds);
+        atomicCAS(&g_sgemm_bad_line, 0, line);
+    }
+    return ok;
+}
+
+#ifdef SGEMM_GB300_CHECKED
+#define SG_IN(cond) (::sgemm_gb300::bounds_ok((cond), __LINE__))
+#else
+#define SG_IN(cond) (true)
+#endif
+
+// Whether `p` addresses an element (r, c) of the rows x cols matrix at
+// `base` (row pitch ld) whose row holds the n elements from c on.
+SG_CHECK_FN bool in_matrix(const float *p, int n, const float *base, long long ld, long long rows, long long cols) {
+    const long long off = p - base;
+    if (off < 0 || ld <= 0) return false;
+    const long long r = off / ld, c = off - r * ld;
+    return r < rows && c + n <= cols;
+}
 
 // Bounded wait for the phase of parity `parity` of `bar`: gives up after
 // `limit_ns` nanoseconds, records `code` in g_sgemm_status and returns false.
@@ -141,6 +185,21 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
         }
     }
     return true;
+}
+
+// This translation unit's status word and failed-test line (host side;
+// synchronise first): copied to *status / *line (either may be NULL), and
+// reset when `clear` is set.
+static inline cudaError_t unit_status(int *status, int *line, bool clear) {
+    cudaError_t e = cudaSuccess;
+    if (status) e = cudaMemcpyFromSymbol(status, g_sgemm_status, sizeof(int));
+    if (e == cudaSuccess && line) e = cudaMemcpyFromSymbol(line, g_sgemm_bad_line, sizeof(int));
+    if (e == cudaSuccess && clear) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_sgemm_status, &zero, sizeof(int));
+        if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_sgemm_bad_line, &zero, sizeof(int));
+    }
+    return e;
 }
 
 // ---------------------------------------------------------------- TMA

@@ -14,6 +14,8 @@
 #pragma once
 #include <cstdint>
 
+#include "ptx.cuh"
+
 #include "../../include/sgemm_gb300.h"
 
 namespace sgemm_gb300 {
@@ -44,6 +46,7 @@ __global__ void __launch_bounds__(THREADS) reduce_sum_kernel(const float *__rest
         const float4 *x4 = reinterpret_cast<const float4 *>(x);
         long long i = gtid;
         for (; i + gstride < n4; i += 2 * gstride) {
+            if (!SG_IN(i >= 0 && 4 * (i + gstride) + 4 <= n)) continue;
             const float4 u = __ldg(x4 + i), v = __ldg(x4 + i + gstride);
             a0 += u.x;
             a1 += u.y;
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(THREADS) reduce_sum_kernel(const float *__rest
             a2 += v.z;
             a3 += v.w;
         }
-        if (i < n4) {
+        if (i < n4 && SG_IN(4 * i + 4 <= n)) {
             const float4 u = __ldg(x4 + i);
             a0 += u.x;
             a1 += u.y;
@@ -63,11 +66,12 @@ __global__ void __launch_bounds__(THREADS) reduce_sum_kernel(const float *__rest
         }
         tail = 4 * n4;
     }
-    for (long long i = tail + gtid; i < n; i += gstride) a0 += __ldg(x + i);
+    for (long long i = tail + gtid; i < n; i += gstride)
+        if (SG_IN(i >= 0)) a0 += __ldg(x + i);
     float v = warp_sum((a0 + a1) + (a2 + a3));
     __shared__ float partial[WARPS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) partial[warp] = v;
+    if (lane == 0 && SG_IN(warp < WARPS)) partial[warp] = v;
     __syncthreads();
     if (warp == 0) {
         v = warp_sum(lane < WARPS ? partial[lane] : 0.f);

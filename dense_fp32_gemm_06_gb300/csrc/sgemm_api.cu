@@ -10,9 +10,8 @@
 #include <mutex>
 
 #include "../../include/sgemm_gb300.h"
-#include "ffma_sgemm.cuh"
-#include "tf32x3_sgemm.cuh"
 #include "reduce_sum.cuh"
+#include "units.h"
 
 using namespace sgemm_gb300;
 
@@ -50,100 +49,6 @@ int fail_cuda(cudaError_t e) {
     return SGEMM_STATUS_CUDA_ERROR;
 }
 
-// FFMA operand loaders by storage: k contiguous -> ScatterLoader; rows
-// contiguous -> DirectLoader with 16-byte (rows 16-byte aligned) or 4-byte
-// copies.  Loader kinds: 0 scatter, 1 direct 16-byte, 2 direct 4-byte.
-template <class FCfg>
-struct FfmaLoaders {
-    using AScatter = ffma::ScatterLoader<FCfg::BM, FCfg::BK, FCfg::THREADS>;
-    using AVec = ffma::DirectLoader<FCfg::BM, FCfg::BK, FCfg::THREADS, true>;
-    using AScalar = ffma::DirectLoader<FCfg::BM, FCfg::BK, FCfg::THREADS, false>;
-    using BScatter = ffma::ScatterLoader<FCfg::BN, FCfg::BK, FCfg::THREADS>;
-    using BVec = ffma::DirectLoader<FCfg::BN, FCfg::BK, FCfg::THREADS, true>;
-    using BScalar = ffma::DirectLoader<FCfg::BN, FCfg::BK, FCfg::THREADS, false>;
-};
-
-template <class FCfg, class AL, class BL>
-cudaError_t set_ffma_attr() {
-    return cudaFuncSetAttribute(ffma::ffma_sgemm_kernel<FCfg, AL, BL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                ffma::Layout<FCfg, AL, BL>::SMEM_BYTES);
-}
-
-template <class FCfg, class AL>
-cudaError_t set_ffma_attr_all_b() {
-    using L = FfmaLoaders<FCfg>;
-    cudaError_t e = set_ffma_attr<FCfg, AL, typename L::BScatter>();
-    if (e == cudaSuccess) e = set_ffma_attr<FCfg, AL, typename L::BVec>();
-    if (e == cudaSuccess) e = set_ffma_attr<FCfg, AL, typename L::BScalar>();
-    return e;
-}
-
-template <class FCfg>
-cudaError_t set_ffma_attr_all() {
-    using L = FfmaLoaders<FCfg>;
-    cudaError_t e = set_ffma_attr_all_b<FCfg, typename L::AScatter>();
-    if (e == cudaSuccess) e = set_ffma_attr_all_b<FCfg, typename L::AVec>();
-    if (e == cudaSuccess) e = set_ffma_attr_all_b<FCfg, typename L::AScalar>();
-    return e;
-}
-
-template <class FCfg, class AL>
-int ffma_smem_b(int bkind) {
-    using L = FfmaLoaders<FCfg>;
-    return bkind == 0 ? ffma::Layout<FCfg, AL, typename L::BScatter>::SMEM_BYTES
-                      : bkind == 1 ? ffma::Layout<FCfg, AL, typename L::BVec>::SMEM_BYTES
-                                   : ffma::Layout<FCfg, AL, typename L::BScalar>::SMEM_BYTES;
-}
-
-template <class FCfg>
-int ffma_smem_bytes(int akind, int bkind) {
-    using L = FfmaLoaders<FCfg>;
-    return akind == 0 ? ffma_smem_b<FCfg, typename L::AScatter>(bkind)
-                      : akind == 1 ? ffma_smem_b<FCfg, typename L::AVec>(bkind)
-                                   : ffma_smem_b<FCfg, typename L::AScalar>(bkind);
-}
-
-template <class Cfg, bool TRANS, bool XM, bool YM, bool XP = false>
-cudaError_t set_tc_attr_one() {
-    return cudaFuncSetAttribute(tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM, XP>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
-}
-
-// The four operand-layout variants of one tile shape (X and Y each K-major
-// or MN-major), and on untransposed single-CTA tiles the two with X read in
-// row phases.
-template <class Cfg, bool TRANS>
-cudaError_t set_tc_attr() {
-    cudaError_t e = set_tc_attr_one<Cfg, TRANS, false, false>();
-    if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, false, true>();
-    if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, true, false>();
-    if (e == cudaSuccess) e = set_tc_attr_one<Cfg, TRANS, true, true>();
-    if constexpr (!TRANS && !Cfg::PAIR) {
-        if (e == cudaSuccess) e = set_tc_attr_one<Cfg, false, false, false, true>();
-        if (e == cudaSuccess) e = set_tc_attr_one<Cfg, false, false, true, true>();
-    }
-    return e;
-}
-
-// Clusters of S CTAs of the tensor-core kernel that can be resident at once
-// (thread-block clusters cannot span GPCs, so this is below sms / S).
-template <class Cfg>
-cudaError_t max_clusters_of(int S, int *out) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(S * 64), 1, 1);
-    cfg.blockDim = dim3((unsigned)tf32x3::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = (size_t)Cfg::SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)S;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    *out = 0;
-    return cudaOccupancyMaxActiveClusters(out, tf32x3::tf32x3_gemm_kernel<Cfg, false, false, true>, &cfg);
-}
-
 // One-time per-device set-up: SM count and kernel attributes.
 int device_state(DeviceState **out) {
     int dev = 0;
@@ -155,17 +60,16 @@ int device_state(DeviceState **out) {
     if (!d.ready) {
         e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr_all<ffma::Default>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_ffma_attr_all<ffma::Wide>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_tc_attr<tf32x3::Wide, false>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_tc_attr<tf32x3::Narrow, false>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_tc_attr<tf32x3::Wide, true>()) != cudaSuccess) return fail_cuda(e);
-        if ((e = set_tc_attr<tf32x3::Pair, false>()) != cudaSuccess) return fail_cuda(e);
+        if ((e = units::ffma_attrs()) != cudaSuccess) return fail_cuda(e);
+        if ((e = units::tc_wide_attrs()) != cudaSuccess) return fail_cuda(e);
+        if ((e = units::tc_narrow_attrs()) != cudaSuccess) return fail_cuda(e);
+        if ((e = units::tc_trans_attrs()) != cudaSuccess) return fail_cuda(e);
+        if ((e = units::tc_pair_attrs()) != cudaSuccess) return fail_cuda(e);
         for (int S = 2; S <= 8; ++S) {
-            if ((e = max_clusters_of<tf32x3::Wide>(S, &d.max_clusters[0][S])) != cudaSuccess) return fail_cuda(e);
-            if ((e = max_clusters_of<tf32x3::Narrow>(S, &d.max_clusters[1][S])) != cudaSuccess) return fail_cuda(e);
+            if ((e = units::tc_wide_clusters(S, &d.max_clusters[0][S])) != cudaSuccess) return fail_cuda(e);
+            if ((e = units::tc_narrow_clusters(S, &d.max_clusters[1][S])) != cudaSuccess) return fail_cuda(e);
         }
-        if ((e = max_clusters_of<tf32x3::Pair>(2, &d.max_clusters[2][2])) != cudaSuccess) return fail_cuda(e);
+        if ((e = units::tc_pair_clusters(2, &d.max_clusters[2][2])) != cudaSuccess) return fail_cuda(e);
         if (d.pool == nullptr) {
             cudaMemPoolProps props = {};
             props.allocType = cudaMemAllocationTypePinned;
@@ -493,7 +397,7 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
     pl->a_vec = op_a == SGEMM_OP_T && aligned(A, 16) && (lda % 4) == 0;
     pl->b_vec = op_b == SGEMM_OP_N && aligned(B, 16) && (ldb % 4) == 0;
     const int akind = op_a == SGEMM_OP_N ? 0 : (pl->a_vec ? 1 : 2), bkind = op_b == SGEMM_OP_T ? 0 : (pl->b_vec ? 1 : 2);
-    pl->smem_bytes = fwide ? ffma_smem_bytes<ffma::Wide>(akind, bkind) : ffma_smem_bytes<ffma::Default>(akind, bkind);
+    pl->smem_bytes = fwide ? ffma::smem_bytes<ffma::Wide>(akind, bkind) : ffma::smem_bytes<ffma::Default>(akind, bkind);
     const int tiles_m = (m + pl->bm - 1) / pl->bm;
     const int tiles_n = (n + pl->bn - 1) / pl->bn;
     pl->tiles = tiles_m * tiles_n;
@@ -656,25 +560,6 @@ int launch_split_b(int k, int n, const float *B, int ldb, float *bt_hi, float *b
     return SGEMM_STATUS_OK;
 }
 
-template <class Cfg, bool TRANS, bool XM, bool YM, bool XP = false>
-cudaError_t launch_tc_one(const cudaLaunchConfig_t &cfg, const CUtensorMap *maps, const tf32x3::Params &a) {
-    return cudaLaunchKernelEx(&cfg, tf32x3::tf32x3_gemm_kernel<Cfg, TRANS, XM, YM, XP>, maps[0], maps[1], maps[2],
-                              maps[3], maps[4], maps[5], a);
-}
-
-// xm / ym: X / Y read MN-major; xp: X read in row phases (untransposed
-// single-CTA tiles only; prepare_gemm rejects the rest)
-template <class Cfg, bool TRANS>
-cudaError_t launch_tc(const cudaLaunchConfig_t &cfg, bool xm, bool ym, bool xp, const CUtensorMap *maps,
-                      const tf32x3::Params &a) {
-    if constexpr (!TRANS && !Cfg::PAIR) {
-        if (xp) return ym ? launch_tc_one<Cfg, false, false, true, true>(cfg, maps, a)
-                          : launch_tc_one<Cfg, false, false, false, true>(cfg, maps, a);
-    }
-    if (xm) return ym ? launch_tc_one<Cfg, TRANS, true, true>(cfg, maps, a) : launch_tc_one<Cfg, TRANS, true, false>(cfg, maps, a);
-    return ym ? launch_tc_one<Cfg, TRANS, false, true>(cfg, maps, a) : launch_tc_one<Cfg, TRANS, false, false>(cfg, maps, a);
-}
-
 // Everything a tensor-core GEMM launch needs, prepared before anything is
 // enqueued (so that a failure here leaves the stream untouched).
 struct GemmLaunch {
@@ -766,13 +651,13 @@ int launch_gemm(const GemmLaunch &L, const sgemm_plan &pl, int batch, cudaStream
     cfg.numAttrs = na;
     cudaError_t e;
     if (pl.pair)
-        e = launch_tc<tf32x3::Pair, false>(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
+        e = units::tc_pair_launch(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
     else if (pl.trans)
-        e = launch_tc<tf32x3::Wide, true>(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
+        e = units::tc_trans_launch(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
     else if (pl.bn == tf32x3::Narrow::BN)
-        e = launch_tc<tf32x3::Narrow, false>(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
+        e = units::tc_narrow_launch(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
     else
-        e = launch_tc<tf32x3::Wide, false>(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
+        e = units::tc_wide_launch(cfg, L.xm, L.ym, L.xp, L.maps, L.prm);
     if (e != cudaSuccess) return fail_cuda(e);
     return SGEMM_STATUS_OK;
 }
@@ -915,35 +800,10 @@ int noalloc_scratch(float **out) {
     return SGEMM_STATUS_OK;
 }
 
-template <class FCfg, class AL, class BL>
-void launch_ffma_t(const GemmArgs &a, dim3 grid, cudaStream_t s) {
-    ffma::ffma_sgemm_kernel<FCfg, AL, BL><<<grid, FCfg::THREADS, ffma::Layout<FCfg, AL, BL>::SMEM_BYTES, s>>>(a);
-}
-
-template <class FCfg, class AL>
-void launch_ffma_b(int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s) {
-    using L = FfmaLoaders<FCfg>;
-    if (bkind == 0) launch_ffma_t<FCfg, AL, typename L::BScatter>(a, grid, s);
-    else if (bkind == 1) launch_ffma_t<FCfg, AL, typename L::BVec>(a, grid, s);
-    else launch_ffma_t<FCfg, AL, typename L::BScalar>(a, grid, s);
-}
-
-template <class FCfg>
-void launch_ffma_cfg(int akind, int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s) {
-    using L = FfmaLoaders<FCfg>;
-    if (akind == 0) launch_ffma_b<FCfg, typename L::AScatter>(bkind, a, grid, s);
-    else if (akind == 1) launch_ffma_b<FCfg, typename L::AVec>(bkind, a, grid, s);
-    else launch_ffma_b<FCfg, typename L::AScalar>(bkind, a, grid, s);
-}
-
 void launch_ffma(const sgemm_plan &pl, const GemmArgs &a, int batch, cudaStream_t s) {
     const int akind = pl.op_a == SGEMM_OP_N ? 0 : (pl.a_vec ? 1 : 2);
     const int bkind = pl.op_b == SGEMM_OP_T ? 0 : (pl.b_vec ? 1 : 2);
-    const dim3 grid((unsigned)pl.grid, (unsigned)batch, 1);
-    if (pl.bn == ffma::Wide::BN)
-        launch_ffma_cfg<ffma::Wide>(akind, bkind, a, grid, s);
-    else
-        launch_ffma_cfg<ffma::Default>(akind, bkind, a, grid, s);
+    units::ffma_launch(pl.bn == ffma::Wide::BN, akind, bkind, a, dim3((unsigned)pl.grid, (unsigned)batch, 1), s);
 }
 
 // Status code of the bounded-wait self-test (sgemm_selftest_wait).
@@ -960,6 +820,37 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns, int *gave_up) 
     mbar_init(smem_u32(&bar), 1);
     fence_mbar_init();
     *gave_up = mbar_wait(smem_u32(&bar), 0, kStatusSelfTest, limit_ns) ? 0 : 1;
+}
+
+// The bounds-check self-test: a store to element n of a buffer of n + 1
+// floats whose check (i < n) fails, so a checked build skips it and records
+// kStatusBounds and the check's line.  (Element n exists, so even a build
+// without checks would stay inside the buffer; it is never launched there.)
+__global__ void selftest_bounds_kernel(float *x, int n) {
+    const int i = n;
+    if (SG_IN(i < n)) x[i] = 1.f;
+}
+
+// The status words and failed-test lines of every translation unit of the
+// library -- this one's split, reduction and self-test kernels, and the
+// kernel units' -- read after a synchronisation: the first non-zero one of
+// each in unit order (each unit keeps the first code its kernels recorded).
+// `clear` resets both in every unit.
+cudaError_t all_units_status(int *status, int *line, bool clear) {
+    using Fn = cudaError_t (*)(int *, int *, bool);
+    static const Fn fns[] = {unit_status,           units::tc_wide_status, units::tc_narrow_status,
+                             units::tc_trans_status, units::tc_pair_status, units::ffma_status};
+    int st = 0, ln = 0;
+    for (Fn f : fns) {
+        int s = 0, l = 0;
+        cudaError_t e = f(&s, &l, clear);
+        if (e != cudaSuccess) return e;
+        if (st == 0) st = s;
+        if (ln == 0) ln = l;
+    }
+    if (status) *status = st;
+    if (line) *line = ln;
+    return cudaSuccess;
 }
 
 }  // namespace
@@ -1245,7 +1136,7 @@ const char *sgemm_status_string(int status) {
         case SGEMM_STATUS_TOO_LARGE:
             return "problem too large for the fixed no-allocation scratch (SGEMM_NOALLOC_SCRATCH_FLOATS)";
         case SGEMM_STATUS_BAD_PATH: return "unknown kernel path";
-        case SGEMM_STATUS_UNSUPPORTED: return "no plan structure given";
+        case SGEMM_STATUS_UNSUPPORTED: return "unsupported request (no plan structure given, or a checked-build-only call)";
         case SGEMM_STATUS_CUDA_ERROR: return "CUDA runtime error (see sgemm_last_cuda_error)";
         default: return "unknown status";
     }
@@ -1257,12 +1148,8 @@ int sgemm_device_status(int *flag, int clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return fail_cuda(e);
     int v = 0;
-    if ((e = cudaMemcpyFromSymbol(&v, g_sgemm_status, sizeof(int))) != cudaSuccess) return fail_cuda(e);
+    if ((e = all_units_status(&v, nullptr, clear != 0)) != cudaSuccess) return fail_cuda(e);
     if (flag) *flag = v;
-    if (clear) {
-        const int zero = 0;
-        if ((e = cudaMemcpyToSymbol(g_sgemm_status, &zero, sizeof(int))) != cudaSuccess) return fail_cuda(e);
-    }
     return SGEMM_STATUS_OK;
 }
 
@@ -1282,6 +1169,41 @@ int sgemm_selftest_wait(unsigned long long limit_ns, int *gave_up) {
     return SGEMM_STATUS_OK;
 }
 
+int sgemm_bounds_line(int *line, int clear) {
+    if (line == nullptr) return 1;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e);
+    int v = 0;
+    if ((e = all_units_status(nullptr, &v, clear != 0)) != cudaSuccess) return fail_cuda(e);
+    *line = v;
+    return SGEMM_STATUS_OK;
+}
+
+int sgemm_selftest_bounds(int *line) {
+#ifndef SGEMM_GB300_CHECKED
+    (void)line;
+    return SGEMM_STATUS_UNSUPPORTED;
+#else
+    if (line == nullptr) return 1;
+    constexpr int n = 32;
+    float *d = nullptr;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void **>(&d), (n + 1) * sizeof(float));
+    if (e != cudaSuccess) return fail_cuda(e);
+    selftest_bounds_kernel<<<1, 1>>>(d, n);
+    if ((e = cudaGetLastError()) == cudaSuccess) e = cudaDeviceSynchronize();
+    int v = 0;
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_sgemm_bad_line, sizeof(int));
+    cudaFree(d);
+    if (e != cudaSuccess) return fail_cuda(e);
+    *line = v;
+    return SGEMM_STATUS_OK;
+#endif
+}
+
+#ifdef SGEMM_GB300_CHECKED
+const char *sgemm_version(void) { return "sgemm_gb300 0.1 (sm_103a, checked)"; }
+#else
 const char *sgemm_version(void) { return "sgemm_gb300 0.1 (sm_103a)"; }
+#endif
 
 }  // extern "C"

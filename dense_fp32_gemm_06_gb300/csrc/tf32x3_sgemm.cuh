@@ -313,6 +313,9 @@ __device__ __forceinline__ void split_rows(const float *__restrict__ A, long lon
         float *h = hi + (long long)row * ka;
         float *l = lo + (long long)row * ka;
         for (int c = bx * (int)blockDim.x + (int)threadIdx.x; c < full4; c += stride) {
+            if (!SG_IN(in_matrix(src + 4 * c, 4, A, lda, m, k) && in_matrix(h + 4 * c, 4, hi, ka, m, ka) &&
+                       in_matrix(l + 4 * c, 4, lo, ka, m, ka)))
+                continue;
             const float4 x = __ldg(reinterpret_cast<const float4 *>(src) + c);
             float4 xh, xl;
             split_one(x.x, xh.x, xl.x);
@@ -323,6 +326,9 @@ __device__ __forceinline__ void split_rows(const float *__restrict__ A, long lon
             reinterpret_cast<float4 *>(l)[c] = xl;
         }
         for (int t = scal0 + bx * (int)blockDim.x + (int)threadIdx.x; t < k; t += stride) {
+            if (!SG_IN(in_matrix(src + t, 1, A, lda, m, k) && in_matrix(h + t, 1, hi, ka, m, ka) &&
+                       in_matrix(l + t, 1, lo, ka, m, ka)))
+                continue;
             float xh, xl;
             split_one(__ldg(src + t), xh, xl);
             h[t] = xh;
@@ -364,7 +370,7 @@ struct SplitJob {
 // is uniform per block.  The transpose is written out here rather than in a
 // device function: that form measured ~19 % slower on GB300 (B of 8192 x
 // 8192: 209.6 against 176.8 us).
-__global__ void __launch_bounds__(256) split_pair_kernel(SplitJob j0, SplitJob j1) {
+static __global__ void __launch_bounds__(256) split_pair_kernel(SplitJob j0, SplitJob j1) {
     griddep_launch_dependents();   // the GEMM may start its set-up meanwhile
     const int n0 = j0.gx * j0.gy;
     const bool first = (int)blockIdx.x < n0;
@@ -394,14 +400,15 @@ __global__ void __launch_bounds__(256) split_pair_kernel(SplitJob j0, SplitJob j
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
                     const int jj = j0_ + 32 * q + tx;
-                    tile[r][32 * q + tx] = (t < k && jj < n) ? __ldg(B + (long long)t * ldb + jj) : 0.f;
+                    const bool in = t < k && jj < n && SG_IN(in_matrix(B + (long long)t * ldb + jj, 1, B, ldb, k, n));
+                    tile[r][32 * q + tx] = in ? __ldg(B + (long long)t * ldb + jj) : 0.f;
                 }
             }
             __syncthreads();
 #pragma unroll
             for (int r = ty; r < 64; r += 8) {
                 const int jj = j0_ + r, t = t0 + tx;
-                if (jj < n && t < k) {
+                if (jj < n && t < k && SG_IN(in_matrix(hi + (long long)jj * ka + t, 1, hi, ka, n, ka))) {
                     float xh, xl;
                     split_one(tile[tx][r], xh, xl);
                     hi[(long long)jj * ka + t] = xh;
@@ -545,7 +552,8 @@ __device__ __forceinline__ void split_phased(uint8_t *hi_slot, uint8_t *lo_slot,
         const int u = (ct >> 5) + (CW / 32) * t;
         const int i = (u & 3) + 8 * (u >> 2) + 4 * (lane >> 4);
         const float *x = stg + i * PHASE_COLS;
-        v[t] = make_float4(x[0], x[1], x[2], x[3]);
+        v[t] = SG_IN(x + 4 <= reinterpret_cast<const float *>(hi_slot) + PHASE_BYTES / 4) ? make_float4(x[0], x[1], x[2], x[3])
+                                                                                       : float4{};
     }
     if constexpr (CW == 32)
         __syncwarp();
@@ -556,6 +564,7 @@ __device__ __forceinline__ void split_phased(uint8_t *hi_slot, uint8_t *lo_slot,
         const int u = (ct >> 5) + (CW / 32) * t;
         const int r = 4 * ((u & 3) + 8 * (u >> 2) + 4 * (lane >> 4)) + j;
         const int off = r * 64 + ((q ^ ((r >> 1) & 3)) << 4);
+        if (!SG_IN(off + 16 <= A_TILE)) continue;
         *reinterpret_cast<float4 *>(hi_slot + off) = v[t];
         *reinterpret_cast<float4 *>(lo_slot + off) = lo4_of_raw(v[t]);
     }
@@ -735,6 +744,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t fb = bar_full + 8 * s;
                     mbar_arrive_expect_tx(fb, tx_bytes);
                     const int kx = (k0 + kt) * BK;
+                    // TMA's innermost coordinate must be 16-byte aligned (a
+                    // skipped load leaves the slot's wait to run out)
+                    if (!SG_IN((kx & 3) == 0 && kx < p.k)) continue;
                     if (x_ph) {
                         // the four row phases of the tile's 128 rows (32 row
                         // groups from x0 / 4), PHASE_COLS columns from kx
@@ -968,7 +980,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (col < p.n) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (r + e < p.m) c[e] = Cb[(long long)(r + e) * p.ldc + col];
+                    if (r + e < p.m && SG_IN(in_matrix(Cb + (long long)(r + e) * p.ldc + col, 1, Cb, p.ldc, p.m, p.n)))
+                        c[e] = Cb[(long long)(r + e) * p.ldc + col];
             }
             return make_float4(c[0], c[1], c[2], c[3]);
         };
@@ -980,7 +993,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (col >= p.n) return;
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                if (r + e < p.m)
+                if (r + e < p.m && SG_IN(in_matrix(Cb + (long long)(r + e) * p.ldc + col, 1, Cb, p.ldc, p.m, p.n)))
                     Cb[(long long)(r + e) * p.ldc + col] = beta != 0.f ? fmaf(alpha, a[e], beta * c[e]) : alpha * a[e];
         };
         // Otherwise a thread's row holds 4 consecutive columns per quad, and
@@ -992,11 +1005,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         // chunk-wise reads both touch every bank once per 128 bytes.
         auto c_at = [&](int row, int col) -> float4 {
             const float *crow = Cb + (long long)row * p.ldc;
-            if (c_vec && col + 3 < p.n) return *reinterpret_cast<const float4 *>(crow + col);
+            if (c_vec && col + 3 < p.n)
+                return SG_IN(in_matrix(crow + col, 4, Cb, p.ldc, p.m, p.n)) ? *reinterpret_cast<const float4 *>(crow + col)
+                                                                            : float4{};
             float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                if (col + e < p.n) c[e] = crow[col + e];
+                if (col + e < p.n && SG_IN(in_matrix(crow + col + e, 1, Cb, p.ldc, p.m, p.n))) c[e] = crow[col + e];
             return make_float4(c[0], c[1], c[2], c[3]);
         };
         auto put_at = [&](int row, int col, float4 v, float4 c) {
@@ -1006,12 +1021,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                                          : make_float4(alpha * v.x, alpha * v.y, alpha * v.z, alpha * v.w);
             float *crow = Cb + (long long)row * p.ldc;
             if (c_vec && col + 3 < p.n) {
-                *reinterpret_cast<float4 *>(crow + col) = o;
+                if (SG_IN(in_matrix(crow + col, 4, Cb, p.ldc, p.m, p.n))) *reinterpret_cast<float4 *>(crow + col) = o;
             } else {
                 const float a[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (col + e < p.n) crow[col + e] = a[e];
+                    if (col + e < p.n && SG_IN(in_matrix(crow + col + e, 1, Cb, p.ldc, p.m, p.n))) crow[col + e] = a[e];
             }
         };
         // the lines of C that this thread's part of tile t covers (TRANS:
@@ -1026,7 +1041,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int row = m0 + half * COLS_PER_THREAD + lane + 32 * i;
-                    if (row < p.m) prefetch_l2(Cb + (long long)row * p.ldc + col);
+                    if (row < p.m && SG_IN(in_matrix(Cb + (long long)row * p.ldc + col, 1, Cb, p.ldc, p.m, p.n)))
+                        prefetch_l2(Cb + (long long)row * p.ldc + col);
                 }
             } else {
                 const int row = m0 + trow;
@@ -1034,7 +1050,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < COLS_PER_THREAD / 32; ++i) {
                     const int col = n0 + half * COLS_PER_THREAD + 32 * i;
-                    if (col < p.n) prefetch_l2(Cb + (long long)row * p.ldc + col);
+                    if (col < p.n && SG_IN(in_matrix(Cb + (long long)row * p.ldc + col, 1, Cb, p.ldc, p.m, p.n)))
+                        prefetch_l2(Cb + (long long)row * p.ldc + col);
                 }
             }
         };
@@ -1113,13 +1130,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr int SLOT = BM * BN / 4;   // float4s per slot
             float4 *const ws = reinterpret_cast<float4 *>(p.sk_ws);
             float4 *mine = ws + ((size_t)blockIdx.x * 2 + my_slot) * SLOT;
+            const bool ws_ok = SG_IN((int)blockIdx.x < p.sk_ctas && g_first >= 0 && g_first <= g_last &&
+                                     g_last < p.sk_ctas && t >= 0 && t < tiles);
 #pragma unroll
             for (int q = 0; q < COLS_PER_THREAD / 4; ++q)
-                mine[(half * (COLS_PER_THREAD / 4) + q) * BM + trow] =
-                    make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                if (ws_ok)
+                    mine[(half * (COLS_PER_THREAD / 4) + q) * BM + trow] =
+                        make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
             __threadfence();
             named_barrier_sync(1, ACC_THREADS);
-            if (threadIdx.x == 64) *sk_last = atomicAdd(p.sk_cnt + t, 1) == g_last - g_first;
+            if (threadIdx.x == 64) *sk_last = ws_ok && atomicAdd(p.sk_cnt + t, 1) == g_last - g_first;
             named_barrier_sync(1, ACC_THREADS);
             const bool last = *sk_last != 0;
             named_barrier_sync(1, ACC_THREADS);   // the flag is read before it is next written
@@ -1213,10 +1233,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // park the partial tile in this CTA's (now idle) stage memory,
                 // rows PART_PITCH floats apart (4 banks apart: conflict-free)
                 float *part = reinterpret_cast<float *>(smem) + trow * PART_PITCH + half * COLS_PER_THREAD;
+                const bool part_ok = SG_IN(trow * PART_PITCH + half * COLS_PER_THREAD + COLS_PER_THREAD <= BM * PART_PITCH);
 #pragma unroll
                 for (int q = 0; q < COLS_PER_THREAD / 4; ++q)
-                    reinterpret_cast<float4 *>(part)[q] =
-                        make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                    if (part_ok)
+                        reinterpret_cast<float4 *>(part)[q] =
+                            make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
             } else if (sk && nk < KT_ALL) {
                 sk_partial(tile, m0, n0);
             } else {
@@ -1257,6 +1279,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int r = TRANS ? r0 + idx % nrows : r0 + idx / (BN / 4);
             const int c4 = TRANS ? idx / nrows : idx % (BN / 4);
             off[it] = part0 + (uint32_t)(r * PART_PITCH + 4 * c4) * 4u;
+            // (an index past this thread's share is never used)
+            if (idx < total && !SG_IN(r >= 0 && r < BM && 4 * c4 + 4 <= BN)) off[it] = part0;
         }
         int flags[8];
 #pragma unroll
@@ -1300,13 +1324,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (cc < p.n) {
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            if (rr + e < p.m) c[e] = Cb[(long long)(rr + e) * p.ldc + cc];
+                            if (rr + e < p.m && SG_IN(in_matrix(Cb + (long long)(rr + e) * p.ldc + cc, 1, Cb, p.ldc, p.m, p.n)))
+                                c[e] = Cb[(long long)(rr + e) * p.ldc + cc];
                     }
                 } else {
                     const int row = cl_m0 + r, col = cl_n0 + 4 * c4;
                     if (row < p.m) {
                         const float *crow = Cb + (long long)row * p.ldc;
-                        if (c_vec && col + 3 < p.n) {
+                        if (c_vec && col + 3 < p.n && SG_IN(in_matrix(crow + col, 4, Cb, p.ldc, p.m, p.n))) {
                             const float4 c4v = *reinterpret_cast<const float4 *>(crow + col);
                             c[0] = c4v.x;
                             c[1] = c4v.y;
@@ -1315,7 +1340,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         } else {
 #pragma unroll
                             for (int e = 0; e < 4; ++e)
-                                if (col + e < p.n) c[e] = crow[col + e];
+                                if (col + e < p.n && SG_IN(in_matrix(crow + col + e, 1, Cb, p.ldc, p.m, p.n)))
+                                    c[e] = crow[col + e];
                         }
                     }
                 }
@@ -1337,18 +1363,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (cc >= p.n) continue;
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (rr + e < p.m) Cb[(long long)(rr + e) * p.ldc + cc] = o[e];
+                        if (rr + e < p.m && SG_IN(in_matrix(Cb + (long long)(rr + e) * p.ldc + cc, 1, Cb, p.ldc, p.m, p.n)))
+                            Cb[(long long)(rr + e) * p.ldc + cc] = o[e];
                     continue;
                 }
                 const int row = cl_m0 + r, col = cl_n0 + 4 * c4;
                 if (row >= p.m) continue;
                 float *crow = Cb + (long long)row * p.ldc;
                 if (c_vec && col + 3 < p.n) {
-                    *reinterpret_cast<float4 *>(crow + col) = make_float4(o[0], o[1], o[2], o[3]);
+                    if (SG_IN(in_matrix(crow + col, 4, Cb, p.ldc, p.m, p.n)))
+                        *reinterpret_cast<float4 *>(crow + col) = make_float4(o[0], o[1], o[2], o[3]);
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        if (col + e < p.n) crow[col + e] = o[e];
+                        if (col + e < p.n && SG_IN(in_matrix(crow + col + e, 1, Cb, p.ldc, p.m, p.n))) crow[col + e] = o[e];
                 }
             }
         }

@@ -77,7 +77,8 @@
  *     SGEMM_STATUS_TOO_LARGE  sgemm_tf32x3_noalloc(): the problem does not fit
  *                            its fixed scratch array;
  *     SGEMM_STATUS_BAD_PATH  sgemm_ex() asked for an unknown path;
- *     SGEMM_STATUS_UNSUPPORTED  sgemm_plan_for() was given a NULL plan;
+ *     SGEMM_STATUS_UNSUPPORTED  sgemm_plan_for() was given a NULL plan, or
+ *                            sgemm_selftest_bounds() ran in a release build;
  *     SGEMM_STATUS_CUDA_ERROR  a CUDA runtime call or launch failed; the CUDA
  *                            error code is kept per thread and returned by
  *                            sgemm_last_cuda_error().
@@ -324,14 +325,45 @@ int sgemm_plan_for(int m, int n, int k, float alpha,
  * pipeline waits are bounded, and a wait that runs out sets a non-zero code
  * (the kernel then abandons its tile instead of hanging).  Synchronises the
  * device, copies the word to *flag and, when `clear` is non-zero, resets it.
- * The first code recorded is kept: 0x201 the TMA producer waited for a free
+ * The first code recorded is kept (per group of kernels the library
+ * compiles together; the first group's non-zero code is returned): 0x201
+ * the TMA producer waited for a free
  * ring slot, 0x202 the MMA issuer for a loaded (or split) slab, 0x203 the
  * accumulator warps for a finished chunk, 0x204 a wait while draining after
  * an earlier timeout, 0x205 the MMA issuer for a free TMEM buffer, 0x206 the
  * splitter warps for a loaded slab.  Each means the result of that call is
- * not valid.  0x207 is recorded only by sgemm_selftest_wait.
+ * not valid.  0x207 is recorded only by sgemm_selftest_wait.  0x208 (checked
+ * builds only, see sgemm_bounds_line): a kernel computed an index outside the
+ * buffer it was about to access, and skipped that access.
  */
 int sgemm_device_status(int *flag, int clear);
+
+/*
+ * Checked builds.  The library can be compiled with SGEMM_GB300_CHECKED
+ * defined (the Python build makes it as a second library,
+ * libsgemm_gb300_checked_<arch>.so): every kernel then tests each global and
+ * shared-memory index it computes against the buffer it addresses (C's m x n
+ * window with row pitch ldc, each operand's rows x k or k x rows window, the
+ * split arrays, the stream-K workspace, each shared-memory region) before
+ * the access.  A failed test skips the access -- nothing outside a buffer is
+ * read or written, no kernel traps -- and records 0x208 in the device status
+ * word and the source line of the test.  The checks cost time; the release
+ * library has none of them.
+ *
+ * sgemm_bounds_line: synchronises the device and copies the source line of
+ * the first failed test to *line (0: none; always 0 in a release build);
+ * `clear` non-zero resets it and the status word (as sgemm_device_status's
+ * `clear` resets both).  Status 1: line is NULL; 100: CUDA error.
+ *
+ * sgemm_selftest_bounds: checked builds run one store whose index test is
+ * made to fail (the store is skipped), so 0x208 is recorded in the status
+ * word (unless an earlier code is kept there) and *line receives the line of
+ * the first failed test; returns 0.  A release build returns
+ * SGEMM_STATUS_UNSUPPORTED and runs nothing.  Status 1: line is NULL; 100:
+ * CUDA error.
+ */
+int sgemm_bounds_line(int *line, int clear);
+int sgemm_selftest_bounds(int *line);
 
 /*
  * Diagnostic for the failure-reporting path: runs one bounded wait on a
@@ -350,7 +382,8 @@ int sgemm_device_status(int *flag, int clear);
  */
 int sgemm_selftest_wait(unsigned long long limit_ns, int *gave_up);
 
-/* Library version string, e.g. "sgemm_gb300 0.1 (sm_103a)". */
+/* Library version string, e.g. "sgemm_gb300 0.1 (sm_103a)"; a checked build
+ * ends in ", checked)". */
 const char *sgemm_version(void);
 
 #ifdef __cplusplus

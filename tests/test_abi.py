@@ -40,6 +40,20 @@ def test_library_loads_and_exports_every_symbol():
         assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
 
 
+def test_checked_library_exports_every_symbol():
+    """The bounds-checking build (SGEMM_GB300_CHECKED) exports the same C ABI
+    and says so in its version string; the release build's bounds self-test
+    is refused (status 99) before any CUDA call."""
+    lib = _native.load(checked=True)
+    for name in header_functions():
+        assert hasattr(lib, name), name
+    assert lib.sgemm_version().endswith(b"checked)")
+    line = ctypes.c_int(-1)
+    assert _native.load().sgemm_selftest_bounds(ctypes.byref(line)) == 99
+    assert line.value == -1
+    assert not _native.load().sgemm_version().endswith(b"checked)")
+
+
 def test_version_and_status_strings():
     lib = _native.load()
     assert b"sm_103a" in lib.sgemm_version()
