@@ -56,13 +56,13 @@ void launch_cfg(int akind, int bkind, const GemmArgs &a, dim3 grid, cudaStream_t
 
 cudaError_t ffma_attrs() {
     cudaError_t e = set_attr_all<ffma::Default>();
-    if (e == cudaSuccess) e = set_attr_all<ffma::Wide>();
+    if (e == cudaSuccess) e = set_attr_all<ffma::Deep>();
     return e;
 }
 
-void ffma_launch(bool wide, int akind, int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s) {
-    if (wide)
-        launch_cfg<ffma::Wide>(akind, bkind, a, grid, s);
+void ffma_launch(bool deep, int akind, int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s) {
+    if (deep)
+        launch_cfg<ffma::Deep>(akind, bkind, a, grid, s);
     else
         launch_cfg<ffma::Default>(akind, bkind, a, grid, s);
 }

@@ -371,14 +371,16 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MIN_BLOCKS) ffma_sgemm_kern
     }
 }
 
-// The configurations the library launches: 128 x 128 tiles of 8 x 8 per
-// thread, two CTAs per SM (most problems), and 128 x 256 tiles of 8 x 16
-// per thread, one CTA per SM, for problems of many waves (6 LDS.128 per 128
-// FMA instead of 4 per 64; measured at 8192^3: 62.2 against 60.4 TFLOPS,
-// but 54.2 against 57.7 at 4096^3, where its 3.4 waves leave the last one a
-// third full at one CTA per SM).
+// The configurations the library launches, both 128 x 128 tiles at two
+// CTAs per SM: 8 x 8 per thread (256 threads) for problems of less than
+// one wave of 2 CTAs per SM, and 8 x 16 per thread (128 threads, up to 256
+// registers each) otherwise -- 6 LDS.128 per 128 FMA instead of 4 per 64,
+// and the other CTA's warps cover a CTA's barrier and slab-boundary
+// bubbles.  Measured (one GB300, interleaved): 8192^3 64.4 against 60.4
+// TFLOPS, 4096^3 60.7 against 57.7, 2048^3 (0.84 waves) 48.0 against 48.5;
+// a 128 x 256 tile of 8 x 16 at one CTA per SM ran 62.2, 54.2 and 52.8.
 using Default = Config<128, 128, 32, 3, 8, 8, 2>;
-using Wide = Config<128, 256, 32, 3, 8, 16, 1>;
+using Deep = Config<128, 128, 32, 3, 8, 16, 2>;
 
 // Operand loaders of a configuration by storage: k contiguous ->
 // ScatterLoader; rows contiguous -> DirectLoader with 16-byte (rows 16-byte

@@ -379,25 +379,25 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         return SGEMM_STATUS_OK;
     }
     pl->kernel = kKernelFfmaCpAsync;
-    // 128 x 256 tiles (one CTA per SM) for problems of at least 8 waves of
-    // them, where the last wave's idle SMs cost little; 128 x 128 (two per
-    // SM) otherwise.  SGEMM_GB300_FFMA_TILE_N (128 / 256) pins the choice.
-    const char *env_fb = std::getenv("SGEMM_GB300_FFMA_TILE_N");
-    const long long wide_tiles = (long long)((m + ffma::Wide::BM - 1) / ffma::Wide::BM) *
-                                 ((n + ffma::Wide::BN - 1) / ffma::Wide::BN) * (batch > 0 ? batch : 1);
-    const bool fwide = env_fb ? std::atoi(env_fb) == ffma::Wide::BN : wide_tiles >= 8LL * num_sms;
-    pl->bm = fwide ? ffma::Wide::BM : ffma::Default::BM;
-    pl->bn = fwide ? ffma::Wide::BN : ffma::Default::BN;
-    pl->bk = fwide ? ffma::Wide::BK : ffma::Default::BK;
-    pl->rm = fwide ? ffma::Wide::TM : ffma::Default::TM;
-    pl->rn = fwide ? ffma::Wide::TN : ffma::Default::TN;
-    pl->threads = fwide ? ffma::Wide::THREADS : ffma::Default::THREADS;
-    pl->stages = fwide ? ffma::Wide::STAGES : ffma::Default::STAGES;
+    // 8 x 16 outputs per thread (128 threads) from one wave of two CTAs per
+    // SM on, 8 x 8 (256 threads) below it, where more threads per tile
+    // pay; both 128 x 128 tiles.  SGEMM_GB300_FFMA_RN (8 / 16) pins it.
+    const char *env_rn = std::getenv("SGEMM_GB300_FFMA_RN");
+    const long long ftiles = (long long)((m + ffma::Deep::BM - 1) / ffma::Deep::BM) *
+                             ((n + ffma::Deep::BN - 1) / ffma::Deep::BN) * (batch > 0 ? batch : 1);
+    const bool fdeep = env_rn ? std::atoi(env_rn) == ffma::Deep::TN : ftiles >= 2LL * num_sms;
+    pl->bm = fdeep ? ffma::Deep::BM : ffma::Default::BM;
+    pl->bn = fdeep ? ffma::Deep::BN : ffma::Default::BN;
+    pl->bk = fdeep ? ffma::Deep::BK : ffma::Default::BK;
+    pl->rm = fdeep ? ffma::Deep::TM : ffma::Default::TM;
+    pl->rn = fdeep ? ffma::Deep::TN : ffma::Default::TN;
+    pl->threads = fdeep ? ffma::Deep::THREADS : ffma::Default::THREADS;
+    pl->stages = fdeep ? ffma::Deep::STAGES : ffma::Default::STAGES;
     // rows-contiguous operands take 16-byte copies when their rows are 16-byte aligned
     pl->a_vec = op_a == SGEMM_OP_T && aligned(A, 16) && (lda % 4) == 0;
     pl->b_vec = op_b == SGEMM_OP_N && aligned(B, 16) && (ldb % 4) == 0;
     const int akind = op_a == SGEMM_OP_N ? 0 : (pl->a_vec ? 1 : 2), bkind = op_b == SGEMM_OP_T ? 0 : (pl->b_vec ? 1 : 2);
-    pl->smem_bytes = fwide ? ffma::smem_bytes<ffma::Wide>(akind, bkind) : ffma::smem_bytes<ffma::Default>(akind, bkind);
+    pl->smem_bytes = fdeep ? ffma::smem_bytes<ffma::Deep>(akind, bkind) : ffma::smem_bytes<ffma::Default>(akind, bkind);
     const int tiles_m = (m + pl->bm - 1) / pl->bm;
     const int tiles_n = (n + pl->bn - 1) / pl->bn;
     pl->tiles = tiles_m * tiles_n;
@@ -803,7 +803,7 @@ int noalloc_scratch(float **out) {
 void launch_ffma(const sgemm_plan &pl, const GemmArgs &a, int batch, cudaStream_t s) {
     const int akind = pl.op_a == SGEMM_OP_N ? 0 : (pl.a_vec ? 1 : 2);
     const int bkind = pl.op_b == SGEMM_OP_T ? 0 : (pl.b_vec ? 1 : 2);
-    units::ffma_launch(pl.bn == ffma::Wide::BN, akind, bkind, a, dim3((unsigned)pl.grid, (unsigned)batch, 1), s);
+    units::ffma_launch(pl.rn == ffma::Deep::TN, akind, bkind, a, dim3((unsigned)pl.grid, (unsigned)batch, 1), s);
 }
 
 // Status code of the bounded-wait self-test (sgemm_selftest_wait).

@@ -30,10 +30,11 @@ SG_TC_UNIT_DECL(trans)
 SG_TC_UNIT_DECL(pair)
 #undef SG_TC_UNIT_DECL
 
-// The FFMA unit: both tile configurations, every loader combination
-// (akind, bkind: 0 scatter, 1 direct 16-byte, 2 direct 4-byte).
+// The FFMA unit: both configurations (deep: 8 x 16 per thread), every
+// loader combination (akind, bkind: 0 scatter, 1 direct 16-byte, 2 direct
+// 4-byte).
 cudaError_t ffma_attrs();
-void ffma_launch(bool wide, int akind, int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s);
+void ffma_launch(bool deep, int akind, int bkind, const GemmArgs &a, dim3 grid, cudaStream_t s);
 cudaError_t ffma_status(int *status, int *line, bool clear);
 
 }  // namespace units

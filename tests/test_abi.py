@@ -118,10 +118,10 @@ def test_plan_matches_blocking_model():
 
 
 def test_ffma_tile_choice(monkeypatch):
-    """The FFMA path takes 128 x 256 tiles (8 x 16 per thread, 256 threads)
-    for at least 8 waves of them on the device's SMs, 128 x 128 (8 x 8)
-    otherwise; SGEMM_GB300_FFMA_TILE_N pins it."""
-    monkeypatch.delenv("SGEMM_GB300_FFMA_TILE_N", raising=False)
+    """The FFMA path runs 128 x 128 tiles at two CTAs per SM: 8 x 16 outputs
+    per thread (128 threads) from one wave of them on the device's SMs, 8 x 8
+    (256 threads) below it; SGEMM_GB300_FFMA_RN pins the per-thread tile."""
+    monkeypatch.delenv("SGEMM_GB300_FFMA_RN", raising=False)
     F = binding.PATH_FFMA
 
     def tile(m, n, k):
@@ -129,13 +129,13 @@ def test_ffma_tile_choice(monkeypatch):
         assert st == 0
         return p["bm"], p["bn"], p["rm"], p["rn"], p["threads"]
 
-    assert tile(8192, 8192, 8192) == (128, 256, 8, 16, 256)   # 2048 tiles = 13.5 waves
-    assert tile(4096, 4096, 4096) == (128, 128, 8, 8, 256)     # 512 tiles = 3.4 waves
-    assert tile(6144, 6144, 64) == (128, 128, 8, 8, 256)       # 1152 tiles < 8 x 152 = 1216
-    assert tile(6400, 6400, 64) == (128, 256, 8, 16, 256)      # 1250 tiles
-    monkeypatch.setenv("SGEMM_GB300_FFMA_TILE_N", "256")
-    assert tile(64, 64, 64) == (128, 256, 8, 16, 256)
-    monkeypatch.setenv("SGEMM_GB300_FFMA_TILE_N", "128")
+    assert tile(8192, 8192, 8192) == (128, 128, 8, 16, 128)   # 4096 tiles
+    assert tile(2432, 2048, 64) == (128, 128, 8, 16, 128)     # 19 x 16 = 304 tiles = 2 x 152
+    assert tile(2048, 2048, 2048) == (128, 128, 8, 8, 256)    # 256 tiles
+    assert tile(64, 64, 64) == (128, 128, 8, 8, 256)
+    monkeypatch.setenv("SGEMM_GB300_FFMA_RN", "16")
+    assert tile(64, 64, 64) == (128, 128, 8, 16, 128)
+    monkeypatch.setenv("SGEMM_GB300_FFMA_RN", "8")
     assert tile(8192, 8192, 8192) == (128, 128, 8, 8, 256)
 
 

@@ -48,7 +48,7 @@ def bounds_line(lib, clear=False):
 @pytest.fixture(autouse=True)
 def _no_failed_test(checked_lib, monkeypatch):
     for v in ("SGEMM_GB300_STREAM_K", "SGEMM_GB300_PAIR", "SGEMM_GB300_SPLIT_K", "SGEMM_GB300_TILE_N",
-              "SGEMM_GB300_TRANS", "SGEMM_GB300_SPLIT_A_IN", "SGEMM_GB300_SPLIT_B_IN", "SGEMM_GB300_FFMA_TILE_N"):
+              "SGEMM_GB300_TRANS", "SGEMM_GB300_SPLIT_A_IN", "SGEMM_GB300_SPLIT_B_IN", "SGEMM_GB300_FFMA_RN"):
         monkeypatch.delenv(v, raising=False)
     binding.device_status(clear=True)
     yield
@@ -94,8 +94,8 @@ def test_pinned_plans_pass_every_bounds_test(monkeypatch, env, m, n, k):
     run_and_check(p, TC)
 
 
-def test_ffma_wide_tile(monkeypatch):
-    monkeypatch.setenv("SGEMM_GB300_FFMA_TILE_N", "256")
+def test_ffma_8x16(monkeypatch):
+    monkeypatch.setenv("SGEMM_GB300_FFMA_RN", "16")
     p = inputs.make_problem(300, 600, 70, alpha=1.0, beta=-1.0, seed=31, a="uniform", b="normal", c="normal")
     run_and_check(p, FFMA)
 

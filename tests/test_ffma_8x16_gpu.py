@@ -1,10 +1,10 @@
-"""GPU parity of the FFMA path's 128 x 256 tile (8 x 16 outputs per thread,
-one CTA per SM), which the library takes for problems of at least 8 waves
-of such tiles and which SGEMM_GB300_FFMA_TILE_N=256 pins here on small
-shapes: ragged edges, padded and misaligned operands, transposed operands,
-strided batches and integer twins against the FP64 oracle; and, because
-both FFMA tiles sum every output in increasing k with one fmaf per
-product, bit-identical results to the 128 x 128 tile on the same inputs."""
+"""GPU parity of the FFMA path's 8 x 16 outputs per thread (128-thread CTAs
+of 128 x 128 tiles, two per SM), which the library takes from one wave of
+such CTAs on and which SGEMM_GB300_FFMA_RN=16 pins here on small shapes:
+ragged edges, padded and misaligned operands, transposed operands, strided
+batches and integer twins against the FP64 oracle; and, because both FFMA
+configurations sum every output in increasing k with one fmaf per product,
+bit-identical results to the 8 x 8 configuration on the same inputs."""
 import numpy as np
 import pytest
 import torch
@@ -19,15 +19,15 @@ FFMA = binding.PATH_FFMA
 
 
 @pytest.fixture(autouse=True)
-def _wide(monkeypatch):
+def _deep(monkeypatch):
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
-    monkeypatch.setenv("SGEMM_GB300_FFMA_TILE_N", "256")
+    monkeypatch.setenv("SGEMM_GB300_FFMA_RN", "16")
 
 
-def test_pinned_plan_is_the_wide_tile():
+def test_pinned_plan_is_8x16():
     st, p = binding.plan(300, 500, 70, path=FFMA)
-    assert st == 0 and (p["bm"], p["bn"], p["rm"], p["rn"], p["threads"]) == (128, 256, 8, 16, 256)
-    assert p["tiles"] == 3 * 2 and p["grid"] == 6
+    assert st == 0 and (p["bm"], p["bn"], p["rm"], p["rn"], p["threads"]) == (128, 128, 8, 16, 128)
+    assert p["tiles"] == 3 * 4 and p["grid"] == 12
 
 
 @pytest.mark.parametrize("m,n,k", [
@@ -97,12 +97,12 @@ def test_strided_batch():
 
 
 @pytest.mark.parametrize("m,n,k", [(1000, 1500, 777), (384, 1024, 2048)])
-def test_same_bits_as_the_narrow_tile(monkeypatch, m, n, k):
+def test_same_bits_as_8x8(monkeypatch, m, n, k):
     p = inputs.make_problem(m, n, k, alpha=1.5, beta=0.5, seed=k, a="normal", b="uniform", c="uniform")
     A, B = torch.from_numpy(p.A).cuda(), torch.from_numpy(p.B).cuda()
     outs = []
-    for tile in ("256", "128"):
-        monkeypatch.setenv("SGEMM_GB300_FFMA_TILE_N", tile)
+    for rn in ("16", "8"):
+        monkeypatch.setenv("SGEMM_GB300_FFMA_RN", rn)
         C = torch.from_numpy(p.C0).cuda()
         st = binding.sgemm_raw(p.m, p.n, p.k, p.alpha, A.data_ptr(), p.lda, B.data_ptr(), p.ldb, p.beta, C.data_ptr(),
                                p.ldc, torch.cuda.current_stream().cuda_stream, FFMA)
