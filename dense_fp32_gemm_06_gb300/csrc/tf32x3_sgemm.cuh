@@ -1145,6 +1145,16 @@ __global__ void __launch_bounds__(THREADS, 1)
             named_barrier_sync(1, ACC_THREADS);   // the flag is read before it is next written
             if (!last) return;
             __threadfence();
+            // the other contributors' partials were written long before
+            // (their runs reach this tile first) and have mostly left L2:
+            // bring them back in bulk while the first block's loads start
+            if (threadIdx.x == 64) {
+                for (int g = g_first; g < g_last; ++g) {
+                    const float4 *src = g == g_first ? ws + ((size_t)g_first * 2 + first_slot) * SLOT
+                                                     : ws + (size_t)g * 2 * SLOT;
+                    bulk_prefetch_l2(src, SLOT * 16u);
+                }
+            }
             // blocks of QB quads: each contributor's QB loads are in flight
             // together (one L2 round trip per block and contributor)
             constexpr int QB = 8;   // = one 32-column block of store_block32
