@@ -155,6 +155,7 @@ bool phase_readable(long long outer, long long ld, int batch, long long stride) 
 void set_pair_plan(int m, int n, int k, sgemm_plan *pl) {
     pl->pair = 1;
     pl->trans = 0;
+    pl->persistent = 0;
     pl->bm = pl->bn = tf32x3::Pair::BN;
     pl->split_k = 1;
     pl->stream_k = 0;
@@ -374,6 +375,18 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         const int tiles_n = (n + pl->bn - 1) / pl->bn;
         pl->tiles = tiles_mt * tiles_n;
         pl->grid = best_sk ? num_sms : pl->tiles * pl->split_k;
+        // whole tiles of more than one wave: one persistent CTA per SM takes
+        // tiles g, g + sms, ... in turn, a tile's epilogue overlapping the
+        // next one's first chunks (measured, whole call, L2 flushed:
+        // 8192^3 3.83 against 3.89 ms, 8192 x 8192 x 4096 1.91 against
+        // 1.99, 16384 x 4096 x 4096 1.89 against 1.96).
+        // SGEMM_GB300_PERSIST (0 / 1) pins it.
+        const char *env_ps = std::getenv("SGEMM_GB300_PERSIST");
+        const int force_ps = env_ps && (env_ps[0] == '0' || env_ps[0] == '1') ? env_ps[0] - '0' : -1;
+        if (!best_sk && best_s == 1 && batch == 1 && pl->tiles > num_sms && force_ps != 0) {
+            pl->persistent = 1;
+            pl->grid = num_sms;
+        }
         pl->k_tiles = (int)KT;
         pl->group_m = tiles_mt < 8 ? tiles_mt : 8;
         return SGEMM_STATUS_OK;
@@ -612,7 +625,8 @@ int prepare_gemm(int m, int n, int k, float alpha, const Operand &a, const Opera
     p.x_src = x.phased ? tf32x3::kPhased : x.raw ? tf32x3::kRaw : tf32x3::kPreSplit;
     p.y_src = y.raw ? tf32x3::kRaw : tf32x3::kPreSplit;
     p.c_vec = pl.c_vec;
-    p.sk_ctas = pl.stream_k;
+    // stream-K over stream_k CTAs, or persistent whole tiles over grid CTAs
+    p.sk_ctas = pl.stream_k > 0 ? pl.stream_k : (pl.persistent ? -pl.grid : 0);
     p.sk_ws = sk_ws;
     p.sk_cnt = sk_cnt;
     return SGEMM_STATUS_OK;

@@ -172,6 +172,9 @@ struct Params {
     // starts in, slot 1 for the one it ends in) and counts itself in
     // sk_cnt[tile] (zeroed before the launch); the last of a tile's CTAs
     // adds all partials in k order and writes the tile.
+    // sk_ctas < 0: persistent whole tiles -- G = -sk_ctas CTAs, CTA g takes
+    // tiles g, g + G, g + 2G, ... (a tile's epilogue overlaps the next
+    // tile's first chunks: the TMEM buffers alternate across tiles).
     int sk_ctas;
     float *sk_ws;
     int *sk_cnt;
@@ -191,14 +194,17 @@ static_assert(sizeof(Params) <= 128, "kernel parameter block");
 __device__ __forceinline__ bool cta_segment(int sk_ctas, int kt_all, int tiles, uint32_t nsplit, uint32_t rank,
                                             int si, int &tile, int &k0, int &nk, int ctas_per_tile) {
     long long it0, it1;
-    if (sk_ctas > 0) {
-        const int whole = tiles / sk_ctas;
+    if (sk_ctas != 0) {
+        // rounds of whole tiles (all of them when persistent)
+        const int G = sk_ctas < 0 ? -sk_ctas : sk_ctas;
+        const int whole = sk_ctas < 0 ? (tiles + G - 1) / G : tiles / G;
         if (si < whole) {
-            tile = (int)blockIdx.x + si * sk_ctas;
+            tile = (int)blockIdx.x + si * G;
             k0 = 0;
             nk = kt_all;
-            return true;
+            return tile < tiles;
         }
+        if (sk_ctas < 0) return false;
         si -= whole;
         const long long base = (long long)whole * sk_ctas * kt_all;
         const long long T = (long long)(tiles - whole * sk_ctas) * kt_all;

@@ -313,6 +313,7 @@ typedef struct sgemm_plan {
                        /*      of all tiles' k slabs, partial tiles meet in a workspace        */
     int b_in_kernel;   /* 1: the same for B (no split pass, no scratch for that operand)       */
     int pair;          /* 1: CTA pairs (cta_group::2) compute 256 x 256 tiles, 2 CTAs per tile */
+    int persistent;    /* 1: grid CTAs take whole tiles g, g + grid, ... in turn (more than a wave) */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

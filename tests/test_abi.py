@@ -210,8 +210,37 @@ def test_auto_policy():
     st, p = hplan(2048, 2048, 2048, path=binding.PATH_TF32X3)     # CTA pairs: 8 x 8 tiles of 256 x 256
     assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"], p["pair"]) == (256, 256, 16, 384, 1)
     assert p["tiles"] == 8 * 8 and p["grid"] == 2 * p["tiles"] and p["k_tiles"] == 128 and p["stream_k"] == 0
-    st, p = hplan(8192, 8192, 8192, path=binding.PATH_TF32X3)     # many waves: single CTAs
-    assert st == 0 and (p["bm"], p["bn"], p["pair"]) == (128, 256, 0) and p["grid"] == p["tiles"] == 64 * 32
+    st, p = hplan(8192, 8192, 8192, path=binding.PATH_TF32X3)     # many waves: persistent single CTAs
+    assert st == 0 and (p["bm"], p["bn"], p["pair"]) == (128, 256, 0) and p["tiles"] == 64 * 32
+    assert p["persistent"] == 1 and p["grid"] == 152 and p["stream_k"] == 0
+
+
+def test_persistent_policy(monkeypatch):
+    """Whole tiles of more than one wave run on one persistent CTA per SM
+    (tiles g, g + 152, ...); not for split-K, stream-K, CTA pairs or
+    batches, nor within one wave; SGEMM_GB300_PERSIST pins it off."""
+    for v in ("SGEMM_GB300_PERSIST", "SGEMM_GB300_STREAM_K", "SGEMM_GB300_PAIR"):
+        monkeypatch.delenv(v, raising=False)
+    TC = binding.PATH_TF32X3
+
+    def plan(m, n, k):
+        st, p = hplan(m, n, k, path=TC)
+        assert st == 0
+        return p
+
+    p = plan(8192, 8192, 4096)
+    assert p["persistent"] == 1 and p["grid"] == 152 and p["tiles"] == 2048
+    p = plan(2176, 2304, 512)                  # 17 x 9 = 153 tiles: one more than a wave
+    assert (p["tiles"], p["persistent"], p["grid"]) == (153, 1, 152)
+    monkeypatch.setenv("SGEMM_GB300_PAIR", "0")
+    p = plan(2048, 2304, 512)                  # 16 x 9 = 144 tiles: one wave
+    assert p["tiles"] == 144 and p["persistent"] == 0 and p["grid"] == p["tiles"] * p["split_k"]
+    monkeypatch.delenv("SGEMM_GB300_PAIR")
+    assert plan(4096, 4096, 4096)["persistent"] == 0          # stream-K
+    assert plan(2048, 2048, 2048)["persistent"] == 0          # CTA pairs
+    monkeypatch.setenv("SGEMM_GB300_PERSIST", "0")
+    p = plan(8192, 8192, 8192)
+    assert p["persistent"] == 0 and p["grid"] == p["tiles"] == 2048
 
 
 def test_stream_k_policy(monkeypatch):
@@ -229,14 +258,15 @@ def test_stream_k_policy(monkeypatch):
     # 8192^3: 13.47 waves, 3.8 % of the last one idle; 2048^3: the estimate ties
     for shape in [(8192, 8192, 8192), (2048, 2048, 2048), (3072, 3072, 3072)]:
         st, p = hplan(*shape, path=TC)
-        assert p["stream_k"] == 0 and p["grid"] == p["tiles"] * p["split_k"] * (2 if p["pair"] else 1), (shape, p)
+        expect = 152 if p["persistent"] else p["tiles"] * p["split_k"] * (2 if p["pair"] else 1)
+        assert p["stream_k"] == 0 and p["grid"] == expect, (shape, p)
     st, p = hplan(256, 256, 8192, path=TC)          # 2 tiles: a split-K cluster instead
     assert p["stream_k"] == 0 and p["split_k"] > 1
     st, p = hplan(4096, 4096, 4096, path=TC, num_sms=64)
-    assert p["stream_k"] == 0 and p["grid"] == 512         # 8 full waves of 64
+    assert p["stream_k"] == 0 and p["tiles"] == 512 and p["grid"] == 64   # 8 full waves of 64: persistent
     monkeypatch.setenv("SGEMM_GB300_STREAM_K", "0")
     st, p = hplan(4096, 4096, 4096, path=TC)
-    assert p["stream_k"] == 0 and p["grid"] == p["tiles"] * p["split_k"]
+    assert p["stream_k"] == 0 and p["persistent"] == 1 and p["grid"] == 152
     monkeypatch.setenv("SGEMM_GB300_STREAM_K", "1")
     for shape in [(256, 256, 8192), (2048, 2048, 2048)]:    # pinned: taken whenever allowed
         st, p = hplan(*shape, path=TC)
@@ -377,5 +407,5 @@ def test_split_k_policy_small_and_large_shapes():
     for (m, n, k), s in expect.items():
         st, p = hplan(m, n, k, lda=k, path=TC, num_sms=152)
         assert st == 0 and p["split_k"] == s and p["stream_k"] == 0, ((m, n, k), p)
-        assert p["grid"] == p["tiles"] * s * (2 if p["pair"] else 1)
+        assert p["grid"] == (152 if p["persistent"] else p["tiles"] * s * (2 if p["pair"] else 1))
         assert p["k_tiles"] // p["split_k"] >= 4 or s == 1

@@ -41,7 +41,7 @@ def _ceil(a, b):
 
 def test_plan_invariants_over_random_problems(monkeypatch):
     rng = np.random.default_rng(20261202)
-    seen = {"ffma": 0, "tc": 0, "pair": 0, "trans": 0, "sk": 0, "split": 0, "phased": 0}
+    seen = {"ffma": 0, "tc": 0, "pair": 0, "trans": 0, "sk": 0, "split": 0, "phased": 0, "persistent": 0}
     for i in range(3600):
         # the last 600 with CTA pairs requested (the default takes them only
         # for one wave of 256 x 256 tiles)
@@ -72,6 +72,7 @@ def test_plan_invariants_over_random_problems(monkeypatch):
         if p["pair"]:
             seen["pair"] += 1
             assert (p["bm"], p["bn"]) == (256, 256) and p["split_k"] == 1 and p["stream_k"] == 0, where
+            assert not p["persistent"], where
             assert p["grid"] == 2 * p["tiles"] == 2 * _ceil(m, 256) * _ceil(n, 256), where
             continue
         if p["trans"]:
@@ -83,9 +84,12 @@ def test_plan_invariants_over_random_problems(monkeypatch):
         assert 1 <= p["split_k"] <= 8, where
         if p["stream_k"]:
             seen["sk"] += 1
-            assert p["split_k"] == 1 and p["grid"] == p["stream_k"] == SMS, where
+            assert p["split_k"] == 1 and p["grid"] == p["stream_k"] == SMS and not p["persistent"], where
+        elif p["persistent"]:
+            seen["persistent"] += 1
+            assert p["split_k"] == 1 and p["grid"] == SMS < p["tiles"], where
         else:
-            assert p["grid"] == p["tiles"] * p["split_k"], where
+            assert p["grid"] == p["tiles"] * p["split_k"] and p["tiles"] * p["split_k"] <= SMS or p["split_k"] == 1, where
         if p["split_k"] > 1:
             seen["split"] += 1
             assert p["k_tiles"] // p["split_k"] >= 4, where
