@@ -293,15 +293,16 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
             }
             // stream-K: W = tiles / G full waves of whole tiles, then the R
             // remaining tiles' slabs shared out evenly (every CTA must get at
-            // least one slab of them: R x KT >= G).  Measured: the fix-up of a
-            // shared tile costs ~10 us, twice when a CTA's share is shorter
-            // than a tile (it then holds parts of two), and stream-K only
-            // pays when whole tiles would leave >= 10 % of the last wave's SMs
-            // idle (4096^3: 17 % faster; 8192^3, 3.8 % idle: 4 % slower).
+            // least one slab of them: R x KT >= G, and a shared tile meets a
+            // few CTAs only: 4 R >= G).  Measured: the fix-up of a shared tile
+            // costs ~10 us, twice when a CTA's share is shorter than a tile
+            // (it then holds parts of two).  Against persistent whole tiles
+            // (interleaved, whole calls): 4096^3 17 % faster, 8192 x 8192 x
+            // 4096 1.88 against 1.94 ms, 6144^3 1.71 against 1.76, 12288 x
+            // 8192 x 4096 2.87 against 2.96, 8192^3 3.80 against 3.82.
             const long long W = tiles / num_sms, R = tiles - W * num_sms;
-            const bool idle_tail = 10 * (num_sms - R) >= (W + 1) * num_sms;
             if (allow_sk && force_sk != 0 && batch == 1 && !(force_s >= 1 && force_s <= 8) && R > 0 &&
-                R * KT >= num_sms && ((4 * R >= num_sms && idle_tail) || force_sk == 1)) {
+                R * KT >= num_sms && (4 * R >= num_sms || force_sk == 1)) {
                 const long long share = (R * KT + num_sms - 1) / num_sms;
                 consider(W * KT * slab + share * slab + (share < KT ? 640 : 320), bn, 1, tr, true);
             }

@@ -210,9 +210,9 @@ def test_auto_policy():
     st, p = hplan(2048, 2048, 2048, path=binding.PATH_TF32X3)     # CTA pairs: 8 x 8 tiles of 256 x 256
     assert st == 0 and (p["bm"], p["bn"], p["bk"], p["threads"], p["pair"]) == (256, 256, 16, 384, 1)
     assert p["tiles"] == 8 * 8 and p["grid"] == 2 * p["tiles"] and p["k_tiles"] == 128 and p["stream_k"] == 0
-    st, p = hplan(8192, 8192, 8192, path=binding.PATH_TF32X3)     # many waves: persistent single CTAs
+    st, p = hplan(8192, 8192, 8192, path=binding.PATH_TF32X3)     # many waves: single CTAs, stream-K
     assert st == 0 and (p["bm"], p["bn"], p["pair"]) == (128, 256, 0) and p["tiles"] == 64 * 32
-    assert p["persistent"] == 1 and p["grid"] == 152 and p["stream_k"] == 0
+    assert p["stream_k"] == 152 and p["grid"] == 152 and p["persistent"] == 0
 
 
 def test_persistent_policy(monkeypatch):
@@ -228,8 +228,10 @@ def test_persistent_policy(monkeypatch):
         assert st == 0
         return p
 
-    p = plan(8192, 8192, 4096)
-    assert p["persistent"] == 1 and p["grid"] == 152 and p["tiles"] == 2048
+    p = plan(8192, 4864, 4096)                 # 64 x 19 = 1216 tiles = 8 waves exactly
+    assert p["persistent"] == 1 and p["grid"] == 152 and p["tiles"] == 1216 and p["stream_k"] == 0
+    p = plan(3000, 2600, 300)                  # 264 tiles: stream-K's fix-up would cost more
+    assert p["persistent"] == 1 and p["stream_k"] == 0
     p = plan(2176, 2304, 512)                  # 17 x 9 = 153 tiles: one more than a wave
     assert (p["tiles"], p["persistent"], p["grid"]) == (153, 1, 152)
     monkeypatch.setenv("SGEMM_GB300_PAIR", "0")
@@ -239,8 +241,8 @@ def test_persistent_policy(monkeypatch):
     assert plan(4096, 4096, 4096)["persistent"] == 0          # stream-K
     assert plan(2048, 2048, 2048)["persistent"] == 0          # CTA pairs
     monkeypatch.setenv("SGEMM_GB300_PERSIST", "0")
-    p = plan(8192, 8192, 8192)
-    assert p["persistent"] == 0 and p["grid"] == p["tiles"] == 2048
+    p = plan(8192, 4864, 4096)
+    assert p["persistent"] == 0 and p["grid"] == p["tiles"] == 1216
 
 
 def test_stream_k_policy(monkeypatch):
@@ -252,11 +254,11 @@ def test_stream_k_policy(monkeypatch):
     for v in ("SGEMM_GB300_STREAM_K", "SGEMM_GB300_TRANS", "SGEMM_GB300_TILE_N", "SGEMM_GB300_SPLIT_K"):
         monkeypatch.delenv(v, raising=False)
     TC = binding.PATH_TF32X3
-    for shape in [(4096, 4096, 4096), (8192, 2048, 8192), (16384, 128, 8192), (65536, 64, 4096)]:
+    for shape in [(4096, 4096, 4096), (8192, 2048, 8192), (16384, 128, 8192), (65536, 64, 4096), (8192, 8192, 8192)]:
         st, p = hplan(*shape, path=TC)
         assert st == 0 and p["stream_k"] == 152 and p["grid"] == 152 and p["split_k"] == 1, (shape, p)
-    # 8192^3: 13.47 waves, 3.8 % of the last one idle; 2048^3: the estimate ties
-    for shape in [(8192, 8192, 8192), (2048, 2048, 2048), (3072, 3072, 3072)]:
+    # 2048^3: CTA pairs; 3072^3: the estimate ties; 8192 x 4864: whole waves
+    for shape in [(2048, 2048, 2048), (3072, 3072, 3072), (8192, 4864, 4096)]:
         st, p = hplan(*shape, path=TC)
         expect = 152 if p["persistent"] else p["tiles"] * p["split_k"] * (2 if p["pair"] else 1)
         assert p["stream_k"] == 0 and p["grid"] == expect, (shape, p)
@@ -406,6 +408,6 @@ def test_split_k_policy_small_and_large_shapes():
               (128, 128, 128): 1, (2048, 2048, 2048): 1, (8192, 8192, 8192): 1}
     for (m, n, k), s in expect.items():
         st, p = hplan(m, n, k, lda=k, path=TC, num_sms=152)
-        assert st == 0 and p["split_k"] == s and p["stream_k"] == 0, ((m, n, k), p)
-        assert p["grid"] == (152 if p["persistent"] else p["tiles"] * s * (2 if p["pair"] else 1))
+        assert st == 0 and p["split_k"] == s, ((m, n, k), p)
+        assert p["grid"] == (152 if p["persistent"] or p["stream_k"] else p["tiles"] * s * (2 if p["pair"] else 1))
         assert p["k_tiles"] // p["split_k"] >= 4 or s == 1
