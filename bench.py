@@ -448,12 +448,16 @@ def device_time_ms(fn, stream, reps, flush=None):
     """Device time of one fn() launch sequence (ms): reps x (flush, fn)
     enqueued back to back minus reps x flush alone, each bracketed by CUDA
     events on `stream`.  For kernels shorter than the host's cost of a call,
-    where per-launch events would also count the GPU waiting for the host."""
+    where per-launch events would also count the GPU waiting for the host:
+    a device-side sleep (a few ms) runs first, so that every launch is
+    queued before the first event and the launches then run back to back."""
     import torch
 
     def run(with_fn):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(4_000_000 + 200_000 * reps)   # clock cycles
         a.record(stream)
         for _ in range(reps):
             if flush is not None:
