@@ -120,7 +120,7 @@ class Plan(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int) for name in (
         "path", "kernel", "bm", "bn", "bk", "rm", "rn", "threads", "stages", "grid", "tiles",
         "k_tiles", "smem_bytes", "b_vec", "c_vec", "group_m", "split_k", "op_a", "op_b", "a_vec",
-        "a_in_kernel", "trans", "stream_k", "b_in_kernel", "pair", "persistent")]
+        "a_in_kernel", "trans", "stream_k", "b_in_kernel", "pair", "persistent", "sk_parts")]
 
 
 def _declare(lib):

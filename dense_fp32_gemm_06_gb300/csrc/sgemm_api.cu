@@ -159,6 +159,7 @@ void set_pair_plan(int m, int n, int k, sgemm_plan *pl) {
     pl->bm = pl->bn = tf32x3::Pair::BN;
     pl->split_k = 1;
     pl->stream_k = 0;
+    pl->sk_parts = 0;
     pl->stages = tf32x3::Pair::STAGES;
     pl->smem_bytes = tf32x3::Pair::SMEM_BYTES;
     const int tm = (m + pl->bm - 1) / pl->bm, tn = (n + pl->bn - 1) / pl->bn;
@@ -387,6 +388,21 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
         if (!best_sk && best_s == 1 && batch == 1 && pl->tiles > num_sms && force_ps != 0) {
             pl->persistent = 1;
             pl->grid = num_sms;
+        }
+        // stream-K after at least two full waves, with S = sms / R >= 2 for
+        // the R remaining tiles: each of those is cut into S equal k parts
+        // (CTA i S + j takes part j of remaining tile i) rather than the
+        // slab sequence into equal runs, so that CTAs on one tile row
+        // (column) read the same k range of its A (B) panel at once and
+        // share it in L2 -- equal runs start at unrelated k offsets, and that
+        // tail then streams every panel from DRAM.
+        // SGEMM_GB300_SK_PARTS (0 / 1) pins it.
+        if (best_sk) {
+            const char *env_sp = std::getenv("SGEMM_GB300_SK_PARTS");
+            const long long W = pl->tiles / num_sms, R = pl->tiles - W * num_sms;
+            const int S = R > 0 ? (int)(num_sms / R) : 0;
+            const bool parts = env_sp && (env_sp[0] == '0' || env_sp[0] == '1') ? env_sp[0] == '1' : W >= 2;
+            if (parts && S >= 2 && KT >= S) pl->sk_parts = S;
         }
         pl->k_tiles = (int)KT;
         pl->group_m = tiles_mt < 8 ? tiles_mt : 8;
@@ -628,6 +644,7 @@ int prepare_gemm(int m, int n, int k, float alpha, const Operand &a, const Opera
     p.c_vec = pl.c_vec;
     // stream-K over stream_k CTAs, or persistent whole tiles over grid CTAs
     p.sk_ctas = pl.stream_k > 0 ? pl.stream_k : (pl.persistent ? -pl.grid : 0);
+    p.sk_parts = pl.stream_k > 0 ? pl.sk_parts : 0;
     p.sk_ws = sk_ws;
     p.sk_cnt = sk_cnt;
     return SGEMM_STATUS_OK;

@@ -175,7 +175,12 @@ struct Params {
     // sk_ctas < 0: persistent whole tiles -- G = -sk_ctas CTAs, CTA g takes
     // tiles g, g + G, g + 2G, ... (a tile's epilogue overlaps the next
     // tile's first chunks: the TMEM buffers alternate across tiles).
+    // sk_parts >= 2 (stream-K, R S <= G): the R remaining tiles are cut
+    // into S equal k ranges instead, part j of tile W G + i going to CTA
+    // i S + j, so that the CTAs of a tile row (column) read the same k
+    // range of its A (B) panel at the same time and share it in L2.
     int sk_ctas;
+    int sk_parts;
     float *sk_ws;
     int *sk_cnt;
 };
@@ -192,7 +197,7 @@ static_assert(sizeof(Params) <= 128, "kernel parameter block");
 // slabs (possibly empty), or all of them.  Recomputed on demand so that no
 // role keeps iteration state next to its accumulators.
 __device__ __forceinline__ bool cta_segment(int sk_ctas, int kt_all, int tiles, uint32_t nsplit, uint32_t rank,
-                                            int si, int &tile, int &k0, int &nk, int ctas_per_tile) {
+                                            int si, int &tile, int &k0, int &nk, int ctas_per_tile, int sk_parts) {
     long long it0, it1;
     if (sk_ctas != 0) {
         // rounds of whole tiles (all of them when persistent)
@@ -206,6 +211,16 @@ __device__ __forceinline__ bool cta_segment(int sk_ctas, int kt_all, int tiles, 
         }
         if (sk_ctas < 0) return false;
         si -= whole;
+        if (sk_parts >= 2) {
+            // one k part of one remaining tile per CTA
+            const int g = (int)blockIdx.x, first = whole * sk_ctas;
+            if (si != 0 || g >= (tiles - first) * sk_parts) return false;
+            tile = first + g / sk_parts;
+            const int j = g % sk_parts;
+            k0 = (int)((long long)kt_all * j / sk_parts);
+            nk = (int)((long long)kt_all * (j + 1) / sk_parts) - k0;
+            return nk > 0;
+        }
         const long long base = (long long)whole * sk_ctas * kt_all;
         const long long T = (long long)(tiles - whole * sk_ctas) * kt_all;
         it0 = base + T * blockIdx.x / sk_ctas;
@@ -649,6 +664,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // stream-K's CTA count (CTA pairs never run stream-K: a constant 0 lets
     // the compiler drop those paths)
     const int SK_CTAS = PAIR ? 0 : p.sk_ctas;
+    const int SK_PARTS = PAIR ? 0 : p.sk_parts;
     const bool sk = SK_CTAS > 0;
     // this CTA's work: whole tiles of the full waves and a share of the
     // remaining tiles' slabs (stream-K), a consecutive range of one tile's
@@ -728,7 +744,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             griddep_wait();
             int tile, k0, nk, g = 0;   // g: slabs issued so far (ring position)
             bool stop = false;
-            for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
+            for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE, SK_PARTS); ++si) {
                 int m0, n0;
                 tile_origin(tile, m0, n0);
                 // PAIR: this CTA's 128 rows of A and Y_ROWS rows of B
@@ -794,7 +810,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             constexpr uint32_t idesc = tc::idesc_tf32_f32<PAIR ? 2 * BM : BM, BN, X_MN, Y_MN>();
             int tile, k0, nk, g = 0, cg = 0;   // g: slabs consumed, cg: chunks started
             bool stop = false;
-            for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
+            for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE, SK_PARTS); ++si) {
               for (int kt = 0; kt < nk; ++kt, ++g) {
                 // each segment's slabs accumulate in chunks of CHUNK_STAGES
                 // slabs, alternating between the two TMEM buffers
@@ -890,7 +906,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // nothing to split (both operands come split), except that the odd
         // CTA of a pair still tells the leader when its slab has landed
         bool stop = !x_raw && !y_raw && !(PAIR && prank == 1);
-        for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
+        for (int si = 0; !stop && cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE, SK_PARTS); ++si) {
           for (int kt = 0; kt < nk; ++kt, ++g) {
             if (CONV_PER_WARP && (g % CONV_WARPS) != mine) continue;
             const int s = g % STAGES;
@@ -1127,11 +1143,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             const long long T = (long long)(tiles - sk_tail0) * KT_ALL, G = p.sk_ctas;
             const long long x0 = (long long)(t - sk_tail0) * KT_ALL, x1 = x0 + KT_ALL;
             // the CTAs whose runs meet [x0, x1): g with T g / G < x1 and T (g + 1) / G > x0
-            const int g_first = (int)(((x0 + 1) * G - 1) / T), g_last = (int)((x1 * G - 1) / T);
+            // (sk_parts >= 2: CTAs (t - sk_tail0) S + j, j = 0 .. S - 1)
+            const int S = p.sk_parts;
+            const int g_first = S >= 2 ? (t - sk_tail0) * S : (int)(((x0 + 1) * G - 1) / T);
+            const int g_last = S >= 2 ? g_first + S - 1 : (int)((x1 * G - 1) / T);
             // a CTA's slot: 0 for the tile its run starts in, 1 for the one it
             // ends in.  Every contributor after the first starts inside the
             // tile (slot 0); only the first may have started before it.
-            const int first_slot = T * g_first / G >= x0 ? 0 : 1;
+            const int first_slot = S >= 2 || T * g_first / G >= x0 ? 0 : 1;
             const int my_slot = (int)blockIdx.x == g_first ? first_slot : 0;
             constexpr int SLOT = BM * BN / 4;   // float4s per slot
             float4 *const ws = reinterpret_cast<float4 *>(p.sk_ws);
@@ -1200,7 +1219,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         };
 
         int tile, k0, nk, cg = 0;   // cg: chunks drained so far
-        for (int si = 0; cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE); ++si) {
+        for (int si = 0; cta_segment(SK_CTAS, KT_ALL, tiles, nsplit, rank, si, tile, k0, nk, CTAS_PER_TILE, SK_PARTS); ++si) {
 #pragma unroll
             for (int j = 0; j < COLS_PER_THREAD; ++j) acc[j] = 0.f;
             const int nc = (nk + CHUNK_STAGES - 1) / CHUNK_STAGES;

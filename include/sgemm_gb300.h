@@ -314,6 +314,8 @@ typedef struct sgemm_plan {
     int b_in_kernel;   /* 1: the same for B (no split pass, no scratch for that operand)       */
     int pair;          /* 1: CTA pairs (cta_group::2) compute 256 x 256 tiles, 2 CTAs per tile */
     int persistent;    /* 1: grid CTAs take whole tiles g, g + grid, ... in turn (more than a wave) */
+    int sk_parts;      /* stream-K, >= 2: the tiles left after the full waves are each cut into */
+                       /*      sk_parts equal k ranges (one per CTA) instead of equal runs    */
 } sgemm_plan;
 
 int sgemm_plan_for(int m, int n, int k, float alpha,

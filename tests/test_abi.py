@@ -247,10 +247,10 @@ def test_persistent_policy(monkeypatch):
 
 def test_stream_k_policy(monkeypatch):
     """Stream-K (one CTA per SM: the full waves as whole tiles, the last
-    wave's tiles shared out by slabs) when whole tiles would leave >= 10 % of
-    the last wave idle and its estimate wins; never for batches, never when
-    a tile would meet too many CTAs (few tiles: split-K clusters instead),
-    never with fewer slabs than CTAs; the tuning variable pins it."""
+    wave's tiles shared out by slabs) when its estimate beats whole tiles and
+    split-K; never for batches, never when a tile would meet too many CTAs
+    (few tiles: split-K clusters instead), never with fewer slabs than CTAs;
+    the tuning variable pins it."""
     for v in ("SGEMM_GB300_STREAM_K", "SGEMM_GB300_TRANS", "SGEMM_GB300_TILE_N", "SGEMM_GB300_SPLIT_K"):
         monkeypatch.delenv(v, raising=False)
     TC = binding.PATH_TF32X3
@@ -275,6 +275,30 @@ def test_stream_k_policy(monkeypatch):
         assert p["stream_k"] == 152 and p["grid"] == 152, (shape, p)
     st, p = hplan(64, 64, 32, path=TC)               # 1 tile x 2 slabs < 152 CTAs
     assert p["stream_k"] == 0
+
+
+def test_stream_k_parts_policy(monkeypatch):
+    """After two or more full waves, a stream-K plan cuts each of the R tiles
+    left into S = sms / R equal k parts, one per CTA (when S >= 2); with no
+    full wave, or S = 1, the slab sequence is cut into equal runs.
+    SGEMM_GB300_SK_PARTS pins the choice."""
+    for v in ("SGEMM_GB300_STREAM_K", "SGEMM_GB300_TRANS", "SGEMM_GB300_TILE_N", "SGEMM_GB300_SPLIT_K",
+              "SGEMM_GB300_SK_PARTS"):
+        monkeypatch.delenv(v, raising=False)
+    TC = binding.PATH_TF32X3
+    # 8192^3: 2048 tiles = 13 x 152 + 72 -> 2 parts; 4096^3: 512 = 3 x 152 + 56 -> 2
+    for shape, S in [((8192, 8192, 8192), 2), ((4096, 4096, 4096), 2), ((8192, 2048, 8192), 2),
+                     ((16384, 128, 8192), 0), ((6144, 6144, 6144), 0)]:
+        st, p = hplan(*shape, path=TC)
+        assert st == 0 and p["stream_k"] == 152 and p["sk_parts"] == S, (shape, p)
+    monkeypatch.setenv("SGEMM_GB300_SK_PARTS", "0")
+    st, p = hplan(8192, 8192, 8192, path=TC)
+    assert p["stream_k"] == 152 and p["sk_parts"] == 0
+    monkeypatch.setenv("SGEMM_GB300_SK_PARTS", "1")
+    st, p = hplan(16384, 128, 8192, path=TC)        # pinned: 64 tiles, 2 parts each
+    assert p["stream_k"] == 152 and p["sk_parts"] == 2
+    st, p = hplan(2048, 2048, 2048, path=TC)        # CTA pairs: no stream-K, no parts
+    assert p["stream_k"] == 0 and p["sk_parts"] == 0
 
 
 def test_in_kernel_split_policy(monkeypatch):

@@ -4,7 +4,9 @@ by the last of them from their partial sums in a workspace), pinned with
 the library's tuning variable SGEMM_GB300_STREAM_K, against the FP64
 oracle: 256-wide, 128-wide and transposed tiles, A split in the kernel and
 by the pre-pass, ragged shapes, beta != 0, tiles shared by 2-3 CTAs and by
-dozens, integer twins bit-exact, and repeatability."""
+dozens, integer twins bit-exact, and repeatability; and the form that cuts
+each tile left after the full waves into S equal k parts (one per CTA,
+SGEMM_GB300_SK_PARTS) on the same kinds of tiles."""
 import pytest
 import torch
 
@@ -24,7 +26,7 @@ def _gpu():
 @pytest.fixture(autouse=True)
 def _clean_env(monkeypatch):
     for v in ("SGEMM_GB300_STREAM_K", "SGEMM_GB300_TRANS", "SGEMM_GB300_TILE_N", "SGEMM_GB300_SPLIT_A_IN",
-              "SGEMM_GB300_SPLIT_K"):
+              "SGEMM_GB300_SPLIT_K", "SGEMM_GB300_SK_PARTS"):
         monkeypatch.delenv(v, raising=False)
 
 
@@ -95,3 +97,39 @@ def test_stream_k_is_deterministic(monkeypatch):
         outs.append(C)
     torch.cuda.synchronize()
     assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+PARTS_CASES = [
+    # m, n, k, beta, extra tuning variables, S expected on 152 SMs
+    (2432, 4608, 256, 0.0, {}, 4),                                  # 342 tiles of 128 x 256 = 2 x 152 + 38
+    (2400, 4600, 250, 0.5, {}, 4),                                  # the same tiles, ragged in m, n and k
+    (25600, 128, 64, -1.0, {"SGEMM_GB300_TRANS": "0"}, 3),          # 200 tiles of 128 x 128 = 152 + 48
+    (51200, 100, 64, 2.0, {"SGEMM_GB300_TRANS": "1"}, 3),           # 200 transposed 256 x 128 tiles
+    (16384, 128, 2048, 1.0, {}, 2),                                 # no full wave: 64 tiles, 2 parts each
+]
+
+
+@pytest.mark.parametrize("m,n,k,beta,env,S", PARTS_CASES)
+def test_stream_k_parts_match_oracle(monkeypatch, m, n, k, beta, env, S):
+    monkeypatch.setenv("SGEMM_GB300_STREAM_K", "1")
+    monkeypatch.setenv("SGEMM_GB300_SK_PARTS", "1")
+    for key, val in env.items():
+        monkeypatch.setenv(key, val)
+    p = inputs.make_problem(m, n, k, alpha=1.25, beta=beta, seed=m + 3 * n + k, a="normal", b="uniform",
+                            c="uniform" if beta else None)
+    plan = _plan(p)
+    assert plan["stream_k"] > 0, plan
+    if torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert plan["sk_parts"] == S, plan
+    assert plan["sk_parts"] >= 2, plan
+    _run(p)
+
+
+def test_stream_k_parts_integer_twin_bit_exact_and_repeatable(monkeypatch):
+    monkeypatch.setenv("SGEMM_GB300_STREAM_K", "1")
+    monkeypatch.setenv("SGEMM_GB300_SK_PARTS", "1")
+    p = inputs.make_problem(2432, 4608, 256, alpha=2.0, beta=0.5, seed=29, a="int", b="int", c="int")
+    assert _plan(p)["sk_parts"] >= 2
+    C = _run(p, exact=True)
+    C2 = _run(p, exact=True)
+    assert torch.equal(torch.as_tensor(C), torch.as_tensor(C2))
