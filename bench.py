@@ -256,11 +256,13 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- helpers
 
 # sources that define each kernel family (a traffic figure is void once any
-# changes); the tensor-core families differ in which operands the GEMM reads
-# as stored (raw) and which come split by the split pass
-_TC_SOURCES = ["tf32x3_sgemm.cuh", "tcgen05.cuh", "ptx.cuh", "raster.cuh"]
+# changes), the planner (sgemm_api.cu) among them: the plan -- tiles, raster
+# groups, schedule -- sets the launch whose traffic a record holds.  The
+# tensor-core families differ in which operands the GEMM reads as stored
+# (raw) and which come split by the split pass.
+_TC_SOURCES = ["tf32x3_sgemm.cuh", "tcgen05.cuh", "ptx.cuh", "raster.cuh", "sgemm_api.cu"]
 KERNEL_SOURCES = {
-    "ffma": ["ffma_sgemm.cuh", "ptx.cuh", "raster.cuh"],
+    "ffma": ["ffma_sgemm.cuh", "ptx.cuh", "raster.cuh", "sgemm_api.cu"],
     "tf32x3_raw_ab": _TC_SOURCES,
     "tf32x3_raw_a": _TC_SOURCES,
     "tf32x3_raw_b": _TC_SOURCES,

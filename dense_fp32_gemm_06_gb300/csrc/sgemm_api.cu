@@ -43,6 +43,8 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 constexpr int kKernelFfmaCpAsync = 0;
 constexpr int kKernelScale = 1;
 constexpr int kKernelTf32x3 = 2;
+// GB300's L2 (the plans are for sm_103a devices; host-only plans too)
+constexpr double kL2Bytes = 129e6;
 
 int fail_cuda(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -405,7 +407,26 @@ int plan(int m, int n, int k, float alpha, const float *A, int lda, const float 
             if (parts && S >= 2 && KT >= S) pl->sk_parts = S;
         }
         pl->k_tiles = (int)KT;
-        pl->group_m = tiles_mt < 8 ? tiles_mt : 8;
+        // Raster groups: a wave of G = sms CTAs covers g tile rows x G / g
+        // tile columns, and reads g A panels (BM rows of k) and G / g B
+        // panels (BN rows) -- 4 bytes a value as stored, 8 split -- which
+        // costs least near g = sqrt(G x B panel / A panel): ~25 for 128 x 256
+        // tiles with B split first.  Where the operands as read exceed twice
+        // L2 (DRAM-streamed), 24 tile rows; otherwise 8, which keeps the
+        // panels of the CTAs running at once together in L2.  Measured
+        // (whole calls, interleaved, L2 flushed): 8192 x 8192 x 4096 1880
+        // against 1920 us, 16384 x 8192 x 4096 3744 against 3818; 8192^3
+        // DRAM per launch 5.27 -> ~3.4 GB and the 300-step bench line, held
+        // at the power cap, 294.2 - 294.5 against 287.5 - 289.6 TFLOPS
+        // (higher clocks at the same power); 4096^3 (operands ~1.5x L2) 0.9 %
+        // slower with 24.  SGEMM_GB300_GROUP_M (1 .. 64) pins it.
+        const double op_bytes = (double)m * k * (pl->a_in_kernel ? 4 : 8) * (batch > 0 ? batch : 1) +
+                                (double)n * k * (pl->b_in_kernel ? 4 : 8) * (batch > 0 ? batch : 1);
+        const char *env_gm = std::getenv("SGEMM_GB300_GROUP_M");
+        const int gm = env_gm && std::atoi(env_gm) >= 1 && std::atoi(env_gm) <= 64 ? std::atoi(env_gm)
+                       : op_bytes > 2.0 * kL2Bytes                                    ? 24
+                                                                                      : 8;
+        pl->group_m = tiles_mt < gm ? tiles_mt : gm;
         return SGEMM_STATUS_OK;
     }
     pl->kernel = kKernelFfmaCpAsync;

@@ -301,6 +301,21 @@ def test_stream_k_parts_policy(monkeypatch):
     assert p["stream_k"] == 0 and p["sk_parts"] == 0
 
 
+def test_raster_group_policy(monkeypatch):
+    """Raster groups of 24 tile rows where the operands as read (4 bytes a
+    value as stored, 8 split) exceed twice L2, of 8 otherwise (capped at the
+    tile rows); SGEMM_GB300_GROUP_M pins it."""
+    monkeypatch.delenv("SGEMM_GB300_GROUP_M", raising=False)
+    TC = binding.PATH_TF32X3
+    for shape, g in [((8192, 8192, 8192), 24), ((8192, 8192, 4096), 24), ((16384, 8192, 4096), 24),
+                     ((4096, 4096, 4096), 8), ((1000, 1500, 777), 8), ((256, 256, 256), 2)]:
+        st, p = hplan(*shape, path=TC)
+        assert st == 0 and p["group_m"] == g, (shape, p)
+    monkeypatch.setenv("SGEMM_GB300_GROUP_M", "12")
+    st, p = hplan(8192, 8192, 8192, path=TC)
+    assert p["group_m"] == 12
+
+
 def test_in_kernel_split_policy(monkeypatch):
     """The tensor-core GEMM reads an operand as stored and splits it itself
     when TMA can load it -- a 16-byte aligned base, rows a multiple of 16
