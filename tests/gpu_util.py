@@ -98,3 +98,31 @@ def check_sampled(p, C, rows, cols, exact=False):
         return ok, 0.0 if ok else float("inf"), None
     C0v = p.C0[rows, cols] if p.beta != 0.0 else None
     return oracle.within_tolerance(got, R, E, p.beta, C0v)
+
+
+def projection_ratios(A, B, C0, C, alpha, beta, seed):
+    """Freivalds' check of every output of C = alpha A B + beta C0 at once,
+    in FP64 on the tensors' device: (max over rows of |C x - ref| / bound,
+    max over columns of |y^T C - ref| / bound) for Gaussian x, y drawn from
+    `seed`.  The bound of a row (column) is the sum over it of the
+    per-element FP32 bound 1e-5 |alpha| sum_t |A_it||B_tj| + 1e-6 |beta C0_ij|
+    (against |x_j|, |y_i|), so a C within that bound everywhere gives ratios
+    <= 1.  C0 is not used when beta = 0."""
+    g = torch.Generator(device=C.device).manual_seed(seed)
+    m, n = C.shape
+    x = torch.randn(n, 1, device=C.device, dtype=torch.float64, generator=g)
+    y = torch.randn(1, m, device=C.device, dtype=torch.float64, generator=g)
+    Ad, Bd, Cd = A.double(), B.double(), C.double()
+    ref_x = alpha * (Ad @ (Bd @ x))
+    tol_x = 1e-5 * abs(alpha) * (Ad.abs() @ (Bd.abs() @ x.abs()))
+    ref_y = alpha * ((y @ Ad) @ Bd)
+    tol_y = 1e-5 * abs(alpha) * ((y.abs() @ Ad.abs()) @ Bd.abs())
+    if beta != 0:
+        C0d = C0.double()
+        ref_x = ref_x + beta * (C0d @ x)
+        tol_x = tol_x + 1e-6 * abs(beta) * (C0d.abs() @ x.abs())
+        ref_y = ref_y + beta * (y @ C0d)
+        tol_y = tol_y + 1e-6 * abs(beta) * (y.abs() @ C0d.abs())
+    rx = ((Cd @ x - ref_x).abs() / tol_x).max().item()
+    ry = ((y @ Cd - ref_y).abs() / tol_y).max().item()
+    return rx, ry

@@ -84,6 +84,32 @@ def test_workload_integer_twin_sampled_bit_exact(name, path):
     run_and_check(p, path, exact=True, sample=inputs.sample_indices(p.m, p.n, 4096, seed=p.seed + 1000))
 
 
+@pytest.mark.parametrize("path", PATHS + [binding.PATH_AUTO], ids=lambda p: PATH_IDS[p])
+@pytest.mark.parametrize("name", LARGE)
+def test_workload_every_output_by_projection(name, path):
+    """Every output of the full-size workloads, through random projections
+    (Freivalds' check, in FP64 on the GPU): C x against alpha A (B x) +
+    beta C0 x and y^T C against alpha (y^T A) B + beta y^T C0, each row
+    (column) within the sum over it of the per-element FP32 bound,
+    1e-5 |alpha| (|A| (|B| |x|)) + 1e-6 |beta| (|C0| |x|).  A tile written
+    wrong, twice or not at all moves its 128 rows (columns) far outside it;
+    with beta = 0, C starts as the sentinel and none may be left."""
+    import gpu_util
+    p = inputs.workload(name)
+    if not path_runs(path, p):
+        pytest.skip(f"path {PATH_IDS[path]} does not take this problem")
+    A = torch.from_numpy(np.ascontiguousarray(p.A[:, :p.k])).cuda()
+    B = torch.from_numpy(np.ascontiguousarray(p.B[:, :p.n])).cuda()
+    C0 = torch.from_numpy(np.ascontiguousarray(p.C0[:, :p.n])).cuda()
+    C = C0.clone() if p.beta != 0 else torch.full((p.m, p.n), float(gpu_util.SENTINEL), device="cuda")
+    binding.sgemm_ex(A, B, C, p.alpha, p.beta, path=path)
+    torch.cuda.synchronize()
+    if p.beta == 0:
+        assert not bool((C == float(gpu_util.SENTINEL)).any()), "an output was never written"
+    rx, ry = gpu_util.projection_ratios(A, B, C0, C, p.alpha, p.beta, p.seed + 77)
+    assert rx <= 1.0 and ry <= 1.0, f"projection residual / bound: rows {rx}, columns {ry}"
+
+
 # ---------------------------------------------------------------- edges and tails
 
 EDGE = [1, 3, 4, 5, 31, 127, 128, 129, 200]
