@@ -190,8 +190,10 @@ static_assert(sizeof(Params) <= 128, "kernel parameter block");
 
 // Segment `si` of the work of CTA blockIdx.x -- one tile and a range
 // [k0, k0 + nk) of its kt_all slabs; false past the last.  Stream-K over
-// sk_ctas > 0 CTAs (see Params): the whole tiles blockIdx.x + w G first, then the CTA's run of
-// the remaining tiles' slab sequence cut at tile boundaries.  Otherwise one
+// sk_ctas > 0 CTAs (see Params): the whole tiles blockIdx.x + w G first, then
+// the CTA's run of the remaining tiles' slab sequence cut at tile
+// boundaries, or (sk_parts >= 2) its one k part of one remaining tile.
+// Persistent whole tiles (sk_ctas < 0): tiles blockIdx.x + w G.  Otherwise one
 // segment of tile blockIdx.x / ctas_per_tile (nsplit for a split-K cluster,
 // 2 for a CTA pair, else 1): split-K cluster rank `rank`'s share of its
 // slabs (possibly empty), or all of them.  Recomputed on demand so that no

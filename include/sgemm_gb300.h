@@ -309,8 +309,9 @@ typedef struct sgemm_plan {
     int a_in_kernel;   /* 1: the tensor-core GEMM reads A as stored (TMA) and splits it itself */
                        /*    (in four row phases when its rows are not 16 bytes apart)      */
     int trans;         /* 1: tensor-core tiles of C^T = B^T A^T (n <= 128; bm = 256, bn = 128) */
-    int stream_k;      /* > 0: stream-K over this many CTAs (grid); each takes an equal share  */
-                       /*      of all tiles' k slabs, partial tiles meet in a workspace        */
+    int stream_k;      /* > 0: stream-K over this many CTAs (grid): the full waves as whole   */
+                       /*      tiles, the rest shared out by k slabs (equal runs, or sk_parts  */
+                       /*      parts a tile); partial tiles meet in a workspace                */
     int b_in_kernel;   /* 1: the same for B (no split pass, no scratch for that operand)       */
     int pair;          /* 1: CTA pairs (cta_group::2) compute 256 x 256 tiles, 2 CTAs per tile */
     int persistent;    /* 1: grid CTAs take whole tiles g, g + grid, ... in turn (more than a wave) */
