@@ -124,3 +124,19 @@ def test_kernel_hash_ignores_comments_only():
     assert bench.strip_comments(code) == bench.strip_comments(code.replace("one more", "plus one"))
     assert bench.strip_comments(code) != bench.strip_comments(code.replace("x + 1", "x + 2"))
     assert "note" not in bench.strip_comments(code) and "return x + 1;" in bench.strip_comments(code)
+
+
+def test_kernel_hash_covers_the_planner(tmp_path, monkeypatch):
+    """The plan (tiles, raster groups, schedule) sets the launch whose
+    traffic a record holds, so a change to the planner's code voids every
+    family's records too."""
+    import shutil
+    src = os.path.join(bench.ROOT, "dense_fp32_gemm_06_gb300", "csrc")
+    dst = tmp_path / "dense_fp32_gemm_06_gb300" / "csrc"
+    shutil.copytree(src, dst)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    before = {f: bench.kernel_source_hash(f) for f in bench.KERNEL_SOURCES}
+    planner = dst / "sgemm_api.cu"
+    planner.write_text(planner.read_text() + "\nstatic int another_plan_constant = 1;\n")
+    after = {f: bench.kernel_source_hash(f) for f in bench.KERNEL_SOURCES}
+    assert all(before[f] != after[f] for f in before)
