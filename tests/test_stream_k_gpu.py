@@ -100,23 +100,24 @@ def test_stream_k_is_deterministic(monkeypatch):
 
 
 PARTS_CASES = [
-    # m, n, k, beta, extra tuning variables, S expected on 152 SMs
-    (2432, 4608, 256, 0.0, {}, 4),                                  # 342 tiles of 128 x 256 = 2 x 152 + 38
-    (2400, 4600, 250, 0.5, {}, 4),                                  # the same tiles, ragged in m, n and k
-    (25600, 128, 64, -1.0, {"SGEMM_GB300_TRANS": "0"}, 3),          # 200 tiles of 128 x 128 = 152 + 48
-    (51200, 100, 64, 2.0, {"SGEMM_GB300_TRANS": "1"}, 3),           # 200 transposed 256 x 128 tiles
-    (16384, 128, 2048, 1.0, {}, 2),                                 # no full wave: 64 tiles, 2 parts each
+    # m, n, k, lda, beta, extra tuning variables, S expected on 152 SMs
+    (2432, 4608, 256, None, 0.0, {}, 4),                            # 342 tiles of 128 x 256 = 2 x 152 + 38
+    (2400, 4600, 250, None, 0.5, {}, 4),                            # the same tiles, ragged in m, n and k
+    (2432, 4608, 256, 257, 0.5, {}, 4),                             # lda odd: A read in row phases
+    (25600, 128, 64, None, -1.0, {"SGEMM_GB300_TRANS": "0"}, 3),    # 200 tiles of 128 x 128 = 152 + 48
+    (51200, 100, 64, None, 2.0, {"SGEMM_GB300_TRANS": "1"}, 3),     # 200 transposed 256 x 128 tiles
+    (16384, 128, 2048, None, 1.0, {}, 2),                           # no full wave: 64 tiles, 2 parts each
 ]
 
 
-@pytest.mark.parametrize("m,n,k,beta,env,S", PARTS_CASES)
-def test_stream_k_parts_match_oracle(monkeypatch, m, n, k, beta, env, S):
+@pytest.mark.parametrize("m,n,k,lda,beta,env,S", PARTS_CASES)
+def test_stream_k_parts_match_oracle(monkeypatch, m, n, k, lda, beta, env, S):
     monkeypatch.setenv("SGEMM_GB300_STREAM_K", "1")
     monkeypatch.setenv("SGEMM_GB300_SK_PARTS", "1")
     for key, val in env.items():
         monkeypatch.setenv(key, val)
     p = inputs.make_problem(m, n, k, alpha=1.25, beta=beta, seed=m + 3 * n + k, a="normal", b="uniform",
-                            c="uniform" if beta else None)
+                            c="uniform" if beta else None, lda=lda)
     plan = _plan(p)
     assert plan["stream_k"] > 0, plan
     if torch.cuda.get_device_properties(0).multi_processor_count == 152:
